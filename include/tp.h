@@ -1,0 +1,217 @@
+/*
+ * libtp: streamed pairwise score consumers for GB300 (sm_103a).
+ *
+ * A pairwise score S[i,j] = f(x_i, y_j) over X [N,D] and Y [M,D] is evaluated tile by tile on the
+ * GPU and consumed in the same pass; the [N,M] matrix is never stored. First derivatives re-evaluate
+ * the pairs ("replay") in a row sweep (dX, row parameters) and a transposed column sweep (dY, dV,
+ * column parameters), without atomics. Source of the method: "Using Torchpairwise in Models"
+ * (torchpairwise guide, ml.html), introduction: bind scores lazily, consume them in bounded tiles or
+ * fused CUDA kernels, never store the matrix, replay tiles for first derivatives; memory scales with
+ * (N+M)*(D+C) plus a tile workspace.
+ *
+ * Canonical score (the guide's "Score Expressions" section: scalar scale, add_rows, add_columns,
+ * weight_rows, weight_columns and exp are the fused nodes; this library fixes their order):
+ *     base_ij = |x_i - y_j|^2                  (TP_SQEUCLIDEAN)
+ *             | x_i . y_j                      (TP_LINEAR)
+ *             | exp(-gamma |x_i - y_j|^2)      (TP_RBF; "Stein Variational Gradient Descent")
+ *     t_ij    = scale * wr_i * wc_j * base_ij + br_i + bc_j   (absent weight = 1, absent bias = 0)
+ *     S_ij    = apply_exp ? exp(t_ij) : t_ij
+ *
+ * Conventions shared by every entry point
+ *   - Layout: every matrix is row-major and contiguous. X [N,D], Y [M,D], V [M,C], outputs [N,*],
+ *     column gradients [M,*]. All element pointers have the dtype of `tp_pairs.dtype` (float or
+ *     double) except top-k indices, which are int64.
+ *   - Sizes: N, M >= 1; 1 <= D <= 64; 1 <= C <= 64 (the guide's fused range, "Task Map"); M and N
+ *     below 2^31.
+ *   - Memory: every pointer is caller-owned DEVICE memory (tp_pairs, tp_score and the scalar
+ *     arguments themselves are host structs read during the call). libtp allocates nothing,
+ *     frees nothing and never synchronises: all work is enqueued on `stream` (a cudaStream_t passed
+ *     as void*, NULL = legacy default stream) and the call returns as soon as it is enqueued.
+ *   - Workspace: `ws` is caller-owned device scratch of at least tp_workspace_size(entry, ...) bytes,
+ *     aligned to 256 bytes (what cudaMalloc returns). Its size depends on the shapes only. It may be
+ *     NULL when the required size is 0. The contents need no initialisation and are garbage after
+ *     the call; the caller must not reuse it on another stream until this call's work is done.
+ *   - Errors: every argument is validated before anything is launched. Status codes only; nothing
+ *     throws across the boundary and nothing traps on the device.
+ *       TP_ERR_INVALID_ARG  NULL required pointer, size out of range, bad metric/dtype/k, exclude_self
+ *                           with N != M, output aliasing an input or another output (except the
+ *                           documented dX/dY alias), misaligned pointer, workspace too small.
+ *       TP_ERR_UNSUPPORTED  a valid request this build has no kernel for.
+ *       TP_ERR_CUDA         a CUDA launch error (the runtime's error text is in tp_last_error()).
+ *     There is no CPU fallback.
+ *   - Backward outputs are written, not accumulated. A NULL gradient output means "not requested";
+ *     its work is skipped. When X and Y are the same points (X == Y, N == M), dY may be the same
+ *     pointer as dX: the sum dX + dY is then written there.
+ *   - Results agree with an exact evaluation within floating tolerance, not bitwise: the sums run in
+ *     a different order (the guide's "What to Check", precision). Top-k values and indices are exact
+ *     whenever the scores are exact in the working precision.
+ *   - Non-finite inputs are not supported; their results are unspecified.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_INVALID_ARG = 1,
+    TP_ERR_UNSUPPORTED = 2,
+    TP_ERR_CUDA = 3,
+    TP_ERR_WORKSPACE = 4, /* reserved: a too-small workspace is reported as TP_ERR_INVALID_ARG */
+    TP_ERR_TIMEOUT = 5    /* reserved: no kernel of this build waits on another block */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_F64 = 1 } tp_dtype;
+
+typedef enum { TP_SQEUCLIDEAN = 0, TP_LINEAR = 1, TP_RBF = 2 } tp_metric;
+
+/* The canonical score (see the file comment). Bias and weight pointers are device arrays of the
+ * problem's dtype, [N] for rows and [M] for columns, or NULL when absent. gamma is used by TP_RBF
+ * only. */
+typedef struct {
+    tp_metric metric;
+    double gamma;
+    double scale;
+    int apply_exp;
+    const void *row_bias, *col_bias, *row_weight, *col_weight;
+} tp_score;
+
+/* The two point sets: X [N,D] and Y [M,D], device, row-major, contiguous. */
+typedef struct {
+    tp_dtype dtype;
+    int64_t N, M, D;
+    const void *X, *Y;
+} tp_pairs;
+
+/* ---------------------------------------------------------------------------------------------- */
+/* forward consumers                                                                              */
+/* ---------------------------------------------------------------------------------------------- */
+
+/* Kernel product out_i = sum_j S_ij V_j, out [N,C].
+ * Guide "Task Map", kernel attention / Nadaraya-Watson row: lazy(X, Y, "rbf", gamma) @ V; with
+ * V = [V | ones] the last output column is the row mass sum_j S_ij. */
+TP_API tp_status tp_pairwise_matmul(const tp_pairs* pairs, const tp_score* score, const void* V, int64_t C,
+                             void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Row log-sum-exp lse_i = log sum_j exp(S_ij), lse [N]; with exclude_self != 0 the pair j == i is
+ * left out (requires N == M; a row with no pair left gives -inf).
+ * Guide "Task Map", InfoNCE / NT-XEnt row: S.logsumexp(-1, exclude_self=True); "Score Expressions"
+ * example -logits.logsumexp(-1).mean(). */
+TP_API tp_status tp_pairwise_logsumexp(const tp_pairs* pairs, const tp_score* score, int exclude_self,
+                                void* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Attention row out_i = sum_j softmax_j(S_ij) V_j, out [N,C]; also writes lse [N] (the row
+ * log-sum-exp of S), which the backward takes back.
+ * Guide introduction example and "Task Map", attention row: (lazy(Q, K, "linear") * s).softmax_matmul(V),
+ * fused without a pair mask. */
+TP_API tp_status tp_pairwise_softmax_matmul(const tp_pairs* pairs, const tp_score* score, const void* V,
+                                     int64_t C, void* out, void* lse, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/* Displacement disp_i = sum_j S_ij (y_j - x_i), out [N,D].
+ * Guide "Stein Variational Gradient Descent": the kernel's displacement method, which streams the
+ * repulsive term sum_j k_ij (x_j - x_i). */
+TP_API tp_status tp_pairwise_displacement(const tp_pairs* pairs, const tp_score* score, void* out, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* SVGD direction phi_i = (1/n) sum_j k_ij (score_j - 2 gamma (x_j - x_i)), phi [n,D], with
+ * k_ij = exp(-gamma |x_i - x_j|^2), n = M, in one sweep (one kernel evaluation per pair).
+ * pairs->X and pairs->Y hold the particles (normally the same array, N == M); score [M,D] is the
+ * target's score at each particle. Only gamma is read from the canonical score: the formula is the
+ * bare rbf kernel.
+ * Guide "Stein Variational Gradient Descent": phi = (K @ score - 2 gamma K.displacement()) / n. */
+TP_API tp_status tp_svgd_direction(const tp_pairs* pairs, double gamma, const void* score, void* phi,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Row top-k: the k smallest S_ij of each row (largest != 0: the k largest), values [N,k] and
+ * indices [N,k] (int64), sorted by value (ascending; descending for largest) and, among equal
+ * values, by ascending column index. 1 <= k <= min(M, 128).
+ * Guide "Task Map", k-NN / retrieval row: lazy(X, R, "sqeuclidean").topk(k, largest=False), fused,
+ * exact tie order; argmin and min are k = 1. */
+TP_API tp_status tp_pairwise_topk(const tp_pairs* pairs, const tp_score* score, int k, int largest,
+                           void* values, int64_t* indices, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* backward by replay (guide introduction: "First derivatives replay the tiles")                  */
+/* Inputs are the forward's inputs plus the upstream gradient; outputs are gradients with the     */
+/* shapes of X [N,D], Y [M,D], V [M,C], row bias/weight [N], column bias/weight [M]. A gradient   */
+/* for a bias or weight that the score does not have must be NULL.                                */
+/* ---------------------------------------------------------------------------------------------- */
+
+/* Gradients of L = sum_ic grad_out_ic out_ic for out = tp_pairwise_matmul(...); grad_out [N,C]. */
+TP_API tp_status tp_pairwise_matmul_backward(const tp_pairs* pairs, const tp_score* score, const void* V,
+                                      int64_t C, const void* grad_out, void* dX, void* dY, void* dV,
+                                      void* d_row_bias, void* d_col_bias, void* d_row_weight,
+                                      void* d_col_weight, void* ws, size_t ws_bytes, void* stream);
+
+/* Gradients of L = sum_i grad_lse_i lse_i; lse [N] is the forward's output, grad_lse [N]. */
+TP_API tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pairs, const tp_score* score,
+                                         int exclude_self, const void* lse, const void* grad_lse,
+                                         void* dX, void* dY, void* d_row_bias, void* d_col_bias,
+                                         void* d_row_weight, void* d_col_weight, void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/* Gradients of L = sum_ic grad_out_ic out_ic for out = tp_pairwise_softmax_matmul(...); out [N,C]
+ * and lse [N] are the forward's outputs, grad_out [N,C]. */
+TP_API tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pairs, const tp_score* score,
+                                              const void* V, int64_t C, const void* out,
+                                              const void* lse, const void* grad_out, void* dX,
+                                              void* dY, void* dV, void* d_row_bias,
+                                              void* d_col_bias, void* d_row_weight,
+                                              void* d_col_weight, void* ws, size_t ws_bytes,
+                                              void* stream);
+
+/* Gradients of L = sum_id grad_out_id disp_id for disp = tp_pairwise_displacement(...);
+ * grad_out [N,D]. */
+TP_API tp_status tp_pairwise_displacement_backward(const tp_pairs* pairs, const tp_score* score,
+                                            const void* grad_out, void* dX, void* dY,
+                                            void* d_row_bias, void* d_col_bias, void* d_row_weight,
+                                            void* d_col_weight, void* ws, size_t ws_bytes,
+                                            void* stream);
+
+/* Gradients of L = sum_it grad_values_it values_it, through the selected pairs only (guide "What to
+ * Check": selections route gradients through the selected pairs, not the indices). indices [N,k]
+ * as returned by tp_pairwise_topk (each in [0, M)); grad_values [N,k]. Column gradients are
+ * gathered per column in a deterministic order, without atomics. */
+TP_API tp_status tp_pairwise_topk_backward(const tp_pairs* pairs, const tp_score* score, int k,
+                                    const int64_t* indices, const void* grad_values, void* dX,
+                                    void* dY, void* d_row_bias, void* d_col_bias,
+                                    void* d_row_weight, void* d_col_weight, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* helpers                                                                                        */
+/* ---------------------------------------------------------------------------------------------- */
+
+/* Workspace bytes an entry point needs for these shapes. `entry` is the entry point's name without
+ * the "tp_" prefix, e.g. "pairwise_logsumexp_backward" or "svgd_direction"; C is V's width (ignored
+ * where there is no V) and k the top-k size (ignored elsewhere). Returns (size_t)-1 for an unknown
+ * entry or invalid sizes. Depends on the shapes only, never on the device. */
+TP_API size_t tp_workspace_size(const char* entry, const tp_pairs* pairs, int64_t C, int k);
+
+/* Static text for a status code. */
+TP_API const char* tp_status_string(tp_status status);
+
+/* Text of the last TP_ERR_* reported by this thread (argument name, CUDA error string). */
+TP_API const char* tp_last_error(void);
+
+/* Number of kernels enqueued by this thread since the counter was last reset (instrumentation for
+ * launch counting; reset = 1 zeroes it and returns the previous value). */
+TP_API int64_t tp_launch_count(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */

@@ -1,0 +1,23 @@
+// Forward logsumexp, displacement and SVGD sweeps, their backward sweeps, merges and the top-k
+// backward, float.
+#include "inst_common.h"
+
+namespace tp {
+TP_DP_LIST(TP_INST_FWD, float, 4, kLse)
+TP_DP_LIST(TP_INST_FWD, float, 4, kDisp)
+#define TP_INST_SVGD(DP, T) template void launch_fwd<T, DP, 4, kSvgd, false>(const SweepArgs&, cudaStream_t);
+TP_DP_LIST(TP_INST_SVGD, float)
+template void launch_fwd_merge<float, kLse>(const SweepArgs&, cudaStream_t);
+template void launch_fwd_merge<float, kDisp>(const SweepArgs&, cudaStream_t);
+template void launch_fwd_merge<float, kSvgd>(const SweepArgs&, cudaStream_t);
+TP_DP_LIST(TP_INST_BWD, float, 4, kBLse, kRow, true, false)
+TP_DP_LIST(TP_INST_BWD, float, 4, kBLse, kCol, true, false)
+TP_DP_LIST(TP_INST_BWD, float, 4, kBDisp, kRow, true, false)
+TP_DP_LIST(TP_INST_BWD, float, 4, kBDisp, kCol, true, false)
+template void launch_bwd_merge<float, kBLse, kRow, true, false>(const SweepArgs&, cudaStream_t);
+template void launch_bwd_merge<float, kBLse, kCol, true, false>(const SweepArgs&, cudaStream_t);
+template void launch_bwd_merge<float, kBDisp, kRow, true, false>(const SweepArgs&, cudaStream_t);
+template void launch_bwd_merge<float, kBDisp, kCol, true, false>(const SweepArgs&, cudaStream_t);
+template void launch_topk_bwd<float>(const SweepArgs&, const SweepArgs&, const int64_t*, const void*, int*, int*,
+                                     int*, int*, cudaStream_t);
+}  // namespace tp

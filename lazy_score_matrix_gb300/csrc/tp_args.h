@@ -1,0 +1,48 @@
+// Launch arguments shared by the host dispatch and the kernels (plain data, no CUDA types).
+#pragma once
+
+#include <stdint.h>
+
+namespace tp {
+
+constexpr int kThreads = 128;  // threads per CTA; every thread owns one point
+constexpr int kTile = 32;      // streamed points per shared-memory tile
+
+struct SweepArgs {
+    const void* P;  // own points [nP, D]
+    const void* Q;  // streamed points [nQ, D]
+    int64_t nP, nQ;
+    int D, C;
+    int metric;
+    double gamma, scale;
+    int apply_exp;
+    const void *pb, *qb, *pw, *qw;  // own/other side bias and weight, or NULL
+    int affine;                     // any bias or weight present
+    const void* Vq;                 // streamed value rows [nQ, VW]
+    const void* Vp;                 // own value rows [nP, *]
+    const void* lse;                // [rows] saved row log-sum-exp
+    const void* glse;               // [rows] upstream gradient of lse
+    const void* delta;              // [rows] softmax: dO_i . out_i
+    int exclude_self;
+    int splits;
+    int64_t cps;  // streamed points per split (multiple of kTile)
+    void* out;
+    void* out2;
+    void* ws;
+    void* gP;   // gradient of the own points [nP, D]
+    void* gPb;  // own-side bias gradient [nP]
+    void* gPw;  // own-side weight gradient [nP]
+    void* gV;   // value gradient [nP, C] (column sweep)
+    int accumulate;  // add the own-point gradient into gP instead of writing it
+    int vecQ, vecV, vecVp;
+    double inv_n;
+    int k, largest;
+};
+
+enum FwdMode : int { kMatmul = 0, kSoftmax = 1, kLse = 2, kDisp = 3, kSvgd = 4 };
+
+enum BwdMode : int { kBMatmul = 0, kBSoftmax = 1, kBLse = 2, kBDisp = 3 };
+enum Side : int { kRow = 0, kCol = 1 };
+
+
+}  // namespace tp

@@ -1,0 +1,155 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/tp.h declares, sizes its
+workspace from the shapes alone, and rejects invalid arguments before launching anything.
+
+Every call made here is invalid on purpose and returns before any CUDA work is enqueued, so the
+fake device addresses are never touched (on a machine with or without a GPU).
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from lazy_score_matrix_gb300 import _lib
+from lazy_score_matrix_gb300 import build as tpbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tpbuild.build()
+    return _lib.load()
+
+
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced
+
+
+def pairs(N=10, M=12, D=3, dtype=_lib.TP_F32, X=FAKE, Y=FAKE + 0x100000):
+    return _lib.tp_pairs(dtype, N, M, D, X, Y)
+
+
+def score(metric=1, **kw):
+    return _lib.tp_score(metric, kw.get("gamma", 1.0), kw.get("scale", 1.0), 0, kw.get("rb"), kw.get("cb"),
+                         kw.get("rw"), kw.get("cw"))
+
+
+def test_exports_every_header_symbol(lib):
+    declared = _lib.header_symbols()
+    assert len(declared) == 15, declared
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, missing
+    for s in declared:
+        assert getattr(lib, s) is not None
+    assert set(declared) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.tp_status_string(s)
+    assert b"INVALID" in lib.tp_status_string(_lib.TP_ERR_INVALID_ARG)
+
+
+def ws(lib, entry, p, C=0, k=0):
+    return lib.tp_workspace_size(entry.encode(), ctypes.byref(p), C, k)
+
+
+def test_workspace_sizes_from_shapes(lib):
+    big = ctypes.c_size_t(-1).value
+    p2 = pairs(8192, 8192, 64)
+    a = ws(lib, "pairwise_logsumexp", p2)
+    assert 0 < a < (1 << 30) and a % 256 == 0
+    assert ws(lib, "pairwise_logsumexp", p2) == a  # deterministic
+    assert ws(lib, "pairwise_logsumexp_backward", p2) >= a
+    # a streamed set of one tile needs no split, hence no workspace
+    assert ws(lib, "pairwise_matmul", pairs(100, 20, 3), C=4) == 0
+    assert ws(lib, "pairwise_topk", pairs(1000, 5000, 16), k=16) > 0
+    assert ws(lib, "pairwise_topk", pairs(1000, 5000, 16), k=0) == big
+    assert ws(lib, "pairwise_matmul", pairs(), C=65) == big
+    assert ws(lib, "no_such_entry", pairs()) == big
+    assert ws(lib, "pairwise_matmul", pairs(D=65), C=4) == big
+    # fp64 partial states are twice the fp32 ones
+    assert ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 64, _lib.TP_F64)) >= 2 * a - 512
+
+
+def call_matmul(lib, p, s, V=FAKE + 0x200000, C=4, out=FAKE + 0x300000, w=None, n=0):
+    return lib.tp_pairwise_matmul(ctypes.byref(p) if p is not None else None, ctypes.byref(s), V, C, out, w, n,
+                                  None)
+
+
+@pytest.mark.parametrize("case", ["null_pairs", "D0", "D65", "C0", "C65", "N0", "dtype", "metric", "unaligned",
+                                  "alias_out_X", "ws_small"])
+def test_invalid_arguments_rejected(lib, case):
+    p, s, kw = pairs(), score(), {}
+    if case == "null_pairs":
+        p = None
+    elif case == "D0":
+        p = pairs(D=0)
+    elif case == "D65":
+        p = pairs(D=65)
+    elif case == "C0":
+        kw["C"] = 0
+    elif case == "C65":
+        kw["C"] = 65
+    elif case == "N0":
+        p = pairs(N=0)
+    elif case == "dtype":
+        p = pairs(dtype=7)
+    elif case == "metric":
+        s = score(metric=9)
+    elif case == "unaligned":
+        p = pairs(X=FAKE + 2)
+    elif case == "alias_out_X":
+        kw["out"] = FAKE + 8
+    elif case == "ws_small":
+        p = pairs(N=100, M=5000, D=3)
+        kw["w"], kw["n"] = FAKE + 0x400000, 16
+    assert call_matmul(lib, p, s, **kw) == _lib.TP_ERR_INVALID_ARG
+    assert lib.tp_last_error()
+
+
+def test_other_entries_reject(lib):
+    p = pairs(N=10, M=12)
+    s = score()
+    # exclude_self needs N == M
+    assert lib.tp_pairwise_logsumexp(ctypes.byref(p), ctypes.byref(s), 1, FAKE + 0x300000, None, 0, None) == \
+        _lib.TP_ERR_INVALID_ARG
+    # k out of range
+    for k in (0, 13, 200):
+        assert lib.tp_pairwise_topk(ctypes.byref(p), ctypes.byref(s), k, 0, FAKE + 0x300000, FAKE + 0x380000, None,
+                                    0, None) == _lib.TP_ERR_INVALID_ARG
+    # k above the compiled list length: unsupported, not invalid
+    pbig = pairs(N=10, M=500)
+    assert lib.tp_pairwise_topk(ctypes.byref(pbig), ctypes.byref(s), 64, 0, FAKE + 0x300000, FAKE + 0x380000, None,
+                                0, None) == _lib.TP_ERR_UNSUPPORTED
+    # dX and dY may only coincide when X and Y are the same points
+    g = FAKE + 0x500000
+    assert lib.tp_pairwise_logsumexp_backward(ctypes.byref(pairs(N=12, M=12)), ctypes.byref(s), 0, FAKE + 0x300000,
+                                              FAKE + 0x310000, g, g, None, None, None, None, None, 0, None) == \
+        _lib.TP_ERR_INVALID_ARG
+    # a parameter gradient for a parameter the score does not have
+    assert lib.tp_pairwise_logsumexp_backward(ctypes.byref(pairs(N=12, M=12)), ctypes.byref(s), 0, FAKE + 0x300000,
+                                              FAKE + 0x310000, g, None, FAKE + 0x600000, None, None, None, None, 0,
+                                              None) == _lib.TP_ERR_INVALID_ARG
+    # outputs overlapping each other
+    assert lib.tp_pairwise_softmax_matmul(ctypes.byref(p), ctypes.byref(s), FAKE + 0x200000, 4, FAKE + 0x300000,
+                                          FAKE + 0x300010, None, 0, None) == _lib.TP_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_fallback():
+    """The package refuses CPU tensors instead of computing on the host."""
+    import torch
+
+    import lazy_score_matrix_gb300 as tp
+    x = torch.randn(4, 3)
+    with pytest.raises((ValueError, ImportError)):
+        tp.lazy(x, x, "linear").logsumexp(-1)
+
+
+def test_package_does_not_import_the_oracle():
+    import pathlib
+    import re
+    pkg = pathlib.Path(_lib.PKG)
+    for f in list(pkg.glob("*.py")) + list(pkg.glob("csrc/*")):
+        text = f.read_text()
+        assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
+        assert "tp_oracle" not in text and "or_matmul" not in text, f
