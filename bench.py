@@ -1,0 +1,440 @@
+"""Benchmark of the streamed pairwise-score hot path on GB300.
+
+Default workload (one GPU): InfoNCE row logsumexp, fp32, z [8192,64] unit rows, S = z z^T / 0.07,
+exclude_self, forward plus the replay backward that gives the gradient in z. One step = the forward
+(every pair evaluated once) plus the backward (every pair replayed in a row sweep and a column sweep)
+through libtp's C ABI. Metric: Gpairs/s = N*M / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libtp|reference] [--workload 1..5]
+
+--impl reference times the oracle (plain fp64 CPU loops) on the host cores, on a bounded sample of
+the same workload, and prints the same JSON line with "impl": "reference".
+Under torchrun each rank runs an independent replica of the workload on its own GPU (weak scaling,
+no collective in the data path); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "Gpairs/s per fused consumer (fwd+bwd) at fp32/fp64; % of FP32/FP64 peak"
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def peaks():
+    p = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+    sm_mhz = float(p.get("sm_max_mhz", 2070.0))
+    return {
+        "hbm_gbs": float(p.get("hbm_gbs", 6800.0)),
+        "sm_max_mhz": sm_mhz,
+        "fp32_tflops": SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12,
+        "fp64_tflops": 1.25,  # nominal GB300 FP64 rate (no measured figure)
+        "source": "MEASURED_PEAKS.json" if p else "fallback",
+    }
+
+
+# ------------------------------------------------------------------------------------------------
+# per-kernel timing through libtp's launch hook
+# ------------------------------------------------------------------------------------------------
+
+
+class KernelTimer:
+    """Records a CUDA event pair around every libtp kernel launch (on the launch stream)."""
+
+    def __init__(self):
+        from lazy_score_matrix_gb300 import _lib
+        self._lib = _lib
+        self.events = []  # (name, start, end)
+        self._open = {}
+        self._cb = _lib.LAUNCH_HOOK(self._hook)
+        self.active = False
+
+    def _hook(self, name, phase, stream, user):
+        if not self.active:
+            return
+        st = torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream()
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(st)
+        key = name.decode()
+        if phase == 0:
+            self._open[key] = ev
+        else:
+            self.events.append((key, self._open.pop(key), ev))
+
+    def __enter__(self):
+        self._lib.load().tp_set_launch_hook(self._cb, None)
+        self.active = True
+        return self
+
+    def __exit__(self, *a):
+        self.active = False
+        self._lib.load().tp_set_launch_hook(None, None)
+
+    def summary(self):
+        out = {}
+        for name, a, b in self.events:
+            d = out.setdefault(name, [0, 0.0])
+            d[0] += 1
+            d[1] += a.elapsed_time(b)
+        return {k: {"launches": v[0], "total_ms": v[1], "avg_ms": v[1] / v[0]} for k, v in out.items()}
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def result(self):
+        win = [l for t, l in self.lines if self.t0 is not None and self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        if not win:
+            win = [l for _, l in self.lines]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in win:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# workloads
+# ------------------------------------------------------------------------------------------------
+
+
+class Workload:
+    """One hot-path step on device-resident inputs, plus the same step end to end from host buffers."""
+    name = ""
+    dtype = "f32"
+    pairs = 0
+    flops_per_pair = {}  # per kernel name: algorithmic flop per pair the launch processes
+    bound = "alu"
+
+    def step(self):
+        raise NotImplementedError
+
+    def e2e_step(self):
+        raise NotImplementedError
+
+
+class InfoNCE(Workload):
+    """Workload 2: InfoNCE row logsumexp fwd + replay bwd, z [8192,64] fp32."""
+
+    def __init__(self, dev, N=8192, D=64):
+        from lazy_score_matrix_gb300 import ops, synth
+        self.ops = ops
+        w = synth.workload(2, N=N, D=D)
+        self.N, self.D = N, D
+        self.pairs = N * N
+        self.name = f"infonce_logsumexp_f32_z{N}x{D}_fwd+bwd"
+        self.score = ops.Score("linear", scale=w["scale"])
+        self.z = w["z"].to(dev)
+        self.gl = w["grad_lse"].to(dev)
+        self.want = (True, True, False, False, False, False, False)
+        # pinned host copies for the end-to-end path
+        self.z_h = w["z"].pin_memory()
+        self.gl_h = w["grad_lse"].pin_memory()
+        self.lse_h = torch.empty(N, dtype=torch.float32).pin_memory()
+        self.grad_h = torch.empty(N, D, dtype=torch.float32).pin_memory()
+        self.z_d = torch.empty_like(self.z)
+        self.gl_d = torch.empty_like(self.gl)
+        self.h2d = self.z_h.numel() * 4 + self.gl_h.numel() * 4
+        self.d2h = self.lse_h.numel() * 4 + self.grad_h.numel() * 4
+        D2 = 2 * D
+        # algorithmic flop per pair and launch (FMA = 2): forward 2D+3; backward 387 = (2D+3) + 2D + 2D,
+        # the row sweep credited with the recompute and dX, the column sweep with dY only
+        self.flops_per_pair = {"fwd_sweep_lse": D2 + 3, "bwd_sweep_lse_row": D2 + 3 + D2, "bwd_sweep_lse_col": D2}
+        self.step_flops_per_pair = (D2 + 3) + (D2 + 3 + D2 + D2)
+
+    def step(self):
+        lse = self.ops.pairwise_logsumexp(self.z, self.z, self.score, True)
+        g = self.ops.pairwise_logsumexp_backward(self.z, self.z, self.score, lse, self.gl, True, self.want, same=True)
+        return lse, g["dX"]
+
+    def e2e_step(self):
+        self.z_d.copy_(self.z_h, non_blocking=True)
+        self.gl_d.copy_(self.gl_h, non_blocking=True)
+        lse = self.ops.pairwise_logsumexp(self.z_d, self.z_d, self.score, True)
+        g = self.ops.pairwise_logsumexp_backward(self.z_d, self.z_d, self.score, lse, self.gl_d, True, self.want,
+                                                 same=True)
+        self.lse_h.copy_(lse, non_blocking=True)
+        self.grad_h.copy_(g["dX"], non_blocking=True)
+
+
+WORKLOADS = {2: InfoNCE}
+
+
+def time_steps(fn, steps, flush):
+    """Per-step CUDA events on the current stream; L2 flushed (untimed) before every step."""
+    total = 0.0
+    pairs = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    for a, b in pairs:
+        total += a.elapsed_time(b)
+    return total  # ms
+
+
+def gpu_arm(args, rank, world):
+    from lazy_score_matrix_gb300 import _lib
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload](dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > 129 MB L2
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    _lib.launch_count(reset=True)
+    clocks.t0 = time.time()
+    timer = KernelTimer()
+    with timer:
+        ms = time_steps(wl.step, args.steps, flush)
+    clocks.t1 = time.time()
+    launches = _lib.launch_count()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    # end to end: host buffers, copies inside the timed region
+    for _ in range(2):
+        wl.e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        wl.e2e_step()
+        torch.cuda.current_stream().synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    clocks.stop()
+    if rank != 0:
+        return None
+    pk = peaks()
+    ms_step = ms / args.steps
+    value = world * wl.pairs * args.steps / (ms / 1e3) / 1e9
+    ksum = timer.summary()
+    dom = max(ksum.items(), key=lambda kv: kv[1]["total_ms"])
+    dname, dstat = dom
+    fpp = wl.flops_per_pair.get(dname)
+    roof = None
+    if fpp is not None:
+        ach = fpp * wl.pairs / (dstat["avg_ms"] / 1e3) / 1e12
+        peak = pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]
+        roof = {"kernel": dname, "bound": wl.bound, "achieved": round(ach, 3), "peak": round(peak, 2),
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname),
+                "peak_source": f"FP32 pipe: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x "
+                               f"{pk['sm_max_mhz']:.0f} MHz (derived)",
+                "flop_per_pair": fpp}
+    step_tflops = wl.step_flops_per_pair * wl.pairs / (ms_step / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the workload)",
+        "config": {"workload": wl.name, "N": wl.N, "M": wl.N, "D": wl.D, "pairs_per_step": wl.pairs,
+                   "l2": "flushed before every timed step (256 MB write, untimed)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "impl": "libtp",
+        "roofline": roof,
+        "step_roofline": {"achieved_tflops": round(step_tflops, 3), "flop_per_pair": wl.step_flops_per_pair,
+                          "frac_fp32": round(step_tflops / pk["fp32_tflops"], 4)},
+        "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_ms"] * 1e3, 2),
+                        "share": round(v["total_ms"] / sum(x["total_ms"] for x in ksum.values()), 4)}
+                    for k, v in sorted(ksum.items(), key=lambda kv: -kv[1]["total_ms"])},
+        "gpu_launches": launches,
+        "e2e": {"value": round(world * wl.pairs * args.steps / e2e_s / 1e9, 4), "unit": "Gpairs/s",
+                "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h},
+        "clocks": clocks.result(),
+    }
+    return line
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash()
+    for l in open(path):
+        parts = l.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[2] == f"src={cur}":
+            return float(parts[1])
+    return None
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lazy_score_matrix_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+
+
+def oracle_infonce(rows: int, threads: int = 0):
+    """Oracle forward + backward of the InfoNCE workload on its first `rows` rows against all columns.
+    Returns (seconds, pairs, threads used)."""
+    from lazy_score_matrix_gb300 import synth
+    from oracle import oracle
+    w = synth.workload(2)
+    z = w["z"].double().numpy()
+    N = z.shape[0]
+    oracle.set_threads(threads)
+    used = oracle.get_threads()
+    # rows 0..rows-1 against every column: column i is row i's own point, so exclude_self drops (i, i)
+    pb = oracle.Problem(z[:rows], z, metric="linear", scale=w["scale"])
+    t0 = time.perf_counter()
+    lse = oracle.logsumexp(pb, exclude_self=True)
+    oracle.logsumexp_backward(pb, lse, np.full(rows, -1.0 / N), exclude_self=True)
+    dt = time.perf_counter() - t0
+    return dt, rows * N, used
+
+
+def cpu_baseline(sample_rows=8192):
+    dt, pairs, used = oracle_infonce(sample_rows)
+    return {"value": round(pairs / dt / 1e9, 6), "unit": "Gpairs/s", "cores": used, "kind": "oracle",
+            "sample": f"oracle fwd+bwd on all {pairs} pairs of the 8192x8192 InfoNCE workload "
+                      f"({sample_rows} rows), {dt:.1f} s"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    rows = 2048 if args.workload == 2 else 0
+    times = []
+    for _ in range(args.warmup):
+        oracle_infonce(256)
+    used = 0
+    for _ in range(args.steps):
+        dt, pairs, used = oracle_infonce(rows)
+        times.append(dt)
+    tot = sum(times)
+    value = pairs * args.steps / tot / 1e9
+    return {"metric": METRIC, "value": round(value, 6), "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": "infonce_logsumexp_f32_z8192x64_fwd+bwd", "N": 8192, "M": 8192, "D": 64,
+                       "sample_rows_per_step": rows},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "Gpairs/s", "cores": used, "kind": "oracle",
+                             "sample": f"{rows} of 8192 rows against all 8192 columns per step"},
+            "e2e": {"value": round(value, 6), "unit": "Gpairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="libtp", choices=["libtp", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    line = gpu_arm(args, rank, world)
+    if line is not None:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline()
+        elif not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline() if rank == 0 else None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

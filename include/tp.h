@@ -210,6 +210,15 @@ TP_API const char* tp_last_error(void);
  * launch counting; reset = 1 zeroes it and returns the previous value). */
 TP_API int64_t tp_launch_count(int reset);
 
+/* Instrumentation hook. When set, hook(kernel, phase, stream, user) is called on the host, on the
+ * launching thread, immediately before (phase 0) and after (phase 1) every kernel launch this library
+ * makes; `kernel` is a static name such as "bwd_sweep_lse_row" and `stream` the launch stream.
+ * A profiler can record CUDA events there to time each kernel inside a real call sequence.
+ * NULL removes the hook. Not thread-safe with respect to concurrent launches: set it while no other
+ * thread is calling into libtp. */
+typedef void (*tp_launch_hook)(const char* kernel, int phase, void* stream, void* user);
+TP_API void tp_set_launch_hook(tp_launch_hook hook, void* user);
+
 #ifdef __cplusplus
 }
 #endif

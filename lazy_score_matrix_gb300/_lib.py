@@ -54,7 +54,10 @@ SIGNATURES = {
     "tp_status_string": ([_INT], ctypes.c_char_p),
     "tp_last_error": ([], ctypes.c_char_p),
     "tp_launch_count": ([_INT], _I64),
+    "tp_set_launch_hook": ([_P, _P], None),
 }
+
+LAUNCH_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_char_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p)
 
 _lock = threading.Lock()
 _lib = None

@@ -22,6 +22,8 @@ namespace {
 
 thread_local std::string g_err;
 thread_local int64_t g_launches = 0;
+tp_launch_hook g_hook = nullptr;
+void* g_hook_user = nullptr;
 
 tp_status fail(tp_status s, const std::string& msg) {
     g_err = msg;
@@ -430,6 +432,12 @@ int run_backward(const SweepArgs& row, const SweepArgs& col, const Grads& g, cud
 
 }  // namespace
 
+namespace tp {
+void launch_hook(const char* kernel, int phase, cudaStream_t s) {
+    if (g_hook) g_hook(kernel, phase, static_cast<void*>(s), g_hook_user);
+}
+}  // namespace tp
+
 // ================================================================================================
 // C ABI
 // ================================================================================================
@@ -449,6 +457,11 @@ const char* tp_status_string(tp_status s) {
 }
 
 const char* tp_last_error(void) { return g_err.c_str(); }
+
+void tp_set_launch_hook(tp_launch_hook hook, void* user) {
+    g_hook = hook;
+    g_hook_user = user;
+}
 
 int64_t tp_launch_count(int reset) {
     const int64_t v = g_launches;
@@ -712,8 +725,11 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return by_dtype(pr->dtype, [&](auto t) {
         using T = decltype(t);
-        softmax_delta_kernel<T><<<(unsigned)cdiv(pr->N, 256), 256, 0, st>>>(
-            static_cast<const T*>(grad_out), static_cast<const T*>(out), pr->N, (int)C, static_cast<T*>(delta));
+        {
+            HookScope h("softmax_delta", st);
+            softmax_delta_kernel<T><<<(unsigned)cdiv(pr->N, 256), 256, 0, st>>>(
+                static_cast<const T*>(grad_out), static_cast<const T*>(out), pr->N, (int)C, static_cast<T*>(delta));
+        }
         return launched(1 + run_backward<T, kBSoftmax>(row, col, g, st));
     });
 }

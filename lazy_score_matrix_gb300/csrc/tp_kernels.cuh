@@ -819,6 +819,21 @@ __global__ void __launch_bounds__(kThreads) topk_bwd_cols(const SweepArgs a, con
 // launchers (explicitly instantiated in the inst_*.cu translation units)
 // ------------------------------------------------------------------------------------------------
 
+constexpr const char* kFwdNames[] = {"fwd_sweep_matmul", "fwd_sweep_softmax", "fwd_sweep_lse", "fwd_sweep_disp",
+                                     "fwd_sweep_svgd"};
+constexpr const char* kFwdMergeNames[] = {"fwd_merge_matmul", "fwd_merge_softmax", "fwd_merge_lse", "fwd_merge_disp",
+                                          "fwd_merge_svgd"};
+// [mode][side][0 = gradients (and dV when fused), 1 = dV only]
+constexpr const char* kBwdNames[4][2][2] = {
+    {{"bwd_sweep_matmul_row", "bwd_sweep_matmul_row"}, {"bwd_sweep_matmul_col", "bwd_sweep_matmul_col_dv"}},
+    {{"bwd_sweep_softmax_row", "bwd_sweep_softmax_row"}, {"bwd_sweep_softmax_col", "bwd_sweep_softmax_col_dv"}},
+    {{"bwd_sweep_lse_row", "bwd_sweep_lse_row"}, {"bwd_sweep_lse_col", "bwd_sweep_lse_col"}},
+    {{"bwd_sweep_disp_row", "bwd_sweep_disp_row"}, {"bwd_sweep_disp_col", "bwd_sweep_disp_col"}}};
+constexpr const char* kBwdMergeNames[4][2] = {{"bwd_merge_matmul_row", "bwd_merge_matmul_col"},
+                                              {"bwd_merge_softmax_row", "bwd_merge_softmax_col"},
+                                              {"bwd_merge_lse_row", "bwd_merge_lse_col"},
+                                              {"bwd_merge_disp_row", "bwd_merge_disp_col"}};
+
 inline dim3 sweep_grid(const SweepArgs& a) {
     return dim3((unsigned)((a.nP + kThreads - 1) / kThreads), (unsigned)a.splits, 1);
 }
@@ -826,26 +841,32 @@ inline dim3 row_grid(int64_t n) { return dim3((unsigned)((n + kThreads - 1) / kT
 
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 void launch_fwd(const SweepArgs& a, cudaStream_t s) {
+    HookScope h(kFwdNames[MODE], s);
     fwd_sweep<T, DP, CP, MODE, AFFINE><<<sweep_grid(a), kThreads, 0, s>>>(a);
 }
 template <class T, int MODE>
 void launch_fwd_merge(const SweepArgs& a, cudaStream_t s) {
+    HookScope h(kFwdMergeNames[MODE], s);
     fwd_merge<T, MODE><<<row_grid(a.nP), kThreads, 0, s>>>(a);
 }
 template <class T, int DP, int K, bool AFFINE>
 void launch_topk(const SweepArgs& a, cudaStream_t s) {
+    HookScope h("topk_sweep", s);
     topk_sweep<T, DP, K, AFFINE><<<sweep_grid(a), kThreads, 0, s>>>(a);
 }
 template <class T, int K>
 void launch_topk_merge(const SweepArgs& a, cudaStream_t s) {
+    HookScope h("topk_merge", s);
     topk_merge<T, K><<<row_grid(a.nP), kThreads, 0, s>>>(a);
 }
 template <class T, int DP, int CP, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd(const SweepArgs& a, cudaStream_t s) {
+    HookScope h(kBwdNames[MODE][SIDE][DO_G ? 0 : 1], s);
     bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V><<<sweep_grid(a), kThreads, 0, s>>>(a);
 }
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd_merge(const SweepArgs& a, cudaStream_t s) {
+    HookScope h(kBwdMergeNames[MODE][SIDE], s);
     bwd_merge<T, MODE, SIDE, DO_G, DO_V><<<row_grid(a.nP), kThreads, 0, s>>>(a);
 }
 // rows: P = X, Q = Y; cols: P = Y, Q = X (parameters swapped). count/start/cursor/bucket come from
@@ -854,13 +875,26 @@ template <class T>
 void launch_topk_bwd(const SweepArgs& rows, const SweepArgs& cols, const int64_t* idx, const void* gv, int* count,
                      int* start, int* cursor, int* bucket, cudaStream_t s) {
     const T* g = static_cast<const T*>(gv);
-    if (rows.gP || rows.gPb || rows.gPw) topk_bwd_rows<T><<<row_grid(rows.nP), kThreads, 0, s>>>(rows, idx, g);
+    if (rows.gP || rows.gPb || rows.gPw) {
+        HookScope h("topk_bwd_rows", s);
+        topk_bwd_rows<T><<<row_grid(rows.nP), kThreads, 0, s>>>(rows, idx, g);
+    }
     if (cols.gP || cols.gPb || cols.gPw) {
         const int64_t n = rows.nP * (int64_t)rows.k;
         const unsigned nb = (unsigned)((n + 255) / 256);
-        topk_bwd_count<<<nb, 256, 0, s>>>(idx, n, cols.nP, count);
-        topk_bwd_scan<<<1, 1024, 0, s>>>(count, cols.nP, start, cursor);
-        topk_bwd_fill<<<nb, 256, 0, s>>>(idx, n, cols.nP, cursor, bucket);
+        {
+            HookScope h("topk_bwd_count", s);
+            topk_bwd_count<<<nb, 256, 0, s>>>(idx, n, cols.nP, count);
+        }
+        {
+            HookScope h("topk_bwd_scan", s);
+            topk_bwd_scan<<<1, 1024, 0, s>>>(count, cols.nP, start, cursor);
+        }
+        {
+            HookScope h("topk_bwd_fill", s);
+            topk_bwd_fill<<<nb, 256, 0, s>>>(idx, n, cols.nP, cursor, bucket);
+        }
+        HookScope h("topk_bwd_cols", s);
         topk_bwd_cols<T><<<row_grid(cols.nP), kThreads, 0, s>>>(cols, start, bucket, g);
     }
 }

@@ -9,6 +9,15 @@
 
 namespace tp {
 
+// Calls the user's launch hook (tp_set_launch_hook), if any, around every launch.
+void launch_hook(const char* kernel, int phase, cudaStream_t s);
+struct HookScope {
+    const char* name;
+    cudaStream_t s;
+    HookScope(const char* n, cudaStream_t st) : name(n), s(st) { launch_hook(name, 0, s); }
+    ~HookScope() { launch_hook(name, 1, s); }
+};
+
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 void launch_fwd(const SweepArgs& a, cudaStream_t s);
 template <class T, int MODE>

@@ -166,8 +166,9 @@ def displacement(pb: Problem):
     return out
 
 
-def svgd_direction(x, score, gamma):
-    pb = Problem(x, x, metric="rbf", gamma=gamma)
+def svgd_direction(x, score, gamma, y=None):
+    """phi for the particles x (rows) against the particles y (default x), score given at y."""
+    pb = Problem(x, x if y is None else y, metric="rbf", gamma=gamma)
     sc = _f64(score)
     out = np.zeros((pb.N, pb.D))
     _check(_load().or_svgd_direction(ctypes.byref(pb.pairs), float(gamma), _ptr(sc), _ptr(out)),

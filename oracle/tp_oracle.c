@@ -249,7 +249,7 @@ static void lse_row(void *c_, int64_t i) {
 }
 
 int or_logsumexp(const or_pairs *p, const or_score *s, int exclude_self, double *lse) {
-    if (exclude_self && p->N != p->M) return 1;
+    if (exclude_self && p->N > p->M) return 1; /* pair (i, i) must exist for every row */
     or_ctx c = {0};
     c.p = p; c.s = s; c.out = lse; c.exclude_self = exclude_self;
     or_parallel_for(p->N, lse_row, &c);
@@ -493,7 +493,7 @@ int or_matmul_backward(const or_pairs *p, const or_score *s, const double *V, in
 int or_logsumexp_backward(const or_pairs *p, const or_score *s, int exclude_self,
                           const double *lse, const double *grad_lse, double *dX, double *dY,
                           double *dbr, double *dbc, double *dwr, double *dwc) {
-    if (exclude_self && p->N != p->M) return 1;
+    if (exclude_self && p->N > p->M) return 1; /* pair (i, i) must exist for every row */
     or_bwd b;
     memset(&b, 0, sizeof b);
     b.p = p; b.s = s; b.kind = OR_K_LSE; b.exclude_self = exclude_self; b.lse = lse;
