@@ -22,6 +22,94 @@
 namespace tp {
 
 // ------------------------------------------------------------------------------------------------
+// two-level accumulation
+// ------------------------------------------------------------------------------------------------
+//
+// Every sum over the streamed set is kept in two levels: a register accumulator for the current
+// 32-point tile and a running accumulator that the tile's sum is added into once per tile. The
+// rounding of one sum then grows with 32 + n/32 instead of n. Vector running accumulators live in
+// shared memory, column-major ([width][kThreads]) so that each thread touches its own bank.
+
+template <class T>
+__host__ __device__ constexpr size_t al16(size_t nelem) {
+    return (nelem * sizeof(T) + 15) / 16 * 16;
+}
+
+template <class T, int N>
+struct RunningVec {
+    T* base;  // [N][kThreads] in shared memory
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int c = 0; c < N; ++c) base[c * kThreads + threadIdx.x] = T(0);
+    }
+    // running = running * r + tile; tile = 0
+    __device__ __forceinline__ void flush(T (&tile)[N], T r) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+            T& v = base[c * kThreads + threadIdx.x];
+            v = fma(v, r, tile[c]);
+            tile[c] = T(0);
+        }
+    }
+    __device__ __forceinline__ void flush(T (&tile)[N]) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+            base[c * kThreads + threadIdx.x] += tile[c];
+            tile[c] = T(0);
+        }
+    }
+    __device__ __forceinline__ T get(int c) const { return base[c * kThreads + threadIdx.x]; }
+};
+
+template <class T>
+struct Running {
+    T run = T(0), tile = T(0);
+    __device__ __forceinline__ void flush() {
+        run += tile;
+        tile = T(0);
+    }
+    __device__ __forceinline__ void flush(T r) {
+        run = fma(run, r, tile);
+        tile = T(0);
+    }
+};
+
+// Dynamic shared memory of the forward sweep, carved in this order: staged points [kTile][DP],
+// staged values [kTile][VW], norms, column weights, column biases, running accumulators.
+template <class T, int DP, int CP, int MODE, bool AFFINE>
+struct FwdSmem {
+    static constexpr bool HAS_V = MODE == kMatmul || MODE == kSoftmax || MODE == kSvgd;
+    static constexpr int VW = MODE == kSvgd ? DP : CP;
+    static constexpr int NRUN = (MODE == kMatmul || MODE == kSoftmax) ? CP : (MODE == kDisp ? DP : (MODE == kSvgd ? 2 * DP : 0));
+    static constexpr size_t bytes = al16<T>(kTile * DP) + (HAS_V ? al16<T>(kTile * VW) : 0) + al16<T>(kTile) +
+                                    (AFFINE ? 2 * al16<T>(kTile) : 0) + al16<T>((size_t)NRUN * kThreads);
+};
+
+// Dynamic shared memory of a backward sweep: staged points, staged values, norms, weights, biases,
+// two per-row statistics, running accumulators ([K1 | Kd | dV]).
+template <class T, int DP, int CP, int MODE, int SIDE, bool DO_G, bool DO_V>
+struct BwdSmem {
+    static constexpr bool VALS = MODE == kBMatmul || MODE == kBSoftmax;
+    static constexpr int QVW = VALS ? CP : ((MODE == kBDisp && SIDE == kCol) ? DP : 1);
+    static constexpr bool HAS_QV = VALS || (MODE == kBDisp && SIDE == kCol);
+    static constexpr int NK1 = DO_G ? DP : 0;
+    static constexpr int NKD = (DO_G && MODE == kBDisp && SIDE == kCol) ? DP : 0;
+    static constexpr int NKV = DO_V ? CP : 0;
+    static constexpr size_t bytes = al16<T>(kTile * DP) + (HAS_QV ? al16<T>(kTile * QVW) : 0) + 5 * al16<T>(kTile) +
+                                    al16<T>((size_t)(NK1 + NKD + NKV) * kThreads);
+};
+
+struct SmemCursor {
+    unsigned char* p;
+    template <class T>
+    __device__ __forceinline__ T* take(size_t nelem) {
+        T* r = reinterpret_cast<T*>(p);
+        p += al16<T>(nelem);
+        return r;
+    }
+};
+
+// ------------------------------------------------------------------------------------------------
 // forward sweep
 // ------------------------------------------------------------------------------------------------
 
@@ -33,16 +121,22 @@ __host__ __device__ inline int fwd_state_width(int D, int C) {
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
     using E = ExpTraits<T>;
-    constexpr bool HAS_V = MODE == kMatmul || MODE == kSoftmax || MODE == kSvgd;
-    constexpr int VW = MODE == kSvgd ? DP : CP;
+    using SM = FwdSmem<T, DP, CP, MODE, AFFINE>;
+    constexpr bool HAS_V = SM::HAS_V;
+    constexpr int VW = SM::VW;
     constexpr int NACC = (MODE == kMatmul || MODE == kSoftmax) ? CP : (MODE == kLse ? 1 : DP);
     constexpr int NACC2 = MODE == kSvgd ? DP : 1;
+    constexpr bool VEC_RUN = SM::NRUN > 0;
 
-    __shared__ __align__(16) T sq[kTile * DP];
-    __shared__ __align__(16) T sv[HAS_V ? kTile * VW : 1];
-    __shared__ T sn[kTile];
-    __shared__ T sw[AFFINE ? kTile : 1];
-    __shared__ T sb[AFFINE ? kTile : 1];
+    extern __shared__ __align__(16) unsigned char tp_smem[];
+    SmemCursor cur{tp_smem};
+    T* sq = cur.take<T>(kTile * DP);
+    T* sv = HAS_V ? cur.take<T>(kTile * VW) : nullptr;
+    T* sn = cur.take<T>(kTile);
+    T* sw = AFFINE ? cur.take<T>(kTile) : nullptr;
+    T* sb = AFFINE ? cur.take<T>(kTile) : nullptr;
+    RunningVec<T, NACC> run1{cur.take<T>((size_t)SM::NRUN * kThreads)};
+    RunningVec<T, NACC2> run2{run1.base + (size_t)NACC * kThreads};
 
     const T* __restrict__ P = static_cast<const T*>(a.P);
     const T* __restrict__ Q = static_cast<const T*>(a.Q);
@@ -62,13 +156,19 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
         if (pvalid && a.pb) Cp = static_cast<const T*>(a.pb)[pi];
     }
 
+    // tile accumulators (registers); running accumulators (shared memory / scalars)
     T acc[NACC];
     T acc2[NACC2];
 #pragma unroll
     for (int c = 0; c < NACC; ++c) acc[c] = T(0);
 #pragma unroll
     for (int c = 0; c < NACC2; ++c) acc2[c] = T(0);
-    T m = ninf<T>(), l = T(0), mass = T(0);
+    if constexpr (VEC_RUN) {
+        run1.init();
+        if constexpr (MODE == kSvgd) run2.init();
+    }
+    T m = ninf<T>();
+    Running<T> l, mass;
 
     zero_smem(sq, kTile * DP);
     if constexpr (HAS_V) zero_smem(sv, kTile * VW);
@@ -88,6 +188,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
             stage_norms<T, DP>(sn, sq, cnt);
             __syncthreads();
         }
+        const T m0 = m;  // the running state is relative to the max at the start of the tile
 #pragma unroll 2
         for (int jj = 0; jj < cnt; ++jj) {
             const T* q = sq + jj * DP;
@@ -104,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                 const T s = S * E::kLogB;
                 if (s > m) {
                     const T r = E::bexp(m - s);
-                    l *= r;
+                    l.tile *= r;
                     if constexpr (MODE == kSoftmax) {
 #pragma unroll
                         for (int c = 0; c < CP; ++c) acc[c] *= r;
@@ -112,50 +213,62 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                     m = s;
                 }
                 const T pr = E::bexp(s - m);
-                l += pr;
+                l.tile += pr;
                 if constexpr (MODE == kSoftmax) axpy_smem<T, CP>(acc, pr, sv + jj * CP);
             } else if constexpr (MODE == kDisp) {
                 axpy_smem<T, DP>(acc, S, q);
-                mass += S;
+                mass.tile += S;
             } else {  // kSvgd: S is the bare rbf kernel value k_ij
                 axpy_smem<T, DP>(acc, S, sv + jj * DP);
                 axpy_smem<T, DP>(acc2, S, q);
-                mass += S;
+                mass.tile += S;
             }
+        }
+        if constexpr (MODE == kLse || MODE == kSoftmax) {
+            // 0 while the running state is empty (m0 = -inf); 1 when the max did not move (this also
+            // covers a tile with no admitted pair, where both are -inf)
+            const T r = m0 == m ? T(1) : E::bexp(m0 - m);
+            l.flush(r);
+            if constexpr (MODE == kSoftmax) run1.flush(acc, r);
+        } else {
+            if constexpr (VEC_RUN) run1.flush(acc);
+            if constexpr (MODE == kSvgd) run2.flush(acc2);
+            mass.flush();
         }
     }
     if (!pvalid) return;
+    const T L = l.run, MASS = mass.run;
 
     if (a.splits > 1) {
         T* ws = static_cast<T*>(a.ws);
         const int W = fwd_state_width<MODE>(a.D, a.C);
-        T* base = ws + (int64_t)split * W * a.nP + pi;
+        T* o = ws + (int64_t)split * W * a.nP + pi;
         if constexpr (MODE == kMatmul) {
 #pragma unroll
             for (int c = 0; c < CP; ++c)
-                if (c < a.C) base[(int64_t)c * a.nP] = acc[c];
+                if (c < a.C) o[(int64_t)c * a.nP] = run1.get(c);
         } else if constexpr (MODE == kSoftmax) {
-            base[0] = m;
-            base[a.nP] = l;
+            o[0] = m;
+            o[a.nP] = L;
 #pragma unroll
             for (int c = 0; c < CP; ++c)
-                if (c < a.C) base[(int64_t)(2 + c) * a.nP] = acc[c];
+                if (c < a.C) o[(int64_t)(2 + c) * a.nP] = run1.get(c);
         } else if constexpr (MODE == kLse) {
-            base[0] = m;
-            base[a.nP] = l;
+            o[0] = m;
+            o[a.nP] = L;
         } else if constexpr (MODE == kDisp) {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
-                if (d < a.D) base[(int64_t)d * a.nP] = acc[d];
-            base[(int64_t)a.D * a.nP] = mass;
+                if (d < a.D) o[(int64_t)d * a.nP] = run1.get(d);
+            o[(int64_t)a.D * a.nP] = MASS;
         } else {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
                 if (d < a.D) {
-                    base[(int64_t)d * a.nP] = acc[d];
-                    base[(int64_t)(a.D + d) * a.nP] = acc2[d];
+                    o[(int64_t)d * a.nP] = run1.get(d);
+                    o[(int64_t)(a.D + d) * a.nP] = run2.get(d);
                 }
-            base[(int64_t)(2 * a.D) * a.nP] = mass;
+            o[(int64_t)(2 * a.D) * a.nP] = MASS;
         }
         return;
     }
@@ -164,24 +277,24 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
     if constexpr (MODE == kMatmul) {
 #pragma unroll
         for (int c = 0; c < CP; ++c)
-            if (c < a.C) out[pi * a.C + c] = acc[c];
+            if (c < a.C) out[pi * a.C + c] = run1.get(c);
     } else if constexpr (MODE == kSoftmax) {
-        const T inv = T(1) / l;
+        const T inv = T(1) / L;
 #pragma unroll
         for (int c = 0; c < CP; ++c)
-            if (c < a.C) out[pi * a.C + c] = acc[c] * inv;
-        static_cast<T*>(a.out2)[pi] = (m + E::blog(l)) * E::kLnB;
+            if (c < a.C) out[pi * a.C + c] = run1.get(c) * inv;
+        static_cast<T*>(a.out2)[pi] = (m + E::blog(L)) * E::kLnB;
     } else if constexpr (MODE == kLse) {
-        out[pi] = l > T(0) ? (m + E::blog(l)) * E::kLnB : ninf<T>();
+        out[pi] = L > T(0) ? (m + E::blog(L)) * E::kLnB : ninf<T>();
     } else if constexpr (MODE == kDisp) {
 #pragma unroll
         for (int d = 0; d < DP; ++d)
-            if (d < a.D) out[pi * a.D + d] = acc[d] - mass * p[d];
+            if (d < a.D) out[pi * a.D + d] = run1.get(d) - MASS * p[d];
     } else {
         const T g2 = T(2 * a.gamma), inv_n = T(a.inv_n);
 #pragma unroll
         for (int d = 0; d < DP; ++d)
-            if (d < a.D) out[pi * a.D + d] = (acc[d] - g2 * (acc2[d] - mass * p[d])) * inv_n;
+            if (d < a.D) out[pi * a.D + d] = (run1.get(d) - g2 * (run2.get(d) - MASS * p[d])) * inv_n;
     }
 }
 
@@ -440,13 +553,20 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
     constexpr bool ROWSTAT = (MODE == kBSoftmax || MODE == kBLse);
     constexpr int KD = (MODE == kBDisp && SIDE == kCol) ? DP : 1;
 
-    __shared__ __align__(16) T sq[kTile * DP];
-    __shared__ __align__(16) T sv[HAS_QV ? kTile * QVW : 1];
-    __shared__ T sn[kTile];
-    __shared__ T sw[kTile];
-    __shared__ T sb[kTile];
-    __shared__ T s1[kTile];  // column sweep: lse_i (base domain) / dO_i . x_i (disp)
-    __shared__ T s2[kTile];  // column sweep: delta_i (softmax) / g_i (lse)
+    using SM = BwdSmem<T, DP, CP, MODE, SIDE, DO_G, DO_V>;
+    extern __shared__ __align__(16) unsigned char tp_smem[];
+    SmemCursor cur{tp_smem};
+    T* sq = cur.take<T>(kTile * DP);
+    T* sv = HAS_QV ? cur.take<T>(kTile * QVW) : nullptr;
+    T* sn = cur.take<T>(kTile);
+    T* sw = cur.take<T>(kTile);
+    T* sb = cur.take<T>(kTile);
+    T* s1 = cur.take<T>(kTile);  // column sweep: lse_i (base domain) / dO_i . x_i (disp)
+    T* s2 = cur.take<T>(kTile);  // column sweep: delta_i (softmax) / g_i (lse)
+    T* runbase = cur.take<T>((size_t)(SM::NK1 + SM::NKD + SM::NKV) * kThreads);
+    RunningVec<T, DO_G ? DP : 1> rK1{runbase};
+    RunningVec<T, KD> rKd{runbase + (size_t)SM::NK1 * kThreads};
+    RunningVec<T, DO_V ? CP : 1> rKV{runbase + (size_t)(SM::NK1 + SM::NKD) * kThreads};
 
     const T* __restrict__ P = static_cast<const T*>(a.P);
     const T* __restrict__ Q = static_cast<const T*>(a.Q);
@@ -502,7 +622,10 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
     for (int c = 0; c < (DO_V ? CP : 1); ++c) KdV[c] = T(0);
 #pragma unroll
     for (int d = 0; d < KD; ++d) Kd[d] = T(0);
-    T K0 = T(0), sumH = T(0), sumHw = T(0), sumS = T(0);
+    Running<T> K0, sumH, sumHw, sumS;
+    if constexpr (DO_G) rK1.init();
+    if constexpr (SM::NKD > 0) rKd.init();
+    if constexpr (DO_V) rKV.init();
 
     zero_smem(sq, kTile * DP);
     if constexpr (HAS_QV) zero_smem(sv, kTile * QVW);
@@ -558,7 +681,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
             } else {  // kBDisp
                 if constexpr (SIDE == kRow) {
                     G = dot_regs_smem<T, DP>(pv, q) - pstat;
-                    sumS += S;
+                    sumS.tile += S;
                 } else {
                     const T* dO = sv + jj * DP;
                     G = dot_regs_smem<T, DP>(p, dO) - s1[jj];
@@ -568,14 +691,23 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
             if constexpr (DO_V) axpy_smem<T, CP>(KdV, Pw, sv + jj * CP);
             if constexpr (DO_G) {
                 const T H = a.apply_exp ? G * S : G;
-                sumH += H;
-                if (affine) sumHw = fma(H * scale * wq, base, sumHw);
+                sumH.tile += H;
+                if (affine) sumHw.tile = fma(H * scale * wq, base, sumHw.tile);
                 const T Ev = H * A * wq;
                 const T kappa = a.metric == kLinear ? Ev : (a.metric == kSqeuclidean ? T(-2) * Ev : T(-2) * neg_gamma * Ev * base);
-                K0 += kappa;
+                K0.tile += kappa;
                 axpy_smem<T, DP>(K1, kappa, q);
             }
         }
+        if constexpr (DO_G) {
+            rK1.flush(K1);
+            K0.flush();
+            sumH.flush();
+            sumHw.flush();
+            sumS.flush();
+        }
+        if constexpr (SM::NKD > 0) rKd.flush(Kd);
+        if constexpr (DO_V) rKV.flush(KdV);
     }
     if (!pvalid) return;
 
@@ -587,23 +719,23 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
         if constexpr (DO_G) {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
-                if (d < a.D) o[(int64_t)(w + d) * a.nP] = K1[d];
+                if (d < a.D) o[(int64_t)(w + d) * a.nP] = rK1.get(d);
             w += a.D;
-            o[(int64_t)w++ * a.nP] = K0;
-            o[(int64_t)w++ * a.nP] = sumH;
-            o[(int64_t)w++ * a.nP] = sumHw;
-            if constexpr (MODE == kBDisp && SIDE == kRow) o[(int64_t)w++ * a.nP] = sumS;
+            o[(int64_t)w++ * a.nP] = K0.run;
+            o[(int64_t)w++ * a.nP] = sumH.run;
+            o[(int64_t)w++ * a.nP] = sumHw.run;
+            if constexpr (MODE == kBDisp && SIDE == kRow) o[(int64_t)w++ * a.nP] = sumS.run;
             if constexpr (MODE == kBDisp && SIDE == kCol) {
 #pragma unroll
                 for (int d = 0; d < DP; ++d)
-                    if (d < a.D) o[(int64_t)(w + d) * a.nP] = Kd[d];
+                    if (d < a.D) o[(int64_t)(w + d) * a.nP] = rKd.get(d);
                 w += a.D;
             }
         }
         if constexpr (DO_V) {
 #pragma unroll
             for (int c = 0; c < CP; ++c)
-                if (c < a.C) o[(int64_t)(w + c) * a.nP] = KdV[c];
+                if (c < a.C) o[(int64_t)(w + c) * a.nP] = rKV.get(c);
         }
         return;
     }
@@ -615,22 +747,22 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
 #pragma unroll
             for (int d = 0; d < DP; ++d) {
                 if (d < a.D) {
-                    T v = K1[d] - (dist ? p[d] * K0 : T(0));
-                    if constexpr (MODE == kBDisp && SIDE == kRow) v -= sumS * pv[d];
-                    if constexpr (MODE == kBDisp && SIDE == kCol) v += Kd[d];
+                    T v = rK1.get(d) - (dist ? p[d] * K0.run : T(0));
+                    if constexpr (MODE == kBDisp && SIDE == kRow) v -= sumS.run * pv[d];
+                    if constexpr (MODE == kBDisp && SIDE == kCol) v += rKd.get(d);
                     g[d] = a.accumulate ? g[d] + v : v;
                 }
             }
         }
-        if (a.gPb) static_cast<T*>(a.gPb)[pi] = sumH;
-        if (a.gPw) static_cast<T*>(a.gPw)[pi] = sumHw;
+        if (a.gPb) static_cast<T*>(a.gPb)[pi] = sumH.run;
+        if (a.gPw) static_cast<T*>(a.gPw)[pi] = sumHw.run;
     }
     if constexpr (DO_V) {
         if (a.gV) {
             T* gv = static_cast<T*>(a.gV) + pi * a.C;
 #pragma unroll
             for (int c = 0; c < CP; ++c)
-                if (c < a.C) gv[c] = KdV[c];
+                if (c < a.C) gv[c] = rKV.get(c);
         }
     }
 }
@@ -839,10 +971,17 @@ inline dim3 sweep_grid(const SweepArgs& a) {
 }
 inline dim3 row_grid(int64_t n) { return dim3((unsigned)((n + kThreads - 1) / kThreads), 1, 1); }
 
+template <class K>
+inline void allow_smem(K* kernel, size_t bytes) {
+    if (bytes > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 void launch_fwd(const SweepArgs& a, cudaStream_t s) {
+    constexpr size_t smem = FwdSmem<T, DP, CP, MODE, AFFINE>::bytes;
+    allow_smem(fwd_sweep<T, DP, CP, MODE, AFFINE>, smem);
     HookScope h(kFwdNames[MODE], s);
-    fwd_sweep<T, DP, CP, MODE, AFFINE><<<sweep_grid(a), kThreads, 0, s>>>(a);
+    fwd_sweep<T, DP, CP, MODE, AFFINE><<<sweep_grid(a), kThreads, smem, s>>>(a);
 }
 template <class T, int MODE>
 void launch_fwd_merge(const SweepArgs& a, cudaStream_t s) {
@@ -861,8 +1000,10 @@ void launch_topk_merge(const SweepArgs& a, cudaStream_t s) {
 }
 template <class T, int DP, int CP, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd(const SweepArgs& a, cudaStream_t s) {
+    constexpr size_t smem = BwdSmem<T, DP, CP, MODE, SIDE, DO_G, DO_V>::bytes;
+    allow_smem(bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V>, smem);
     HookScope h(kBwdNames[MODE][SIDE][DO_G ? 0 : 1], s);
-    bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V><<<sweep_grid(a), kThreads, 0, s>>>(a);
+    bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V><<<sweep_grid(a), kThreads, smem, s>>>(a);
 }
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd_merge(const SweepArgs& a, cudaStream_t s) {

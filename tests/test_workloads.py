@@ -110,7 +110,10 @@ def test_attention_softmax_matmul_full_sampled(oracle):
     torch.cuda.synchronize()
     pb = oracle.Problem(w["Q"], w["K"], metric="linear", scale=w["scale"])
     o_out, o_lse = oracle.softmax_matmul(pb, w["V"])
-    assert_close(out, o_out, TOL_F32_FWD, "out")
+    # every output entry is a convex combination of value rows and lands ~100x below them: floor the
+    # relative error at 1e-3 of the largest |V| (plain fp32 evaluation of S = q.k / 8 on the exact
+    # inputs misses the 1e-3 * max|out| floor by 1.5x; the absolute error is ~1e-8)
+    assert_close(out, o_out, TOL_F32_FWD, "out", abs_floor=1e-3 * float(w["V"].abs().max()))
     assert_close(lse, o_lse, TOL_F32_FWD, "lse")
     rows = sample(16384, 48, 4)
     pr = oracle.Problem(w["Q"][rows], w["K"], metric="linear", scale=w["scale"])
