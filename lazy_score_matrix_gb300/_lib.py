@@ -40,6 +40,7 @@ _SCORE = ctypes.POINTER(tp_score)
 SIGNATURES = {
     "tp_pairwise_matmul": ([_PAIRS, _SCORE, _P, _I64, _P, _P, _SZ, _P], _INT),
     "tp_pairwise_logsumexp": ([_PAIRS, _SCORE, _INT, _P, _P, _SZ, _P], _INT),
+    "tp_pairwise_logsumexp_noalloc": ([_PAIRS, _SCORE, _INT, _P, _P], _INT),
     "tp_pairwise_softmax_matmul": ([_PAIRS, _SCORE, _P, _I64, _P, _P, _P, _SZ, _P], _INT),
     "tp_pairwise_displacement": ([_PAIRS, _SCORE, _P, _P, _SZ, _P], _INT),
     "tp_svgd_direction": ([_PAIRS, ctypes.c_double, _P, _P, _P, _SZ, _P], _INT),

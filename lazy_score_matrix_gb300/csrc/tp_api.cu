@@ -433,6 +433,8 @@ int run_backward(const SweepArgs& row, const SweepArgs& col, const Grads& g, cud
 }  // namespace
 
 namespace tp {
+void set_last_error(const std::string& msg) { g_err = msg; }
+
 void launch_hook(const char* kernel, int phase, cudaStream_t s) {
     if (g_hook) g_hook(kernel, phase, static_cast<void*>(s), g_hook_user);
 }
