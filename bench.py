@@ -46,6 +46,8 @@ def peaks():
         "sm_max_mhz": sm_mhz,
         "fp32_tflops": SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12,
         "fp64_tflops": 1.25,  # nominal GB300 FP64 rate (no measured figure)
+        # tf32 tensor peak: the measured bf16 burst peak x the nominal tf32/bf16 ratio (1.1 / 2.25)
+        "tf32_tflops": float(p.get("bf16_tflops", 1900.0)) * 1.1 / 2.25,
         "source": "MEASURED_PEAKS.json" if p else "fallback",
     }
 
@@ -200,8 +202,12 @@ class InfoNCE(Workload):
         self.d2h = self.lse_h.numel() * 4 + self.grad_h.numel() * 4
         D2 = 2 * D
         # algorithmic flop per pair and launch (FMA = 2): forward 2D+3; backward 387 = (2D+3) + 2D + 2D,
-        # the row sweep credited with the recompute and dX, the column sweep with dY only
-        self.flops_per_pair = {"fwd_sweep_lse": D2 + 3, "bwd_sweep_lse_row": D2 + 3 + D2, "bwd_sweep_lse_col": D2}
+        # the row sweep credited with the recompute and dX, the column sweep with dY only; a kernel
+        # that produces the whole backward (X = Y, one symmetric sweep) is credited with all of it.
+        # (kernel: (flop per pair, bound)); "tensor" kernels run the contraction on tcgen05 (tf32)
+        self.flops_per_pair = {"fwd_sweep_lse": (D2 + 3, "alu"), "bwd_sweep_lse_row": (D2 + 3 + D2, "alu"),
+                               "bwd_sweep_lse_col": (D2, "alu"), "bwd_sweep_lse_sym": (D2 + 3 + D2 + D2, "alu"),
+                               "lse_fwd_tc": (D2 + 3, "tensor"), "lse_bwd_sym_tc": (D2 + 3 + D2 + D2, "tensor")}
         self.step_flops_per_pair = (D2 + 3) + (D2 + 3 + D2 + D2)
 
     def step(self):
@@ -219,7 +225,170 @@ class InfoNCE(Workload):
         self.grad_h.copy_(g["dX"], non_blocking=True)
 
 
-WORKLOADS = {2: InfoNCE}
+class RbfMatmul(Workload):
+    """Workload 1: rbf kernel product K @ [V | 1] fp32, X, Y [1024,3], fwd + grads in X, Y, V."""
+
+    def __init__(self, dev):
+        from lazy_score_matrix_gb300 import ops, synth
+        self.ops = ops
+        w = synth.workload(1)
+        self.N, self.D = w["X"].shape
+        self.M = w["Y"].shape[0]
+        self.C = w["V"].shape[1]
+        self.pairs = self.N * self.M
+        self.name = "rbf_kernel_matmul_f32_X1024x3_Y1024x3_V1024x4_fwd+bwd"
+        self.score = ops.Score("rbf", gamma=w["gamma"])
+        self.X, self.Y, self.V, self.G = (w[k].to(dev) for k in ("X", "Y", "V", "grad_out"))
+        self.host = {k: w[k].pin_memory() for k in ("X", "Y", "V", "grad_out")}
+        self.dev_in = {k: torch.empty_like(v) for k, v in ((k, getattr(self, kk)) for k, kk in
+                                                         (("X", "X"), ("Y", "Y"), ("V", "V"), ("grad_out", "G")))}
+        self.out_h = torch.empty(self.N, self.C).pin_memory()
+        self.h2d = sum(v.numel() * 4 for v in self.host.values())
+        self.d2h = self.out_h.numel() * 4 + (self.N + self.M) * self.D * 4 + self.M * self.C * 4
+        D, C = self.D, self.C
+        # fwd 2D+2 (distance) + 1 (scale) + 2C; bwd recompute 2D+3, dS 2C, dV 2C, coef 2, dX 2D+1, dY 2D+1
+        self.flops_per_pair = {"fwd_sweep_matmul": (2 * D + 3 + 2 * C, "alu"),
+                               "bwd_sweep_matmul_row": (2 * D + 3 + 2 * C + 2 + 2 * D + 1, "alu"),
+                               "bwd_sweep_matmul_col": (2 * C + 2 * D + 1, "alu")}
+        self.step_flops_per_pair = (2 * D + 3 + 2 * C) + (2 * D + 3 + 4 * C + 2 + 4 * D + 2)
+        self.grads_h = [torch.empty(self.N, D).pin_memory(), torch.empty(self.M, D).pin_memory(),
+                        torch.empty(self.M, C).pin_memory()]
+
+    def step(self):
+        out = self.ops.pairwise_matmul(self.X, self.Y, self.V, self.score)
+        g = self.ops.pairwise_matmul_backward(self.X, self.Y, self.V, self.score, self.G,
+                                              (True, True, True, False, False, False, False))
+        return out, g
+
+    def e2e_step(self):
+        for k, v in self.host.items():
+            self.dev_in[k].copy_(v, non_blocking=True)
+        d = self.dev_in
+        out = self.ops.pairwise_matmul(d["X"], d["Y"], d["V"], self.score)
+        g = self.ops.pairwise_matmul_backward(d["X"], d["Y"], d["V"], self.score, d["grad_out"],
+                                              (True, True, True, False, False, False, False))
+        self.out_h.copy_(out, non_blocking=True)
+        for h, k in zip(self.grads_h, ("dX", "dY", "dV")):
+            h.copy_(g[k], non_blocking=True)
+
+
+class Knn(Workload):
+    """Workload 3: exact k-NN top-16, X [65536,16] vs R [1048576,16] integers in [-8,8], fp32."""
+
+    def __init__(self, dev):
+        from lazy_score_matrix_gb300 import ops, synth
+        self.ops = ops
+        w = synth.workload(3)
+        self.N, self.D = w["X"].shape
+        self.M = w["R"].shape[0]
+        self.k = w["k"]
+        self.pairs = self.N * self.M
+        self.name = "knn_topk16_f32_X65536x16_R1048576x16_fwd"
+        self.score = ops.Score("sqeuclidean")
+        self.X, self.R = w["X"].to(dev), w["R"].to(dev)
+        self.X_h, self.R_h = w["X"].pin_memory(), w["R"].pin_memory()
+        self.X_d, self.R_d = torch.empty_like(self.X), torch.empty_like(self.R)
+        self.v_h = torch.empty(self.N, self.k).pin_memory()
+        self.i_h = torch.empty(self.N, self.k, dtype=torch.int64).pin_memory()
+        self.h2d = (self.X_h.numel() + self.R_h.numel()) * 4
+        self.d2h = self.N * self.k * 12
+        self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu")}
+        self.step_flops_per_pair = 2 * self.D + 2
+
+    def step(self):
+        return self.ops.pairwise_topk(self.X, self.R, self.score, self.k, False)
+
+    def e2e_step(self):
+        self.X_d.copy_(self.X_h, non_blocking=True)
+        self.R_d.copy_(self.R_h, non_blocking=True)
+        v, i = self.ops.pairwise_topk(self.X_d, self.R_d, self.score, self.k, False)
+        self.v_h.copy_(v, non_blocking=True)
+        self.i_h.copy_(i, non_blocking=True)
+
+
+class Attention(Workload):
+    """Workload 4: softmax_matmul attention fp32, Q, K, V [16384,64], scale 1/8, fwd + grads."""
+
+    def __init__(self, dev):
+        from lazy_score_matrix_gb300 import ops, synth
+        self.ops = ops
+        w = synth.workload(4)
+        self.N, self.D = w["Q"].shape
+        self.M = w["K"].shape[0]
+        self.C = w["V"].shape[1]
+        self.pairs = self.N * self.M
+        self.name = "attention_softmax_matmul_f32_QKV16384x64_fwd+bwd"
+        self.score = ops.Score("linear", scale=w["scale"])
+        self.Q, self.K, self.V, self.G = (w[k].to(dev) for k in ("Q", "K", "V", "grad_out"))
+        self.host = {k: w[k].pin_memory() for k in ("Q", "K", "V", "grad_out")}
+        self.dev_in = {k: torch.empty_like(v) for k, v in
+                       (("Q", self.Q), ("K", self.K), ("V", self.V), ("grad_out", self.G))}
+        self.out_h = torch.empty(self.N, self.C).pin_memory()
+        self.grads_h = [torch.empty(self.N, self.D).pin_memory(), torch.empty(self.M, self.D).pin_memory(),
+                        torch.empty(self.M, self.C).pin_memory()]
+        self.h2d = sum(v.numel() * 4 for v in self.host.values())
+        self.d2h = (self.N * self.C + (self.N + self.M) * self.D + self.M * self.C) * 4
+        D, C = self.D, self.C
+        # fwd 2D + 2C + 3; bwd: S 2D, dV 2C, dP 2C, dS 2, dQ 2D, dK 2D (dQ row sweep: S, dP, dS, dQ)
+        self.flops_per_pair = {"fwd_sweep_softmax": (2 * D + 2 * C + 3, "alu"),
+                               "bwd_sweep_softmax_row": (2 * D + 2 * C + 2 + 2 * D, "alu"),
+                               "bwd_sweep_softmax_col": (2 * D, "alu"),
+                               "bwd_sweep_softmax_col_dv": (2 * C, "alu")}
+        self.step_flops_per_pair = (2 * D + 2 * C + 3) + (2 * D + 2 * C + 2 * C + 2 + 2 * D + 2 * D)
+
+    def step(self):
+        out, lse = self.ops.pairwise_softmax_matmul(self.Q, self.K, self.V, self.score)
+        g = self.ops.pairwise_softmax_matmul_backward(self.Q, self.K, self.V, self.score, out, lse, self.G,
+                                                      (True, True, True, False, False, False, False))
+        return out, g
+
+    def e2e_step(self):
+        for k, v in self.host.items():
+            self.dev_in[k].copy_(v, non_blocking=True)
+        d = self.dev_in
+        out, lse = self.ops.pairwise_softmax_matmul(d["Q"], d["K"], d["V"], self.score)
+        g = self.ops.pairwise_softmax_matmul_backward(d["Q"], d["K"], d["V"], self.score, out, lse, d["grad_out"],
+                                                      (True, True, True, False, False, False, False))
+        self.out_h.copy_(out, non_blocking=True)
+        for h, k in zip(self.grads_h, ("dX", "dY", "dV")):
+            h.copy_(g[k], non_blocking=True)
+
+
+class Svgd(Workload):
+    """Workload 5: SVGD direction fp64, x [131072,8], score = -x, rbf gamma 0.1, one fused sweep."""
+    dtype = "f64"
+
+    def __init__(self, dev):
+        from lazy_score_matrix_gb300 import ops, synth
+        self.ops = ops
+        w = synth.workload(5)
+        self.N, self.D = w["x"].shape
+        self.M = self.N
+        self.gamma = w["gamma"]
+        self.pairs = self.N * self.N
+        self.name = "svgd_direction_f64_x131072x8_fwd"
+        self.x, self.sc = w["x"].to(dev), w["score"].to(dev)
+        self.x_h, self.s_h = w["x"].pin_memory(), w["score"].pin_memory()
+        self.x_d, self.s_d = torch.empty_like(self.x), torch.empty_like(self.sc)
+        self.phi_h = torch.empty(self.N, self.D, dtype=torch.float64).pin_memory()
+        self.h2d = 2 * self.N * self.D * 8
+        self.d2h = self.N * self.D * 8
+        D = self.D
+        # one sweep with V = [score | x | 1]: distance 2D+2, -gamma scale 1, accumulate 2(2D+1)
+        self.flops_per_pair = {"fwd_sweep_svgd": (2 * D + 3 + 2 * (2 * D + 1), "alu")}
+        self.step_flops_per_pair = 2 * D + 3 + 2 * (2 * D + 1)
+
+    def step(self):
+        return self.ops.svgd_direction(self.x, self.sc, self.gamma)
+
+    def e2e_step(self):
+        self.x_d.copy_(self.x_h, non_blocking=True)
+        self.s_d.copy_(self.s_h, non_blocking=True)
+        phi = self.ops.svgd_direction(self.x_d, self.s_d, self.gamma)
+        self.phi_h.copy_(phi, non_blocking=True)
+
+
+WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd}
 
 
 def time_steps(fn, steps, flush):
@@ -294,28 +463,35 @@ def gpu_arm(args, rank, world):
     ksum = timer.summary()
     dom = max(ksum.items(), key=lambda kv: kv[1]["total_ms"])
     dname, dstat = dom
-    fpp = wl.flops_per_pair.get(dname)
+    credit = wl.flops_per_pair.get(dname)
     roof = None
-    if fpp is not None:
+    if credit is not None:
+        fpp, bound = credit
         ach = fpp * wl.pairs / (dstat["avg_ms"] / 1e3) / 1e12
-        peak = pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]
-        roof = {"kernel": dname, "bound": wl.bound, "achieved": round(ach, 3), "peak": round(peak, 2),
+        if bound == "tensor":
+            peak = pk["tf32_tflops"]
+            src = (f"tf32 tensor: measured bf16 {pk['tf32_tflops'] * 2.25 / 1.1:.0f} TFLOP/s x 1.1/2.25 "
+                   f"(nominal tf32/bf16), of measured")
+        else:
+            peak = pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]
+            src = (f"FP32 pipe: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x {pk['sm_max_mhz']:.0f} MHz "
+                   f"(derived from unit counts and the measured max clock)")
+        roof = {"kernel": dname, "bound": bound, "achieved": round(ach, 3), "peak": round(peak, 2),
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname),
-                "peak_source": f"FP32 pipe: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x "
-                               f"{pk['sm_max_mhz']:.0f} MHz (derived)",
-                "flop_per_pair": fpp}
+                "peak_source": src, "flop_per_pair": fpp}
     step_tflops = wl.step_flops_per_pair * wl.pairs / (ms_step / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the workload)",
-        "config": {"workload": wl.name, "N": wl.N, "M": wl.N, "D": wl.D, "pairs_per_step": wl.pairs,
+        "config": {"workload": wl.name, "N": wl.N, "M": getattr(wl, "M", wl.N), "D": wl.D, "pairs_per_step": wl.pairs,
                    "l2": "flushed before every timed step (256 MB write, untimed)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "impl": "libtp",
         "roofline": roof,
         "step_roofline": {"achieved_tflops": round(step_tflops, 3), "flop_per_pair": wl.step_flops_per_pair,
-                          "frac_fp32": round(step_tflops / pk["fp32_tflops"], 4)},
+                          "frac_fp32_pipe" if wl.dtype == "f32" else "frac_fp64_pipe":
+                              round(step_tflops / (pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]), 4)},
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_ms"] * 1e3, 2),
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in ksum.values()), 4)}
                     for k, v in sorted(ksum.items(), key=lambda kv: -kv[1]["total_ms"])},
@@ -427,10 +603,8 @@ def main():
         torch.distributed.init_process_group("nccl")
     line = gpu_arm(args, rank, world)
     if line is not None:
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and args.workload == 2:
             line["cpu_baseline"] = cpu_baseline()
-        elif not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline() if rank == 0 else None
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

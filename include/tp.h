@@ -146,11 +146,11 @@ TP_API tp_status tp_pairwise_topk(const tp_pairs* pairs, const tp_score* score, 
  * they need it: code running inside another allocator's critical section or out-of-memory callback,
  * real-time loops that forbid allocation after start-up, hosts that cannot size and own a workspace.
  * The guide has no counterpart to this entry point; it exists for those callers only.
- * There is no workspace argument: the scratch is a fixed 4 MiB array of device memory owned by this
+ * There is no workspace argument: the scratch is a fixed 16 MiB array of device memory owned by this
  * library, held on every GPU that loads it until the process exits. A problem whose workspace
- * (tp_workspace_size("pairwise_logsumexp", ...)) exceeds 4 MiB is rejected with TP_ERR_INVALID_ARG
- * and a message in tp_last_error(); with this build's split plan every shape needs at most about
- * 1.2 MiB (fp32) or 2.4 MiB (fp64), so none is rejected today.
+ * (tp_workspace_size("pairwise_logsumexp", ...)) exceeds 16 MiB is rejected with TP_ERR_INVALID_ARG
+ * and a message in tp_last_error(): with fp32 and D = 64 that is beyond about 30000 distinct points
+ * (N, plus M when Y is not X); other shapes need at most 2.4 MiB.
  * The first call on a device looks up the array's address (with that device current); make that
  * first call before any stream capture. Every call shares the array and finds the previous call's
  * contents there; nothing in it needs clearing, but calls whose GPU work overlaps (different streams

@@ -15,6 +15,8 @@ TP_DP_LIST(TP_INST_BWD, float, 4, kBLse, kCol, true, false)
 TP_DP_LIST(TP_INST_BWD, float, 4, kBDisp, kRow, true, false)
 TP_DP_LIST(TP_INST_BWD, float, 4, kBDisp, kCol, true, false)
 template void launch_bwd_merge<float, kBLse, kRow, true, false>(const SweepArgs&, cudaStream_t);
+TP_DP_LIST(TP_INST_BWD, float, 4, kBLseSym, kRow, true, false)
+template void launch_bwd_merge<float, kBLseSym, kRow, true, false>(const SweepArgs&, cudaStream_t);
 template void launch_bwd_merge<float, kBLse, kCol, true, false>(const SweepArgs&, cudaStream_t);
 template void launch_bwd_merge<float, kBDisp, kRow, true, false>(const SweepArgs&, cudaStream_t);
 template void launch_bwd_merge<float, kBDisp, kCol, true, false>(const SweepArgs&, cudaStream_t);

@@ -6,7 +6,9 @@
 // Expressions", "Stein Variational Gradient Descent").
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <type_traits>
@@ -17,6 +19,13 @@
 #include "tp_launch.h"
 
 using namespace tp;
+
+namespace tp {
+size_t lse_tc_workspace(int64_t N, int64_t M, bool same);                  // tp_tc_lse.cu
+int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s);  // tp_tc_lse.cu
+size_t lse_bwd_tc_workspace(int64_t N);                                       // tp_tc_lse.cu
+int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s);                // tp_tc_lse.cu
+}  // namespace tp
 
 namespace {
 
@@ -164,6 +173,25 @@ SweepArgs side_args(const tp_pairs* p, const tp_score* s, bool col) {
     return a;
 }
 
+// TP_FORCE_SIMT=1 in the environment routes every call to the SIMT kernels (A/B comparisons).
+bool force_simt() {
+    static const bool v = [] {
+        const char* e = getenv("TP_FORCE_SIMT");
+        return e && e[0] && e[0] != '0';
+    }();
+    return v;
+}
+
+// The tensor-core symmetric backward stays off until its TMEM-operand MMA layout is validated.
+constexpr bool kTcBackward = false;
+
+// The tensor-core log-sum-exp covers fp32, D = 64, no row/column parameters, 16-byte aligned points.
+bool lse_tc_shape(const tp_pairs* p) { return p->dtype == TP_F32 && p->D == 64; }
+bool lse_tc_eligible(const tp_pairs* p, const tp_score* s) {
+    return !force_simt() && lse_tc_shape(p) && !s->row_bias && !s->col_bias && !s->row_weight && !s->col_weight &&
+           aligned(p->X, 16) && aligned(p->Y, 16);
+}
+
 tp_status launched(int n) {
     g_launches += n;
     const cudaError_t e = cudaGetLastError();
@@ -288,7 +316,10 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     if (needC && (C < 1 || C > 64)) return (size_t)-1;
     if (e == "pairwise_matmul") return partial_bytes(r, fwd_width(kMatmul, D, (int)C), es);
     if (e == "pairwise_softmax_matmul") return partial_bytes(r, fwd_width(kSoftmax, D, (int)C), es);
-    if (e == "pairwise_logsumexp") return partial_bytes(r, fwd_width(kLse, D, 0), es);
+    if (e == "pairwise_logsumexp") {
+        const size_t simt = partial_bytes(r, fwd_width(kLse, D, 0), es);
+        return lse_tc_shape(p) ? std::max(simt, lse_tc_workspace(p->N, p->M, p->X == p->Y)) : simt;
+    }
     if (e == "pairwise_displacement") return partial_bytes(r, fwd_width(kDisp, D, 0), es);
     if (e == "svgd_direction") return partial_bytes(r, fwd_width(kSvgd, D, 0), es);
     if (e == "pairwise_topk") {
@@ -298,7 +329,11 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     }
     if (e == "pairwise_matmul_backward") return bwd_ws(p, kBMatmul, C, 0);
     if (e == "pairwise_softmax_matmul_backward") return bwd_ws(p, kBSoftmax, C, align_up(p->N * es));
-    if (e == "pairwise_logsumexp_backward") return bwd_ws(p, kBLse, 0, 0);
+    if (e == "pairwise_logsumexp_backward") {
+        const size_t simt = bwd_ws(p, kBLse, 0, 0);
+        const bool sym = p->X == p->Y && p->N == p->M;
+        return kTcBackward && lse_tc_shape(p) && sym ? std::max(simt, lse_bwd_tc_workspace(p->N)) : simt;
+    }
     if (e == "pairwise_displacement_backward") return bwd_ws(p, kBDisp, 0, 0);
     if (e == "pairwise_topk_backward") {
         if (k < 1 || k > p->M) return (size_t)-1;
@@ -526,6 +561,11 @@ tp_status tp_pairwise_logsumexp(const tp_pairs* pr, const tp_score* sc, int excl
     a.out = lse;
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (lse_tc_eligible(pr, sc)) {
+        const int n = launch_lse_tc(a, lse, pr->X == pr->Y, st);
+        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        return launched(n);
+    }
     return by_dtype(pr->dtype, [&](auto t) { return launched(run_fwd_plain<decltype(t), kLse>(a, st)); });
 }
 
@@ -685,6 +725,24 @@ tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pr, const tp_score* sc,
     row.exclude_self = col.exclude_self = exclude_self ? 1 : 0;
     row.ws = col.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Same points, summed gradient wanted, no row/column parameters: the score is symmetric and one
+    // sweep gives sum_j (H_kj + H_jk) dt_kj/dz_k, each pair evaluated once.
+    const bool symmetric = dX && dX == dY && pr->X == pr->Y && pr->N == pr->M && !sc->row_bias && !sc->col_bias &&
+                           !sc->row_weight && !sc->col_weight;
+    if (symmetric) {
+        row.gP = dX;
+        if (kTcBackward && lse_tc_eligible(pr, sc)) {
+            const int n = launch_lse_bwd_sym_tc(row, st);
+            if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+            return launched(n);
+        }
+        return by_dtype(pr->dtype, [&](auto t) {
+            using T = decltype(t);
+            int n = 0;
+            with_dp(pad_bucket(row.D), [&](auto dp) { n = bwd_step<T, decltype(dp)::value, 4, kBLseSym, kRow, true, false>(row, st); });
+            return launched(n);
+        });
+    }
     return by_dtype(pr->dtype, [&](auto t) { return launched(run_backward<decltype(t), kBLse>(row, col, g, st)); });
 }
 

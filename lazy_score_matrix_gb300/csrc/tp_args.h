@@ -41,7 +41,9 @@ struct SweepArgs {
 
 enum FwdMode : int { kMatmul = 0, kSoftmax = 1, kLse = 2, kDisp = 3, kSvgd = 4 };
 
-enum BwdMode : int { kBMatmul = 0, kBSoftmax = 1, kBLse = 2, kBDisp = 3 };
+// kBLseSym: logsumexp backward when X and Y are the same points and the score is symmetric (no
+// row/column parameters): one sweep gives the summed gradient sum_j (H_kj + H_jk) dt_kj/dz_k.
+enum BwdMode : int { kBMatmul = 0, kBSoftmax = 1, kBLse = 2, kBDisp = 3, kBLseSym = 4 };
 enum Side : int { kRow = 0, kCol = 1 };
 
 

@@ -550,7 +550,8 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
     // staged value rows: row sweep V_j (CP); column sweep dO_i (CP; DP for disp)
     constexpr int QVW = VALS ? CP : ((MODE == kBDisp && SIDE == kCol) ? DP : 1);
     constexpr bool HAS_QV = VALS || (MODE == kBDisp && SIDE == kCol);
-    constexpr bool ROWSTAT = (MODE == kBSoftmax || MODE == kBLse);
+    constexpr bool ROWSTAT = (MODE == kBSoftmax || MODE == kBLse || MODE == kBLseSym);
+    constexpr bool QSTAT = (SIDE == kCol && ROWSTAT) || MODE == kBLseSym;  // per-streamed-point lse, g
     constexpr int KD = (MODE == kBDisp && SIDE == kCol) ? DP : 1;
 
     using SM = BwdSmem<T, DP, CP, MODE, SIDE, DO_G, DO_V>;
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
         if constexpr (SIDE == kRow) {
             if constexpr (ROWSTAT) plse = static_cast<const T*>(a.lse)[pi] * E::kLogB;
             if constexpr (MODE == kBSoftmax) pstat = static_cast<const T*>(a.delta)[pi];
-            if constexpr (MODE == kBLse) pstat = static_cast<const T*>(a.glse)[pi];
+            if constexpr (MODE == kBLse || MODE == kBLseSym) pstat = static_cast<const T*>(a.glse)[pi];
             if constexpr (MODE == kBDisp) {
                 T c0 = T(0);
 #pragma unroll
@@ -638,7 +639,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
             stage_rows<T, QVW>(sv, static_cast<const T*>(a.Vq), j0, cnt, MODE == kBDisp ? a.D : a.C, a.vecV);
         stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
         stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
-        if constexpr (SIDE == kCol && ROWSTAT) {
+        if constexpr (QSTAT) {
             for (int e = threadIdx.x; e < cnt; e += kThreads) {
                 s1[e] = static_cast<const T*>(a.lse)[j0 + e] * E::kLogB;
                 s2[e] = MODE == kBSoftmax ? static_cast<const T*>(a.delta)[j0 + e]
@@ -678,6 +679,13 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
                 const T g = SIDE == kRow ? pstat : s2[jj];
                 const bool excluded = a.exclude_self && (j0 + jj == pi);
                 G = (excluded || !(lse_b > ninf<T>())) ? T(0) : g * E::bexp(S * E::kLogB - lse_b);
+            } else if constexpr (MODE == kBLseSym) {
+                // the pair seen from row k (this thread) and from row j (the streamed point)
+                const bool excluded = a.exclude_self && (j0 + jj == pi);
+                const T sb2 = S * E::kLogB;
+                const T gk = plse > ninf<T>() ? pstat * E::bexp(sb2 - plse) : T(0);
+                const T gj = s1[jj] > ninf<T>() ? s2[jj] * E::bexp(sb2 - s1[jj]) : T(0);
+                G = excluded ? T(0) : gk + gj;
             } else {  // kBDisp
                 if constexpr (SIDE == kRow) {
                     G = dot_regs_smem<T, DP>(pv, q) - pstat;
@@ -956,15 +964,17 @@ constexpr const char* kFwdNames[] = {"fwd_sweep_matmul", "fwd_sweep_softmax", "f
 constexpr const char* kFwdMergeNames[] = {"fwd_merge_matmul", "fwd_merge_softmax", "fwd_merge_lse", "fwd_merge_disp",
                                           "fwd_merge_svgd"};
 // [mode][side][0 = gradients (and dV when fused), 1 = dV only]
-constexpr const char* kBwdNames[4][2][2] = {
+constexpr const char* kBwdNames[5][2][2] = {
     {{"bwd_sweep_matmul_row", "bwd_sweep_matmul_row"}, {"bwd_sweep_matmul_col", "bwd_sweep_matmul_col_dv"}},
     {{"bwd_sweep_softmax_row", "bwd_sweep_softmax_row"}, {"bwd_sweep_softmax_col", "bwd_sweep_softmax_col_dv"}},
     {{"bwd_sweep_lse_row", "bwd_sweep_lse_row"}, {"bwd_sweep_lse_col", "bwd_sweep_lse_col"}},
-    {{"bwd_sweep_disp_row", "bwd_sweep_disp_row"}, {"bwd_sweep_disp_col", "bwd_sweep_disp_col"}}};
-constexpr const char* kBwdMergeNames[4][2] = {{"bwd_merge_matmul_row", "bwd_merge_matmul_col"},
+    {{"bwd_sweep_disp_row", "bwd_sweep_disp_row"}, {"bwd_sweep_disp_col", "bwd_sweep_disp_col"}},
+    {{"bwd_sweep_lse_sym", "bwd_sweep_lse_sym"}, {"bwd_sweep_lse_sym", "bwd_sweep_lse_sym"}}};
+constexpr const char* kBwdMergeNames[5][2] = {{"bwd_merge_matmul_row", "bwd_merge_matmul_col"},
                                               {"bwd_merge_softmax_row", "bwd_merge_softmax_col"},
                                               {"bwd_merge_lse_row", "bwd_merge_lse_col"},
-                                              {"bwd_merge_disp_row", "bwd_merge_disp_col"}};
+                                              {"bwd_merge_disp_row", "bwd_merge_disp_col"},
+                                              {"bwd_merge_lse_sym", "bwd_merge_lse_sym"}};
 
 inline dim3 sweep_grid(const SweepArgs& a) {
     return dim3((unsigned)((a.nP + kThreads - 1) / kThreads), (unsigned)a.splits, 1);

@@ -32,9 +32,11 @@ void set_last_error(const std::string& msg);  // tp_api.cu: the text tp_last_err
 
 namespace {
 
-// 4 MiB per device. Under this build's split plan the log-sum-exp needs at most about 1.2 MiB (fp32)
-// or 2.4 MiB (fp64) for any shape; the size check below still guards the limit.
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+// 16 MiB per device. The SIMT log-sum-exp needs at most about 1.2 MiB (fp32) or 2.4 MiB (fp64) for
+// any shape; the fp32 D = 64 tensor-core path needs the hi/lo split of the points (512 bytes per
+// distinct point) plus about 0.3 MiB, so it fits up to ~30000 distinct points. Larger problems are
+// rejected by the size check below.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -1,0 +1,867 @@
+// Row log-sum-exp on the Blackwell tensor cores (fp32 data, D = 64 features, no row/column
+// parameters): torchpairwise guide "Using Torchpairwise in Models", Task Map (InfoNCE row:
+// S.logsumexp(-1, exclude_self=True) on S = lazy(z, z, "linear") / t) and Score Expressions.
+//
+// The contraction X Y^T (D = 64) runs on tcgen05.mma kind::tf32 with a hi/lo split of both operands
+// (x = hi + lo, hi = x with its low 13 mantissa bits cleared): X Y^T ~ Xh Yh^T + Xh Yl^T + Xl Yh^T,
+// which keeps fp32-level accuracy (the dropped Xl Yl^T and the truncation of lo are ~2^-21 relative).
+// The 128 x 128 score tile lands in TMEM; four epilogue warps read it back one row per thread
+// (tcgen05.ld) and run the online log-sum-exp in base 2, with the metric, scale, exp and exclude_self
+// applied per element. The matrix never leaves the SM.
+//
+// Schedule: persistent, one CTA per SM. The (row block, column tile) pairs are numbered row-block
+// major and cut into equal contiguous ranges, one per CTA; a CTA's range spans at most a few row
+// blocks, and for each it writes a partial (max, sum) per row. A merge kernel combines the partials
+// of each row in CTA order, so results are deterministic.
+//
+// Warp roles (192 threads): warp 0 lane 0 loads tiles with TMA (128-byte swizzle), warp 1 owns the
+// TMEM allocation and its lane 0 issues the MMAs, warps 2..5 are the epilogue. Operand ring: the row
+// block's A tile (hi, lo: 64 KB) plus two stages of B tiles (hi, lo: 64 KB each); accumulators: two
+// TMEM buffers of 128 columns, so the MMAs of tile i+1 overlap the epilogue of tile i.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tp_args.h"
+#include "tp_device.cuh"
+#include "tp_launch.h"
+#include "tp_tc.cuh"
+
+namespace tp {
+namespace tc {
+
+constexpr int kBM = 128;                     // rows per tile (TMEM lanes)
+constexpr int kBN = 128;                     // columns per tile
+constexpr int kChunk = kBM * 128;            // one 128-row x 32-fp32 swizzled chunk: 16 KB
+constexpr int kOperand = 2 * kChunk;         // 64 features: two chunks, 32 KB
+constexpr int kPair = 2 * kOperand;          // hi + lo: 64 KB
+constexpr int kStages = 2;
+constexpr int kTcThreads = 192;      // backward kernel: producer, MMA, 4 epilogue warps
+constexpr int kTcThreadsF = 320;     // forward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
+constexpr int kTmemCols = 256;
+constexpr int kGrid = 152;                   // persistent CTAs: one per GB300 SM
+constexpr size_t kSmemBytes = (size_t)kPair * (1 + kStages) + 256 + 1024;  // + barriers, + alignment slack
+
+struct LseTcParams {
+    int64_t N, M;
+    int64_t T;   // total tiles = RB * CT
+    int CT;      // column tiles per row block
+    int G;       // CTAs
+    int smax;    // partial slots per CTA
+    int metric;
+    int apply_exp;
+    int exclude_self;
+    float scale;
+    float neg_gamma_log2;  // -gamma * log2(e)
+    const float* xn;       // |x_i|^2 (distance metrics)
+    const float* yn;       // |y_j|^2
+    float* part;           // [G][smax][2 halves][2][128] partial (max, sum) in base 2
+    int* err;
+    int same;              // X and Y are the same array: the self-distance is exactly 0
+};
+
+__host__ __device__ inline int64_t range_start(int64_t T, int G, int c) { return (T * c) / G; }
+
+// Score of one element in base-2 units from the dot product (metric, scale, exp), or -inf.
+template <int METRIC, bool EXP>
+__device__ __forceinline__ float tile_score(float dot, float xn, float yn, const LseTcParams& p) {
+    constexpr float kL2E = 1.4426950408889634f;
+    float base;
+    if (METRIC == kLinear) {
+        base = dot;
+    } else {
+        const float d2 = fmaxf(fmaf(-2.f, dot, xn + yn), 0.f);
+        base = METRIC == kRbf ? ExpTraits<float>::bexp(p.neg_gamma_log2 * d2) : d2;
+    }
+    const float t = p.scale * base;
+    const float S = EXP ? ExpTraits<float>::bexp(t * kL2E) : t;
+    return S * kL2E;
+}
+
+template <int METRIC, bool EXP>
+__global__ void __launch_bounds__(kTcThreadsF, 1)
+    lse_fwd_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
+               const __grid_constant__ CUtensorMap mYh, const __grid_constant__ CUtensorMap mYl, const LseTcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = sm;                      // [hi: 2 chunks][lo: 2 chunks]
+    unsigned char* sB = sm + kPair;              // stage s at sB + s * kPair
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kPair * (1 + kStages));
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* b_full = bars + 2;     // [kStages]
+    uint64_t* b_empty = bars + 4;    // [kStages]
+    uint64_t* acc_full = bars + 6;   // [2]
+    uint64_t* acc_empty = bars + 8;  // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(b_empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 256);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, kTmemCols);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer
+            int64_t rb_cur = -1;
+            int a_uses = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 11);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, kPair);
+                    tma_load_2d(sA, &mXh, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kChunk, &mXh, 32, rb * kBM, a_full);
+                    tma_load_2d(sA + kOperand, &mXl, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kOperand + kChunk, &mXl, 32, rb * kBM, a_full);
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStages), r = (int)(i / kStages);
+                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 12);
+                if (!ok) break;
+                unsigned char* dst = sB + s * kPair;
+                mbar_expect_tx(b_full + s, kPair);
+                tma_load_2d(dst, &mYh, 0, ct * kBN, b_full + s);
+                tma_load_2d(dst + kChunk, &mYh, 32, ct * kBN, b_full + s);
+                tma_load_2d(dst + kOperand, &mYl, 0, ct * kBN, b_full + s);
+                tma_load_2d(dst + kOperand + kChunk, &mYl, 32, ct * kBN, b_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_tf32(kBM, kBN);
+            int64_t rb_cur = -1;
+            int a_uses = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = (int)(t / p.CT);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);  // the previous A is free once its MMAs finish
+                    ok = mbar_wait(a_full, a_uses & 1, p.err, 13);
+                    if (!ok) break;
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStages), r = (int)(i / kStages), b = (int)(i & 1), rr = (int)(i >> 1);
+                ok = mbar_wait(b_full + s, r & 1, p.err, 14);
+                if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 15);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(b * kBN);
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kPair);
+                // Xh Yh^T + Xh Yl^T + Xl Yh^T over K = 64 in steps of 8 (32 bytes)
+                const uint32_t ao[3] = {0u, 0u, (uint32_t)kOperand};
+                const uint32_t bo[3] = {0u, (uint32_t)kOperand, 0u};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int prod = 0; prod < 3; ++prod) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t koff = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
+                        mma_tf32(d, desc_kmajor_sw128(a0 + ao[prod] + koff), desc_kmajor_sw128(b0 + bo[prod] + koff),
+                                 idesc, acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(b_empty + s);
+                mma_commit(acc_full + b);
+            }
+        }
+    } else {  // ---------------- epilogue: warps 2..9, one row per thread, half of the tile's columns
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;       // columns [64 * half, 64 * half + 64) of each tile
+        const int lr = q * 32 + lane;           // row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        int64_t rb_cur = -1;
+        int seg = 0;
+        float m = ninf<float>(), l = 0.f, xn = 0.f;
+        bool ok = true;
+        auto flush = [&]() {
+            float* o = p.part + ((size_t)((blockIdx.x * p.smax + seg) * 2 + half) * 2) * kBM;
+            o[lr] = m;
+            o[kBM + lr] = l;
+            ++seg;
+        };
+        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            const int64_t i = t - t_begin;
+            const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+            const int64_t row = (int64_t)rb * kBM + lr;
+            if (rb != rb_cur) {
+                if (rb_cur >= 0) flush();
+                m = ninf<float>();
+                l = 0.f;
+                rb_cur = rb;
+                xn = (METRIC != kLinear && row < p.N) ? p.xn[row] : 0.f;
+            }
+            const int b = (int)(i & 1), rr = (int)(i >> 1);
+            ok = mbar_wait(acc_full + b, rr & 1, p.err, 16);
+            if (!ok) break;
+            fence_after_sync();
+            const int64_t j0 = (int64_t)ct * kBN + half * 64;
+            const bool diag = row >= j0 && row < j0 + 64;
+            const bool masked = p.M - j0 < 64 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tmem_ld32(lane_base + (uint32_t)(b * kBN + c * 32), v);
+                const int64_t jc = j0 + c * 32;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int64_t j = jc + u;
+                    float dot = v[u];
+                    if (METRIC != kLinear && masked && p.same && j == row) dot = xn;  // |x - x|^2 = 0 exactly
+                    const float yn = (METRIC != kLinear && j < p.M) ? __ldg(p.yn + j) : 0.f;
+                    float sc = tile_score<METRIC, EXP>(dot, xn, yn, p);
+                    if (masked && (j >= p.M || (p.exclude_self && j == row))) sc = ninf<float>();
+                    v[u] = sc;
+                }
+                float c4[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) c4[a] = ninf<float>();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) c4[u & 3] = fmaxf(c4[u & 3], v[u]);
+                const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+                if (cmax == ninf<float>()) continue;
+                if (cmax > m) {
+                    l *= ExpTraits<float>::bexp(m - cmax);
+                    m = cmax;
+                }
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u = 0; u < 32; ++u) s4[u & 3] += ExpTraits<float>::bexp(v[u] - m);
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            }
+            fence_before_sync();
+            mbar_arrive(acc_empty + b);
+        }
+        if (ok && rb_cur >= 0) flush();
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Partials of each row, in CTA order, into lse (natural log).
+__global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.N) return;
+    const int rb = (int)(i / kBM), lr = (int)(i % kBM);
+    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
+    // first CTA whose range holds t0, last whose range holds t1 (ranges are sorted and contiguous)
+    auto cta_of = [&](int64_t t) {
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (range_start(p.T, p.G, mid) <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
+    float m = ninf<float>();
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
+        for (int h = 0; h < 2; ++h) m = fmaxf(m, p.part[((size_t)((c * p.smax + seg) * 2 + h) * 2) * kBM + lr]);
+    }
+    float l = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
+        for (int h = 0; h < 2; ++h) {
+            const float* o = p.part + ((size_t)((c * p.smax + seg) * 2 + h) * 2) * kBM;
+            if (o[lr] > ninf<float>()) l += o[kBM + lr] * ExpTraits<float>::bexp(o[lr] - m);
+        }
+    }
+    lse[i] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : ninf<float>();
+}
+
+// hi/lo split of a [n, 64] fp32 array and its row squared norms.
+__global__ void tc_split64(const float* __restrict__ x, int64_t n, float* __restrict__ hi, float* __restrict__ lo,
+                           float* __restrict__ norm) {
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 16) + threadIdx.x / 16;  // 16 threads per row
+    const int q = threadIdx.x & 15;
+    if (r >= n) return;
+    const float4 v = reinterpret_cast<const float4*>(x + r * 64)[q];
+    float e[4] = {v.x, v.y, v.z, v.w}, h[4], lo4[4];
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        h[u] = __uint_as_float(__float_as_uint(e[u]) & 0xFFFFE000u);
+        lo4[u] = e[u] - h[u];
+        s = fmaf(e[u], e[u], s);
+    }
+    reinterpret_cast<float4*>(hi + r * 64)[q] = make_float4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<float4*>(lo + r * 64)[q] = make_float4(lo4[0], lo4[1], lo4[2], lo4[3]);
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off, 16);
+    if (q == 0) norm[r] = s;
+}
+
+
+// ------------------------------------------------------------------------------------------------
+// Symmetric backward (X = Y = z, no row/column parameters): z.grad_k = sum_j kappa_kj z_j
+// - [distance metric] z_k sum_j kappa_kj, with kappa_kj the coefficient of z_j in d/dz_k of
+// g_k lse_k + g_j lse_j: G = g_k P_kj + g_j P_jk (P_kj = exp(S_kj - lse_k)), H = G (times S with
+// exp), E = H * scale, kappa = E (linear), -2E (sqeuclidean), 2 gamma E base (rbf). Each pair is
+// evaluated once: the replay of introduction "First derivatives replay the tiles", for both sides
+// of the pair at the same time.
+//
+// Per 64-column tile: S = Zrows Ztile^T (tf32 hi/lo, 3 products) into TMEM; the epilogue turns S
+// into kappa, splits it hi/lo and stores it back into TMEM; then dZ += kappa_hi Zh + kappa_hi Zl +
+// kappa_lo Zh, with kappa as the A operand read from TMEM and the same staged tile as an MN-major B
+// operand. dZ (128 x 64) accumulates in TMEM over the CTA's tiles of a row block and is written as a
+// partial; a merge kernel adds the partials of each row in CTA order.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kBNb = 64;                   // columns per backward tile
+constexpr int kChunkB = kBNb * 128;        // 64-row x 32-fp32 chunk: 8 KB
+constexpr int kOperandB = 2 * kChunkB;     // 16 KB
+constexpr int kPairB = 2 * kOperandB;      // hi + lo: 32 KB
+constexpr int kStagesB = 4;
+constexpr int kTmemColsB = 512;            // S/kappa_hi x2 (64 each), kappa_lo x2, dZ (64)
+constexpr size_t kSmemBytesB = (size_t)kPair + (size_t)kPairB * kStagesB + (size_t)kStagesB * kBNb * 8 + 256 + 1024;
+
+struct LseBwdTcParams {
+    int64_t N;
+    int64_t T;
+    int CT, G, smax;
+    int metric, apply_exp, exclude_self;
+    float scale, neg_gamma_log2, two_gamma;
+    const float* zn;      // |z_k|^2
+    const float* lse2g;   // [ceil(N/64)*64][2]: (lse_j * log2 e, g_j), padded with (+inf, 0)
+    float* part;          // [G][smax][65][128]: dZ columns then sum of kappa, row-minor
+    int* err;
+};
+
+template <int METRIC, bool EXP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    lse_bwd_sym_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
+                   const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
+                   const LseBwdTcParams p) {
+    constexpr float kL2E = 1.4426950408889634f;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = sm;                                    // row block: hi (2 chunks) | lo (2 chunks)
+    unsigned char* sB = sm + kPair;                            // stage s at sB + s * kPairB
+    float* sStat = reinterpret_cast<float*>(sB + kPairB * kStagesB);  // [stage][64][2]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStagesB * kBNb * 2);
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* b_full = bars + 2;    // [4]
+    uint64_t* b_empty = bars + 6;   // [4]
+    uint64_t* s_full = bars + 10;   // [2]
+    uint64_t* w_full = bars + 12;   // [2]
+    uint64_t* dz_full = bars + 14;
+    uint64_t* dz_empty = bars + 15;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
+    auto rb_of = [&](int64_t t) { return (int)(t / p.CT); };
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < kStagesB; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(b_empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full + b, 1);
+            mbar_init(w_full + b, 128);
+        }
+        mbar_init(dz_full, 1);
+        mbar_init(dz_empty, 128);
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, kTmemColsB);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t tS = tmem, tLo = tmem + 2 * kBNb, tDZ = tmem + 4 * kBNb;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = rb_of(t), ct = (int)(t % p.CT);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 21);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, kPair);
+                    tma_load_2d(sA, &mAh, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kChunk, &mAh, 32, rb * kBM, a_full);
+                    tma_load_2d(sA + kOperand, &mAl, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kOperand + kChunk, &mAl, 32, rb * kBM, a_full);
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStagesB), r = (int)(i / kStagesB);
+                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 22);
+                if (!ok) break;
+                unsigned char* dst = sB + s * kPairB;
+                mbar_expect_tx(b_full + s, kPairB + kBNb * 8);
+                tma_load_2d(dst, &mBh, 0, ct * kBNb, b_full + s);
+                tma_load_2d(dst + kChunkB, &mBh, 32, ct * kBNb, b_full + s);
+                tma_load_2d(dst + kOperandB, &mBl, 0, ct * kBNb, b_full + s);
+                tma_load_2d(dst + kOperandB + kChunkB, &mBl, 32, ct * kBNb, b_full + s);
+                bulk_load(sStat + s * kBNb * 2, p.lse2g + (size_t)ct * kBNb * 2, kBNb * 8, b_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            constexpr uint32_t idS = idesc_tf32(kBM, kBNb);       // S: M 128, N 64 (K = 64 features)
+            constexpr uint32_t idZ = idesc_tf32_bmn(kBM, 64);      // dZ: M 128, N 64 features, K = 64 points
+            int a_uses = 0, dz_uses = 0;
+            bool ok = true;
+            // dZ for tile i (already in TMEM as kappa): issue after its epilogue is done
+            auto issue_dz = [&](int64_t i) -> bool {
+                const int64_t t = t_begin + i;
+                const int b = (int)(i & 1), s = (int)(i % kStagesB);
+                if (!mbar_wait(w_full + b, (uint32_t)((i >> 1) & 1), p.err, 25)) return false;
+                fence_after_sync();
+                const bool first = (i == 0) || rb_of(t - 1) != rb_of(t);
+                const bool last = (t + 1 == t_end) || rb_of(t + 1) != rb_of(t);
+                if (first && dz_uses > 0 && !mbar_wait(dz_empty, (dz_uses - 1) & 1, p.err, 26)) return false;
+                const uint32_t bz = smem_u32(sB + s * kPairB);
+                const uint32_t kh = tS + (uint32_t)(b * kBNb), kl = tLo + (uint32_t)(b * kBNb);
+                // kappa_hi Zh + kappa_hi Zl + kappa_lo Zh, K = 64 points in steps of 8 (1024-byte atoms)
+                const uint32_t ka[3] = {kh, kh, kl};
+                const uint32_t zb[3] = {0u, (uint32_t)kOperandB, 0u};
+                uint32_t acc = first ? 0u : 1u;
+#pragma unroll
+                for (int prod = 0; prod < 3; ++prod) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        mma_tf32_ta(tDZ, ka[prod] + (uint32_t)(ks * 8),
+                                    desc_mnmajor_sw128(bz + zb[prod] + (uint32_t)(ks * 1024), (uint32_t)kChunkB), idZ,
+                                    acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(b_empty + s);
+                if (last) {
+                    mma_commit(dz_full);
+                    ++dz_uses;
+                }
+                return true;
+            };
+            int rb_cur = -1;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = rb_of(t);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);
+                    ok = mbar_wait(a_full, a_uses & 1, p.err, 23);
+                    if (!ok) break;
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStagesB), r = (int)(i / kStagesB), b = (int)(i & 1);
+                ok = mbar_wait(b_full + s, r & 1, p.err, 24);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kPairB);
+                const uint32_t ao[3] = {0u, 0u, (uint32_t)kOperand};
+                const uint32_t bo[3] = {0u, (uint32_t)kOperandB, 0u};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int prod = 0; prod < 3; ++prod) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t ka = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
+                        const uint32_t kb = (uint32_t)((ks >> 2) * kChunkB + (ks & 3) * 32);
+                        mma_tf32(tS + (uint32_t)(b * kBNb), desc_kmajor_sw128(a0 + ao[prod] + ka),
+                                 desc_kmajor_sw128(b0 + bo[prod] + kb), idS, acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(s_full + b);
+                if (i > 0) ok = issue_dz(i - 1);
+            }
+            if (ok && t_end > t_begin) issue_dz(t_end - t_begin - 1);
+        }
+    } else {  // ---------------- epilogue: warps 2..5
+        const int q = warp & 3;
+        const int lr = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int seg = 0, dz_uses = 0;
+        float K0 = 0.f, lse2k = 0.f, gk = 0.f, zn_k = 0.f;
+        bool ok = true;
+        auto readout = [&](int rb) -> bool {  // dZ of the finished row-block segment -> partial
+            if (!mbar_wait(dz_full, dz_uses & 1, p.err, 27)) return false;
+            ++dz_uses;
+            fence_after_sync();
+            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * 65 * kBM;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tmem_ld32(tDZ + lane_off + (uint32_t)(c * 32), v);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) o[(size_t)(c * 32 + u) * kBM + lr] = v[u];
+            }
+            o[(size_t)64 * kBM + lr] = K0;
+            fence_before_sync();
+            mbar_arrive(dz_empty);
+            ++seg;
+            return true;
+        };
+        int rb_cur = -1;
+        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            const int64_t i = t - t_begin;
+            const int rb = rb_of(t), ct = (int)(t % p.CT);
+            const int64_t row = (int64_t)rb * kBM + lr;
+            if (rb != rb_cur) {
+                if (rb_cur >= 0) ok = readout(rb_cur);
+                if (!ok) break;
+                rb_cur = rb;
+                K0 = 0.f;
+                const bool live = row < p.N;
+                lse2k = live ? p.lse2g[2 * row] : __int_as_float(0x7f800000);
+                gk = live ? p.lse2g[2 * row + 1] : 0.f;
+                zn_k = (METRIC != kLinear && live) ? p.zn[row] : 0.f;
+            }
+            const int b = (int)(i & 1), s = (int)(i % kStagesB);
+            ok = mbar_wait(s_full + b, (uint32_t)((i >> 1) & 1), p.err, 28);
+            if (!ok) break;
+            fence_after_sync();
+            const int64_t j0 = (int64_t)ct * kBNb;
+            const float* st = sStat + s * kBNb * 2;
+            float ksum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tmem_ld32(tS + lane_off + (uint32_t)(b * kBNb + c * 32), v);
+                float lo[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int64_t j = j0 + c * 32 + u;
+                    const float2 lg = reinterpret_cast<const float2*>(st)[c * 32 + u];
+                    const float dot = v[u];
+                    float base;
+                    if (METRIC == kLinear) {
+                        base = dot;
+                    } else {
+                        const float d2 = fmaxf(fmaf(-2.f, dot, zn_k + __ldg(p.zn + (j < p.N ? j : 0))), 0.f);
+                        base = METRIC == kRbf ? ExpTraits<float>::bexp(p.neg_gamma_log2 * d2) : d2;
+                    }
+                    const float tt = p.scale * base;
+                    const float S = EXP ? ExpTraits<float>::bexp(tt * kL2E) : tt;
+                    const float s2 = S * kL2E;
+                    const float G = gk * ExpTraits<float>::bexp(s2 - lse2k) + lg.y * ExpTraits<float>::bexp(s2 - lg.x);
+                    const bool dead = j >= p.N || (p.exclude_self && j == row);
+                    const float H = EXP ? G * S : G;
+                    const float E = H * p.scale;
+                    float kap = METRIC == kLinear ? E : (METRIC == kSqeuclidean ? -2.f * E : p.two_gamma * E * base);
+                    kap = dead ? 0.f : kap;
+                    ksum += kap;
+                    const float hi = __uint_as_float(__float_as_uint(kap) & 0xFFFFE000u);
+                    lo[u] = kap - hi;
+                    v[u] = hi;
+                }
+                tmem_st32(tS + lane_off + (uint32_t)(b * kBNb + c * 32), v);
+                tmem_st32(tLo + lane_off + (uint32_t)(b * kBNb + c * 32), lo);
+            }
+            K0 += ksum;
+            tmem_st_wait();
+            fence_before_sync();
+            mbar_arrive(w_full + b);
+        }
+        if (ok && rb_cur >= 0) readout(rb_cur);
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kTmemColsB);
+}
+
+// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa
+__global__ void lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z, float* __restrict__ grad) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row, feature), feature fastest
+    if (e >= p.N * 64) return;
+    const int64_t i = e / 64;
+    const int f = (int)(e % 64);
+    const int rb = (int)(i / kBM), lr = (int)(i % kBM);
+    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
+    auto cta_of = [&](int64_t t) {
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (range_start(p.T, p.G, mid) <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
+    float dz = 0.f, k0 = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
+        const float* o = p.part + (size_t)(c * p.smax + seg) * 65 * kBM;
+        dz += o[(size_t)f * kBM + lr];
+        k0 += o[(size_t)64 * kBM + lr];
+    }
+    grad[e] = p.metric == kLinear ? dz : dz - z[e] * k0;
+}
+
+// (lse_j log2 e, g_j) pairs, padded to a multiple of 64 rows with (+inf, 0)
+__global__ void lse_bwd_stats(const float* __restrict__ lse, const float* __restrict__ g, int64_t N, int64_t Npad,
+                              float* __restrict__ out) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= Npad) return;
+    const bool live = j < N;
+    out[2 * j] = live ? lse[j] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    out[2 * j + 1] = live ? g[j] : 0.f;
+}
+
+// ------------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// [rows, 64] fp32, box 32 x box_rows, 128-byte swizzle; rows past the end read as zeros
+static bool make_map_rows(CUtensorMap* m, const float* base, int64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {64 * sizeof(float)};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+static bool make_map(CUtensorMap* m, const float* base, int64_t rows) { return make_map_rows(m, base, rows, kBM); }
+
+struct LseTcPlan {
+    int64_t T;
+    int CT, G, smax;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_part, off_err, bytes;
+};
+
+static size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
+    LseTcPlan pl;
+    const int64_t RB = (N + kBM - 1) / kBM;
+    pl.CT = (int)((M + kBN - 1) / kBN);
+    pl.T = RB * pl.CT;
+    pl.G = (int)(pl.T < kGrid ? pl.T : kGrid);
+    const int64_t per = (pl.T + pl.G - 1) / pl.G;
+    pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
+    size_t o = 0;
+    pl.off_xh = o; o += al256((size_t)N * 64 * 4);
+    pl.off_xl = o; o += al256((size_t)N * 64 * 4);
+    if (same) {
+        pl.off_yh = pl.off_xh;
+        pl.off_yl = pl.off_xl;
+    } else {
+        pl.off_yh = o; o += al256((size_t)M * 64 * 4);
+        pl.off_yl = o; o += al256((size_t)M * 64 * 4);
+    }
+    pl.off_xn = o; o += al256((size_t)N * 4);
+    if (same) pl.off_yn = pl.off_xn;
+    else { pl.off_yn = o; o += al256((size_t)M * 4); }
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 2 * 2 * kBM * 4);
+    pl.off_err = o; o += 256;
+    pl.bytes = o;
+    return pl;
+}
+
+
+struct LseBwdTcPlan {
+    int64_t T, Npad;
+    int CT, G, smax;
+    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_err, bytes;
+};
+
+static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
+    LseBwdTcPlan pl;
+    const int64_t RB = (N + kBM - 1) / kBM;
+    pl.CT = (int)((N + kBNb - 1) / kBNb);
+    pl.Npad = (int64_t)pl.CT * kBNb;
+    pl.T = RB * pl.CT;
+    pl.G = (int)(pl.T < kGrid ? pl.T : kGrid);
+    const int64_t per = (pl.T + pl.G - 1) / pl.G;
+    pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
+    size_t o = 0;
+    pl.off_zh = o; o += al256((size_t)N * 64 * 4);
+    pl.off_zl = o; o += al256((size_t)N * 64 * 4);
+    pl.off_zn = o; o += al256((size_t)N * 4);
+    pl.off_stat = o; o += al256((size_t)pl.Npad * 8);
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 65 * kBM * 4);
+    pl.off_err = o; o += 256;
+    pl.bytes = o;
+    return pl;
+}
+
+}  // namespace tc
+
+size_t lse_tc_workspace(int64_t N, int64_t M, bool same) { return tc::lse_tc_plan(N, M, same).bytes; }
+
+// Launches the tensor-core log-sum-exp; returns the number of kernels launched, or -1 when the
+// tensor maps cannot be built (the caller then reports TP_ERR_CUDA).
+int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
+    using namespace tc;
+    const LseTcPlan pl = lse_tc_plan(a.nP, a.nQ, same);
+    char* ws = static_cast<char*>(a.ws);
+    float* xh = reinterpret_cast<float*>(ws + pl.off_xh);
+    float* xl = reinterpret_cast<float*>(ws + pl.off_xl);
+    float* yh = reinterpret_cast<float*>(ws + pl.off_yh);
+    float* yl = reinterpret_cast<float*>(ws + pl.off_yl);
+    float* xn = reinterpret_cast<float*>(ws + pl.off_xn);
+    float* yn = reinterpret_cast<float*>(ws + pl.off_yn);
+    CUtensorMap mxh, mxl, myh, myl;
+    if (!make_map(&mxh, xh, a.nP) || !make_map(&mxl, xl, a.nP) || !make_map(&myh, yh, a.nQ) ||
+        !make_map(&myl, yl, a.nQ))
+        return -1;
+    int n = 0;
+    {
+        HookScope h("tc_split64", s);
+        tc_split64<<<(unsigned)((a.nP + 15) / 16), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, xh, xl, xn);
+        ++n;
+    }
+    if (!same) {
+        HookScope h("tc_split64", s);
+        tc_split64<<<(unsigned)((a.nQ + 15) / 16), 256, 0, s>>>(static_cast<const float*>(a.Q), a.nQ, yh, yl, yn);
+        ++n;
+    }
+    LseTcParams p;
+    p.N = a.nP;
+    p.M = a.nQ;
+    p.T = pl.T;
+    p.CT = pl.CT;
+    p.G = pl.G;
+    p.smax = pl.smax;
+    p.metric = a.metric;
+    p.apply_exp = a.apply_exp;
+    p.exclude_self = a.exclude_self;
+    p.scale = (float)a.scale;
+    p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
+    p.xn = xn;
+    p.yn = yn;
+    p.part = reinterpret_cast<float*>(ws + pl.off_part);
+    p.err = reinterpret_cast<int*>(ws + pl.off_err);
+    p.same = same ? 1 : 0;
+    auto go = [&](auto kernel) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        HookScope h("lse_fwd_tc", s);
+        kernel<<<pl.G, kTcThreadsF, kSmemBytes, s>>>(mxh, mxl, myh, myl, p);
+    };
+    const bool ex = a.apply_exp != 0;
+    if (a.metric == kLinear) ex ? go(lse_fwd_tc<kLinear, true>) : go(lse_fwd_tc<kLinear, false>);
+    else if (a.metric == kSqeuclidean) ex ? go(lse_fwd_tc<kSqeuclidean, true>) : go(lse_fwd_tc<kSqeuclidean, false>);
+    else ex ? go(lse_fwd_tc<kRbf, true>) : go(lse_fwd_tc<kRbf, false>);
+    ++n;
+    {
+        HookScope h("lse_tc_merge", s);
+        lse_tc_merge<<<(unsigned)((a.nP + 127) / 128), 128, 0, s>>>(p, static_cast<float*>(lse));
+        ++n;
+    }
+    return n;
+}
+
+size_t lse_bwd_tc_workspace(int64_t N) { return tc::lse_bwd_tc_plan(N).bytes; }
+
+// Tensor-core symmetric backward: writes the summed gradient (dX + dY) of the same points into a.gP.
+// `a` is the row-side sweep arguments (P = Q = z, lse, glse, metric, scale, exp, exclude_self).
+int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
+    using namespace tc;
+    const LseBwdTcPlan pl = lse_bwd_tc_plan(a.nP);
+    char* ws = static_cast<char*>(a.ws);
+    float* zh = reinterpret_cast<float*>(ws + pl.off_zh);
+    float* zl = reinterpret_cast<float*>(ws + pl.off_zl);
+    float* zn = reinterpret_cast<float*>(ws + pl.off_zn);
+    float* stat = reinterpret_cast<float*>(ws + pl.off_stat);
+    CUtensorMap mah, mal, mbh, mbl;
+    if (!make_map(&mah, zh, a.nP) || !make_map(&mal, zl, a.nP) || !make_map_rows(&mbh, zh, a.nP, kBNb) ||
+        !make_map_rows(&mbl, zl, a.nP, kBNb))
+        return -1;
+    int n = 0;
+    {
+        HookScope h("tc_split64", s);
+        tc_split64<<<(unsigned)((a.nP + 15) / 16), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, zh, zl, zn);
+        ++n;
+    }
+    {
+        HookScope h("lse_bwd_stats", s);
+        lse_bwd_stats<<<(unsigned)((pl.Npad + 255) / 256), 256, 0, s>>>(
+            static_cast<const float*>(a.lse), static_cast<const float*>(a.glse), a.nP, pl.Npad, stat);
+        ++n;
+    }
+    LseBwdTcParams p;
+    p.N = a.nP;
+    p.T = pl.T;
+    p.CT = pl.CT;
+    p.G = pl.G;
+    p.smax = pl.smax;
+    p.metric = a.metric;
+    p.apply_exp = a.apply_exp;
+    p.exclude_self = a.exclude_self;
+    p.scale = (float)a.scale;
+    p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
+    p.two_gamma = (float)(2.0 * a.gamma);
+    p.zn = zn;
+    p.lse2g = stat;
+    p.part = reinterpret_cast<float*>(ws + pl.off_part);
+    p.err = reinterpret_cast<int*>(ws + pl.off_err);
+    auto go = [&](auto kernel) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesB);
+        HookScope h("lse_bwd_sym_tc", s);
+        kernel<<<pl.G, kTcThreads, kSmemBytesB, s>>>(mah, mal, mbh, mbl, p);
+    };
+    const bool ex = a.apply_exp != 0;
+    if (a.metric == kLinear) ex ? go(lse_bwd_sym_tc<kLinear, true>) : go(lse_bwd_sym_tc<kLinear, false>);
+    else if (a.metric == kSqeuclidean) ex ? go(lse_bwd_sym_tc<kSqeuclidean, true>) : go(lse_bwd_sym_tc<kSqeuclidean, false>);
+    else ex ? go(lse_bwd_sym_tc<kRbf, true>) : go(lse_bwd_sym_tc<kRbf, false>);
+    ++n;
+    {
+        HookScope h("lse_bwd_tc_merge", s);
+        lse_bwd_tc_merge<<<(unsigned)((a.nP * 64 + 255) / 256), 256, 0, s>>>(p, static_cast<const float*>(a.P),
+                                                                             static_cast<float*>(a.gP));
+        ++n;
+    }
+    return n;
+}
+
+}  // namespace tp

@@ -67,8 +67,13 @@ def test_workspace_sizes_from_shapes(lib):
     assert ws(lib, "pairwise_matmul", pairs(), C=65) == big
     assert ws(lib, "no_such_entry", pairs()) == big
     assert ws(lib, "pairwise_matmul", pairs(D=65), C=4) == big
-    # fp64 partial states are twice the fp32 ones
-    assert ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 64, _lib.TP_F64)) >= 2 * a - 512
+    # fp64 partial states are twice the fp32 ones (D = 32: no tensor-core path)
+    a32 = ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 32))
+    assert ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 32, _lib.TP_F64)) >= 2 * a32 - 512
+    # fp32, D = 64: room for the tensor-core path's hi/lo split (512 bytes per distinct point)
+    assert a >= 2 * 8192 * 512
+    same = ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 64, X=FAKE, Y=FAKE))
+    assert 8192 * 512 <= same < a
 
 
 def call_matmul(lib, p, s, V=FAKE + 0x200000, C=4, out=FAKE + 0x300000, w=None, n=0):

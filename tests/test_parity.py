@@ -306,3 +306,27 @@ def test_deterministic_and_native(oracle):
     g2 = ops.pairwise_softmax_matmul_backward(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc), a, l, G)
     for k in ("dX", "dY", "dV"):
         assert torch.equal(g1[k], g2[k]), k
+
+
+@pytest.mark.parametrize("apply_exp", [False, True])
+@pytest.mark.parametrize("exclude_self", [False, True])
+@pytest.mark.parametrize("metric", ["sqeuclidean", "linear", "rbf"])
+@pytest.mark.parametrize("dt", [torch.float32, torch.float64])
+@pytest.mark.parametrize("ND", [(300, 16), (257, 64), (70, 3)])
+def test_logsumexp_same_points_symmetric(oracle, ND, dt, metric, exclude_self, apply_exp):
+    """X and Y the same points with no row/column parameters: libtp computes the summed gradient
+    dX + dY in one symmetric sweep; it must equal the oracle's row and column loops added."""
+    N, D = ND
+    X = gen(101, (N, D), dt)
+    scale = (-0.5 if metric == "sqeuclidean" else 0.5) / D ** 0.5 * (0.5 if apply_exp else 1.0)
+    sc = dict(metric=metric, gamma=0.5 / D, scale=scale if metric != "rbf" else 0.8, apply_exp=apply_exp)
+    gl = gen(102, (N,), dt)
+    Xd = X.to(DEV)
+    lse = ops.pairwise_logsumexp(Xd, Xd, gpu_score(sc), exclude_self)
+    g = ops.pairwise_logsumexp_backward(Xd, Xd, gpu_score(sc), lse, gl.to(DEV), exclude_self, same=True)
+    pb = oracle.Problem(X, X, **sc)
+    ol = oracle.logsumexp(pb, exclude_self)
+    og = oracle.logsumexp_backward(pb, ol, gl, exclude_self)
+    ftol, gtol = tols(dt)
+    assert_close(lse, ol, ftol, "lse", STRESS_FLOOR)
+    assert_close(g["dX"], og["dX"] + og["dY"], gtol, "dX + dY", STRESS_FLOOR)
