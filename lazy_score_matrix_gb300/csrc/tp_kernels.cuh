@@ -776,10 +776,15 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
 }
 
 // Sum the per-split partial states of a backward sweep (splits in ascending order) and finalise.
+// One thread per (feature, point), points fastest, so every partial-state read is coalesced; the
+// feature-0 thread of a point also writes its bias and weight gradients.
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 __global__ void __launch_bounds__(kThreads) bwd_merge(const SweepArgs a) {
-    const int64_t pi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (pi >= a.nP) return;
+    const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int F = DO_G && DO_V ? (a.D > a.C ? a.D : a.C) : (DO_G ? a.D : a.C);
+    if (e >= (int64_t)F * a.nP) return;
+    const int f = (int)(e / a.nP);
+    const int64_t pi = e - (int64_t)f * a.nP;
     const T* ws = static_cast<const T*>(a.ws);
     const int W = bwd_state_width<MODE, SIDE, DO_G, DO_V>(a.D, a.C);
     const int64_t ss = (int64_t)W * a.nP;
@@ -790,31 +795,26 @@ __global__ void __launch_bounds__(kThreads) bwd_merge(const SweepArgs a) {
     };
     int w = 0;
     if constexpr (DO_G) {
-        const T K0 = sum(a.D);
-        const T sumH = sum(a.D + 1);
-        const T sumHw = sum(a.D + 2);
-        const T sumS = (MODE == kBDisp && SIDE == kRow) ? sum(a.D + 3) : T(0);
-        if (a.gP) {
-            const T* P = static_cast<const T*>(a.P);
-            const T* dO = static_cast<const T*>(a.Vp);
-            T* g = static_cast<T*>(a.gP) + pi * a.D;
-            const bool dist = a.metric != kLinear;
-            for (int d = 0; d < a.D; ++d) {
-                T v = sum(d) - (dist ? P[pi * a.D + d] * K0 : T(0));
-                if (MODE == kBDisp && SIDE == kRow) v -= sumS * dO[pi * a.D + d];
-                if (MODE == kBDisp && SIDE == kCol) v += sum(a.D + 3 + d);
-                g[d] = a.accumulate ? g[d] + v : v;
+        if (f < a.D) {
+            if (a.gP) {
+                const T* P = static_cast<const T*>(a.P);
+                const T* dO = static_cast<const T*>(a.Vp);
+                const bool dist = a.metric != kLinear;
+                T v = sum(f) - (dist ? P[pi * a.D + f] * sum(a.D) : T(0));
+                if (MODE == kBDisp && SIDE == kRow) v -= sum(a.D + 3) * dO[pi * a.D + f];
+                if (MODE == kBDisp && SIDE == kCol) v += sum(a.D + 3 + f);
+                T* g = static_cast<T*>(a.gP) + pi * a.D + f;
+                *g = a.accumulate ? *g + v : v;
+            }
+            if (f == 0) {
+                if (a.gPb) static_cast<T*>(a.gPb)[pi] = sum(a.D + 1);
+                if (a.gPw) static_cast<T*>(a.gPw)[pi] = sum(a.D + 2);
             }
         }
-        if (a.gPb) static_cast<T*>(a.gPb)[pi] = sumH;
-        if (a.gPw) static_cast<T*>(a.gPw)[pi] = sumHw;
         w = a.D + 3 + (MODE == kBDisp ? (SIDE == kRow ? 1 : a.D) : 0);
     }
     if constexpr (DO_V) {
-        if (a.gV) {
-            T* gv = static_cast<T*>(a.gV) + pi * a.C;
-            for (int c = 0; c < a.C; ++c) gv[c] = sum(w + c);
-        }
+        if (a.gV && f < a.C) static_cast<T*>(a.gV)[pi * a.C + f] = sum(w + f);
     }
 }
 
@@ -1017,8 +1017,9 @@ void launch_bwd(const SweepArgs& a, cudaStream_t s) {
 }
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd_merge(const SweepArgs& a, cudaStream_t s) {
+    const int F = DO_G && DO_V ? (a.D > a.C ? a.D : a.C) : (DO_G ? a.D : a.C);
     HookScope h(kBwdMergeNames[MODE][SIDE], s);
-    bwd_merge<T, MODE, SIDE, DO_G, DO_V><<<row_grid(a.nP), kThreads, 0, s>>>(a);
+    bwd_merge<T, MODE, SIDE, DO_G, DO_V><<<row_grid((int64_t)F * a.nP), kThreads, 0, s>>>(a);
 }
 // rows: P = X, Q = Y; cols: P = Y, Q = X (parameters swapped). count/start/cursor/bucket come from
 // the workspace; count must be zero on entry.
