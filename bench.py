@@ -391,6 +391,20 @@ class Svgd(Workload):
 WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time (weak scaling: every rank runs its own replica)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gpairs(world: int, pairs: int, steps: int, seconds: float) -> float:
+    """Pairs processed by all ranks per second of the slowest rank, in Gpairs/s."""
+    return world * pairs * steps / seconds / 1e9
+
+
 def time_steps(fn, steps, flush):
     """Per-step CUDA events on the current stream; L2 flushed (untimed) before every step."""
     total = 0.0
@@ -436,9 +450,7 @@ def gpu_arm(args, rank, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     # end to end: host buffers, copies inside the timed region
     for _ in range(2):
         wl.e2e_step()
@@ -449,17 +461,13 @@ def gpu_arm(args, rank, world):
     for _ in range(args.steps):
         wl.e2e_step()
         torch.cuda.current_stream().synchronize()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     clocks.stop()
     if rank != 0:
         return None
     pk = peaks()
     ms_step = ms / args.steps
-    value = world * wl.pairs * args.steps / (ms / 1e3) / 1e9
+    value = whole_job_gpairs(world, wl.pairs, args.steps, ms / 1e3)
     ksum = timer.summary()
     dom = max(ksum.items(), key=lambda kv: kv[1]["total_ms"])
     dname, dstat = dom
@@ -496,7 +504,7 @@ def gpu_arm(args, rank, world):
                         "share": round(v["total_ms"] / sum(x["total_ms"] for x in ksum.values()), 4)}
                     for k, v in sorted(ksum.items(), key=lambda kv: -kv[1]["total_ms"])},
         "gpu_launches": launches,
-        "e2e": {"value": round(world * wl.pairs * args.steps / e2e_s / 1e9, 4), "unit": "Gpairs/s",
+        "e2e": {"value": round(whole_job_gpairs(world, wl.pairs, args.steps, e2e_s), 4), "unit": "Gpairs/s",
                 "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h},
         "clocks": clocks.result(),
     }

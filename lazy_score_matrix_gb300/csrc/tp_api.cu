@@ -25,6 +25,8 @@ size_t lse_tc_workspace(int64_t N, int64_t M, bool same);                  // tp
 int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s);  // tp_tc_lse.cu
 size_t lse_bwd_tc_workspace(int64_t N);                                       // tp_tc_lse.cu
 int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s);                // tp_tc_lse.cu
+size_t topk_tc_workspace(int64_t N, int64_t M, int D, int k, bool same);                        // tp_tc_topk.cu
+int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same, cudaStream_t s);  // tp_tc_topk.cu
 }  // namespace tp
 
 namespace {
@@ -182,14 +184,22 @@ bool force_simt() {
     return v;
 }
 
-// The tensor-core symmetric backward stays off until its TMEM-operand MMA layout is validated.
+// The tensor-core symmetric backward (fp32, D = 64, X = Y, no row/column parameters) and the
+// tensor-core top-k are switched on once their parity tests pass on the GPU.
 constexpr bool kTcBackward = false;
+constexpr bool kTcTopk = false;
 
 // The tensor-core log-sum-exp covers fp32, D = 64, no row/column parameters, 16-byte aligned points.
 bool lse_tc_shape(const tp_pairs* p) { return p->dtype == TP_F32 && p->D == 64; }
 bool lse_tc_eligible(const tp_pairs* p, const tp_score* s) {
     return !force_simt() && lse_tc_shape(p) && !s->row_bias && !s->col_bias && !s->row_weight && !s->col_weight &&
            aligned(p->X, 16) && aligned(p->Y, 16);
+}
+
+// The tensor-core top-k covers fp32, D <= 64, k <= 32, no row/column parameters.
+bool topk_tc_shape(const tp_pairs* p, int k) { return p->dtype == TP_F32 && p->D <= 64 && k >= 1 && k <= kTopkMax; }
+bool topk_tc_eligible(const tp_pairs* p, const tp_score* s, int k) {
+    return kTcTopk && !force_simt() && topk_tc_shape(p, k) && !s->row_bias && !s->col_bias && !s->row_weight && !s->col_weight;
 }
 
 tp_status launched(int n) {
@@ -325,7 +335,8 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     if (e == "pairwise_topk") {
         if (k < 1 || k > p->M || k > kTopkMax) return (size_t)-1;
         const int K = topk_bucket(k);
-        return r.splits > 1 ? align_up((size_t)r.splits * K * r.nP * (es + 4)) : 0;
+        const size_t simt = r.splits > 1 ? align_up((size_t)r.splits * K * r.nP * (es + 4)) : 0;
+        return kTcTopk && topk_tc_shape(p, k) ? std::max(simt, topk_tc_workspace(p->N, p->M, D, k, p->X == p->Y)) : simt;
     }
     if (e == "pairwise_matmul_backward") return bwd_ws(p, kBMatmul, C, 0);
     if (e == "pairwise_softmax_matmul_backward") return bwd_ws(p, kBSoftmax, C, align_up(p->N * es));
@@ -660,6 +671,11 @@ tp_status tp_pairwise_topk(const tp_pairs* pr, const tp_score* sc, int k, int la
     a.out2 = indices;
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (topk_tc_eligible(pr, sc, k)) {
+        const int n = launch_topk_tc(a, values, indices, pr->X == pr->Y, st);
+        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        return launched(n);
+    }
     return by_dtype(pr->dtype, [&](auto t) {
         using T = decltype(t);
         int n = 1;

@@ -359,48 +359,6 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const SweepArgs a) {
 // top-k (k smallest keys; key = S, or -S for largest), exact (value, index) order
 // ------------------------------------------------------------------------------------------------
 
-// Insert (key, idx) into the sorted list when it beats the last entry. Entries of equal key keep
-// their order, so streaming indices in ascending order gives ascending indices among ties.
-template <class T, int K>
-__device__ __forceinline__ void topk_insert(T (&kv)[K], int (&ki)[K], T key, int idx) {
-    if (!(key < kv[K - 1])) return;
-    bool placed = false;
-#pragma unroll
-    for (int t = K - 1; t > 0; --t) {
-        const bool shift = kv[t - 1] > key;
-        if (!placed) {
-            kv[t] = shift ? kv[t - 1] : key;
-            ki[t] = shift ? ki[t - 1] : idx;
-            placed = !shift;
-        }
-    }
-    if (!placed) {
-        kv[0] = key;
-        ki[0] = idx;
-    }
-}
-
-// Lexicographic (key, index) insertion, used where candidates arrive out of index order.
-template <class T, int K>
-__device__ __forceinline__ void topk_insert_lex(T (&kv)[K], int (&ki)[K], T key, int idx) {
-    auto less = [](T av, int ai, T bv, int bi) { return av < bv || (av == bv && ai < bi); };
-    if (!less(key, idx, kv[K - 1], ki[K - 1])) return;
-    bool placed = false;
-#pragma unroll
-    for (int t = K - 1; t > 0; --t) {
-        const bool shift = less(key, idx, kv[t - 1], ki[t - 1]);
-        if (!placed) {
-            kv[t] = shift ? kv[t - 1] : key;
-            ki[t] = shift ? ki[t - 1] : idx;
-            placed = !shift;
-        }
-    }
-    if (!placed) {
-        kv[0] = key;
-        ki[0] = idx;
-    }
-}
-
 constexpr int kNoIndex = 0x7fffffff;
 
 template <class T, int DP, int K, bool AFFINE>

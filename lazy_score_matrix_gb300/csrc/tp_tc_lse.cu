@@ -27,6 +27,7 @@
 #include "tp_device.cuh"
 #include "tp_launch.h"
 #include "tp_tc.cuh"
+#include "tp_tc_host.h"
 
 namespace tp {
 namespace tc {
@@ -37,7 +38,7 @@ constexpr int kChunk = kBM * 128;            // one 128-row x 32-fp32 swizzled c
 constexpr int kOperand = 2 * kChunk;         // 64 features: two chunks, 32 KB
 constexpr int kPair = 2 * kOperand;          // hi + lo: 64 KB
 constexpr int kStages = 2;
-constexpr int kTcThreads = 192;      // backward kernel: producer, MMA, 4 epilogue warps
+constexpr int kTcThreads = 320;      // backward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
 constexpr int kTcThreadsF = 320;     // forward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
 constexpr int kTmemCols = 256;
 constexpr int kGrid = 152;                   // persistent CTAs: one per GB300 SM
@@ -330,18 +331,23 @@ __global__ void tc_split64(const float* __restrict__ x, int64_t n, float* __rest
 //
 // Per 64-column tile: S = Zrows Ztile^T (tf32 hi/lo, 3 products) into TMEM; the epilogue turns S
 // into kappa, splits it hi/lo and stores it back into TMEM; then dZ += kappa_hi Zh + kappa_hi Zl +
-// kappa_lo Zh, with kappa as the A operand read from TMEM and the same staged tile as an MN-major B
-// operand. dZ (128 x 64) accumulates in TMEM over the CTA's tiles of a row block and is written as a
-// partial; a merge kernel adds the partials of each row in CTA order.
+// kappa_lo Zh, with kappa as the A operand read from TMEM and the tile's feature-major copy (from a
+// transposed hi/lo copy of z made by the pre-pass) as a K-major B operand. Each tile's dZ (128 x 64)
+// lands in its own (double-buffered) TMEM block and the epilogue adds it into a per-row register
+// accumulator: the tensor core's accumulation then never spans more than one tile (long accumulation
+// chains in TMEM drift), and the rows' sums are two-level like everywhere else. At the end of the
+// CTA's share of a row block the accumulator is written as a partial; a merge kernel adds the
+// partials of each row in CTA order.
 // ------------------------------------------------------------------------------------------------
 
 constexpr int kBNb = 64;                   // columns per backward tile
 constexpr int kChunkB = kBNb * 128;        // 64-row x 32-fp32 chunk: 8 KB
 constexpr int kOperandB = 2 * kChunkB;     // 16 KB
 constexpr int kPairB = 2 * kOperandB;      // hi + lo: 32 KB
-constexpr int kStagesB = 4;
-constexpr int kTmemColsB = 512;            // S/kappa_hi x2 (64 each), kappa_lo x2, dZ (64)
-constexpr size_t kSmemBytesB = (size_t)kPair + (size_t)kPairB * kStagesB + (size_t)kStagesB * kBNb * 8 + 256 + 1024;
+constexpr int kStagesB = 2;
+constexpr int kStageBytesB = 2 * kPairB;   // point-major tile (hi, lo) + feature-major tile (hi, lo)
+constexpr int kTmemColsB = 512;            // S/kappa_hi x2 (64 each), kappa_lo x2, dZ x2
+constexpr size_t kSmemBytesB = (size_t)kPair + (size_t)kStageBytesB * kStagesB + (size_t)kStagesB * kBNb * 8 + 256 + 1024;
 
 struct LseBwdTcParams {
     int64_t N;
@@ -351,7 +357,7 @@ struct LseBwdTcParams {
     float scale, neg_gamma_log2, two_gamma;
     const float* zn;      // |z_k|^2
     const float* lse2g;   // [ceil(N/64)*64][2]: (lse_j * log2 e, g_j), padded with (+inf, 0)
-    float* part;          // [G][smax][65][128]: dZ columns then sum of kappa, row-minor
+    float* part;          // [G][smax][66][128]: dZ features, then the two halves' sums of kappa, row-minor
     int* err;
 };
 
@@ -359,23 +365,24 @@ template <int METRIC, bool EXP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     lse_bwd_sym_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
                    const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
+                   const __grid_constant__ CUtensorMap mTh, const __grid_constant__ CUtensorMap mTl,
                    const LseBwdTcParams p) {
     constexpr float kL2E = 1.4426950408889634f;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                    // row block: hi (2 chunks) | lo (2 chunks)
-    unsigned char* sB = sm + kPair;                            // stage s at sB + s * kPairB
-    float* sStat = reinterpret_cast<float*>(sB + kPairB * kStagesB);  // [stage][64][2]
+    unsigned char* sB = sm + kPair;  // stage s at sB + s * kStageBytesB: [Zh | Zl | ZTh | ZTl]
+    float* sStat = reinterpret_cast<float*>(sB + kStageBytesB * kStagesB);  // [stage][64][2]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStagesB * kBNb * 2);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
-    uint64_t* b_full = bars + 2;    // [4]
-    uint64_t* b_empty = bars + 6;   // [4]
-    uint64_t* s_full = bars + 10;   // [2]
-    uint64_t* w_full = bars + 12;   // [2]
-    uint64_t* dz_full = bars + 14;
-    uint64_t* dz_empty = bars + 15;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+    uint64_t* b_full = bars + 2;    // [kStagesB]
+    uint64_t* b_empty = bars + 4;   // [kStagesB]
+    uint64_t* s_full = bars + 6;    // [2]
+    uint64_t* w_full = bars + 8;    // [2]
+    uint64_t* dz_full = bars + 10;  // [2]
+    uint64_t* dz_empty = bars + 12; // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
@@ -390,10 +397,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + b, 1);
-            mbar_init(w_full + b, 128);
+            mbar_init(w_full + b, 256);
+            mbar_init(dz_full + b, 1);
+            mbar_init(dz_empty + b, 256);
         }
-        mbar_init(dz_full, 1);
-        mbar_init(dz_empty, 128);
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tslot, kTmemColsB);
@@ -424,51 +431,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int s = (int)(i % kStagesB), r = (int)(i / kStagesB);
                 if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 22);
                 if (!ok) break;
-                unsigned char* dst = sB + s * kPairB;
-                mbar_expect_tx(b_full + s, kPairB + kBNb * 8);
+                unsigned char* dst = sB + s * kStageBytesB;
+                mbar_expect_tx(b_full + s, kStageBytesB + kBNb * 8);
                 tma_load_2d(dst, &mBh, 0, ct * kBNb, b_full + s);
                 tma_load_2d(dst + kChunkB, &mBh, 32, ct * kBNb, b_full + s);
                 tma_load_2d(dst + kOperandB, &mBl, 0, ct * kBNb, b_full + s);
                 tma_load_2d(dst + kOperandB + kChunkB, &mBl, 32, ct * kBNb, b_full + s);
+                // feature-major copy: 64 feature rows x 32 points per chunk
+                unsigned char* dT = dst + kPairB;
+                tma_load_2d(dT, &mTh, ct * kBNb, 0, b_full + s);
+                tma_load_2d(dT + kChunkB, &mTh, ct * kBNb + 32, 0, b_full + s);
+                tma_load_2d(dT + kOperandB, &mTl, ct * kBNb, 0, b_full + s);
+                tma_load_2d(dT + kOperandB + kChunkB, &mTl, ct * kBNb + 32, 0, b_full + s);
                 bulk_load(sStat + s * kBNb * 2, p.lse2g + (size_t)ct * kBNb * 2, kBNb * 8, b_full + s);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idS = idesc_tf32(kBM, kBNb);       // S: M 128, N 64 (K = 64 features)
-            constexpr uint32_t idZ = idesc_tf32_bmn(kBM, 64);      // dZ: M 128, N 64 features, K = 64 points
-            int a_uses = 0, dz_uses = 0;
+            constexpr uint32_t idZ = idesc_tf32(kBM, 64);          // dZ: M 128, N 64 features, K = 64 points
+            int a_uses = 0;
             bool ok = true;
-            // dZ for tile i (already in TMEM as kappa): issue after its epilogue is done
+            // dZ for tile i (kappa already in TMEM): issue once its epilogue is done, into the dZ buffer
+            // the epilogue drained two tiles ago
             auto issue_dz = [&](int64_t i) -> bool {
-                const int64_t t = t_begin + i;
                 const int b = (int)(i & 1), s = (int)(i % kStagesB);
                 if (!mbar_wait(w_full + b, (uint32_t)((i >> 1) & 1), p.err, 25)) return false;
+                if (i >= 2 && !mbar_wait(dz_empty + b, (uint32_t)(((i >> 1) - 1) & 1), p.err, 26)) return false;
                 fence_after_sync();
-                const bool first = (i == 0) || rb_of(t - 1) != rb_of(t);
-                const bool last = (t + 1 == t_end) || rb_of(t + 1) != rb_of(t);
-                if (first && dz_uses > 0 && !mbar_wait(dz_empty, (dz_uses - 1) & 1, p.err, 26)) return false;
-                const uint32_t bz = smem_u32(sB + s * kPairB);
+                const uint32_t bz = smem_u32(sB + s * kStageBytesB + kPairB);  // feature-major tile
                 const uint32_t kh = tS + (uint32_t)(b * kBNb), kl = tLo + (uint32_t)(b * kBNb);
-                // kappa_hi Zh + kappa_hi Zl + kappa_lo Zh, K = 64 points in steps of 8 (1024-byte atoms)
+                const uint32_t dz = tDZ + (uint32_t)(b * 64);
+                // kappa_hi ZTh + kappa_hi ZTl + kappa_lo ZTh, K = 64 points in steps of 8 (32 bytes)
                 const uint32_t ka[3] = {kh, kh, kl};
                 const uint32_t zb[3] = {0u, (uint32_t)kOperandB, 0u};
-                uint32_t acc = first ? 0u : 1u;
+                uint32_t acc = 0;
 #pragma unroll
                 for (int prod = 0; prod < 3; ++prod) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        mma_tf32_ta(tDZ, ka[prod] + (uint32_t)(ks * 8),
-                                    desc_mnmajor_sw128(bz + zb[prod] + (uint32_t)(ks * 1024), (uint32_t)kChunkB), idZ,
-                                    acc);
+                        const uint32_t kb = (uint32_t)((ks >> 2) * kChunkB + (ks & 3) * 32);
+                        mma_tf32_ta(dz, ka[prod] + (uint32_t)(ks * 8), desc_kmajor_sw128(bz + zb[prod] + kb), idZ, acc);
                         acc = 1;
                     }
                 }
                 mma_commit(b_empty + s);
-                if (last) {
-                    mma_commit(dz_full);
-                    ++dz_uses;
-                }
+                mma_commit(dz_full + b);
                 return true;
             };
             int rb_cur = -1;
@@ -486,7 +494,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = mbar_wait(b_full + s, r & 1, p.err, 24);
                 if (!ok) break;
                 fence_after_sync();
-                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kPairB);
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kStageBytesB);
                 const uint32_t ao[3] = {0u, 0u, (uint32_t)kOperand};
                 const uint32_t bo[3] = {0u, (uint32_t)kOperandB, 0u};
                 uint32_t acc = 0;
@@ -506,41 +514,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (ok && t_end > t_begin) issue_dz(t_end - t_begin - 1);
         }
-    } else {  // ---------------- epilogue: warps 2..5
+    } else {  // ---------------- epilogue: warps 2..9, two per TMEM lane quarter
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;  // tile columns [32 half, 32 half + 32), dZ features likewise
         const int lr = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        int seg = 0, dz_uses = 0;
+        int seg = 0;
         float K0 = 0.f, lse2k = 0.f, gk = 0.f, zn_k = 0.f;
-        bool ok = true;
-        auto readout = [&](int rb) -> bool {  // dZ of the finished row-block segment -> partial
-            if (!mbar_wait(dz_full, dz_uses & 1, p.err, 27)) return false;
-            ++dz_uses;
-            fence_after_sync();
-            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * 65 * kBM;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(tDZ + lane_off + (uint32_t)(c * 32), v);
+        float dacc[32];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) o[(size_t)(c * 32 + u) * kBM + lr] = v[u];
-            }
-            o[(size_t)64 * kBM + lr] = K0;
+        for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
+        bool ok = true;
+        auto drain = [&](int64_t j) -> bool {  // add this half of tile j's dZ block into the row accumulator
+            const int b = (int)(j & 1);
+            if (!mbar_wait(dz_full + b, (uint32_t)((j >> 1) & 1), p.err, 27)) return false;
+            fence_after_sync();
+            float v[32];
+            tmem_ld32(tDZ + lane_off + (uint32_t)(b * 64 + half * 32), v);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) dacc[u] += v[u];
             fence_before_sync();
-            mbar_arrive(dz_empty);
-            ++seg;
+            mbar_arrive(dz_empty + b);
             return true;
         };
+        auto write_partial = [&]() {
+            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * 66 * kBM;
+#pragma unroll
+            for (int f = 0; f < 32; ++f) o[(size_t)(half * 32 + f) * kBM + lr] = dacc[f];
+            o[(size_t)(64 + half) * kBM + lr] = K0;
+            ++seg;
+        };
         int rb_cur = -1;
+        int64_t pending = -1;
         for (int64_t t = t_begin; t < t_end && ok; ++t) {
             const int64_t i = t - t_begin;
             const int rb = rb_of(t), ct = (int)(t % p.CT);
             const int64_t row = (int64_t)rb * kBM + lr;
             if (rb != rb_cur) {
-                if (rb_cur >= 0) ok = readout(rb_cur);
-                if (!ok) break;
+                if (pending >= 0) {
+                    ok = drain(pending);
+                    pending = -1;
+                    if (!ok) break;
+                }
+                if (rb_cur >= 0) write_partial();
                 rb_cur = rb;
                 K0 = 0.f;
+#pragma unroll
+                for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
                 const bool live = row < p.N;
                 lse2k = live ? p.lse2g[2 * row] : __int_as_float(0x7f800000);
                 gk = live ? p.lse2g[2 * row + 1] : 0.f;
@@ -550,19 +570,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = mbar_wait(s_full + b, (uint32_t)((i >> 1) & 1), p.err, 28);
             if (!ok) break;
             fence_after_sync();
-            const int64_t j0 = (int64_t)ct * kBNb;
-            const float* st = sStat + s * kBNb * 2;
+            const int64_t j0 = (int64_t)ct * kBNb + half * 32;
+            const float* st = sStat + s * kBNb * 2 + half * 64;
             float ksum = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            {
                 float v[32];
-                tmem_ld32(tS + lane_off + (uint32_t)(b * kBNb + c * 32), v);
+                const uint32_t col = (uint32_t)(b * kBNb + half * 32);
+                tmem_ld32(tS + lane_off + col, v);
                 float lo[32];
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
-                    const int64_t j = j0 + c * 32 + u;
-                    const float2 lg = reinterpret_cast<const float2*>(st)[c * 32 + u];
-                    const float dot = v[u];
+                    const int64_t j = j0 + u;
+                    const float2 lg = reinterpret_cast<const float2*>(st)[u];
+                    float dot = v[u];
+                    if (METRIC != kLinear && j == row) dot = zn_k;  // |z - z|^2 = 0 exactly
                     float base;
                     if (METRIC == kLinear) {
                         base = dot;
@@ -584,15 +605,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     lo[u] = kap - hi;
                     v[u] = hi;
                 }
-                tmem_st32(tS + lane_off + (uint32_t)(b * kBNb + c * 32), v);
-                tmem_st32(tLo + lane_off + (uint32_t)(b * kBNb + c * 32), lo);
+                tmem_st32(tS + lane_off + col, v);
+                tmem_st32(tLo + lane_off + col, lo);
             }
             K0 += ksum;
             tmem_st_wait();
             fence_before_sync();
             mbar_arrive(w_full + b);
+            if (pending >= 0) {
+                ok = drain(pending);
+                if (!ok) break;
+            }
+            pending = i;
         }
-        if (ok && rb_cur >= 0) readout(rb_cur);
+        if (ok && pending >= 0) ok = drain(pending);
+        if (ok && rb_cur >= 0) write_partial();
     }
 
     fence_before_sync();
@@ -621,11 +648,35 @@ __global__ void lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z, 
     float dz = 0.f, k0 = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-        const float* o = p.part + (size_t)(c * p.smax + seg) * 65 * kBM;
+        const float* o = p.part + (size_t)(c * p.smax + seg) * 66 * kBM;
         dz += o[(size_t)f * kBM + lr];
-        k0 += o[(size_t)64 * kBM + lr];
+        k0 += o[(size_t)64 * kBM + lr] + o[(size_t)65 * kBM + lr];
     }
     grad[e] = p.metric == kLinear ? dz : dz - z[e] * k0;
+}
+
+// Feature-major copies of the hi/lo arrays: t[f][j] = a[j][f] for j < N, 0 for N <= j < Npad.
+// 32 x 32 tiles through shared memory (block 32 x 8).
+__global__ void tc_transpose64(const float* __restrict__ hi, const float* __restrict__ lo, int64_t N, int64_t Npad,
+                               float* __restrict__ thi, float* __restrict__ tlo) {
+    __shared__ float th[32][33], tl[32][33];
+    const int64_t j0 = (int64_t)blockIdx.x * 32;
+    const int f0 = blockIdx.y * 32;
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int64_t j = j0 + r;
+        const bool live = j < N;
+        th[r][threadIdx.x] = live ? hi[j * 64 + f0 + threadIdx.x] : 0.f;
+        tl[r][threadIdx.x] = live ? lo[j * 64 + f0 + threadIdx.x] : 0.f;
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int f = f0 + r;
+        const int64_t j = j0 + threadIdx.x;
+        if (j < Npad) {
+            thi[(int64_t)f * Npad + j] = th[threadIdx.x][r];
+            tlo[(int64_t)f * Npad + j] = tl[threadIdx.x][r];
+        }
+    }
 }
 
 // (lse_j log2 e, g_j) pairs, padded to a multiple of 64 rows with (+inf, 0)
@@ -642,44 +693,12 @@ __global__ void lse_bwd_stats(const float* __restrict__ lse, const float* __rest
 // host side
 // ------------------------------------------------------------------------------------------------
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &f, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// [rows, 64] fp32, box 32 x box_rows, 128-byte swizzle; rows past the end read as zeros
-static bool make_map_rows(CUtensorMap* m, const float* base, int64_t rows, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {64 * sizeof(float)};
-    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-static bool make_map(CUtensorMap* m, const float* base, int64_t rows) { return make_map_rows(m, base, rows, kBM); }
-
 struct LseTcPlan {
     int64_t T;
     int CT, G, smax;
     size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_part, off_err, bytes;
 };
 
-static size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
     LseTcPlan pl;
@@ -712,7 +731,7 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
 struct LseBwdTcPlan {
     int64_t T, Npad;
     int CT, G, smax;
-    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_err, bytes;
+    size_t off_zh, off_zl, off_zth, off_ztl, off_zn, off_stat, off_part, off_err, bytes;
 };
 
 static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
@@ -727,9 +746,11 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     size_t o = 0;
     pl.off_zh = o; o += al256((size_t)N * 64 * 4);
     pl.off_zl = o; o += al256((size_t)N * 64 * 4);
+    pl.off_zth = o; o += al256((size_t)pl.Npad * 64 * 4);
+    pl.off_ztl = o; o += al256((size_t)pl.Npad * 64 * 4);
     pl.off_zn = o; o += al256((size_t)N * 4);
     pl.off_stat = o; o += al256((size_t)pl.Npad * 8);
-    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 65 * kBM * 4);
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 66 * kBM * 4);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -811,16 +832,23 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     char* ws = static_cast<char*>(a.ws);
     float* zh = reinterpret_cast<float*>(ws + pl.off_zh);
     float* zl = reinterpret_cast<float*>(ws + pl.off_zl);
+    float* zth = reinterpret_cast<float*>(ws + pl.off_zth);
+    float* ztl = reinterpret_cast<float*>(ws + pl.off_ztl);
     float* zn = reinterpret_cast<float*>(ws + pl.off_zn);
     float* stat = reinterpret_cast<float*>(ws + pl.off_stat);
-    CUtensorMap mah, mal, mbh, mbl;
+    CUtensorMap mah, mal, mbh, mbl, mth, mtl;
     if (!make_map(&mah, zh, a.nP) || !make_map(&mal, zl, a.nP) || !make_map_rows(&mbh, zh, a.nP, kBNb) ||
-        !make_map_rows(&mbl, zl, a.nP, kBNb))
+        !make_map_rows(&mbl, zl, a.nP, kBNb) || !make_map_t(&mth, zth, pl.Npad) || !make_map_t(&mtl, ztl, pl.Npad))
         return -1;
     int n = 0;
     {
         HookScope h("tc_split64", s);
         tc_split64<<<(unsigned)((a.nP + 15) / 16), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, zh, zl, zn);
+        ++n;
+    }
+    {
+        HookScope h("tc_transpose64", s);
+        tc_transpose64<<<dim3((unsigned)(pl.Npad / 32), 2), dim3(32, 8), 0, s>>>(zh, zl, a.nP, pl.Npad, zth, ztl);
         ++n;
     }
     {
@@ -848,7 +876,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesB);
         HookScope h("lse_bwd_sym_tc", s);
-        kernel<<<pl.G, kTcThreads, kSmemBytesB, s>>>(mah, mal, mbh, mbl, p);
+        kernel<<<pl.G, kTcThreads, kSmemBytesB, s>>>(mah, mal, mbh, mbl, mth, mtl, p);
     };
     const bool ex = a.apply_exp != 0;
     if (a.metric == kLinear) ex ? go(lse_bwd_sym_tc<kLinear, true>) : go(lse_bwd_sym_tc<kLinear, false>);

@@ -1,0 +1,439 @@
+// Row top-k on the Blackwell tensor cores (fp32 data, D <= 64, no row/column parameters): torchpairwise
+// guide "Using Torchpairwise in Models", Task Map (k-NN / retrieval row: lazy(X, R, "sqeuclidean")
+// .topk(k, largest=False), fused, exact tie order; argmin and min are k = 1).
+//
+// The contraction X R^T runs on tcgen05.mma kind::tf32 with the hi/lo split of both operands (three
+// products); points whose coordinates are exact in tf32 (integers up to 2^11, for instance) have lo = 0,
+// so their dot products, norms and distances are exact and the selection is bit-identical to an exact
+// evaluation. The 128 x 128 score tile lands in TMEM; eight epilogue warps (two per TMEM lane quarter,
+// each owning half of the tile's columns) turn each dot product into the score and keep a sorted
+// (value, index) list per row in registers, inserting only on a strict improvement, so equal values
+// keep ascending index order. The lists of the two halves and of every CTA that saw part of a row are
+// merged lexicographically on (value, index) by a second kernel: the result is unique.
+//
+// Schedule and warp roles as in the log-sum-exp kernel: persistent CTAs over contiguous ranges of
+// (row block, column tile) pairs; warp 0 loads with TMA, warp 1 issues the MMAs, warps 2..9 select.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "tp_args.h"
+#include "tp_device.cuh"
+#include "tp_launch.h"
+#include "tp_tc.cuh"
+#include "tp_tc_host.h"
+
+namespace tp {
+namespace tc {
+
+constexpr int kKBM = 128, kKBN = 128;
+constexpr int kKThreads = 320;
+constexpr int kKGrid = 152;
+
+template <int DP>
+struct TopkTcShape {
+    static constexpr int kChunks = DP / 32;                 // 128-byte K chunks per operand
+    static constexpr int kOperand = kChunks * 128 * 128;    // 128 rows x DP fp32
+    static constexpr int kPair = 2 * kOperand;              // hi + lo
+    static constexpr int kStages = DP == 32 ? 4 : 2;
+    static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + 256 + 1024;
+};
+
+struct TopkTcParams {
+    int64_t N, M, T;
+    int CT, G, smax, k;
+    int metric, apply_exp, largest;
+    float scale, neg_gamma_log2;
+    const float* xn;
+    const float* yn;   // padded to CT * 128 entries
+    float* pv;         // [G][smax][2 halves][K][128] keys
+    int* pi;           // same layout, column indices
+    int* err;
+};
+
+template <int METRIC, bool EXP>
+__device__ __forceinline__ float topk_score(float dot, float xn, float yn, float scale, float ngl2) {
+    float base;
+    if (METRIC == kLinear) {
+        base = dot;
+    } else {
+        const float d2 = fmaxf(fmaf(-2.f, dot, xn + yn), 0.f);
+        base = METRIC == kRbf ? ExpTraits<float>::bexp(ngl2 * d2) : d2;
+    }
+    const float t = scale * base;
+    return EXP ? ExpTraits<float>::bexp(t * 1.4426950408889634f) : t;
+}
+
+template <int DP, int K, int METRIC, bool EXP>
+__global__ void __launch_bounds__(kKThreads, 1)
+    topk_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
+            const __grid_constant__ CUtensorMap mYh, const __grid_constant__ CUtensorMap mYl, const TopkTcParams p) {
+    using SH = TopkTcShape<DP>;
+    constexpr int kChunk = 128 * 128;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = sm;
+    unsigned char* sB = sm + SH::kPair;
+    float* sYn = reinterpret_cast<float*>(sB + (size_t)SH::kPair * SH::kStages);  // [stage][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sYn + SH::kStages * kKBN);
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* b_full = bars + 2;               // [kStages]
+    uint64_t* b_empty = bars + 2 + SH::kStages;
+    uint64_t* acc_full = bars + 2 + 2 * SH::kStages;   // [2]
+    uint64_t* acc_empty = acc_full + 2;                // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = (p.T * blockIdx.x) / p.G, t_end = (p.T * (blockIdx.x + 1)) / p.G;
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < SH::kStages; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(b_empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 256);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, 256);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 31);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, SH::kPair);
+                    for (int c = 0; c < SH::kChunks; ++c) {
+                        tma_load_2d(sA + c * kChunk, &mXh, c * 32, rb * kKBM, a_full);
+                        tma_load_2d(sA + SH::kOperand + c * kChunk, &mXl, c * 32, rb * kKBM, a_full);
+                    }
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages);
+                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 32);
+                if (!ok) break;
+                unsigned char* dst = sB + (size_t)s * SH::kPair;
+                mbar_expect_tx(b_full + s, SH::kPair + kKBN * 4);
+                for (int c = 0; c < SH::kChunks; ++c) {
+                    tma_load_2d(dst + c * kChunk, &mYh, c * 32, ct * kKBN, b_full + s);
+                    tma_load_2d(dst + SH::kOperand + c * kChunk, &mYl, c * 32, ct * kKBN, b_full + s);
+                }
+                bulk_load(sYn + s * kKBN, p.yn + (size_t)ct * kKBN, kKBN * 4, b_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_tf32(kKBM, kKBN);
+            constexpr int KS = DP / 8;
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+                const int64_t i = t - t_begin;
+                const int rb = (int)(t / p.CT);
+                if (rb != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);
+                    ok = mbar_wait(a_full, a_uses & 1, p.err, 33);
+                    if (!ok) break;
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages), b = (int)(i & 1), rr = (int)(i >> 1);
+                ok = mbar_wait(b_full + s, r & 1, p.err, 34);
+                if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 35);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(b * kKBN);
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * SH::kPair);
+                const uint32_t ao[3] = {0u, 0u, (uint32_t)SH::kOperand};
+                const uint32_t bo[3] = {0u, (uint32_t)SH::kOperand, 0u};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int prod = 0; prod < 3; ++prod) {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const uint32_t koff = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
+                        mma_tf32(d, desc_kmajor_sw128(a0 + ao[prod] + koff), desc_kmajor_sw128(b0 + bo[prod] + koff),
+                                 idesc, acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(b_empty + s);
+                mma_commit(acc_full + b);
+            }
+        }
+    } else {  // ---------------- selection: warps 2..9, one row per thread, half of each tile
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int lr = q * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        const float sgn = p.largest ? -1.f : 1.f;
+        float kv[K];
+        int ki[K];
+        int rb_cur = -1, seg = 0;
+        float xn = 0.f;
+        bool ok = true;
+        auto reset = [&]() {
+#pragma unroll
+            for (int t = 0; t < K; ++t) {
+                kv[t] = pinf<float>();
+                ki[t] = 0x7fffffff;
+            }
+        };
+        auto flush = [&]() {
+            const size_t base = (((size_t)blockIdx.x * p.smax + seg) * 2 + half) * K * kKBM;
+#pragma unroll
+            for (int t = 0; t < K; ++t) {
+                p.pv[base + (size_t)t * kKBM + lr] = kv[t];
+                p.pi[base + (size_t)t * kKBM + lr] = ki[t];
+            }
+            ++seg;
+        };
+        reset();
+        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            const int64_t i = t - t_begin;
+            const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+            if (rb != rb_cur) {
+                if (rb_cur >= 0) flush();
+                reset();
+                rb_cur = rb;
+                const int64_t row = (int64_t)rb * kKBM + lr;
+                xn = (METRIC != kLinear && row < p.N) ? p.xn[row] : 0.f;
+            }
+            const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
+            ok = mbar_wait(acc_full + b, rr & 1, p.err, 36);
+            if (!ok) break;
+            fence_after_sync();
+            const int j0 = ct * kKBN + half * 64;
+            const int lim = (int)(p.M - j0 < 64 ? p.M - j0 : 64);  // valid columns of this half
+            const float* yn = sYn + s * kKBN + half * 64;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                float v[32];
+                tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int cu = c * 32 + u;
+                    const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yn[cu], p.scale, p.neg_gamma_log2);
+                    if (cu < lim && key < kv[K - 1]) topk_insert<float, K>(kv, ki, key, j0 + cu);
+                }
+            }
+            fence_before_sync();
+            mbar_arrive(acc_empty + b);
+        }
+        if (ok && rb_cur >= 0) flush();
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// Per row: the lists of every (CTA, half) that saw part of it, merged on (key, index).
+template <int K>
+__global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_t* __restrict__ indices) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.N) return;
+    const int rb = (int)(i / kKBM), lr = (int)(i % kKBM);
+    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
+    auto start = [&](int c) { return (p.T * c) / p.G; };
+    auto cta_of = [&](int64_t t) {
+        int lo = 0, hi = p.G - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start(mid) <= t) lo = mid;
+            else hi = mid - 1;
+        }
+        return lo;
+    };
+    float kv[K];
+    int ki[K];
+#pragma unroll
+    for (int t = 0; t < K; ++t) {
+        kv[t] = pinf<float>();
+        ki[t] = 0x7fffffff;
+    }
+    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - (int)(start(c) / p.CT);
+        for (int h = 0; h < 2; ++h) {
+            const size_t base = (((size_t)c * p.smax + seg) * 2 + h) * K * kKBM;
+            for (int t = 0; t < p.k; ++t)
+                topk_insert_lex<float, K>(kv, ki, p.pv[base + (size_t)t * kKBM + lr], p.pi[base + (size_t)t * kKBM + lr]);
+        }
+    }
+    const float sgn = p.largest ? -1.f : 1.f;
+#pragma unroll
+    for (int t = 0; t < K; ++t)
+        if (t < p.k) {
+            values[i * p.k + t] = sgn * kv[t];
+            indices[i * p.k + t] = ki[t];
+        }
+}
+
+// hi/lo split of a [n, D] fp32 array into [n, DP] (zero padded), row squared norms, and (for the
+// streamed set) norms padded with zeros to `npad` rows.
+__global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int DP, float* __restrict__ hi,
+                             float* __restrict__ lo, float* __restrict__ norm, int64_t npad) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;
+    if (r >= npad) return;
+    float s = 0.f;
+    for (int f = threadIdx.x; f < DP; f += 32) {
+        const float e = (r < n && f < D) ? x[r * D + f] : 0.f;
+        const float h = __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
+        if (r < n) {
+            hi[r * DP + f] = h;
+            lo[r * DP + f] = e - h;
+        }
+        s = fmaf(e, e, s);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (threadIdx.x == 0) norm[r] = s;
+}
+
+struct TopkTcPlan {
+    int64_t T;
+    int CT, G, smax, DP, KB;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, off_err, bytes;
+};
+
+inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
+    TopkTcPlan pl;
+    pl.DP = D <= 32 ? 32 : 64;
+    pl.KB = topk_bucket(k);
+    const int64_t RB = (N + kKBM - 1) / kKBM;
+    pl.CT = (int)((M + kKBN - 1) / kKBN);
+    pl.T = RB * pl.CT;
+    pl.G = (int)(pl.T < kKGrid ? pl.T : kKGrid);
+    const int64_t per = (pl.T + pl.G - 1) / pl.G;
+    pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
+    size_t o = 0;
+    pl.off_xh = o; o += al256((size_t)N * pl.DP * 4);
+    pl.off_xl = o; o += al256((size_t)N * pl.DP * 4);
+    if (same) {
+        pl.off_yh = pl.off_xh;
+        pl.off_yl = pl.off_xl;
+    } else {
+        pl.off_yh = o; o += al256((size_t)M * pl.DP * 4);
+        pl.off_yl = o; o += al256((size_t)M * pl.DP * 4);
+    }
+    pl.off_xn = o; o += al256((size_t)N * 4);
+    pl.off_yn = o; o += al256((size_t)pl.CT * kKBN * 4);
+    const size_t lists = (size_t)pl.G * pl.smax * 2 * pl.KB * kKBM;
+    pl.off_pv = o; o += al256(lists * 4);
+    pl.off_pi = o; o += al256(lists * 4);
+    pl.off_err = o; o += 256;
+    pl.bytes = o;
+    return pl;
+}
+
+}  // namespace tc
+
+size_t topk_tc_workspace(int64_t N, int64_t M, int D, int k, bool same) {
+    return tc::topk_tc_plan(N, M, D, k, same).bytes;
+}
+
+// Tensor-core top-k; returns the number of kernels launched or -1 (tensor maps could not be built).
+int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same, cudaStream_t s) {
+    using namespace tc;
+    const TopkTcPlan pl = topk_tc_plan(a.nP, a.nQ, a.D, a.k, same);
+    char* ws = static_cast<char*>(a.ws);
+    float* xh = reinterpret_cast<float*>(ws + pl.off_xh);
+    float* xl = reinterpret_cast<float*>(ws + pl.off_xl);
+    float* yh = reinterpret_cast<float*>(ws + pl.off_yh);
+    float* yl = reinterpret_cast<float*>(ws + pl.off_yl);
+    float* xn = reinterpret_cast<float*>(ws + pl.off_xn);
+    float* yn = reinterpret_cast<float*>(ws + pl.off_yn);
+    CUtensorMap mxh, mxl, myh, myl;
+    if (!make_map_2d(&mxh, xh, pl.DP, a.nP, 128) || !make_map_2d(&mxl, xl, pl.DP, a.nP, 128) ||
+        !make_map_2d(&myh, yh, pl.DP, a.nQ, 128) || !make_map_2d(&myl, yl, pl.DP, a.nQ, 128))
+        return -1;
+    int n = 0;
+    {
+        HookScope h("tc_split_pad", s);
+        tc_split_pad<<<(unsigned)((a.nP + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.P), a.nP, a.D,
+                                                                        pl.DP, xh, xl, xn, a.nP);
+        ++n;
+    }
+    {
+        // the streamed set's norms are always needed padded (the producer copies whole tiles of them)
+        HookScope h("tc_split_pad", s);
+        const int64_t npad = (int64_t)pl.CT * kKBN;
+        tc_split_pad<<<(unsigned)((npad + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.Q), a.nQ, a.D,
+                                                                        pl.DP, yh, yl, yn, npad);
+        ++n;
+    }
+    TopkTcParams p;
+    p.N = a.nP;
+    p.M = a.nQ;
+    p.T = pl.T;
+    p.CT = pl.CT;
+    p.G = pl.G;
+    p.smax = pl.smax;
+    p.k = a.k;
+    p.metric = a.metric;
+    p.apply_exp = a.apply_exp;
+    p.largest = a.largest;
+    p.scale = (float)a.scale;
+    p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
+    p.xn = xn;
+    p.yn = yn;
+    p.pv = reinterpret_cast<float*>(ws + pl.off_pv);
+    p.pi = reinterpret_cast<int*>(ws + pl.off_pi);
+    p.err = reinterpret_cast<int*>(ws + pl.off_err);
+    auto go = [&](auto kernel, size_t smem) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        HookScope h("topk_tc", s);
+        kernel<<<pl.G, kKThreads, smem, s>>>(mxh, mxl, myh, myl, p);
+    };
+    auto with_metric = [&](auto dp, auto kk) {
+        constexpr int DP = decltype(dp)::value, KB = decltype(kk)::value;
+        constexpr size_t sm = TopkTcShape<DP>::kSmem;
+        const bool ex = a.apply_exp != 0;
+        if (a.metric == kLinear) ex ? go(topk_tc<DP, KB, kLinear, true>, sm) : go(topk_tc<DP, KB, kLinear, false>, sm);
+        else if (a.metric == kSqeuclidean)
+            ex ? go(topk_tc<DP, KB, kSqeuclidean, true>, sm) : go(topk_tc<DP, KB, kSqeuclidean, false>, sm);
+        else ex ? go(topk_tc<DP, KB, kRbf, true>, sm) : go(topk_tc<DP, KB, kRbf, false>, sm);
+    };
+    auto with_k = [&](auto dp) {
+        switch (pl.KB) {
+            case 1: with_metric(dp, std::integral_constant<int, 1>{}); break;
+            case 4: with_metric(dp, std::integral_constant<int, 4>{}); break;
+            case 8: with_metric(dp, std::integral_constant<int, 8>{}); break;
+            case 16: with_metric(dp, std::integral_constant<int, 16>{}); break;
+            default: with_metric(dp, std::integral_constant<int, 32>{}); break;
+        }
+    };
+    if (pl.DP == 32) with_k(std::integral_constant<int, 32>{});
+    else with_k(std::integral_constant<int, 64>{});
+    ++n;
+    {
+        HookScope h("topk_tc_merge", s);
+        const unsigned nb = (unsigned)((a.nP + 127) / 128);
+        switch (pl.KB) {
+            case 1: topk_tc_merge<1><<<nb, 128, 0, s>>>(p, static_cast<float*>(values), indices); break;
+            case 4: topk_tc_merge<4><<<nb, 128, 0, s>>>(p, static_cast<float*>(values), indices); break;
+            case 8: topk_tc_merge<8><<<nb, 128, 0, s>>>(p, static_cast<float*>(values), indices); break;
+            case 16: topk_tc_merge<16><<<nb, 128, 0, s>>>(p, static_cast<float*>(values), indices); break;
+            default: topk_tc_merge<32><<<nb, 128, 0, s>>>(p, static_cast<float*>(values), indices); break;
+        }
+        ++n;
+    }
+    return n;
+}
+
+}  // namespace tp
