@@ -186,7 +186,7 @@ bool force_simt() {
 
 // The tensor-core symmetric backward (fp32, D = 64, X = Y, no row/column parameters) and the
 // tensor-core top-k are switched on once their parity tests pass on the GPU.
-constexpr bool kTcBackward = false;
+constexpr bool kTcBackward = true;
 constexpr bool kTcTopk = false;
 
 // The tensor-core log-sum-exp covers fp32, D = 64, no row/column parameters, 16-byte aligned points.

@@ -56,6 +56,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 __device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+// tf32 operand split x ~ hi + lo. hi keeps the sign, exponent and top 10 mantissa bits (truncation);
+// lo = x - hi is exact in fp32 but has up to 13 significant bits, one or two more than tf32 holds, and
+// the MMA would truncate it toward zero, shrinking every vector by up to 2^-20 of its length in the
+// same direction. Rounding lo to the nearest tf32 value here (add half a tf32 ulp to the magnitude
+// bits, then clear the low 13 bits) makes that error unbiased and at most 2^-21.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+__device__ __forceinline__ float tf32_lo(float x, float hi) {
+    return __uint_as_float((__float_as_uint(x - hi) + 0x1000u) & 0xFFFFE000u);
+}
+
 __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // TMEM allocation by one whole warp; the base address is written to *slot.

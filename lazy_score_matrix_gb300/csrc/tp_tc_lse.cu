@@ -3,8 +3,11 @@
 // S.logsumexp(-1, exclude_self=True) on S = lazy(z, z, "linear") / t) and Score Expressions.
 //
 // The contraction X Y^T (D = 64) runs on tcgen05.mma kind::tf32 with a hi/lo split of both operands
-// (x = hi + lo, hi = x with its low 13 mantissa bits cleared): X Y^T ~ Xh Yh^T + Xh Yl^T + Xl Yh^T,
-// which keeps fp32-level accuracy (the dropped Xl Yl^T and the truncation of lo are ~2^-21 relative).
+// (x ~ hi + lo, hi = x with its low 13 mantissa bits cleared, lo = x - hi rounded to the nearest tf32):
+// X Y^T ~ Xh Yl^T + Xl Yh^T + Xh Yh^T, which keeps fp32-level accuracy (the dropped Xl Yl^T and the
+// rounding of lo are ~2^-21 relative and unbiased). The tensor core's accumulator truncates toward
+// zero after each instruction, so the two small products go first: the truncations that happen at
+// the full magnitude of the dot product are then only the eight of Xh Yh^T.
 // The 128 x 128 score tile lands in TMEM; four epilogue warps read it back one row per thread
 // (tcgen05.ld) and run the online log-sum-exp in base 2, with the metric, scale, exp and exclude_self
 // applied per element. The matrix never leaves the SM.
@@ -39,7 +42,8 @@ constexpr int kOperand = 2 * kChunk;         // 64 features: two chunks, 32 KB
 constexpr int kPair = 2 * kOperand;          // hi + lo: 64 KB
 constexpr int kStages = 2;
 constexpr int kTcThreads = 320;      // backward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
-constexpr int kTcThreadsF = 320;     // forward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
+constexpr int kEpiF = 16;            // forward epilogue warps: 4 per TMEM lane quarter, 32 columns each
+constexpr int kTcThreadsF = 32 * (2 + kEpiF);
 constexpr int kTmemCols = 256;
 constexpr int kGrid = 152;                   // persistent CTAs: one per GB300 SM
 constexpr size_t kSmemBytes = (size_t)kPair * (1 + kStages) + 256 + 1024;  // + barriers, + alignment slack
@@ -57,7 +61,7 @@ struct LseTcParams {
     float neg_gamma_log2;  // -gamma * log2(e)
     const float* xn;       // |x_i|^2 (distance metrics)
     const float* yn;       // |y_j|^2
-    float* part;           // [G][smax][2 halves][2][128] partial (max, sum) in base 2
+    float* part;           // [G][smax][4 column quarters][2][128] partial (max, sum) in base 2
     int* err;
     int same;              // X and Y are the same array: the self-distance is exactly 0
 };
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 256);
+            mbar_init(acc_empty + b, 32 * kEpiF);
         }
         mbar_fence_init();
     }
@@ -173,8 +177,8 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
                 const uint32_t d = tmem + (uint32_t)(b * kBN);
                 const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kPair);
                 // Xh Yh^T + Xh Yl^T + Xl Yh^T over K = 64 in steps of 8 (32 bytes)
-                const uint32_t ao[3] = {0u, 0u, (uint32_t)kOperand};
-                const uint32_t bo[3] = {0u, (uint32_t)kOperand, 0u};
+                const uint32_t ao[3] = {0u, (uint32_t)kOperand, 0u};  // Xh Yl, Xl Yh, then Xh Yh
+                const uint32_t bo[3] = {(uint32_t)kOperand, 0u, 0u};
                 uint32_t acc = 0;
 #pragma unroll
                 for (int prod = 0; prod < 3; ++prod) {
@@ -190,17 +194,20 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
                 mma_commit(acc_full + b);
             }
         }
-    } else {  // ---------------- epilogue: warps 2..9, one row per thread, half of the tile's columns
+    } else {  // ---------------- epilogue: warps 2..17, one row per thread, 32 of the tile's columns
+        constexpr float kL2E = 1.4426950408889634f;
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;       // columns [64 * half, 64 * half + 64) of each tile
+        const int sub = (warp - 2) >> 2;        // columns [32 sub, 32 sub + 32) of each tile
         const int lr = q * 32 + lane;           // row within the tile
-        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * 32);
+        // base-2 score of a plain scaled base: s = base * (scale log2 e)
+        const float c1 = p.scale * kL2E;
         int64_t rb_cur = -1;
         int seg = 0;
         float m = ninf<float>(), l = 0.f, xn = 0.f;
         bool ok = true;
         auto flush = [&]() {
-            float* o = p.part + ((size_t)((blockIdx.x * p.smax + seg) * 2 + half) * 2) * kBM;
+            float* o = p.part + ((size_t)((blockIdx.x * p.smax + seg) * 4 + sub) * 2) * kBM;
             o[lr] = m;
             o[kBM + lr] = l;
             ++seg;
@@ -220,31 +227,38 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
             ok = mbar_wait(acc_full + b, rr & 1, p.err, 16);
             if (!ok) break;
             fence_after_sync();
-            const int64_t j0 = (int64_t)ct * kBN + half * 64;
-            const bool diag = row >= j0 && row < j0 + 64;
-            const bool masked = p.M - j0 < 64 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                float v[32];
-                tmem_ld32(lane_base + (uint32_t)(b * kBN + c * 32), v);
-                const int64_t jc = j0 + c * 32;
+            float v[32];
+            tmem_ld32(lane_base + (uint32_t)(b * kBN), v);
+            fence_before_sync();
+            mbar_arrive(acc_empty + b);  // the values are in registers: the MMA may reuse the buffer
+            const int64_t j0 = (int64_t)ct * kBN + sub * 32;
+            const bool diag = row >= j0 && row < j0 + 32;
+            const bool masked = p.M - j0 < 32 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int64_t j = jc + u;
+            for (int u = 0; u < 32; ++u) {
+                float sc;
+                if (METRIC == kLinear && !EXP) {
+                    sc = v[u] * c1;
+                } else {
+                    const int64_t j = j0 + u;
                     float dot = v[u];
                     if (METRIC != kLinear && masked && p.same && j == row) dot = xn;  // |x - x|^2 = 0 exactly
                     const float yn = (METRIC != kLinear && j < p.M) ? __ldg(p.yn + j) : 0.f;
-                    float sc = tile_score<METRIC, EXP>(dot, xn, yn, p);
-                    if (masked && (j >= p.M || (p.exclude_self && j == row))) sc = ninf<float>();
-                    v[u] = sc;
+                    sc = tile_score<METRIC, EXP>(dot, xn, yn, p);
                 }
-                float c4[4];
+                if (masked) {
+                    const int64_t j = j0 + u;
+                    if (j >= p.M || (p.exclude_self && j == row)) sc = ninf<float>();
+                }
+                v[u] = sc;
+            }
+            float c4[4];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) c4[a] = ninf<float>();
+            for (int a = 0; a < 4; ++a) c4[a] = ninf<float>();
 #pragma unroll
-                for (int u = 0; u < 32; ++u) c4[u & 3] = fmaxf(c4[u & 3], v[u]);
-                const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
-                if (cmax == ninf<float>()) continue;
+            for (int u = 0; u < 32; ++u) c4[u & 3] = fmaxf(c4[u & 3], v[u]);
+            const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+            if (cmax != ninf<float>()) {
                 if (cmax > m) {
                     l *= ExpTraits<float>::bexp(m - cmax);
                     m = cmax;
@@ -254,8 +268,6 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
                 for (int u = 0; u < 32; ++u) s4[u & 3] += ExpTraits<float>::bexp(v[u] - m);
                 l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
-            fence_before_sync();
-            mbar_arrive(acc_empty + b);
         }
         if (ok && rb_cur >= 0) flush();
     }
@@ -285,13 +297,13 @@ __global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
     float m = ninf<float>();
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-        for (int h = 0; h < 2; ++h) m = fmaxf(m, p.part[((size_t)((c * p.smax + seg) * 2 + h) * 2) * kBM + lr]);
+        for (int h = 0; h < 4; ++h) m = fmaxf(m, p.part[((size_t)((c * p.smax + seg) * 4 + h) * 2) * kBM + lr]);
     }
     float l = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-        for (int h = 0; h < 2; ++h) {
-            const float* o = p.part + ((size_t)((c * p.smax + seg) * 2 + h) * 2) * kBM;
+        for (int h = 0; h < 4; ++h) {
+            const float* o = p.part + ((size_t)((c * p.smax + seg) * 4 + h) * 2) * kBM;
             if (o[lr] > ninf<float>()) l += o[kBM + lr] * ExpTraits<float>::bexp(o[lr] - m);
         }
     }
@@ -309,8 +321,8 @@ __global__ void tc_split64(const float* __restrict__ x, int64_t n, float* __rest
     float s = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        h[u] = __uint_as_float(__float_as_uint(e[u]) & 0xFFFFE000u);
-        lo4[u] = e[u] - h[u];
+        h[u] = tf32_hi(e[u]);
+        lo4[u] = tf32_lo(e[u], h[u]);
         s = fmaf(e[u], e[u], s);
     }
     reinterpret_cast<float4*>(hi + r * 64)[q] = make_float4(h[0], h[1], h[2], h[3]);
@@ -462,9 +474,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t bz = smem_u32(sB + s * kStageBytesB + kPairB);  // feature-major tile
                 const uint32_t kh = tS + (uint32_t)(b * kBNb), kl = tLo + (uint32_t)(b * kBNb);
                 const uint32_t dz = tDZ + (uint32_t)(b * 64);
-                // kappa_hi ZTh + kappa_hi ZTl + kappa_lo ZTh, K = 64 points in steps of 8 (32 bytes)
-                const uint32_t ka[3] = {kh, kh, kl};
-                const uint32_t zb[3] = {0u, (uint32_t)kOperandB, 0u};
+                // kappa_hi ZTl + kappa_lo ZTh + kappa_hi ZTh, K = 64 points in steps of 8 (32 bytes)
+                const uint32_t ka[3] = {kh, kl, kh};
+                const uint32_t zb[3] = {(uint32_t)kOperandB, 0u, 0u};
                 uint32_t acc = 0;
 #pragma unroll
                 for (int prod = 0; prod < 3; ++prod) {
@@ -495,8 +507,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kStageBytesB);
-                const uint32_t ao[3] = {0u, 0u, (uint32_t)kOperand};
-                const uint32_t bo[3] = {0u, (uint32_t)kOperandB, 0u};
+                const uint32_t ao[3] = {0u, (uint32_t)kOperand, 0u};  // Zh Ztl, Zl Zth, then Zh Zth
+                const uint32_t bo[3] = {(uint32_t)kOperandB, 0u, 0u};
                 uint32_t acc = 0;
 #pragma unroll
                 for (int prod = 0; prod < 3; ++prod) {
@@ -601,8 +613,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float kap = METRIC == kLinear ? E : (METRIC == kSqeuclidean ? -2.f * E : p.two_gamma * E * base);
                     kap = dead ? 0.f : kap;
                     ksum += kap;
-                    const float hi = __uint_as_float(__float_as_uint(kap) & 0xFFFFE000u);
-                    lo[u] = kap - hi;
+                    const float hi = tf32_hi(kap);
+                    lo[u] = tf32_lo(kap, hi);
                     v[u] = hi;
                 }
                 tmem_st32(tS + lane_off + col, v);
@@ -721,7 +733,7 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
     pl.off_xn = o; o += al256((size_t)N * 4);
     if (same) pl.off_yn = pl.off_xn;
     else { pl.off_yn = o; o += al256((size_t)M * 4); }
-    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 2 * 2 * kBM * 4);
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 4 * 2 * kBM * 4);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;

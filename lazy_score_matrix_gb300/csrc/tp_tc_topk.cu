@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         mbar_init(a_empty, 1);
         for (int s = 0; s < SH::kStages; ++s) {
             mbar_init(b_full + s, 1);
-            mbar_init(b_empty + s, 1);
+            // freed by the MMA (operands consumed) and by the 256 selection threads (norms consumed)
+            mbar_init(b_empty + s, 1 + 256);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
@@ -158,8 +159,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
                 fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(b * kKBN);
                 const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * SH::kPair);
-                const uint32_t ao[3] = {0u, 0u, (uint32_t)SH::kOperand};
-                const uint32_t bo[3] = {0u, (uint32_t)SH::kOperand, 0u};
+                const uint32_t ao[3] = {0u, (uint32_t)SH::kOperand, 0u};  // Xh Yl, Xl Yh, then Xh Yh
+                const uint32_t bo[3] = {(uint32_t)SH::kOperand, 0u, 0u};
                 uint32_t acc = 0;
 #pragma unroll
                 for (int prod = 0; prod < 3; ++prod) {
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
             }
             fence_before_sync();
             mbar_arrive(acc_empty + b);
+            mbar_arrive(b_empty + s);
         }
         if (ok && rb_cur >= 0) flush();
     }
@@ -293,10 +295,10 @@ __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int 
     float s = 0.f;
     for (int f = threadIdx.x; f < DP; f += 32) {
         const float e = (r < n && f < D) ? x[r * D + f] : 0.f;
-        const float h = __uint_as_float(__float_as_uint(e) & 0xFFFFE000u);
+        const float h = tf32_hi(e);
         if (r < n) {
             hi[r * DP + f] = h;
-            lo[r * DP + f] = e - h;
+            lo[r * DP + f] = tf32_lo(e, h);
         }
         s = fmaf(e, e, s);
     }
