@@ -236,6 +236,22 @@ TP_API int64_t tp_launch_count(int reset);
 typedef void (*tp_launch_hook)(const char* kernel, int phase, void* stream, void* user);
 TP_API void tp_set_launch_hook(tp_launch_hook hook, void* user);
 
+/* Kernel timer: per-launch device durations with no host callback in the launch path.
+ * tp_timer_start(capacity) creates (or reuses) 2 * capacity CUDA events on the current device and
+ * starts recording: immediately before and after every kernel launch this library makes, one event is
+ * recorded on the launch stream (the host cost is the two cudaEventRecord calls). Launches beyond
+ * `capacity` are not timed. Returns TP_ERR_INVALID_ARG for capacity < 1, TP_ERR_CUDA if events cannot
+ * be created.
+ * tp_timer_stop() stops recording and returns the number of launches timed.
+ * tp_timer_read(i, &kernel, &ms) waits for the i-th timed launch (0-based, launch order) to complete,
+ * then stores its static kernel name and its duration in milliseconds. Returns TP_ERR_INVALID_ARG for
+ * an index outside the last recording, TP_ERR_CUDA if the events cannot be read.
+ * Process-wide: start and stop it while no other thread is calling into libtp. The events stay owned by
+ * the library (released at process exit). */
+TP_API tp_status tp_timer_start(int64_t capacity);
+TP_API int64_t tp_timer_stop(void);
+TP_API tp_status tp_timer_read(int64_t index, const char** kernel, float* ms);
+
 #ifdef __cplusplus
 }
 #endif

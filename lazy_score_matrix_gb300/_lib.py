@@ -56,6 +56,9 @@ SIGNATURES = {
     "tp_last_error": ([], ctypes.c_char_p),
     "tp_launch_count": ([_INT], _I64),
     "tp_set_launch_hook": ([_P, _P], None),
+    "tp_timer_start": ([_I64], _INT),
+    "tp_timer_stop": ([], _I64),
+    "tp_timer_read": ([_I64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)], _INT),
 }
 
 LAUNCH_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_char_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p)

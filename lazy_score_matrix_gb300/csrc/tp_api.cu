@@ -36,6 +36,16 @@ thread_local int64_t g_launches = 0;
 tp_launch_hook g_hook = nullptr;
 void* g_hook_user = nullptr;
 
+// kernel timer (tp_timer_*): an event pair per launch, recorded from the launch path
+struct KernelTimer {
+    std::vector<cudaEvent_t> ev;     // 2 per slot
+    std::vector<const char*> name;   // per slot
+    int device = -1;
+    int64_t capacity = 0, count = 0, recorded = 0;
+    bool on = false;
+};
+KernelTimer g_timer;
+
 tp_status fail(tp_status s, const std::string& msg) {
     g_err = msg;
     return s;
@@ -185,9 +195,10 @@ bool force_simt() {
 }
 
 // The tensor-core symmetric backward (fp32, D = 64, X = Y, no row/column parameters) and the
-// tensor-core top-k are switched on once their parity tests pass on the GPU.
+// tensor-core top-k (fp32, D <= 64, k <= 32): both pass every parity test on the GPU and are faster
+// than the SIMT sweeps they replace (InfoNCE backward 168 us vs 0.8 ms; k-NN 43 ms vs 130 ms).
 constexpr bool kTcBackward = true;
-constexpr bool kTcTopk = false;
+constexpr bool kTcTopk = true;
 
 // The tensor-core log-sum-exp covers fp32, D = 64, no row/column parameters, 16-byte aligned points.
 bool lse_tc_shape(const tp_pairs* p) { return p->dtype == TP_F32 && p->D == 64; }
@@ -482,6 +493,10 @@ namespace tp {
 void set_last_error(const std::string& msg) { g_err = msg; }
 
 void launch_hook(const char* kernel, int phase, cudaStream_t s) {
+    if (g_timer.on && g_timer.count < g_timer.capacity) {
+        cudaEventRecord(g_timer.ev[2 * g_timer.count + phase], s);
+        if (phase == 1) g_timer.name[g_timer.count++] = kernel;
+    }
     if (g_hook) g_hook(kernel, phase, static_cast<void*>(s), g_hook_user);
 }
 }  // namespace tp
@@ -509,6 +524,45 @@ const char* tp_last_error(void) { return g_err.c_str(); }
 void tp_set_launch_hook(tp_launch_hook hook, void* user) {
     g_hook = hook;
     g_hook_user = user;
+}
+
+tp_status tp_timer_start(int64_t capacity) {
+    if (capacity < 1) return fail(TP_ERR_INVALID_ARG, "tp_timer_start: capacity must be >= 1");
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(TP_ERR_CUDA, "tp_timer_start: no current device");
+    if (dev != g_timer.device) {  // events belong to the device current at their creation
+        for (cudaEvent_t e : g_timer.ev) cudaEventDestroy(e);
+        g_timer.ev.clear();
+        g_timer.device = dev;
+    }
+    while ((int64_t)g_timer.ev.size() < 2 * capacity) {
+        cudaEvent_t e;
+        const cudaError_t ce = cudaEventCreate(&e);
+        if (ce != cudaSuccess) return fail(TP_ERR_CUDA, std::string("tp_timer_start: ") + cudaGetErrorString(ce));
+        g_timer.ev.push_back(e);
+    }
+    g_timer.name.assign((size_t)capacity, nullptr);
+    g_timer.capacity = capacity;
+    g_timer.count = 0;
+    g_timer.recorded = 0;
+    g_timer.on = true;
+    return TP_OK;
+}
+
+int64_t tp_timer_stop(void) {
+    g_timer.on = false;
+    g_timer.recorded = g_timer.count;
+    return g_timer.recorded;
+}
+
+tp_status tp_timer_read(int64_t i, const char** kernel, float* ms) {
+    if (i < 0 || i >= g_timer.recorded || !kernel || !ms)
+        return fail(TP_ERR_INVALID_ARG, "tp_timer_read: index outside the last recording");
+    cudaError_t ce = cudaEventSynchronize(g_timer.ev[2 * i + 1]);
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(ms, g_timer.ev[2 * i], g_timer.ev[2 * i + 1]);
+    if (ce != cudaSuccess) return fail(TP_ERR_CUDA, std::string("tp_timer_read: ") + cudaGetErrorString(ce));
+    *kernel = g_timer.name[i];
+    return TP_OK;
 }
 
 int64_t tp_launch_count(int reset) {

@@ -41,7 +41,8 @@ constexpr int kChunk = kBM * 128;            // one 128-row x 32-fp32 swizzled c
 constexpr int kOperand = 2 * kChunk;         // 64 features: two chunks, 32 KB
 constexpr int kPair = 2 * kOperand;          // hi + lo: 64 KB
 constexpr int kStages = 2;
-constexpr int kTcThreads = 320;      // backward kernel: producer, MMA, 8 epilogue warps (2 per lane quarter)
+constexpr int kEpiB = 16;            // backward epilogue warps: 4 per TMEM lane quarter
+constexpr int kTcThreadsB = 32 * (2 + kEpiB);
 constexpr int kEpiF = 16;            // forward epilogue warps: 4 per TMEM lane quarter, 32 columns each
 constexpr int kTcThreadsF = 32 * (2 + kEpiF);
 constexpr int kTmemCols = 256;
@@ -67,6 +68,8 @@ struct LseTcParams {
 };
 
 __host__ __device__ inline int64_t range_start(int64_t T, int G, int c) { return (T * c) / G; }
+// The CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1).
+__host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) { return (int)(((int64_t)G * (t + 1) - 1) / T); }
 
 // Score of one element in base-2 units from the dot product (metric, scale, exp), or -inf.
 template <int METRIC, bool EXP>
@@ -284,16 +287,7 @@ __global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
     const int rb = (int)(i / kBM), lr = (int)(i % kBM);
     const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
     // first CTA whose range holds t0, last whose range holds t1 (ranges are sorted and contiguous)
-    auto cta_of = [&](int64_t t) {
-        int lo = 0, hi = p.G - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (range_start(p.T, p.G, mid) <= t) lo = mid;
-            else hi = mid - 1;
-        }
-        return lo;
-    };
-    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float m = ninf<float>();
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
@@ -356,10 +350,19 @@ constexpr int kBNb = 64;                   // columns per backward tile
 constexpr int kChunkB = kBNb * 128;        // 64-row x 32-fp32 chunk: 8 KB
 constexpr int kOperandB = 2 * kChunkB;     // 16 KB
 constexpr int kPairB = 2 * kOperandB;      // hi + lo: 32 KB
-constexpr int kStagesB = 2;
-constexpr int kStageBytesB = 2 * kPairB;   // point-major tile (hi, lo) + feature-major tile (hi, lo)
+// Two operand rings: the point-major tile (hi, lo) feeds the S MMA and is free once S is done; the
+// feature-major tile (hi, lo) and the tile's (lse, g) pairs feed dZ and the epilogue and are free once dZ
+// is done, which is a whole epilogue later. Separate rings let the S operands of later tiles load
+// while a tile's dZ is still waiting for its epilogue.
+constexpr int kStagesS = 3;
+constexpr int kStagesT = 2;
 constexpr int kTmemColsB = 512;            // S/kappa_hi x2 (64 each), kappa_lo x2, dZ x2
-constexpr size_t kSmemBytesB = (size_t)kPair + (size_t)kStageBytesB * kStagesB + (size_t)kStagesB * kBNb * 8 + 256 + 1024;
+constexpr int kPartsB = kEpiB / 4;         // epilogue warps per lane quarter, each owning a column range
+constexpr int kColsB = kBNb / kPartsB;     // tile columns (and dZ features) per epilogue warp
+constexpr int kPartRowsB = 64 + kPartsB;   // rows of one partial: 64 dZ features + one kappa sum per part
+static_assert(kEpiB % 4 == 0 && (kColsB == 16 || kColsB == 32), "whole lane quarters, 16 or 32 columns each");
+constexpr size_t kSmemBytesB = (size_t)kPair + (size_t)kPairB * (kStagesS + kStagesT) + (size_t)kStagesT * kBNb * 8 + 256 + 1024;
+static_assert(kSmemBytesB <= 232448, "dynamic shared memory per CTA");
 
 struct LseBwdTcParams {
     int64_t N;
@@ -369,12 +372,12 @@ struct LseBwdTcParams {
     float scale, neg_gamma_log2, two_gamma;
     const float* zn;      // |z_k|^2
     const float* lse2g;   // [ceil(N/64)*64][2]: (lse_j * log2 e, g_j), padded with (+inf, 0)
-    float* part;          // [G][smax][66][128]: dZ features, then the two halves' sums of kappa, row-minor
+    float* part;          // [G][smax][64 + kPartsB][128]: dZ features, then each part's sum of kappa, row-minor
     int* err;
 };
 
 template <int METRIC, bool EXP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreadsB, 1)
     lse_bwd_sym_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
                    const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
                    const __grid_constant__ CUtensorMap mTh, const __grid_constant__ CUtensorMap mTl,
@@ -383,18 +386,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                    // row block: hi (2 chunks) | lo (2 chunks)
-    unsigned char* sB = sm + kPair;  // stage s at sB + s * kStageBytesB: [Zh | Zl | ZTh | ZTl]
-    float* sStat = reinterpret_cast<float*>(sB + kStageBytesB * kStagesB);  // [stage][64][2]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStagesB * kBNb * 2);
+    unsigned char* sB = sm + kPair;                        // S ring: stage s at sB + s * kPairB, [Zh | Zl]
+    unsigned char* sT = sB + (size_t)kPairB * kStagesS;    // T ring: stage s at sT + s * kPairB, [ZTh | ZTl]
+    float* sStat = reinterpret_cast<float*>(sT + (size_t)kPairB * kStagesT);  // [T stage][64][2]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStagesT * kBNb * 2);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
-    uint64_t* b_full = bars + 2;    // [kStagesB]
-    uint64_t* b_empty = bars + 4;   // [kStagesB]
-    uint64_t* s_full = bars + 6;    // [2]
-    uint64_t* w_full = bars + 8;    // [2]
-    uint64_t* dz_full = bars + 10;  // [2]
-    uint64_t* dz_empty = bars + 12; // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 14);
+    uint64_t* bs_full = bars + 2;                 // [kStagesS]
+    uint64_t* bs_empty = bs_full + kStagesS;      // [kStagesS]
+    uint64_t* bt_full = bs_empty + kStagesS;      // [kStagesT]
+    uint64_t* bt_empty = bt_full + kStagesT;      // [kStagesT]
+    uint64_t* s_full = bt_empty + kStagesT;       // [2]
+    uint64_t* w_full = s_full + 2;                // [2]
+    uint64_t* dz_full = w_full + 2;               // [2]
+    uint64_t* dz_empty = dz_full + 2;             // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dz_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
@@ -403,15 +409,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
-        for (int s = 0; s < kStagesB; ++s) {
-            mbar_init(b_full + s, 1);
-            mbar_init(b_empty + s, 1);
+        for (int s = 0; s < kStagesS; ++s) {
+            mbar_init(bs_full + s, 1);
+            mbar_init(bs_empty + s, 1);
+        }
+        for (int s = 0; s < kStagesT; ++s) {
+            mbar_init(bt_full + s, 1);
+            mbar_init(bt_empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + b, 1);
-            mbar_init(w_full + b, 256);
+            mbar_init(w_full + b, 32 * kEpiB);
             mbar_init(dz_full + b, 1);
-            mbar_init(dz_empty + b, 256);
+            mbar_init(dz_empty + b, 32 * kEpiB);
         }
         mbar_fence_init();
     }
@@ -423,15 +433,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tS = tmem, tLo = tmem + 2 * kBNb, tDZ = tmem + 4 * kBNb;
 
     if (warp == 0) {
-        if (lane == 0) {  // ---------------- TMA producer
+        if (lane == 0) {  // ---------------- TMA producer: S operands run one tile ahead of T operands
             int rb_cur = -1, a_uses = 0;
-            bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
-                const int64_t i = t - t_begin;
+            const int64_t n = t_end - t_begin;
+            auto load_s = [&](int64_t i) -> bool {
+                const int64_t t = t_begin + i;
                 const int rb = rb_of(t), ct = (int)(t % p.CT);
                 if (rb != rb_cur) {
-                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 21);
-                    if (!ok) break;
+                    if (a_uses > 0 && !mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 21)) return false;
                     mbar_expect_tx(a_full, kPair);
                     tma_load_2d(sA, &mAh, 0, rb * kBM, a_full);
                     tma_load_2d(sA + kChunk, &mAh, 32, rb * kBM, a_full);
@@ -440,22 +449,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ++a_uses;
                     rb_cur = rb;
                 }
-                const int s = (int)(i % kStagesB), r = (int)(i / kStagesB);
-                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 22);
-                if (!ok) break;
-                unsigned char* dst = sB + s * kStageBytesB;
-                mbar_expect_tx(b_full + s, kStageBytesB + kBNb * 8);
-                tma_load_2d(dst, &mBh, 0, ct * kBNb, b_full + s);
-                tma_load_2d(dst + kChunkB, &mBh, 32, ct * kBNb, b_full + s);
-                tma_load_2d(dst + kOperandB, &mBl, 0, ct * kBNb, b_full + s);
-                tma_load_2d(dst + kOperandB + kChunkB, &mBl, 32, ct * kBNb, b_full + s);
-                // feature-major copy: 64 feature rows x 32 points per chunk
-                unsigned char* dT = dst + kPairB;
-                tma_load_2d(dT, &mTh, ct * kBNb, 0, b_full + s);
-                tma_load_2d(dT + kChunkB, &mTh, ct * kBNb + 32, 0, b_full + s);
-                tma_load_2d(dT + kOperandB, &mTl, ct * kBNb, 0, b_full + s);
-                tma_load_2d(dT + kOperandB + kChunkB, &mTl, ct * kBNb + 32, 0, b_full + s);
-                bulk_load(sStat + s * kBNb * 2, p.lse2g + (size_t)ct * kBNb * 2, kBNb * 8, b_full + s);
+                const int s = (int)(i % kStagesS), r = (int)(i / kStagesS);
+                if (r >= 1 && !mbar_wait(bs_empty + s, (r - 1) & 1, p.err, 22)) return false;
+                unsigned char* dst = sB + (size_t)s * kPairB;
+                mbar_expect_tx(bs_full + s, kPairB);
+                tma_load_2d(dst, &mBh, 0, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kChunkB, &mBh, 32, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kOperandB, &mBl, 0, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kOperandB + kChunkB, &mBl, 32, ct * kBNb, bs_full + s);
+                return true;
+            };
+            auto load_t = [&](int64_t i) -> bool {
+                const int ct = (int)((t_begin + i) % p.CT);
+                const int s = (int)(i % kStagesT), r = (int)(i / kStagesT);
+                if (r >= 1 && !mbar_wait(bt_empty + s, (r - 1) & 1, p.err, 29)) return false;
+                unsigned char* dT = sT + (size_t)s * kPairB;  // 64 feature rows x 32 points per chunk
+                mbar_expect_tx(bt_full + s, kPairB + kBNb * 8);
+                tma_load_2d(dT, &mTh, ct * kBNb, 0, bt_full + s);
+                tma_load_2d(dT + kChunkB, &mTh, ct * kBNb + 32, 0, bt_full + s);
+                tma_load_2d(dT + kOperandB, &mTl, ct * kBNb, 0, bt_full + s);
+                tma_load_2d(dT + kOperandB + kChunkB, &mTl, ct * kBNb + 32, 0, bt_full + s);
+                bulk_load(sStat + s * kBNb * 2, p.lse2g + (size_t)ct * kBNb * 2, kBNb * 8, bt_full + s);
+                return true;
+            };
+            bool ok = true;
+            int64_t ns = 0;  // S tiles loaded
+            for (int64_t i = 0; i < n && ok; ++i) {
+                while (ok && ns < n && ns <= i + 1) ok = load_s(ns++);
+                if (ok) ok = load_t(i);
             }
         }
     } else if (warp == 1) {
@@ -467,11 +488,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // dZ for tile i (kappa already in TMEM): issue once its epilogue is done, into the dZ buffer
             // the epilogue drained two tiles ago
             auto issue_dz = [&](int64_t i) -> bool {
-                const int b = (int)(i & 1), s = (int)(i % kStagesB);
+                const int b = (int)(i & 1), s = (int)(i % kStagesT);
                 if (!mbar_wait(w_full + b, (uint32_t)((i >> 1) & 1), p.err, 25)) return false;
                 if (i >= 2 && !mbar_wait(dz_empty + b, (uint32_t)(((i >> 1) - 1) & 1), p.err, 26)) return false;
+                if (!mbar_wait(bt_full + s, (uint32_t)((i / kStagesT) & 1), p.err, 30)) return false;
                 fence_after_sync();
-                const uint32_t bz = smem_u32(sB + s * kStageBytesB + kPairB);  // feature-major tile
+                const uint32_t bz = smem_u32(sT + (size_t)s * kPairB);  // feature-major tile
                 const uint32_t kh = tS + (uint32_t)(b * kBNb), kl = tLo + (uint32_t)(b * kBNb);
                 const uint32_t dz = tDZ + (uint32_t)(b * 64);
                 // kappa_hi ZTl + kappa_lo ZTh + kappa_hi ZTh, K = 64 points in steps of 8 (32 bytes)
@@ -487,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         acc = 1;
                     }
                 }
-                mma_commit(b_empty + s);
+                mma_commit(bt_empty + s);
                 mma_commit(dz_full + b);
                 return true;
             };
@@ -502,11 +524,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ++a_uses;
                     rb_cur = rb;
                 }
-                const int s = (int)(i % kStagesB), r = (int)(i / kStagesB), b = (int)(i & 1);
-                ok = mbar_wait(b_full + s, r & 1, p.err, 24);
+                const int s = (int)(i % kStagesS), r = (int)(i / kStagesS), b = (int)(i & 1);
+                ok = mbar_wait(bs_full + s, r & 1, p.err, 24);
                 if (!ok) break;
                 fence_after_sync();
-                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + s * kStageBytesB);
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kPairB);
                 const uint32_t ao[3] = {0u, (uint32_t)kOperand, 0u};  // Zh Ztl, Zl Zth, then Zh Zth
                 const uint32_t bo[3] = {(uint32_t)kOperandB, 0u, 0u};
                 uint32_t acc = 0;
@@ -521,47 +543,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         acc = 1;
                     }
                 }
+                mma_commit(bs_empty + s);
                 mma_commit(s_full + b);
                 if (i > 0) ok = issue_dz(i - 1);
             }
             if (ok && t_end > t_begin) issue_dz(t_end - t_begin - 1);
         }
-    } else {  // ---------------- epilogue: warps 2..9, two per TMEM lane quarter
+    } else {  // ---------------- epilogue: warps 2..2+kEpiB, kPartsB per TMEM lane quarter
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;  // tile columns [32 half, 32 half + 32), dZ features likewise
+        const int part = (warp - 2) >> 2;  // tile columns [kColsB part, kColsB (part + 1)), dZ features likewise
         const int lr = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int N32 = (int)p.N;
         int seg = 0;
         float K0 = 0.f, lse2k = 0.f, gk = 0.f, zn_k = 0.f;
-        float dacc[32];
+        float dacc[kColsB];
 #pragma unroll
-        for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
+        for (int f = 0; f < kColsB; ++f) dacc[f] = 0.f;
         bool ok = true;
-        auto drain = [&](int64_t j) -> bool {  // add this half of tile j's dZ block into the row accumulator
+        auto drain = [&](int64_t j) -> bool {  // add this part of tile j's dZ block into the row accumulator
             const int b = (int)(j & 1);
             if (!mbar_wait(dz_full + b, (uint32_t)((j >> 1) & 1), p.err, 27)) return false;
             fence_after_sync();
-            float v[32];
-            tmem_ld32(tDZ + lane_off + (uint32_t)(b * 64 + half * 32), v);
+            float v[kColsB];
+            tmem_ld<kColsB>(tDZ + lane_off + (uint32_t)(b * 64 + part * kColsB), v);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) dacc[u] += v[u];
+            for (int u = 0; u < kColsB; ++u) dacc[u] += v[u];
             fence_before_sync();
             mbar_arrive(dz_empty + b);
             return true;
         };
         auto write_partial = [&]() {
-            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * 66 * kBM;
+            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * kPartRowsB * kBM;
 #pragma unroll
-            for (int f = 0; f < 32; ++f) o[(size_t)(half * 32 + f) * kBM + lr] = dacc[f];
-            o[(size_t)(64 + half) * kBM + lr] = K0;
+            for (int f = 0; f < kColsB; ++f) o[(size_t)(part * kColsB + f) * kBM + lr] = dacc[f];
+            o[(size_t)(64 + part) * kBM + lr] = K0;
             ++seg;
         };
-        int rb_cur = -1;
+        int rb_cur = -1, row = 0;
         int64_t pending = -1;
         for (int64_t t = t_begin; t < t_end && ok; ++t) {
             const int64_t i = t - t_begin;
             const int rb = rb_of(t), ct = (int)(t % p.CT);
-            const int64_t row = (int64_t)rb * kBM + lr;
             if (rb != rb_cur) {
                 if (pending >= 0) {
                     ok = drain(pending);
@@ -570,44 +593,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (rb_cur >= 0) write_partial();
                 rb_cur = rb;
+                row = rb * kBM + lr;
                 K0 = 0.f;
 #pragma unroll
-                for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
-                const bool live = row < p.N;
+                for (int f = 0; f < kColsB; ++f) dacc[f] = 0.f;
+                const bool live = row < N32;
                 lse2k = live ? p.lse2g[2 * row] : __int_as_float(0x7f800000);
                 gk = live ? p.lse2g[2 * row + 1] : 0.f;
                 zn_k = (METRIC != kLinear && live) ? p.zn[row] : 0.f;
             }
-            const int b = (int)(i & 1), s = (int)(i % kStagesB);
-            ok = mbar_wait(s_full + b, (uint32_t)((i >> 1) & 1), p.err, 28);
+            const int b = (int)(i & 1), s = (int)(i % kStagesT);
+            ok = mbar_wait(s_full + b, (uint32_t)((i >> 1) & 1), p.err, 28) &&
+                 mbar_wait(bt_full + s, (uint32_t)((i / kStagesT) & 1), p.err, 31);  // the tile's (lse, g)
             if (!ok) break;
             fence_after_sync();
-            const int64_t j0 = (int64_t)ct * kBNb + half * 32;
-            const float* st = sStat + s * kBNb * 2 + half * 64;
+            const int j0 = ct * kBNb + part * kColsB;
+            const int lim = N32 - j0;                       // columns u >= lim are padding
+            const int self = row - j0;                      // column u == self is the pair (row, row)
+            const int dead_self = p.exclude_self ? self : -1;
+            const float* st = sStat + s * kBNb * 2 + part * kColsB * 2;
             float ksum = 0.f;
             {
-                float v[32];
-                const uint32_t col = (uint32_t)(b * kBNb + half * 32);
-                tmem_ld32(tS + lane_off + col, v);
-                float lo[32];
+                float v[kColsB];
+                const uint32_t col = (uint32_t)(b * kBNb + part * kColsB);
+                tmem_ld<kColsB>(tS + lane_off + col, v);
+                float lo[kColsB];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int64_t j = j0 + u;
+                for (int u = 0; u < kColsB; ++u) {
                     const float2 lg = reinterpret_cast<const float2*>(st)[u];
                     float dot = v[u];
-                    if (METRIC != kLinear && j == row) dot = zn_k;  // |z - z|^2 = 0 exactly
+                    if (METRIC != kLinear && u == self) dot = zn_k;  // |z - z|^2 = 0 exactly
                     float base;
                     if (METRIC == kLinear) {
                         base = dot;
                     } else {
-                        const float d2 = fmaxf(fmaf(-2.f, dot, zn_k + __ldg(p.zn + (j < p.N ? j : 0))), 0.f);
+                        const float d2 = fmaxf(fmaf(-2.f, dot, zn_k + __ldg(p.zn + (u < lim ? j0 + u : 0))), 0.f);
                         base = METRIC == kRbf ? ExpTraits<float>::bexp(p.neg_gamma_log2 * d2) : d2;
                     }
                     const float tt = p.scale * base;
                     const float S = EXP ? ExpTraits<float>::bexp(tt * kL2E) : tt;
                     const float s2 = S * kL2E;
                     const float G = gk * ExpTraits<float>::bexp(s2 - lse2k) + lg.y * ExpTraits<float>::bexp(s2 - lg.x);
-                    const bool dead = j >= p.N || (p.exclude_self && j == row);
+                    const bool dead = u >= lim || u == dead_self;
                     const float H = EXP ? G * S : G;
                     const float E = H * p.scale;
                     float kap = METRIC == kLinear ? E : (METRIC == kSqeuclidean ? -2.f * E : p.two_gamma * E * base);
@@ -617,8 +644,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     lo[u] = tf32_lo(kap, hi);
                     v[u] = hi;
                 }
-                tmem_st32(tS + lane_off + col, v);
-                tmem_st32(tLo + lane_off + col, lo);
+                tmem_st<kColsB>(tS + lane_off + col, v);
+                tmem_st<kColsB>(tLo + lane_off + col, lo);
             }
             K0 += ksum;
             tmem_st_wait();
@@ -639,71 +666,109 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemColsB);
 }
 
-// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa
-__global__ void lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z, float* __restrict__ grad) {
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (row, feature), feature fastest
-    if (e >= p.N * 64) return;
-    const int64_t i = e / 64;
-    const int f = (int)(e % 64);
-    const int rb = (int)(i / kBM), lr = (int)(i % kBM);
+// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa. One block per row block:
+// the partials ([64 + kPartsB][128] floats each, feature-major) are read coalesced, summed in CTA order in
+// registers, and transposed through shared memory so the gradient rows are written coalesced too.
+constexpr int kMergeThreads = 256;
+static_assert((64 * kBM) % kMergeThreads == 0 && (kPartsB * kBM) % kMergeThreads == 0, "merge thread mapping");
+__global__ void __launch_bounds__(kMergeThreads) lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z,
+                                                                 float* __restrict__ grad) {
+    __shared__ float sd[64][kBM + 1];
+    __shared__ float sk[kPartsB * kBM];
+    const int rb = blockIdx.x;
     const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
-    auto cta_of = [&](int64_t t) {
-        int lo = 0, hi = p.G - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (range_start(p.T, p.G, mid) <= t) lo = mid;
-            else hi = mid - 1;
-        }
-        return lo;
-    };
-    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
-    float dz = 0.f, k0 = 0.f;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
+    constexpr int kPer = 64 * kBM / kMergeThreads;  // 32 (feature, row) elements per thread
+    float acc[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
+    constexpr int kPerK = kPartsB * kBM / kMergeThreads;  // kappa sums (part, row) per thread
+    float k0[kPerK];
+#pragma unroll
+    for (int u = 0; u < kPerK; ++u) k0[u] = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-        const float* o = p.part + (size_t)(c * p.smax + seg) * 66 * kBM;
-        dz += o[(size_t)f * kBM + lr];
-        k0 += o[(size_t)64 * kBM + lr] + o[(size_t)65 * kBM + lr];
+        const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsB * kBM;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) acc[u] += o[u * kMergeThreads + threadIdx.x];
+#pragma unroll
+        for (int u = 0; u < kPerK; ++u) k0[u] += o[64 * kBM + u * kMergeThreads + threadIdx.x];
     }
-    grad[e] = p.metric == kLinear ? dz : dz - z[e] * k0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int e = u * kMergeThreads + threadIdx.x;
+        sd[e / kBM][e % kBM] = acc[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kPerK; ++u) sk[u * kMergeThreads + threadIdx.x] = k0[u];
+    __syncthreads();
+    for (int e = threadIdx.x; e < 64 * kBM; e += kMergeThreads) {
+        const int lr = e / 64, f = e % 64;
+        const int64_t i = (int64_t)rb * kBM + lr;
+        if (i >= p.N) break;  // rows only grow with e
+        const float dz = sd[f][lr];
+        float ks = 0.f;
+#pragma unroll
+        for (int q = 0; q < kPartsB; ++q) ks += sk[q * kBM + lr];
+        grad[i * 64 + f] = p.metric == kLinear ? dz : dz - z[i * 64 + f] * ks;
+    }
 }
 
-// Feature-major copies of the hi/lo arrays: t[f][j] = a[j][f] for j < N, 0 for N <= j < Npad.
-// 32 x 32 tiles through shared memory (block 32 x 8).
-__global__ void tc_transpose64(const float* __restrict__ hi, const float* __restrict__ lo, int64_t N, int64_t Npad,
-                               float* __restrict__ thi, float* __restrict__ tlo) {
-    __shared__ float th[32][33], tl[32][33];
+// Backward pre-pass over 32 points per block (block 256): the hi/lo split of z (point-major, for the
+// row operand and the S tile), its squared norms, the feature-major hi/lo copy (the K-major B operand
+// of dZ = kappa Z, zero for the padding points N <= j < Npad) and the (lse_j log2 e, g_j) pairs
+// (+inf, 0 for padding).
+__global__ void __launch_bounds__(256) lse_bwd_prep(const float* __restrict__ z, const float* __restrict__ lse,
+                                                    const float* __restrict__ g, int64_t N, int64_t Npad,
+                                                    float* __restrict__ zh, float* __restrict__ zl,
+                                                    float* __restrict__ zn, float* __restrict__ thi,
+                                                    float* __restrict__ tlo, float* __restrict__ stat) {
+    __shared__ float sh[32][65], sl[32][65];
     const int64_t j0 = (int64_t)blockIdx.x * 32;
-    const int f0 = blockIdx.y * 32;
-    for (int r = threadIdx.y; r < 32; r += 8) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int q4 = u * 256 + threadIdx.x;  // float4 index within the 32 x 64 block
+        const int r = q4 / 16, c = (q4 % 16) * 4;
         const int64_t j = j0 + r;
         const bool live = j < N;
-        th[r][threadIdx.x] = live ? hi[j * 64 + f0 + threadIdx.x] : 0.f;
-        tl[r][threadIdx.x] = live ? lo[j * 64 + f0 + threadIdx.x] : 0.f;
+        float4 v = live ? reinterpret_cast<const float4*>(z + j * 64)[q4 % 16] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float e[4] = {v.x, v.y, v.z, v.w};
+        float h[4], l[4], ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            h[w] = tf32_hi(e[w]);
+            l[w] = tf32_lo(e[w], h[w]);
+            ss = fmaf(e[w], e[w], ss);
+            sh[r][c + w] = h[w];
+            sl[r][c + w] = l[w];
+        }
+        if (live) {
+            reinterpret_cast<float4*>(zh + j * 64)[q4 % 16] = make_float4(h[0], h[1], h[2], h[3]);
+            reinterpret_cast<float4*>(zl + j * 64)[q4 % 16] = make_float4(l[0], l[1], l[2], l[3]);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, 16);
+        if ((q4 % 16) == 0 && live) zn[j] = ss;
     }
     __syncthreads();
-    for (int r = threadIdx.y; r < 32; r += 8) {
-        const int f = f0 + r;
+    for (int e = threadIdx.x; e < 64 * 32; e += 256) {
+        const int f = e / 32, r = e % 32;
+        const int64_t j = j0 + r;
+        if (j < Npad) {
+            thi[(int64_t)f * Npad + j] = sh[r][f];
+            tlo[(int64_t)f * Npad + j] = sl[r][f];
+        }
+    }
+    if (threadIdx.x < 32) {
         const int64_t j = j0 + threadIdx.x;
         if (j < Npad) {
-            thi[(int64_t)f * Npad + j] = th[threadIdx.x][r];
-            tlo[(int64_t)f * Npad + j] = tl[threadIdx.x][r];
+            const bool live = j < N;
+            stat[2 * j] = live ? lse[j] * 1.4426950408889634f : __int_as_float(0x7f800000);
+            stat[2 * j + 1] = live ? g[j] : 0.f;
         }
     }
 }
 
-// (lse_j log2 e, g_j) pairs, padded to a multiple of 64 rows with (+inf, 0)
-__global__ void lse_bwd_stats(const float* __restrict__ lse, const float* __restrict__ g, int64_t N, int64_t Npad,
-                              float* __restrict__ out) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= Npad) return;
-    const bool live = j < N;
-    out[2 * j] = live ? lse[j] * 1.4426950408889634f : __int_as_float(0x7f800000);
-    out[2 * j + 1] = live ? g[j] : 0.f;
-}
-
-// ------------------------------------------------------------------------------------------------
-// host side
-// ------------------------------------------------------------------------------------------------
 
 struct LseTcPlan {
     int64_t T;
@@ -762,7 +827,7 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     pl.off_ztl = o; o += al256((size_t)pl.Npad * 64 * 4);
     pl.off_zn = o; o += al256((size_t)N * 4);
     pl.off_stat = o; o += al256((size_t)pl.Npad * 8);
-    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 66 * kBM * 4);
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * kPartRowsB * kBM * 4);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -854,19 +919,10 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         return -1;
     int n = 0;
     {
-        HookScope h("tc_split64", s);
-        tc_split64<<<(unsigned)((a.nP + 15) / 16), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, zh, zl, zn);
-        ++n;
-    }
-    {
-        HookScope h("tc_transpose64", s);
-        tc_transpose64<<<dim3((unsigned)(pl.Npad / 32), 2), dim3(32, 8), 0, s>>>(zh, zl, a.nP, pl.Npad, zth, ztl);
-        ++n;
-    }
-    {
-        HookScope h("lse_bwd_stats", s);
-        lse_bwd_stats<<<(unsigned)((pl.Npad + 255) / 256), 256, 0, s>>>(
-            static_cast<const float*>(a.lse), static_cast<const float*>(a.glse), a.nP, pl.Npad, stat);
+        HookScope h("lse_bwd_prep", s);
+        lse_bwd_prep<<<(unsigned)(pl.Npad / 32), 256, 0, s>>>(
+            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse), a.nP,
+            pl.Npad, zh, zl, zn, zth, ztl, stat);
         ++n;
     }
     LseBwdTcParams p;
@@ -888,7 +944,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesB);
         HookScope h("lse_bwd_sym_tc", s);
-        kernel<<<pl.G, kTcThreads, kSmemBytesB, s>>>(mah, mal, mbh, mbl, mth, mtl, p);
+        kernel<<<pl.G, kTcThreadsB, kSmemBytesB, s>>>(mah, mal, mbh, mbl, mth, mtl, p);
     };
     const bool ex = a.apply_exp != 0;
     if (a.metric == kLinear) ex ? go(lse_bwd_sym_tc<kLinear, true>) : go(lse_bwd_sym_tc<kLinear, false>);
@@ -897,8 +953,8 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     ++n;
     {
         HookScope h("lse_bwd_tc_merge", s);
-        lse_bwd_tc_merge<<<(unsigned)((a.nP * 64 + 255) / 256), 256, 0, s>>>(p, static_cast<const float*>(a.P),
-                                                                             static_cast<float*>(a.gP));
+        lse_bwd_tc_merge<<<(unsigned)((a.nP + kBM - 1) / kBM), kMergeThreads, 0, s>>>(
+            p, static_cast<const float*>(a.P), static_cast<float*>(a.gP));
         ++n;
     }
     return n;

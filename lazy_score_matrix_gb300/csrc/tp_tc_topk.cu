@@ -35,7 +35,9 @@ struct TopkTcShape {
     static constexpr int kOperand = kChunks * 128 * 128;    // 128 rows x DP fp32
     static constexpr int kPair = 2 * kOperand;              // hi + lo
     static constexpr int kStages = DP == 32 ? 4 : 2;
-    static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + 256 + 1024;
+    static constexpr size_t kKeyBuf = 8 * 32 * 32 * 4;      // per selection warp: 32 columns x 32 lanes of keys
+    static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + 256 + 1024;
+    static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
 struct TopkTcParams {
@@ -74,7 +76,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
     unsigned char* sA = sm;
     unsigned char* sB = sm + SH::kPair;
     float* sYn = reinterpret_cast<float*>(sB + (size_t)SH::kPair * SH::kStages);  // [stage][128]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sYn + SH::kStages * kKBN);
+    float* sKeys = sYn + SH::kStages * kKBN;                                         // [warp][32 u][32 lanes]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKeys + SH::kKeyBuf / 4);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
     uint64_t* b_full = bars + 2;               // [kStages]
@@ -221,15 +224,38 @@ __global__ void __launch_bounds__(kKThreads, 1)
             const int j0 = ct * kKBN + half * 64;
             const int lim = (int)(p.M - j0 < 64 ? p.M - j0 : 64);  // valid columns of this half
             const float* yn = sYn + s * kKBN + half * 64;
+            float* wkeys = sKeys + (warp - 2) * 32 * 32;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 float v[32];
                 tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
+                // keys, and the columns that beat this row's current k-th key (the threshold only falls,
+                // so every column the insertion would take is in the mask)
+                const float thr = kv[K - 1];
+                uint32_t cand = 0;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int cu = c * 32 + u;
-                    const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yn[cu], p.scale, p.neg_gamma_log2);
-                    if (cu < lim && key < kv[K - 1]) topk_insert<float, K>(kv, ki, key, j0 + cu);
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
+                    const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int u = u4 * 4 + w;
+                        const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yv[w], p.scale, p.neg_gamma_log2);
+                        v[u] = key;
+                        cand |= (c * 32 + u < lim && key < thr) ? (1u << u) : 0u;
+                    }
+                }
+                // rare once the lists are full: stage the keys and insert the candidates in column order
+                if (__any_sync(0xffffffffu, cand != 0u)) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) wkeys[u * 32 + lane] = v[u];
+                    __syncwarp();
+                    while (cand) {
+                        const int u = __ffs(cand) - 1;
+                        cand &= cand - 1u;
+                        topk_insert<float, K>(kv, ki, wkeys[u * 32 + lane], j0 + c * 32 + u);
+                    }
+                    __syncwarp();
                 }
             }
             fence_before_sync();
@@ -252,15 +278,8 @@ __global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_
     const int rb = (int)(i / kKBM), lr = (int)(i % kKBM);
     const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
     auto start = [&](int c) { return (p.T * c) / p.G; };
-    auto cta_of = [&](int64_t t) {
-        int lo = 0, hi = p.G - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (start(mid) <= t) lo = mid;
-            else hi = mid - 1;
-        }
-        return lo;
-    };
+    // the CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1)
+    auto cta_of = [&](int64_t t) { return (int)(((int64_t)p.G * (t + 1) - 1) / p.T); };
     float kv[K];
     int ki[K];
 #pragma unroll

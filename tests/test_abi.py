@@ -33,7 +33,7 @@ def score(metric=1, **kw):
 
 def test_exports_every_header_symbol(lib):
     declared = _lib.header_symbols()
-    assert len(declared) == 17, declared
+    assert len(declared) == 20, declared
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     missing = [s for s in declared if s not in exported]
@@ -47,6 +47,15 @@ def test_status_strings(lib):
     for s in range(6):
         assert lib.tp_status_string(s)
     assert b"INVALID" in lib.tp_status_string(_lib.TP_ERR_INVALID_ARG)
+
+
+def test_timer_argument_checks(lib):
+    # host-only paths: no CUDA call is made before these checks
+    assert lib.tp_timer_start(0) == _lib.TP_ERR_INVALID_ARG
+    assert lib.tp_timer_stop() == 0
+    name, ms = ctypes.c_char_p(), ctypes.c_float()
+    assert lib.tp_timer_read(0, ctypes.byref(name), ctypes.byref(ms)) == _lib.TP_ERR_INVALID_ARG
+    assert lib.tp_timer_read(-1, ctypes.byref(name), ctypes.byref(ms)) == _lib.TP_ERR_INVALID_ARG
 
 
 def ws(lib, entry, p, C=0, k=0):

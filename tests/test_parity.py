@@ -8,6 +8,7 @@ the wider 1e-2 floor (STRESS_FLOOR, see tests/_util.py); the benchmark workloads
 distributions are checked with the 1e-3 floor in test_workloads.py. Top-k on integer-valued inputs is
 bit-exact in values and indices.
 """
+import ctypes
 import numpy as np
 import pytest
 import torch
@@ -290,6 +291,29 @@ def test_lazy_expression_folding_and_param_grads(oracle):
         assert_close(got, g[k], TOL_F64, k)
     with pytest.raises(NotImplementedError):
         (tp.lazy(X, Y).add_rows(b) * 2.0)
+
+
+def test_kernel_timer_times_every_launch():
+    lib = _lib.load()
+    X, Y, V, sc = problem("wide", torch.float32, "linear", False, False)
+    Xd, Yd, Vd = X.to(DEV), Y.to(DEV), V.to(DEV)
+    ops.pairwise_softmax_matmul(Xd, Yd, Vd, gpu_score(sc))
+    torch.cuda.synchronize()
+    _lib.launch_count(reset=True)
+    _lib.check(lib.tp_timer_start(3), "tp_timer_start")
+    for _ in range(2):
+        ops.pairwise_softmax_matmul(Xd, Yd, Vd, gpu_score(sc))
+    n = lib.tp_timer_stop()
+    launched = _lib.launch_count()
+    assert n == min(launched, 3) and launched >= 2
+    name, ms = ctypes.c_char_p(), ctypes.c_float()
+    for i in range(n):
+        _lib.check(lib.tp_timer_read(i, ctypes.byref(name), ctypes.byref(ms)), "tp_timer_read")
+        assert name.value and 0.0 < ms.value < 1e3
+    assert lib.tp_timer_read(n, ctypes.byref(name), ctypes.byref(ms)) == _lib.TP_ERR_INVALID_ARG
+    # a stopped timer records nothing more
+    ops.pairwise_softmax_matmul(Xd, Yd, Vd, gpu_score(sc))
+    assert lib.tp_timer_stop() == n
 
 
 def test_deterministic_and_native(oracle):
