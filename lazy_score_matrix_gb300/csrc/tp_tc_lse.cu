@@ -336,9 +336,13 @@ __global__ void tc_split64(const float* __restrict__ x, int64_t n, float* __rest
 // of the pair at the same time.
 //
 // Per 64-column tile: S = Zrows Ztile^T (tf32 hi/lo, 3 products) into TMEM; the epilogue turns S
-// into kappa, splits it hi/lo and stores it back into TMEM; then dZ += kappa_hi Zh + kappa_hi Zl +
+// into kappa, splits it hi/lo and stores it back into TMEM; then dZ = kappa_hi Zh + kappa_hi Zl +
 // kappa_lo Zh, with kappa as the A operand read from TMEM and the tile's feature-major copy (from a
-// transposed hi/lo copy of z made by the pre-pass) as a K-major B operand. Each tile's dZ (128 x 64)
+// transposed hi/lo copy of z made by the pre-pass) as a K-major B operand. A tcgen05.mma with M = 128
+// costs the same for N = 64 as for N = 128 (about 64 cycles per K step, measured on the GB300), so the
+// hi and lo tiles of the B operand are stacked into one 128-row operand: each product pair that shares
+// its A operand is one N = 128 MMA, with hi*hi landing in TMEM columns apart from the small products,
+// which the epilogue adds in fp32. That is 32 MMAs per tile instead of 48. Each tile's dZ (128 x 64)
 // lands in its own (double-buffered) TMEM block and the epilogue adds it into a per-row register
 // accumulator: the tensor core's accumulation then never spans more than one tile (long accumulation
 // chains in TMEM drift), and the rows' sums are two-level like everywhere else. At the end of the
@@ -348,15 +352,17 @@ __global__ void tc_split64(const float* __restrict__ x, int64_t n, float* __rest
 
 constexpr int kBNb = 64;                   // columns per backward tile
 constexpr int kChunkB = kBNb * 128;        // 64-row x 32-fp32 chunk: 8 KB
-constexpr int kOperandB = 2 * kChunkB;     // 16 KB
-constexpr int kPairB = 2 * kOperandB;      // hi + lo: 32 KB
+constexpr int kChunkPairB = 2 * kChunkB;   // [hi chunk c | lo chunk c]: one 128-row K-major operand, 16 KB
+constexpr int kPairB = 2 * kChunkPairB;    // both K chunks of hi and lo: 32 KB
 // Two operand rings: the point-major tile (hi, lo) feeds the S MMA and is free once S is done; the
 // feature-major tile (hi, lo) and the tile's (lse, g) pairs feed dZ and the epilogue and are free once dZ
 // is done, which is a whole epilogue later. Separate rings let the S operands of later tiles load
 // while a tile's dZ is still waiting for its epilogue.
 constexpr int kStagesS = 3;
 constexpr int kStagesT = 2;
-constexpr int kTmemColsB = 512;            // S/kappa_hi x2 (64 each), kappa_lo x2, dZ x2
+// TMEM, two buffers of each: S as [hi*hi | hi*lo + lo*hi] (128 columns), overwritten by the epilogue
+// with [kappa_hi | kappa_lo]; dZ likewise as [kappa_hi*Zh | kappa_hi*Zl + kappa_lo*Zh] (128 columns).
+constexpr int kTmemColsB = 512;
 constexpr int kPartsB = kEpiB / 4;         // epilogue warps per lane quarter, each owning a column range
 constexpr int kColsB = kBNb / kPartsB;     // tile columns (and dZ features) per epilogue warp
 constexpr int kPartRowsB = 64 + kPartsB;   // rows of one partial: 64 dZ features + one kappa sum per part
@@ -430,7 +436,7 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tLo = tmem + 2 * kBNb, tDZ = tmem + 4 * kBNb;
+    const uint32_t tS = tmem, tDZ = tmem + 256;
 
     if (warp == 0) {
         if (lane == 0) {  // ---------------- TMA producer: S operands run one tile ahead of T operands
@@ -454,9 +460,9 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 unsigned char* dst = sB + (size_t)s * kPairB;
                 mbar_expect_tx(bs_full + s, kPairB);
                 tma_load_2d(dst, &mBh, 0, ct * kBNb, bs_full + s);
-                tma_load_2d(dst + kChunkB, &mBh, 32, ct * kBNb, bs_full + s);
-                tma_load_2d(dst + kOperandB, &mBl, 0, ct * kBNb, bs_full + s);
-                tma_load_2d(dst + kOperandB + kChunkB, &mBl, 32, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kChunkB, &mBl, 0, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kChunkPairB, &mBh, 32, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kChunkPairB + kChunkB, &mBl, 32, ct * kBNb, bs_full + s);
                 return true;
             };
             auto load_t = [&](int64_t i) -> bool {
@@ -466,9 +472,9 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 unsigned char* dT = sT + (size_t)s * kPairB;  // 64 feature rows x 32 points per chunk
                 mbar_expect_tx(bt_full + s, kPairB + kBNb * 8);
                 tma_load_2d(dT, &mTh, ct * kBNb, 0, bt_full + s);
-                tma_load_2d(dT + kChunkB, &mTh, ct * kBNb + 32, 0, bt_full + s);
-                tma_load_2d(dT + kOperandB, &mTl, ct * kBNb, 0, bt_full + s);
-                tma_load_2d(dT + kOperandB + kChunkB, &mTl, ct * kBNb + 32, 0, bt_full + s);
+                tma_load_2d(dT + kChunkB, &mTl, ct * kBNb, 0, bt_full + s);
+                tma_load_2d(dT + kChunkPairB, &mTh, ct * kBNb + 32, 0, bt_full + s);
+                tma_load_2d(dT + kChunkPairB + kChunkB, &mTl, ct * kBNb + 32, 0, bt_full + s);
                 bulk_load(sStat + s * kBNb * 2, p.lse2g + (size_t)ct * kBNb * 2, kBNb * 8, bt_full + s);
                 return true;
             };
@@ -482,7 +488,9 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
     } else if (warp == 1) {
         if (lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idS = idesc_tf32(kBM, kBNb);       // S: M 128, N 64 (K = 64 features)
+            constexpr uint32_t idS2 = idesc_tf32(kBM, 2 * kBNb);  // S against [Zth; Ztl]: N 128
             constexpr uint32_t idZ = idesc_tf32(kBM, 64);          // dZ: M 128, N 64 features, K = 64 points
+            constexpr uint32_t idZ2 = idesc_tf32(kBM, 128);        // dZ against [ZTh; ZTl]: N 128
             int a_uses = 0;
             bool ok = true;
             // dZ for tile i (kappa already in TMEM): issue once its epilogue is done, into the dZ buffer
@@ -494,20 +502,15 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 if (!mbar_wait(bt_full + s, (uint32_t)((i / kStagesT) & 1), p.err, 30)) return false;
                 fence_after_sync();
                 const uint32_t bz = smem_u32(sT + (size_t)s * kPairB);  // feature-major tile
-                const uint32_t kh = tS + (uint32_t)(b * kBNb), kl = tLo + (uint32_t)(b * kBNb);
-                const uint32_t dz = tDZ + (uint32_t)(b * 64);
-                // kappa_hi ZTl + kappa_lo ZTh + kappa_hi ZTh, K = 64 points in steps of 8 (32 bytes)
-                const uint32_t ka[3] = {kh, kl, kh};
-                const uint32_t zb[3] = {(uint32_t)kOperandB, 0u, 0u};
-                uint32_t acc = 0;
+                const uint32_t kh = tS + (uint32_t)(b * 128), kl = kh + 64;  // kappa_hi, kappa_lo columns
+                const uint32_t dz = tDZ + (uint32_t)(b * 128);
+                // per 8 points: kappa_hi [ZTh; ZTl] (N 128: hi*hi into columns 0..63, hi*lo into 64..127),
+                // then kappa_lo ZTh (N 64) into columns 64..127
 #pragma unroll
-                for (int prod = 0; prod < 3; ++prod) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t kb = (uint32_t)((ks >> 2) * kChunkB + (ks & 3) * 32);
-                        mma_tf32_ta(dz, ka[prod] + (uint32_t)(ks * 8), desc_kmajor_sw128(bz + zb[prod] + kb), idZ, acc);
-                        acc = 1;
-                    }
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kb = bz + (uint32_t)((ks >> 2) * kChunkPairB + (ks & 3) * 32);
+                    mma_tf32_ta(dz, kh + (uint32_t)(ks * 8), desc_kmajor_sw128(kb), idZ2, ks > 0 ? 1u : 0u);
+                    mma_tf32_ta(dz + 64, kl + (uint32_t)(ks * 8), desc_kmajor_sw128(kb), idZ, 1u);
                 }
                 mma_commit(bt_empty + s);
                 mma_commit(dz_full + b);
@@ -529,19 +532,15 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kPairB);
-                const uint32_t ao[3] = {0u, (uint32_t)kOperand, 0u};  // Zh Ztl, Zl Zth, then Zh Zth
-                const uint32_t bo[3] = {(uint32_t)kOperandB, 0u, 0u};
-                uint32_t acc = 0;
+                const uint32_t d = tS + (uint32_t)(b * 128);
+                // per 8 features: Zh [Zth; Ztl] (N 128: hi*hi into columns 0..63, hi*lo into 64..127), then
+                // Zl Zth (N 64) into columns 64..127. hi*hi accumulates alone, the small products together.
 #pragma unroll
-                for (int prod = 0; prod < 3; ++prod) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t ka = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
-                        const uint32_t kb = (uint32_t)((ks >> 2) * kChunkB + (ks & 3) * 32);
-                        mma_tf32(tS + (uint32_t)(b * kBNb), desc_kmajor_sw128(a0 + ao[prod] + ka),
-                                 desc_kmajor_sw128(b0 + bo[prod] + kb), idS, acc);
-                        acc = 1;
-                    }
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t ka = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
+                    const uint32_t kb = b0 + (uint32_t)((ks >> 2) * kChunkPairB + (ks & 3) * 32);
+                    mma_tf32(d, desc_kmajor_sw128(a0 + ka), desc_kmajor_sw128(kb), idS2, ks > 0 ? 1u : 0u);
+                    mma_tf32(d + 64, desc_kmajor_sw128(a0 + kOperand + ka), desc_kmajor_sw128(kb), idS, 1u);
                 }
                 mma_commit(bs_empty + s);
                 mma_commit(s_full + b);
@@ -565,10 +564,12 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
             const int b = (int)(j & 1);
             if (!mbar_wait(dz_full + b, (uint32_t)((j >> 1) & 1), p.err, 27)) return false;
             fence_after_sync();
-            float v[kColsB];
-            tmem_ld<kColsB>(tDZ + lane_off + (uint32_t)(b * 64 + part * kColsB), v);
+            float v[kColsB], w[kColsB];
+            const uint32_t col = (uint32_t)(b * 128 + part * kColsB);
+            tmem_ld<kColsB>(tDZ + lane_off + col, v);
+            tmem_ld<kColsB>(tDZ + lane_off + col + 64, w);
 #pragma unroll
-            for (int u = 0; u < kColsB; ++u) dacc[u] += v[u];
+            for (int u = 0; u < kColsB; ++u) dacc[u] += v[u] + w[u];
             fence_before_sync();
             mbar_arrive(dz_empty + b);
             return true;
@@ -615,13 +616,14 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
             float ksum = 0.f;
             {
                 float v[kColsB];
-                const uint32_t col = (uint32_t)(b * kBNb + part * kColsB);
-                tmem_ld<kColsB>(tS + lane_off + col, v);
+                const uint32_t col = (uint32_t)(b * 128 + part * kColsB);
                 float lo[kColsB];
+                tmem_ld<kColsB>(tS + lane_off + col, v);        // hi*hi
+                tmem_ld<kColsB>(tS + lane_off + col + 64, lo);  // hi*lo + lo*hi
 #pragma unroll
                 for (int u = 0; u < kColsB; ++u) {
                     const float2 lg = reinterpret_cast<const float2*>(st)[u];
-                    float dot = v[u];
+                    float dot = v[u] + lo[u];
                     if (METRIC != kLinear && u == self) dot = zn_k;  // |z - z|^2 = 0 exactly
                     float base;
                     if (METRIC == kLinear) {
@@ -644,8 +646,8 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                     lo[u] = tf32_lo(kap, hi);
                     v[u] = hi;
                 }
-                tmem_st<kColsB>(tS + lane_off + col, v);
-                tmem_st<kColsB>(tLo + lane_off + col, lo);
+                tmem_st<kColsB>(tS + lane_off + col, v);         // kappa_hi
+                tmem_st<kColsB>(tS + lane_off + col + 64, lo);   // kappa_lo
             }
             K0 += ksum;
             tmem_st_wait();
