@@ -105,6 +105,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
     return d;
 }
 
+// (row block, column tile) of consecutive tiles t = rb * CT + ct, advanced without dividing: a 64-bit
+// division per tile costs the single MMA-issuing thread (and every epilogue thread) many issue slots.
+struct TileCursor {
+    int rb, ct, CT;
+    __device__ __forceinline__ TileCursor(int64_t t, int CT_) : rb((int)(t / CT_)), ct((int)(t % CT_)), CT(CT_) {}
+    __device__ __forceinline__ void next() {
+        if (++ct == CT) {
+            ct = 0;
+            ++rb;
+        }
+    }
+};
+
 // Instruction descriptor: kind::tf32, fp32 accumulate, both operands K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

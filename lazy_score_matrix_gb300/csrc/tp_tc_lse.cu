@@ -131,9 +131,10 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
             int64_t rb_cur = -1;
             int a_uses = 0;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
                 const int64_t i = t - t_begin;
-                const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+                const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
                     if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 11);
                     if (!ok) break;
@@ -162,9 +163,10 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
             int64_t rb_cur = -1;
             int a_uses = 0;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
                 const int64_t i = t - t_begin;
-                const int rb = (int)(t / p.CT);
+                const int rb = cur.rb;
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);  // the previous A is free once its MMAs finish
                     ok = mbar_wait(a_full, a_uses & 1, p.err, 13);
@@ -215,9 +217,10 @@ __global__ void __launch_bounds__(kTcThreadsF, 1)
             o[kBM + lr] = l;
             ++seg;
         };
-        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        TileCursor cur(t_begin, p.CT);
+        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
             const int64_t i = t - t_begin;
-            const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+            const int rb = cur.rb, ct = cur.ct;
             const int64_t row = (int64_t)rb * kBM + lr;
             if (rb != rb_cur) {
                 if (rb_cur >= 0) flush();
@@ -410,7 +413,6 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
-    auto rb_of = [&](int64_t t) { return (int)(t / p.CT); };
 
     if (threadIdx.x == 0) {
         mbar_init(a_full, 1);
@@ -442,9 +444,10 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
         if (lane == 0) {  // ---------------- TMA producer: S operands run one tile ahead of T operands
             int rb_cur = -1, a_uses = 0;
             const int64_t n = t_end - t_begin;
+            TileCursor cs(t_begin, p.CT), cq(t_begin, p.CT);  // next S load, next T load (each in order)
             auto load_s = [&](int64_t i) -> bool {
-                const int64_t t = t_begin + i;
-                const int rb = rb_of(t), ct = (int)(t % p.CT);
+                const int rb = cs.rb, ct = cs.ct;
+                cs.next();
                 if (rb != rb_cur) {
                     if (a_uses > 0 && !mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 21)) return false;
                     mbar_expect_tx(a_full, kPair);
@@ -466,7 +469,8 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 return true;
             };
             auto load_t = [&](int64_t i) -> bool {
-                const int ct = (int)((t_begin + i) % p.CT);
+                const int ct = cq.ct;
+                cq.next();
                 const int s = (int)(i % kStagesT), r = (int)(i / kStagesT);
                 if (r >= 1 && !mbar_wait(bt_empty + s, (r - 1) & 1, p.err, 29)) return false;
                 unsigned char* dT = sT + (size_t)s * kPairB;  // 64 feature rows x 32 points per chunk
@@ -517,9 +521,10 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
                 return true;
             };
             int rb_cur = -1;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
                 const int64_t i = t - t_begin;
-                const int rb = rb_of(t);
+                const int rb = cur.rb;
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);
                     ok = mbar_wait(a_full, a_uses & 1, p.err, 23);
@@ -583,9 +588,10 @@ __global__ void __launch_bounds__(kTcThreadsB, 1)
         };
         int rb_cur = -1, row = 0;
         int64_t pending = -1;
-        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        TileCursor cur(t_begin, p.CT);
+        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
             const int64_t i = t - t_begin;
-            const int rb = rb_of(t), ct = (int)(t % p.CT);
+            const int rb = cur.rb, ct = cur.ct;
             if (rb != rb_cur) {
                 if (pending >= 0) {
                     ok = drain(pending);

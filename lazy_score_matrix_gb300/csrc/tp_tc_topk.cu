@@ -113,9 +113,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
         if (lane == 0) {  // ---------------- TMA producer
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
                 const int64_t i = t - t_begin;
-                const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+                const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
                     if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 31);
                     if (!ok) break;
@@ -145,9 +146,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
             constexpr int KS = DP / 8;
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            for (int64_t t = t_begin; t < t_end && ok; ++t) {
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
                 const int64_t i = t - t_begin;
-                const int rb = (int)(t / p.CT);
+                const int rb = cur.rb;
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);
                     ok = mbar_wait(a_full, a_uses & 1, p.err, 33);
@@ -207,9 +209,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
             ++seg;
         };
         reset();
-        for (int64_t t = t_begin; t < t_end && ok; ++t) {
+        TileCursor cur(t_begin, p.CT);
+        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
             const int64_t i = t - t_begin;
-            const int rb = (int)(t / p.CT), ct = (int)(t % p.CT);
+            const int rb = cur.rb, ct = cur.ct;
             if (rb != rb_cur) {
                 if (rb_cur >= 0) flush();
                 reset();
