@@ -49,6 +49,20 @@ inline bool make_map(CUtensorMap* m, const float* base, int64_t rows) { return m
 // feature-major [64, cols] arrays (cols a multiple of 64): boxes of 32 columns x 64 feature rows
 inline bool make_map_t(CUtensorMap* m, const float* base, int64_t cols) { return make_map_2d(m, base, cols, 64, 64); }
 
+// Row-major [rows, 64] fp16 (128-byte rows) with boxes of the full row x box_rows rows, 128-byte swizzle;
+// rows past the end read as zeros.
+inline bool make_map_f16(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace tc

@@ -79,10 +79,10 @@ def test_workspace_sizes_from_shapes(lib):
     # fp64 partial states are twice the fp32 ones (D = 32: no tensor-core path)
     a32 = ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 32))
     assert ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 32, _lib.TP_F64)) >= 2 * a32 - 512
-    # fp32, D = 64: room for the tensor-core path's hi/lo split (512 bytes per distinct point)
-    assert a >= 2 * 8192 * 512
+    # fp32, D = 64: room for the tensor-core path's fp16 hi/lo split (256 bytes per distinct point)
+    assert a >= 2 * 8192 * 256
     same = ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 64, X=FAKE, Y=FAKE))
-    assert 8192 * 512 <= same < a
+    assert 8192 * 256 <= same < a
 
 
 def call_matmul(lib, p, s, V=FAKE + 0x200000, C=4, out=FAKE + 0x300000, w=None, n=0):
