@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
                 float t0[16], t1[16];
-                tmem_ld16(lane_base + (uint32_t)(b * 256 + hlf * 16), t0);
-                tmem_ld16(lane_base + (uint32_t)(b * 256 + 128 + hlf * 16), t1);
+                tmem_ld16x2(lane_base + (uint32_t)(b * 256 + hlf * 16), lane_base + (uint32_t)(b * 256 + 128 + hlf * 16),
+                            t0, t1);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) v[hlf * 16 + u] = t0[u] + t1[u];
             }
@@ -559,8 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait(dz_full, (uint32_t)(j & 1), p.err, 27)) return false;
             fence_after_sync();
             float v[kColsB], w[kColsB];
-            tmem_ld<kColsB>(tDZ + lane_off + (uint32_t)(part * kColsB), v);
-            tmem_ld<kColsB>(tDZ + lane_off + (uint32_t)(64 + part * kColsB), w);
+            tmem_ld16x2(tDZ + lane_off + (uint32_t)(part * kColsB), tDZ + lane_off + (uint32_t)(64 + part * kColsB), v, w);
 #pragma unroll
             for (int u = 0; u < kColsB; ++u) dacc[u] += (v[u] + w[u]) * inv;
             fence_before_sync();
@@ -611,8 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float4* st = sStat + s * kBNb + part * kColsB;
             const uint32_t col = (uint32_t)(b * 128 + part * kColsB);
             float v[kColsB], w[kColsB];
-            tmem_ld<kColsB>(tmem + lane_off + col, v);       // hi*hi
-            tmem_ld<kColsB>(tmem + lane_off + col + 64, w);  // hi*lo + lo*hi
+            tmem_ld16x2(tmem + lane_off + col, tmem + lane_off + col + 64, v, w);  // hi*hi, hi*lo + lo*hi
             float ksum = 0.f, pm = 0.f;
 #pragma unroll
             for (int u = 0; u < kColsB; ++u) {
