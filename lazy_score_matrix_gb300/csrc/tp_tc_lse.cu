@@ -276,6 +276,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool diag = row >= j0 && row < j0 + 32;
             const bool masked = p.M - j0 < 32 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
             const float4* ys4 = reinterpret_cast<const float4*>(p.ys + j0);  // padded: 32 readable entries
+            if (METRIC == kLinear && !EXP && !masked && c1r > 0.f) {
+                // common case: score c1r * (x.y 2^(e_x+e_y)) 2^-e_y with c1r = scale log2(e) 2^-e_x > 0. The
+                // row factor commutes with the max and folds into the exp's FMA.
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                    const float4 c4 = __ldg(ys4 + u4);
+                    v[u4 * 4 + 0] *= c4.x;
+                    v[u4 * 4 + 1] *= c4.y;
+                    v[u4 * 4 + 2] *= c4.z;
+                    v[u4 * 4 + 3] *= c4.w;
+                }
+                float c4m[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) c4m[a] = ninf<float>();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) c4m[u & 3] = fmaxf(c4m[u & 3], v[u]);
+                const float cmax = fmaxf(fmaxf(c4m[0], c4m[1]), fmaxf(c4m[2], c4m[3])) * c1r;
+                if (cmax > m) {
+                    l *= ExpTraits<float>::bexp(m - cmax);
+                    m = cmax;
+                }
+                float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u = 0; u < 32; ++u) s4[u & 3] += ExpTraits<float>::bexp(fmaf(v[u], c1r, -m));
+                l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                continue;
+            }
 #pragma unroll
             for (int u4 = 0; u4 < 8; ++u4) {
                 const float4 c4 = __ldg(ys4 + u4);
@@ -397,7 +424,7 @@ struct LseBwdTcParams {
     int metric, apply_exp, exclude_self;
     float scale, neg_gamma_log2, two_gamma;
     const float* zn;      // |z_k|^2
-    const float4* stat;   // [ceil(N/64)*64]: (lse_j log2 e, g_j, 2^-e_j, 0), padded with (+inf, 0, 0, 0)
+    const float4* stat;   // [ceil(N/64)*64]: (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j), padding (+inf, 0, 0, 0)
     float* part;          // [G][smax][kPartRowsB][128]: dZ features, then each part's sum of kappa, row-minor
     int* err;
 };
@@ -549,7 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int N32 = (int)p.N;
         int seg = 0;
-        float K0 = 0.f, lse2k = 0.f, gk = 0.f, zn_k = 0.f, rs_k = 0.f;
+        float K0 = 0.f, lse2k = 0.f, gk = 0.f, zn_k = 0.f, rs_k = 0.f, rsl = 0.f;
         float dacc[kColsB];
 #pragma unroll
         for (int f = 0; f < kColsB; ++f) dacc[f] = 0.f;
@@ -596,6 +623,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 lse2k = st.x;
                 gk = st.y;
                 rs_k = st.z;
+                rsl = rs_k * p.scale * kL2E;
                 zn_k = (METRIC != kLinear && live) ? p.zn[row] : 0.f;
             }
             const int b = (int)(i % kSBuf), s = (int)(i % kStagesS);
@@ -612,9 +640,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float v[kColsB], w[kColsB];
             tmem_ld16x2(tmem + lane_off + col, tmem + lane_off + col + 64, v, w);  // hi*hi, hi*lo + lo*hi
             float ksum = 0.f, pm = 0.f;
+            // columns that need care in this warp: padding past N, or the pair (row, row)
+            const bool edge = lim < kColsB || (self >= 0 && self < kColsB && (p.exclude_self || METRIC != kLinear));
+            if (METRIC == kLinear && !EXP && !__any_sync(0xffffffffu, edge)) {
+                // common case: s2 = (x.y 2^(e_k+e_j)) 2^-e_j 2^-e_k scale log2(e); kappa 2^-e_j = G scale 2^-e_j
+#pragma unroll
+                for (int u = 0; u < kColsB; ++u) {
+                    const float4 sj = st[u];
+                    const float s2 = (v[u] + w[u]) * sj.z * rsl;
+                    const float G = gk * ExpTraits<float>::bexp(s2 - lse2k) + sj.y * ExpTraits<float>::bexp(s2 - sj.x);
+                    const float kp = G * sj.w;
+                    v[u] = kp;
+                    pm = fmaxf(pm, fabsf(kp));
+                }
+            } else {
 #pragma unroll
             for (int u = 0; u < kColsB; ++u) {
-                const float4 sj = st[u];                     // (lse_j log2 e, g_j, 2^-e_j, 0)
+                const float4 sj = st[u];                     // (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j)
                 float dot = (v[u] + w[u]) * sj.z * rs_k;
                 if (METRIC != kLinear && u == self) dot = zn_k;  // |z - z|^2 = 0 exactly
                 float base;
@@ -637,6 +679,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float kp = kap * sj.z;                 // z_j = 2^-e_j (z_j 2^e_j): fold the column's scale
                 v[u] = kp;
                 pm = fmaxf(pm, fabsf(kp));
+            }
             }
             K0 += ksum;
             // the row's largest |kappa 2^-e_j| over the tile: the four parts of the quarter exchange theirs
@@ -732,9 +775,9 @@ __global__ void __launch_bounds__(kMergeThreads) lse_bwd_tc_merge(LseBwdTcParams
 }
 
 // Backward pre-pass, one warp per row over the padded rows: the fp16 hi/lo split of z 2^e, |z|^2 and the
-// column stats (lse_j log2 e, g_j, 2^-e_j, 0), (+inf, 0, 0, 0) for padding rows.
+// column stats (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j), (+inf, 0, 0, 0) for padding rows.
 __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ z, const float* __restrict__ lse,
-                                                      const float* __restrict__ g, int64_t N, int64_t Npad,
+                                                      const float* __restrict__ g, float scale, int64_t N, int64_t Npad,
                                                       __half2* __restrict__ hi, __half2* __restrict__ lo,
                                                       float* __restrict__ zn, float4* __restrict__ stat) {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -760,7 +803,7 @@ __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ 
     lo[r * 32 + lane] = __floats2half2_rn(a - hf.x, b - hf.y);
     if (lane == 0) {
         zn[r] = ss;
-        stat[r] = make_float4(lse[r] * 1.4426950408889634f, g[r], pow2i(-e), 0.f);
+        stat[r] = make_float4(lse[r] * 1.4426950408889634f, g[r], pow2i(-e), scale * pow2i(-e));
     }
 }
 
@@ -917,8 +960,8 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     {
         HookScope h("lse_bwd_prep", s);
         lse_bwd_prep16<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
-            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse), a.nP,
-            pl.Npad, zh, zl, zn, stat);
+            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
+            (float)a.scale, a.nP, pl.Npad, zh, zl, zn, stat);
         ++n;
     }
     LseBwdTcParams p;
