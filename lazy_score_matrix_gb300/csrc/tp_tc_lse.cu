@@ -353,7 +353,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Partials of each row, in CTA order, into lse (natural log).
+// Partials of each row, in CTA order, into lse (natural log): one pass, combining the (max, sum) pairs
+// online in a fixed order, so the result does not depend on timing.
 __global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.N) return;
@@ -361,24 +362,29 @@ __global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
     const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
     // first CTA whose range holds t0, last whose range holds t1 (ranges are sorted and contiguous)
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
-    float m = ninf<float>();
+    float m = ninf<float>(), l = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-        for (int h = 0; h < 4; ++h) m = fmaxf(m, p.part[((size_t)((c * p.smax + seg) * 4 + h) * 2) * kBM + lr]);
-    }
-    float l = 0.f;
-    if (m > ninf<float>()) {
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
-            for (int h = 0; h < 4; ++h) {
-                const float* o = p.part + ((size_t)((c * p.smax + seg) * 4 + h) * 2) * kBM;
-                if (o[lr] > ninf<float>()) l += o[kBM + lr] * ExpTraits<float>::bexp(o[lr] - m);
+        const float* o = p.part + ((size_t)((c * p.smax + seg) * 4) * 2) * kBM + lr;
+        float pm[4], pl[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            pm[h] = o[(size_t)h * 2 * kBM];
+            pl[h] = o[(size_t)h * 2 * kBM + kBM];
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if (pm[h] == ninf<float>()) continue;
+            if (pm[h] > m) {
+                l = l * ExpTraits<float>::bexp(m - pm[h]) + pl[h];
+                m = pm[h];
+            } else {
+                l += pl[h] * ExpTraits<float>::bexp(pm[h] - m);
             }
         }
     }
     lse[i] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : ninf<float>();
 }
-
 
 // ------------------------------------------------------------------------------------------------
 // Symmetric backward (X = Y = z, no row/column parameters): z.grad_k = sum_j kappa_kj z_j
@@ -727,50 +733,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa. One block per row block:
-// the partials ([kPartRowsB][128] floats each, feature-major) are read coalesced, summed in CTA order in
-// registers, and transposed through shared memory so the gradient rows are written coalesced too.
+// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa. One block per (row block,
+// 16 features): the partials ([kPartRowsB][128] floats each, feature-major) are read coalesced, summed
+// in CTA order in registers, and transposed through shared memory so the gradient is written in
+// 64-byte row segments.
 constexpr int kMergeThreads = 256;
-static_assert((64 * kBM) % kMergeThreads == 0 && (kPartsB * kBM) % kMergeThreads == 0, "merge thread mapping");
+constexpr int kMergeF = 16;  // features per block
+static_assert((kMergeF * kBM) % kMergeThreads == 0 && kPartsB * kBM <= 2 * kMergeThreads, "merge thread mapping");
 __global__ void __launch_bounds__(kMergeThreads) lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z,
                                                                  float* __restrict__ grad) {
-    __shared__ float sd[64][kBM + 1];
-    __shared__ float sk[kPartsB * kBM];
-    const int rb = blockIdx.x;
+    __shared__ float sd[kMergeF][kBM + 1];
+    __shared__ float sk[kBM];
+    const int rb = blockIdx.x, f0 = blockIdx.y * kMergeF;
     const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
-    constexpr int kPer = 64 * kBM / kMergeThreads;       // (feature, row) elements per thread
-    constexpr int kPerK = kPartsB * kBM / kMergeThreads;  // kappa sums (part, row) per thread
-    float acc[kPer], k0[kPerK];
+    constexpr int kPer = kMergeF * kBM / kMergeThreads;  // (feature, row) elements per thread
+    float acc[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
-#pragma unroll
-    for (int u = 0; u < kPerK; ++u) k0[u] = 0.f;
+    float k0 = 0.f;  // threads < 128: the kappa sums of row threadIdx.x over the parts
     for (int c = c_lo; c <= c_hi; ++c) {
         const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
         const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsB * kBM;
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) acc[u] += o[u * kMergeThreads + threadIdx.x];
+        for (int u = 0; u < kPer; ++u) acc[u] += o[(size_t)f0 * kBM + u * kMergeThreads + threadIdx.x];
+        if (p.metric != kLinear && threadIdx.x < kBM) {
 #pragma unroll
-        for (int u = 0; u < kPerK; ++u) k0[u] += o[64 * kBM + u * kMergeThreads + threadIdx.x];
+            for (int qq = 0; qq < kPartsB; ++qq) k0 += o[(size_t)(64 + qq) * kBM + threadIdx.x];
+        }
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int e = u * kMergeThreads + threadIdx.x;
         sd[e / kBM][e % kBM] = acc[u];
     }
-#pragma unroll
-    for (int u = 0; u < kPerK; ++u) sk[u * kMergeThreads + threadIdx.x] = k0[u];
+    if (threadIdx.x < kBM) sk[threadIdx.x] = k0;
     __syncthreads();
-    for (int e = threadIdx.x; e < 64 * kBM; e += kMergeThreads) {
-        const int lr = e / 64, f = e % 64;
+    for (int e = threadIdx.x; e < kMergeF * kBM; e += kMergeThreads) {
+        const int lr = e / kMergeF, f = e % kMergeF;
         const int64_t i = (int64_t)rb * kBM + lr;
         if (i >= p.N) break;  // rows only grow with e
         const float dz = sd[f][lr];
-        float ks = 0.f;
-#pragma unroll
-        for (int qq = 0; qq < kPartsB; ++qq) ks += sk[qq * kBM + lr];
-        grad[i * 64 + f] = p.metric == kLinear ? dz : dz - z[i * 64 + f] * ks;
+        grad[i * 64 + f0 + f] = p.metric == kLinear ? dz : dz - z[i * 64 + f0 + f] * sk[lr];
     }
 }
 
@@ -936,7 +940,7 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     ++n;
     {
         HookScope h("lse_tc_merge", s);
-        lse_tc_merge<<<(unsigned)((a.nP + 127) / 128), 128, 0, s>>>(p, static_cast<float*>(lse));
+        lse_tc_merge<<<(unsigned)((a.nP + 31) / 32), 32, 0, s>>>(p, static_cast<float*>(lse));
         ++n;
     }
     return n;
@@ -992,7 +996,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     ++n;
     {
         HookScope h("lse_bwd_tc_merge", s);
-        lse_bwd_tc_merge<<<(unsigned)((a.nP + kBM - 1) / kBM), kMergeThreads, 0, s>>>(
+        lse_bwd_tc_merge<<<dim3((unsigned)((a.nP + kBM - 1) / kBM), 64 / kMergeF), kMergeThreads, 0, s>>>(
             p, static_cast<const float*>(a.P), static_cast<float*>(a.gP));
         ++n;
     }
