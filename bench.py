@@ -46,7 +46,8 @@ def peaks():
         "sm_max_mhz": sm_mhz,
         "fp32_tflops": SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12,
         "fp64_tflops": 1.25,  # nominal GB300 FP64 rate (no measured figure)
-        # tf32 tensor peak: the measured bf16 burst peak x the nominal tf32/bf16 ratio (1.1 / 2.25)
+        # fp16 tensor peak = the measured bf16 burst peak (same rate); tf32 = that x the nominal 1.1 / 2.25
+        "f16_tflops": float(p.get("bf16_tflops", 1900.0)),
         "tf32_tflops": float(p.get("bf16_tflops", 1900.0)) * 1.1 / 2.25,
         "source": "MEASURED_PEAKS.json" if p else "fallback",
     }
@@ -193,10 +194,11 @@ class InfoNCE(Workload):
         # algorithmic flop per pair and launch (FMA = 2): forward 2D+3; backward 387 = (2D+3) + 2D + 2D,
         # the row sweep credited with the recompute and dX, the column sweep with dY only; a kernel
         # that produces the whole backward (X = Y, one symmetric sweep) is credited with all of it.
-        # (kernel: (flop per pair, bound)); "tensor" kernels run the contraction on tcgen05 (tf32)
+        # (kernel: (flop per pair, bound)); "tensor-f16" kernels run the contraction on tcgen05 kind::f16
+        # (scaled fp16 hi/lo split), credited with the algorithmic flop against the fp16 tensor peak
         self.flops_per_pair = {"fwd_sweep_lse": (D2 + 3, "alu"), "bwd_sweep_lse_row": (D2 + 3 + D2, "alu"),
                                "bwd_sweep_lse_col": (D2, "alu"), "bwd_sweep_lse_sym": (D2 + 3 + D2 + D2, "alu"),
-                               "lse_fwd_tc": (D2 + 3, "tensor"), "lse_bwd_sym_tc": (D2 + 3 + D2 + D2, "tensor")}
+                               "lse_fwd_tc": (D2 + 3, "tensor-f16"), "lse_bwd_sym_tc": (D2 + 3 + D2 + D2, "tensor-f16")}
         self.step_flops_per_pair = (D2 + 3) + (D2 + 3 + D2 + D2)
 
     def step(self):
@@ -283,7 +285,7 @@ class Knn(Workload):
         self.d2h = self.N * self.k * 12
         # the SIMT sweep runs the distance on the FP32 pipe; the tensor-core kernel runs the contraction
         # on tcgen05 (tf32) and the selection on the ALUs: it is credited with the same algorithmic flop
-        self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu"), "topk_tc": (2 * self.D + 2, "tensor")}
+        self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu"), "topk_tc": (2 * self.D + 2, "tensor-tf32")}
         self.step_flops_per_pair = 2 * self.D + 2
 
     def step(self):
@@ -467,15 +469,20 @@ def gpu_arm(args, rank, world):
     if credit is not None:
         fpp, bound = credit
         ach = fpp * wl.pairs / (dstat["avg_ms"] / 1e3) / 1e12
-        if bound == "tensor":
+        if bound == "tensor-f16":
+            peak = pk["f16_tflops"]
+            src = f"fp16 tensor (kind::f16 operands): measured bf16 {pk['f16_tflops']:.0f} TFLOP/s, same rate, of measured"
+        elif bound == "tensor-tf32":
             peak = pk["tf32_tflops"]
-            src = (f"tf32 tensor: measured bf16 {pk['tf32_tflops'] * 2.25 / 1.1:.0f} TFLOP/s x 1.1/2.25 "
+            src = (f"tf32 tensor: measured bf16 {pk['f16_tflops']:.0f} TFLOP/s x 1.1/2.25 "
                    f"(nominal tf32/bf16), of measured")
         else:
             peak = pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]
             src = (f"FP32 pipe: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x {pk['sm_max_mhz']:.0f} MHz "
                    f"(derived from unit counts and the measured max clock)")
-        roof = {"kernel": dname, "bound": bound, "achieved": round(ach, 3), "peak": round(peak, 2),
+        roof = {"kernel": dname, "bound": "tensor" if bound.startswith("tensor") else bound,
+                "operands": bound[len("tensor-"):] if bound.startswith("tensor") else "fp32",
+                "achieved": round(ach, 3), "peak": round(peak, 2),
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname),
                 "peak_source": src, "flop_per_pair": fpp}
     step_tflops = wl.step_flops_per_pair * wl.pairs / (ms_step / 1e3) / 1e12
