@@ -11,7 +11,8 @@
 namespace tp {
 namespace tc {
 
-constexpr int kWaitLimit = 1 << 24;  // polls of an mbarrier before a wait gives up
+constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait on an mbarrier gives up after 2 s
+constexpr uint32_t kSuspendNs = 20000;                   // longest a single poll may sleep in hardware
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -20,20 +21,33 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
+// One poll: true once the phase with the given parity has completed. The suspend-time hint lets the
+// hardware park the thread until the phase completes (or the hint expires) instead of spinning, so
+// waiting warps leave their issue slots to the warps that work.
 __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false (and *err set) after kWaitLimit polls.
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; false (and *err set) after kWaitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
-    for (int i = 0; i < kWaitLimit; ++i)
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
         if (mbar_try(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
     atomicExch(err, code);
     return false;
 }

@@ -38,9 +38,21 @@ constexpr int kEpi = 16;                    // epilogue warps: 4 per TMEM lane q
 constexpr int kTcThreads = 32 * (2 + kEpi);
 constexpr int kGrid = 152;                  // persistent CTAs: one per GB300 SM
 
-__host__ __device__ inline int64_t range_start(int64_t T, int G, int c) { return (T * c) / G; }
+// First tile of CTA c: floor(T c / G). 32-bit division whenever T G fits (every practical size).
+__host__ __device__ inline int64_t range_start(int64_t T, int G, int c) {
+    if ((unsigned long long)T * (unsigned)G < (1ull << 32)) return (int64_t)((uint32_t)T * (uint32_t)c / (uint32_t)G);
+    return (T * c) / G;
+}
 // The CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1).
-__host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) { return (int)(((int64_t)G * (t + 1) - 1) / T); }
+__host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) {
+    if ((unsigned long long)T * (unsigned)G < (1ull << 32))
+        return (int)(((uint32_t)G * (uint32_t)(t + 1) - 1u) / (uint32_t)T);
+    return (int)(((int64_t)G * (t + 1) - 1) / T);
+}
+// Row block of tile t (t < T).
+__host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
+    return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
+}
 
 // Base-2 score of one element from its dot product (metric, scale, exp).
 template <int METRIC, bool EXP>
@@ -364,7 +376,7 @@ __global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float m = ninf<float>(), l = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
         const float* o = p.part + ((size_t)((c * p.smax + seg) * 4) * 2) * kBM + lr;
         float pm[4], pl[4];
 #pragma unroll
@@ -753,7 +765,7 @@ __global__ void __launch_bounds__(kMergeThreads) lse_bwd_tc_merge(LseBwdTcParams
     for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
     float k0 = 0.f;  // threads < 128: the kappa sums of row threadIdx.x over the parts
     for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - (int)(range_start(p.T, p.G, c) / p.CT);
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
         const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsB * kBM;
 #pragma unroll
         for (int u = 0; u < kPer; ++u) acc[u] += o[(size_t)f0 * kBM + u * kMergeThreads + threadIdx.x];
