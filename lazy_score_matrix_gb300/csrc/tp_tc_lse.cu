@@ -77,12 +77,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
 }
 
 // Per point row: the fp16 hi/lo split of x 2^e, 2^-e, and |x|^2. One warp per row, two features per
-// lane. rows: rows of x; rows_pad: rows of inv_scale and norm (zeros past rows).
+// lane. rows: rows of x; rows_pad: rows of inv_scale and norm (zeros past rows); cnt (optional): ncnt
+// counters zeroed for the kernel that follows (ncnt <= rows_pad).
 __global__ void __launch_bounds__(256) tc_split16(const float* __restrict__ x, int64_t rows, int64_t rows_pad,
                                                   __half2* __restrict__ hi, __half2* __restrict__ lo,
-                                                  float* __restrict__ inv_scale, float* __restrict__ norm) {
+                                                  float* __restrict__ inv_scale, float* __restrict__ norm,
+                                                  int* __restrict__ cnt, int64_t ncnt) {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    if (cnt && lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
     if (r >= rows_pad) return;
     if (r >= rows) {
         if (lane == 0) {
@@ -136,8 +139,39 @@ struct LseTcParams {
     const float* xn;       // |x_i|^2 (distance metrics)
     const float* yn;       // |y_j|^2
     float* part;           // [G][smax][4 column parts][2][128] partial (max, sum) in base 2
+    int* cnt;              // [RB] CTAs done with each row block (zeroed by the split pre-pass)
+    float* lse;            // [N] output
     int* err;
 };
+
+// lse of row `row` of row block rb from the partials of every CTA that saw it, in CTA order (one
+// pass, combining the (max, sum) pairs online in a fixed order: the result does not depend on timing).
+__device__ __noinline__ float lse_merge_row(const LseTcParams& p, int rb, int lr) {
+    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
+    float m = ninf<float>(), l = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
+        const float* o = p.part + ((size_t)((c * p.smax + seg) * 4) * 2) * kBM + lr;
+        float pm[4], pl[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            pm[h] = __ldcg(o + (size_t)h * 2 * kBM);
+            pl[h] = __ldcg(o + (size_t)h * 2 * kBM + kBM);
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if (pm[h] == ninf<float>()) continue;
+            if (pm[h] > m) {
+                l = l * ExpTraits<float>::bexp(m - pm[h]) + pl[h];
+                m = pm[h];
+            } else {
+                l += pl[h] * ExpTraits<float>::bexp(pm[h] - m);
+            }
+        }
+    }
+    return l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : ninf<float>();
+}
 
 template <int METRIC, bool EXP>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -154,7 +188,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* b_empty = b_full + kStagesF;       // [kStagesF]
     uint64_t* acc_full = b_empty + kStagesF;     // [2]
     uint64_t* acc_empty = acc_full + 2;          // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* fl_bar = acc_empty + 2;            // the epilogue wrote its partials of a row block
+    uint64_t* dec_bar = fl_bar + 1;              // the CTA knows whether it merges that row block
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
+    volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
@@ -170,6 +207,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(acc_full + b, 1);
             mbar_init(acc_empty + b, 32 * kEpi);
         }
+        mbar_init(fl_bar, 32 * kEpi);
+        mbar_init(dec_bar, 1);
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tslot, 512);
@@ -248,10 +287,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int rb_cur = -1, seg = 0;
         float m = ninf<float>(), l = 0.f, xn = 0.f, c1r = 0.f, xs = 0.f;
         bool ok = true;
+        const int etid = threadIdx.x - 64;  // 0 .. 32 kEpi - 1
+        // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
+        // of the CTAs whose tile ranges meet it to count itself in) merges its rows into lse.
         auto flush = [&]() {
             float* o = p.part + ((size_t)((blockIdx.x * p.smax + seg) * 4 + sub) * 2) * kBM;
             o[lr] = m;
             o[kBM + lr] = l;
+            __threadfence();
+            mbar_arrive(fl_bar);
+            if (etid == 0) {
+                int last = 0;
+                if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 17)) {
+                    const int64_t t0 = (int64_t)rb_cur * p.CT;
+                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
+                    __threadfence();
+                }
+                *sflag = last;
+                mbar_arrive(dec_bar);
+            }
+            if (mbar_wait(dec_bar, (uint32_t)(seg & 1), p.err, 18) && *sflag && etid < kBM) {
+                const int64_t r = (int64_t)rb_cur * kBM + etid;
+                if (r < p.N) p.lse[r] = lse_merge_row(p, rb_cur, etid);
+            }
             ++seg;
         };
         TileCursor cur(t_begin, p.CT);
@@ -365,39 +424,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Partials of each row, in CTA order, into lse (natural log): one pass, combining the (max, sum) pairs
-// online in a fixed order, so the result does not depend on timing.
-__global__ void lse_tc_merge(LseTcParams p, float* __restrict__ lse) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= p.N) return;
-    const int rb = (int)(i / kBM), lr = (int)(i % kBM);
-    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
-    // first CTA whose range holds t0, last whose range holds t1 (ranges are sorted and contiguous)
-    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
-    float m = ninf<float>(), l = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
-        const float* o = p.part + ((size_t)((c * p.smax + seg) * 4) * 2) * kBM + lr;
-        float pm[4], pl[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            pm[h] = o[(size_t)h * 2 * kBM];
-            pl[h] = o[(size_t)h * 2 * kBM + kBM];
-        }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            if (pm[h] == ninf<float>()) continue;
-            if (pm[h] > m) {
-                l = l * ExpTraits<float>::bexp(m - pm[h]) + pl[h];
-                m = pm[h];
-            } else {
-                l += pl[h] * ExpTraits<float>::bexp(pm[h] - m);
-            }
-        }
-    }
-    lse[i] = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : ninf<float>();
-}
-
 // ------------------------------------------------------------------------------------------------
 // Symmetric backward (X = Y = z, no row/column parameters): z.grad_k = sum_j kappa_kj z_j
 // - [distance metric] z_k sum_j kappa_kj, with kappa_kj the coefficient of z_j in d/dz_k of
@@ -444,8 +470,46 @@ struct LseBwdTcParams {
     const float* zn;      // |z_k|^2
     const float4* stat;   // [ceil(N/64)*64]: (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j), padding (+inf, 0, 0, 0)
     float* part;          // [G][smax][kPartRowsB][128]: dZ features, then each part's sum of kappa, row-minor
+    int* cnt;             // [RB] CTAs done with each row block (zeroed by the pre-pass)
+    const float* z;       // [N][64] the points (distance metrics subtract z_k sum_j kappa_kj)
+    float* grad;          // [N][64] output: z.grad
     int* err;
 };
+
+// z.grad for features [16 fg, 16 fg + 16) of row lr of row block rb from the partials of every CTA that
+// saw the row block, added in CTA order: dZ - [distance metric] z sum kappa.
+__device__ __noinline__ void bwd_merge_row(const LseBwdTcParams& p, int rb, int lr, int fg) {
+    const int64_t row = (int64_t)rb * kBM + lr;
+    if (row >= p.N) return;
+    const int64_t t0 = (int64_t)rb * p.CT;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t0 + p.CT - 1);
+    float acc[16], k0 = 0.f;
+#pragma unroll
+    for (int f = 0; f < 16; ++f) acc[f] = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
+        const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsB * kBM + lr;
+#pragma unroll
+        for (int f = 0; f < 16; ++f) acc[f] += __ldcg(o + (size_t)(fg * 16 + f) * kBM);
+        if (p.metric != kLinear) {
+#pragma unroll
+            for (int qq = 0; qq < kPartsB; ++qq) k0 += __ldcg(o + (size_t)(64 + qq) * kBM);
+        }
+    }
+    float4* g4 = reinterpret_cast<float4*>(p.grad + row * 64 + fg * 16);
+    if (p.metric == kLinear) {
+#pragma unroll
+        for (int f4 = 0; f4 < 4; ++f4) g4[f4] = make_float4(acc[4 * f4], acc[4 * f4 + 1], acc[4 * f4 + 2], acc[4 * f4 + 3]);
+    } else {
+        const float4* z4 = reinterpret_cast<const float4*>(p.z + row * 64 + fg * 16);
+#pragma unroll
+        for (int f4 = 0; f4 < 4; ++f4) {
+            const float4 zz = z4[f4];
+            g4[f4] = make_float4(acc[4 * f4] - zz.x * k0, acc[4 * f4 + 1] - zz.y * k0, acc[4 * f4 + 2] - zz.z * k0,
+                                 acc[4 * f4 + 3] - zz.w * k0);
+        }
+    }
+}
 
 template <int METRIC, bool EXP>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -469,7 +533,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* dz_full = w_full + kSBuf;
     uint64_t* dz_empty = dz_full + 1;
     uint64_t* xch = dz_empty + 1;                // [quarter][parity]: the row-maximum exchange
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(xch + 8);
+    uint64_t* fl_bar = xch + 8;                  // the epilogue wrote its partials of a row block
+    uint64_t* dec_bar = fl_bar + 1;              // the CTA knows whether it merges that row block
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
+    volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
@@ -489,6 +556,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(dz_full, 1);
         mbar_init(dz_empty, 32 * kEpi);
         for (int x = 0; x < 8; ++x) mbar_init(xch + x, 32 * kPartsB);
+        mbar_init(fl_bar, 32 * kEpi);
+        mbar_init(dec_bar, 1);
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tslot, 512);
@@ -611,14 +680,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(dz_empty);
             return true;
         };
+        int rb_cur = -1, row = 0;
+        const int etid = threadIdx.x - 64;  // 0 .. 32 kEpi - 1
+        // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
+        // of the CTAs whose tile ranges meet it to count itself in) merges it into z.grad.
         auto write_partial = [&]() {
             float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * kPartRowsB * kBM;
 #pragma unroll
             for (int f = 0; f < kColsB; ++f) o[(size_t)(part * kColsB + f) * kBM + lr] = dacc[f];
             o[(size_t)(64 + part) * kBM + lr] = K0;
+            __threadfence();
+            mbar_arrive(fl_bar);
+            if (etid == 0) {
+                int last = 0;
+                if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 33)) {
+                    const int64_t t0 = (int64_t)rb_cur * p.CT;
+                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
+                    __threadfence();
+                }
+                *sflag = last;
+                mbar_arrive(dec_bar);
+            }
+            if (mbar_wait(dec_bar, (uint32_t)(seg & 1), p.err, 34) && *sflag) bwd_merge_row(p, rb_cur, etid % kBM, etid / kBM);
             ++seg;
         };
-        int rb_cur = -1, row = 0;
         int64_t pending = -1;
         float pend_inv = 0.f;
         TileCursor cur(t_begin, p.CT);
@@ -745,59 +831,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// z.grad rows from the partials (CTA order): dZ - [distance] z * sum kappa. One block per (row block,
-// 16 features): the partials ([kPartRowsB][128] floats each, feature-major) are read coalesced, summed
-// in CTA order in registers, and transposed through shared memory so the gradient is written in
-// 64-byte row segments.
-constexpr int kMergeThreads = 256;
-constexpr int kMergeF = 16;  // features per block
-static_assert((kMergeF * kBM) % kMergeThreads == 0 && kPartsB * kBM <= 2 * kMergeThreads, "merge thread mapping");
-__global__ void __launch_bounds__(kMergeThreads) lse_bwd_tc_merge(LseBwdTcParams p, const float* __restrict__ z,
-                                                                 float* __restrict__ grad) {
-    __shared__ float sd[kMergeF][kBM + 1];
-    __shared__ float sk[kBM];
-    const int rb = blockIdx.x, f0 = blockIdx.y * kMergeF;
-    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
-    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
-    constexpr int kPer = kMergeF * kBM / kMergeThreads;  // (feature, row) elements per thread
-    float acc[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) acc[u] = 0.f;
-    float k0 = 0.f;  // threads < 128: the kappa sums of row threadIdx.x over the parts
-    for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
-        const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsB * kBM;
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) acc[u] += o[(size_t)f0 * kBM + u * kMergeThreads + threadIdx.x];
-        if (p.metric != kLinear && threadIdx.x < kBM) {
-#pragma unroll
-            for (int qq = 0; qq < kPartsB; ++qq) k0 += o[(size_t)(64 + qq) * kBM + threadIdx.x];
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int e = u * kMergeThreads + threadIdx.x;
-        sd[e / kBM][e % kBM] = acc[u];
-    }
-    if (threadIdx.x < kBM) sk[threadIdx.x] = k0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < kMergeF * kBM; e += kMergeThreads) {
-        const int lr = e / kMergeF, f = e % kMergeF;
-        const int64_t i = (int64_t)rb * kBM + lr;
-        if (i >= p.N) break;  // rows only grow with e
-        const float dz = sd[f][lr];
-        grad[i * 64 + f0 + f] = p.metric == kLinear ? dz : dz - z[i * 64 + f0 + f] * sk[lr];
-    }
-}
-
 // Backward pre-pass, one warp per row over the padded rows: the fp16 hi/lo split of z 2^e, |z|^2 and the
 // column stats (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j), (+inf, 0, 0, 0) for padding rows.
 __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ z, const float* __restrict__ lse,
                                                       const float* __restrict__ g, float scale, int64_t N, int64_t Npad,
                                                       __half2* __restrict__ hi, __half2* __restrict__ lo,
-                                                      float* __restrict__ zn, float4* __restrict__ stat) {
+                                                      float* __restrict__ zn, float4* __restrict__ stat,
+                                                      int* __restrict__ cnt, int64_t ncnt) {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    if (lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
     if (r >= Npad) return;
     if (r >= N) {
         if (lane == 0) stat[r] = make_float4(__int_as_float(0x7f800000), 0.f, 0.f, 0.f);
@@ -826,7 +869,7 @@ __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ 
 struct LseTcPlan {
     int64_t T, Xpad, Ypad;
     int CT, G, smax;
-    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_err, bytes;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_cnt, off_err, bytes;
 };
 
 static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
@@ -856,6 +899,7 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
         pl.off_yn = o; o += al256((size_t)pl.Ypad * 4);
     }
     pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 4 * 2 * kBM * 4);
+    pl.off_cnt = o; o += al256((size_t)RB * 4);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -864,7 +908,7 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
 struct LseBwdTcPlan {
     int64_t T, Npad;
     int CT, G, smax;
-    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_err, bytes;
+    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_cnt, off_err, bytes;
 };
 
 static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
@@ -882,6 +926,7 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     pl.off_zn = o; o += al256((size_t)N * 4);
     pl.off_stat = o; o += al256((size_t)pl.Npad * 16);
     pl.off_part = o; o += al256((size_t)pl.G * pl.smax * kPartRowsB * kBM * 4);
+    pl.off_cnt = o; o += al256((size_t)RB * 4);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -903,6 +948,7 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     float* ys = reinterpret_cast<float*>(ws + pl.off_ys);
     float* xn = reinterpret_cast<float*>(ws + pl.off_xn);
     float* yn = reinterpret_cast<float*>(ws + pl.off_yn);
+    int* cnt = reinterpret_cast<int*>(ws + pl.off_cnt);
     CUtensorMap mxh, mxl, myh, myl;
     if (!make_map_f16(&mxh, xh, a.nP, kBM) || !make_map_f16(&mxl, xl, a.nP, kBM) ||
         !make_map_f16(&myh, yh, a.nQ, kBN) || !make_map_f16(&myl, yl, a.nQ, kBN))
@@ -912,13 +958,13 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     {
         HookScope h("tc_split16", s);
         tc_split16<<<(unsigned)((xrows + 7) / 8), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, xrows, xh, xl, xs,
-                                                              xn);
+                                                              xn, cnt, pl.Xpad / kBM);
         ++n;
     }
     if (!same) {
         HookScope h("tc_split16", s);
         tc_split16<<<(unsigned)((pl.Ypad + 7) / 8), 256, 0, s>>>(static_cast<const float*>(a.Q), a.nQ, pl.Ypad, yh, yl,
-                                                                ys, yn);
+                                                                ys, yn, nullptr, 0);
         ++n;
     }
     LseTcParams p;
@@ -939,6 +985,8 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     p.xn = xn;
     p.yn = yn;
     p.part = reinterpret_cast<float*>(ws + pl.off_part);
+    p.cnt = cnt;
+    p.lse = static_cast<float*>(lse);
     p.err = reinterpret_cast<int*>(ws + pl.off_err);
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemF);
@@ -950,11 +998,6 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     else if (a.metric == kSqeuclidean) ex ? go(lse_fwd_tc<kSqeuclidean, true>) : go(lse_fwd_tc<kSqeuclidean, false>);
     else ex ? go(lse_fwd_tc<kRbf, true>) : go(lse_fwd_tc<kRbf, false>);
     ++n;
-    {
-        HookScope h("lse_tc_merge", s);
-        lse_tc_merge<<<(unsigned)((a.nP + 31) / 32), 32, 0, s>>>(p, static_cast<float*>(lse));
-        ++n;
-    }
     return n;
 }
 
@@ -968,6 +1011,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     __half2* zl = reinterpret_cast<__half2*>(ws + pl.off_zl);
     float* zn = reinterpret_cast<float*>(ws + pl.off_zn);
     float4* stat = reinterpret_cast<float4*>(ws + pl.off_stat);
+    int* cnt = reinterpret_cast<int*>(ws + pl.off_cnt);
     CUtensorMap mah, mal, mbh, mbl;
     if (!make_map_f16(&mah, zh, a.nP, kBM) || !make_map_f16(&mal, zl, a.nP, kBM) ||
         !make_map_f16(&mbh, zh, a.nP, kBNb) || !make_map_f16(&mbl, zl, a.nP, kBNb))
@@ -977,7 +1021,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         HookScope h("lse_bwd_prep", s);
         lse_bwd_prep16<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
             static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
-            (float)a.scale, a.nP, pl.Npad, zh, zl, zn, stat);
+            (float)a.scale, a.nP, pl.Npad, zh, zl, zn, stat, cnt, (a.nP + kBM - 1) / kBM);
         ++n;
     }
     LseBwdTcParams p;
@@ -995,6 +1039,9 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     p.zn = zn;
     p.stat = stat;
     p.part = reinterpret_cast<float*>(ws + pl.off_part);
+    p.cnt = cnt;
+    p.z = static_cast<const float*>(a.P);
+    p.grad = static_cast<float*>(a.gP);
     p.err = reinterpret_cast<int*>(ws + pl.off_err);
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemB);
@@ -1006,12 +1053,6 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     else if (a.metric == kSqeuclidean) ex ? go(lse_bwd_sym_tc<kSqeuclidean, true>) : go(lse_bwd_sym_tc<kSqeuclidean, false>);
     else ex ? go(lse_bwd_sym_tc<kRbf, true>) : go(lse_bwd_sym_tc<kRbf, false>);
     ++n;
-    {
-        HookScope h("lse_bwd_tc_merge", s);
-        lse_bwd_tc_merge<<<dim3((unsigned)((a.nP + kBM - 1) / kBM), 64 / kMergeF), kMergeThreads, 0, s>>>(
-            p, static_cast<const float*>(a.P), static_cast<float*>(a.gP));
-        ++n;
-    }
     return n;
 }
 
