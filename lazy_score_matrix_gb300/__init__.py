@@ -5,6 +5,7 @@ the same pass and never stored; first derivatives replay the pairs (torchpairwis
 Torchpairwise in Models"). The C ABI is include/tp.h; this package is its Python binding.
 """
 from .lazy import LazyScores, TopK, lazy, svgd_direction
+from .losses import mmd_statistics, sinkhorn_divergence
 from .ops import Score
 
-__all__ = ["LazyScores", "TopK", "lazy", "svgd_direction", "Score"]
+__all__ = ["LazyScores", "TopK", "lazy", "svgd_direction", "mmd_statistics", "sinkhorn_divergence", "Score"]

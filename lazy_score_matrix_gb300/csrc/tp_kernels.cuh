@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                     }
                     m = s;
                 }
-                const T pr = E::bexp(s - m);
+                const T pr = s > ninf<T>() ? E::bexp(s - m) : T(0);  // an empty element (-inf) adds 0, not NaN
                 l.tile += pr;
                 if constexpr (MODE == kSoftmax) axpy_smem<T, CP>(acc, pr, sv + jj * CP);
             } else if constexpr (MODE == kDisp) {

@@ -60,6 +60,7 @@ class LazyScores:
         o = LazyScores.__new__(LazyScores)
         o.X, o.Y, o._meta = self.X, self.Y, self._meta
         o.row_bias, o.col_bias, o.row_weight, o.col_weight = self.row_bias, self.col_bias, self.row_weight, self.col_weight
+        o._row_keep, o._col_keep = getattr(self, "_row_keep", None), getattr(self, "_col_keep", None)
         for k, v in kw.items():
             if k == "meta":
                 o._meta = v
@@ -117,46 +118,139 @@ class LazyScores:
     def score(self) -> Score:
         return self._meta.score(self.row_bias, self.col_bias, self.row_weight, self.col_weight)
 
+    @property
+    def T(self) -> "LazyScores":
+        """The transposed [M,N] matrix: S^T_ji = S_ij. Exact, because every base is symmetric in its two
+        points; the row and column parameters trade places."""
+        o = self._with(row_bias=self.col_bias, col_bias=self.row_bias, row_weight=self.col_weight,
+                       col_weight=self.row_weight)
+        o.X, o.Y = self.Y, self.X
+        return o
+
+    def mask_columns(self, keep: torch.Tensor) -> "LazyScores":
+        """Boolean column mask ("Score Expressions": boolean row/column masks stay fused): columns with
+        keep[j] False drop out of every reduction over a row. Lowered onto the fused form: a column
+        bias of -inf for logsumexp / softmax_matmul (their terms exp(-inf) = 0) and for K @ V, sum and
+        mean of an exp score; a zero column weight for K @ V, sum and mean without exp or biases; a
+        column bias of +inf (smallest) or -inf (largest) for top-k, so masked columns are never chosen
+        while k does not exceed the kept columns. logsumexp / softmax_matmul of an exp score cannot
+        be masked this way (exp(-inf) = 0 is still a term) and raise NotImplementedError."""
+        keep = keep.to(device=self.Y.device, dtype=torch.bool)
+        if keep.shape != (self.Y.shape[0],):
+            raise ValueError("mask_columns: keep must be a bool vector of length M")
+        o = self._with()
+        o._col_keep = keep if getattr(self, "_col_keep", None) is None else (self._col_keep & keep)
+        return o
+
+    def mask_rows(self, keep: torch.Tensor) -> "LazyScores":
+        """Boolean row mask: rows with keep[i] False drop out of every reduction over a column (dim=-2)."""
+        keep = keep.to(device=self.X.device, dtype=torch.bool)
+        if keep.shape != (self.X.shape[0],):
+            raise ValueError("mask_rows: keep must be a bool vector of length N")
+        o = self._with()
+        o._row_keep = keep if getattr(self, "_row_keep", None) is None else (self._row_keep & keep)
+        return o
+
+    def _masked(self, kind: str) -> "LazyScores":
+        """The expression with the column mask folded in, for a reduction over each row of `kind`
+        ("lse", "sum", "topk_min", "topk_max"). A row mask only affects reductions over columns."""
+        keep = getattr(self, "_col_keep", None)
+        if keep is None:
+            return self
+        dtype = self.Y.dtype
+        if kind == "lse" and self._meta.apply_exp:
+            _unsupported("a column mask on logsumexp / softmax_matmul of an exp score (exp(-inf) = 0 still counts)")
+        if kind in ("lse", "topk_max", "topk_min") or (kind == "sum" and self._meta.apply_exp):
+            fill = float("inf") if kind == "topk_min" else float("-inf")
+            extra = torch.where(keep, torch.zeros((), dtype=dtype, device=keep.device),
+                                torch.full((), fill, dtype=dtype, device=keep.device))
+            cb = extra if self.col_bias is None else self.col_bias + extra
+            o = self._with(col_bias=cb)
+        elif kind == "sum":
+            if self.row_bias is not None or self.col_bias is not None:
+                _unsupported("a column mask on K @ V with biases and no exp")
+            w = keep.to(dtype)
+            o = self._with(col_weight=w if self.col_weight is None else self.col_weight * w)
+        else:
+            raise ValueError(kind)
+        o._col_keep = None
+        return o
+
     def _params(self):
         return (self.row_bias, self.col_bias, self.row_weight, self.col_weight)
 
     # --- consumers -----------------------------------------------------------------------------
     def matmul(self, V: torch.Tensor) -> torch.Tensor:
         """out_i = sum_j S_ij V_j ("Task Map", kernel attention; [V | ones] gives the row mass)."""
-        return _MatmulFn.apply(self.X, self.Y, V, *self._params(), self._meta)
+        e = self._masked("sum")
+        return _MatmulFn.apply(e.X, e.Y, V, *e._params(), e._meta)
+
+    def sum(self, dim: int = -1) -> torch.Tensor:
+        """sum_j S_ij per row (dim=-1) or sum_i S_ij per column (dim=-2): K @ ones."""
+        if dim in (-2, 0):
+            return self._col_view().sum(-1)
+        if dim not in (-1, 1):
+            raise ValueError("sum: dim must be -1 or -2")
+        ones = torch.ones(self.Y.shape[0], 1, dtype=self.Y.dtype, device=self.Y.device)
+        return self.matmul(ones)[:, 0]
+
+    def mean(self, dim: int = -1) -> torch.Tensor:
+        """Mean over each row (dim=-1) or column (dim=-2), over the kept entries under a mask."""
+        if dim in (-2, 0):
+            return self._col_view().mean(-1)
+        keep = getattr(self, "_col_keep", None)
+        count = float(self.Y.shape[0]) if keep is None else keep.sum().to(self.Y.dtype)
+        return self.sum(-1) / count
+
+    def _col_view(self) -> "LazyScores":
+        """The transposed matrix with the row mask turned into its column mask."""
+        t = self.T
+        t._col_keep, t._row_keep = getattr(self, "_row_keep", None), getattr(self, "_col_keep", None)
+        return t
 
     __matmul__ = matmul
 
     def logsumexp(self, dim: int = -1, exclude_self: bool = False) -> torch.Tensor:
         """lse_i = log sum_j exp S_ij over each row ("Task Map", InfoNCE)."""
+        if dim in (-2, 0):
+            return self._col_view().logsumexp(-1, exclude_self)
         if dim not in (-1, 1):
-            _unsupported("logsumexp over the row axis (use the transposed lazy(Y, X))")
-        return _LseFn.apply(self.X, self.Y, *self._params(), self._meta, bool(exclude_self))
+            raise ValueError("logsumexp: dim must be -1 or -2")
+        e = self._masked("lse")
+        return _LseFn.apply(e.X, e.Y, *e._params(), e._meta, bool(exclude_self))
 
     def softmax_matmul(self, V: torch.Tensor, mask=None) -> torch.Tensor:
         """out_i = sum_j softmax_j(S_ij) V_j ("Task Map", attention; fused without a pair mask)."""
         if mask is not None:
             _unsupported("a pair mask")
-        return _SoftmaxFn.apply(self.X, self.Y, V, *self._params(), self._meta)
+        e = self._masked("lse")
+        return _SoftmaxFn.apply(e.X, e.Y, V, *e._params(), e._meta)
 
     def displacement(self) -> torch.Tensor:
         """disp_i = sum_j S_ij (y_j - x_i) ("Stein Variational Gradient Descent")."""
-        return _DispFn.apply(self.X, self.Y, *self._params(), self._meta)
+        e = self._masked("sum")
+        return _DispFn.apply(e.X, e.Y, *e._params(), e._meta)
 
     def topk(self, k: int, dim: int = -1, largest: bool = True) -> TopK:
         """k best entries per row, sorted, ties by lower column index ("Task Map", k-NN)."""
+        if dim in (-2, 0):
+            v, i = self._col_view().topk(k, -1, largest)
+            return TopK(v.t(), i.t())
         if dim not in (-1, 1):
-            _unsupported("topk over the row axis (use the transposed lazy(Y, X))")
-        v, i = _TopkFn.apply(self.X, self.Y, *self._params(), self._meta, int(k), bool(largest))
+            raise ValueError("topk: dim must be -1 or -2")
+        e = self._masked("topk_max" if largest else "topk_min")
+        v, i = _TopkFn.apply(e.X, e.Y, *e._params(), e._meta, int(k), bool(largest))
         return TopK(v, i)
 
     def min(self, dim: int = -1) -> TopK:
+        """Smallest entry per row (dim=-1) or per column (dim=-2), with its index ("Task Map",
+        Chamfer-style losses: D.min(-1) and D.min(-2))."""
         v, i = self.topk(1, dim=dim, largest=False)
-        return TopK(v[:, 0], i[:, 0])
+        return TopK(v.reshape(-1), i.reshape(-1))
 
     def max(self, dim: int = -1) -> TopK:
         v, i = self.topk(1, dim=dim, largest=True)
-        return TopK(v[:, 0], i[:, 0])
+        return TopK(v.reshape(-1), i.reshape(-1))
 
     def argmin(self, dim: int = -1) -> torch.Tensor:
         return self.min(dim).indices
