@@ -5,14 +5,15 @@
 // The contraction X R^T runs on tcgen05.mma kind::tf32 with the hi/lo split of both operands (three
 // products); points whose coordinates are exact in tf32 (integers up to 2^11, for instance) have lo = 0,
 // so their dot products, norms and distances are exact and the selection is bit-identical to an exact
-// evaluation. The 128 x 128 score tile lands in TMEM; eight epilogue warps (two per TMEM lane quarter,
-// each owning half of the tile's columns) turn each dot product into the score and keep a sorted
+// evaluation. The 128 x 128 score tile lands in TMEM; the selection warps (sixteen for D <= 32, four
+// per TMEM lane quarter owning 32 of the tile's columns each; eight for D <= 64, two per quarter
+// owning 64 columns) turn each dot product into the score and keep a sorted
 // (value, index) list per row in registers, inserting only on a strict improvement, so equal values
-// keep ascending index order. The lists of the two halves and of every CTA that saw part of a row are
-// merged lexicographically on (value, index) by a second kernel: the result is unique.
+// keep ascending index order. The lists of the column parts and of every unit (column chunk) of a row
+// block are merged lexicographically on (value, index) by a second kernel: the result is unique.
 //
-// Schedule and warp roles as in the log-sum-exp kernel: persistent CTAs over contiguous ranges of
-// (row block, column tile) pairs; warp 0 loads with TMA, warp 1 issues the MMAs, warps 2..9 select.
+// Schedule: persistent CTAs over units of (row block, chunk of column tiles) dealt round-robin (see
+// UnitCursor); warp 0 loads with TMA, warp 1 issues the MMAs, warps 2..9 select.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -26,30 +27,67 @@ namespace tp {
 namespace tc {
 
 constexpr int kKBM = 128, kKBN = 128;
-constexpr int kKThreads = 320;
+constexpr int kKLists = 4;   // sorted lists per row and unit in the partials (the most selection parts)
 constexpr int kKGrid = 152;
 
-template <int DP>
+// selection warps: 16 (four per TMEM lane quarter, 32 columns each) where shared memory and registers
+// allow it (D <= 32, k <= 16), else 8 (two per quarter, 64 columns each)
+__host__ __device__ constexpr int sel_warps(int DP, int K) { return DP == 32 && K <= 16 ? 16 : 8; }
+
+template <int DP, int SEL>
 struct TopkTcShape {
     static constexpr int kChunks = DP / 32;                 // 128-byte K chunks per operand
     static constexpr int kOperand = kChunks * 128 * 128;    // 128 rows x DP fp32
     static constexpr int kPair = 2 * kOperand;              // hi + lo
-    static constexpr int kStages = DP == 32 ? 4 : 2;
-    static constexpr size_t kKeyBuf = 8 * 32 * 32 * 4;      // per selection warp: 32 columns x 32 lanes of keys
+    static constexpr int kStages = DP == 32 ? (SEL == 16 ? 3 : 4) : 2;
+    static constexpr int kSel = SEL;
+    static constexpr int kParts = kSel / 4;
+    static constexpr int kCols = kKBN / kParts;
+    static constexpr int kThreads = 32 * (2 + kSel);
+    static constexpr size_t kKeyBuf = (size_t)kSel * 32 * 32 * 4;  // per selection warp: 32 columns x 32 lanes
     static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + 256 + 1024;
     static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
 struct TopkTcParams {
-    int64_t N, M, T;
-    int CT, G, smax, k;
+    int64_t N, M;
+    int CT, G, k;
+    int H, U, chunk;   // column chunks per row block, units (row block, chunk), column tiles per chunk
+    int parts;         // selection parts (sorted lists) per row and unit
     int metric, apply_exp, largest;
     float scale, neg_gamma_log2;
     const float* xn;
     const float* yn;   // padded to CT * 128 entries
-    float* pv;         // [G][smax][2 halves][K][128] keys
+    float* pv;         // [U][kKLists][K][128] keys (parts beyond `parts` unused)
     int* pi;           // same layout, column indices
     int* err;
+};
+
+// Work units are (row block, chunk of column tiles), numbered u = rb * H + chunk and dealt round-robin:
+// CTA c takes u = c, c + G, c + 2G, ... At any moment the CTAs work on one "wave" of G consecutive
+// units, which stream the same one or two regions of the reference set (so a tile is read from HBM
+// about once per wave), and each unit owns its partial lists, so the merge needs no map from CTAs to
+// row blocks. (On the k-NN workload the time did not change with this schedule: the kernel is bound
+// by its selection epilogue, not by the reference set's traffic.)
+struct UnitCursor {
+    int u, rb, ct, ct_end;
+    bool valid;
+    __device__ __forceinline__ explicit UnitCursor(const TopkTcParams& p) { set(p, blockIdx.x); }
+    __device__ __forceinline__ void set(const TopkTcParams& p, int uu) {
+        u = uu;
+        valid = u < p.U;
+        if (valid) {
+            rb = u / p.H;
+            ct = (u - rb * p.H) * p.chunk;
+            ct_end = ct + p.chunk < p.CT ? ct + p.chunk : p.CT;
+        }
+    }
+    // next tile; true when it starts a new unit (or none is left)
+    __device__ __forceinline__ bool next(const TopkTcParams& p) {
+        if (++ct < ct_end) return false;
+        set(p, u + p.G);
+        return true;
+    }
 };
 
 template <int METRIC, bool EXP>
@@ -66,10 +104,10 @@ __device__ __forceinline__ float topk_score(float dot, float xn, float yn, float
 }
 
 template <int DP, int K, int METRIC, bool EXP>
-__global__ void __launch_bounds__(kKThreads, 1)
+__global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1)
     topk_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
             const __grid_constant__ CUtensorMap mYh, const __grid_constant__ CUtensorMap mYl, const TopkTcParams p) {
-    using SH = TopkTcShape<DP>;
+    using SH = TopkTcShape<DP, sel_warps(DP, K)>;
     constexpr int kChunk = 128 * 128;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -87,7 +125,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t_begin = (p.T * blockIdx.x) / p.G, t_end = (p.T * (blockIdx.x + 1)) / p.G;
 
     if (threadIdx.x == 0) {
         mbar_init(a_full, 1);
@@ -95,11 +132,11 @@ __global__ void __launch_bounds__(kKThreads, 1)
         for (int s = 0; s < SH::kStages; ++s) {
             mbar_init(b_full + s, 1);
             // freed by the MMA (operands consumed) and by the 256 selection threads (norms consumed)
-            mbar_init(b_empty + s, 1 + 256);
+            mbar_init(b_empty + s, 1 + 32 * SH::kSel);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 256);
+            mbar_init(acc_empty + b, 32 * SH::kSel);
         }
         mbar_fence_init();
     }
@@ -113,9 +150,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         if (lane == 0) {  // ---------------- TMA producer
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
-            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
-                const int64_t i = t - t_begin;
+            int64_t i = 0;
+            for (UnitCursor cur(p); cur.valid && ok; ++i, cur.next(p)) {
                 const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
                     if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 31);
@@ -146,9 +182,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
             constexpr int KS = DP / 8;
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
-            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
-                const int64_t i = t - t_begin;
+            int64_t i = 0;
+            for (UnitCursor cur(p); cur.valid && ok; ++i, cur.next(p)) {
                 const int rb = cur.rb;
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);
@@ -181,15 +216,14 @@ __global__ void __launch_bounds__(kKThreads, 1)
                 mma_commit(acc_full + b);
             }
         }
-    } else {  // ---------------- selection: warps 2..9, one row per thread, half of each tile
+    } else {  // ---------------- selection: one row per thread, kCols of each tile per warp
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - 2) >> 2;  // column part of this warp
         const int lr = q * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 64);
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * SH::kCols);
         const float sgn = p.largest ? -1.f : 1.f;
         float kv[K];
         int ki[K];
-        int rb_cur = -1, seg = 0;
         float xn = 0.f;
         bool ok = true;
         auto reset = [&]() {
@@ -199,37 +233,34 @@ __global__ void __launch_bounds__(kKThreads, 1)
                 ki[t] = 0x7fffffff;
             }
         };
-        auto flush = [&]() {
-            const size_t base = (((size_t)blockIdx.x * p.smax + seg) * 2 + half) * K * kKBM;
+        auto flush = [&](int u) {
+            const size_t base = ((size_t)u * kKLists + half) * K * kKBM;
 #pragma unroll
             for (int t = 0; t < K; ++t) {
                 p.pv[base + (size_t)t * kKBM + lr] = kv[t];
                 p.pi[base + (size_t)t * kKBM + lr] = ki[t];
             }
-            ++seg;
         };
-        reset();
-        TileCursor cur(t_begin, p.CT);
-        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
-            const int64_t i = t - t_begin;
+        bool fresh = true;
+        int64_t i = 0;
+        for (UnitCursor cur(p); cur.valid && ok; ++i) {
             const int rb = cur.rb, ct = cur.ct;
-            if (rb != rb_cur) {
-                if (rb_cur >= 0) flush();
+            if (fresh) {
                 reset();
-                rb_cur = rb;
                 const int64_t row = (int64_t)rb * kKBM + lr;
                 xn = (METRIC != kLinear && row < p.N) ? p.xn[row] : 0.f;
+                fresh = false;
             }
             const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
             ok = mbar_wait(acc_full + b, rr & 1, p.err, 36);
             if (!ok) break;
             fence_after_sync();
-            const int j0 = ct * kKBN + half * 64;
-            const int lim = (int)(p.M - j0 < 64 ? p.M - j0 : 64);  // valid columns of this half
-            const float* yn = sYn + s * kKBN + half * 64;
+            const int j0 = ct * kKBN + half * SH::kCols;
+            const int lim = (int)(p.M - j0 < SH::kCols ? p.M - j0 : SH::kCols);  // valid columns of this part
+            const float* yn = sYn + s * kKBN + half * SH::kCols;
             float* wkeys = sKeys + (warp - 2) * 32 * 32;
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < SH::kCols / 32; ++c) {
                 float v[32];
                 tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
                 // keys, and the columns that beat this row's current k-th key (the threshold only falls,
@@ -264,8 +295,12 @@ __global__ void __launch_bounds__(kKThreads, 1)
             fence_before_sync();
             mbar_arrive(acc_empty + b);
             mbar_arrive(b_empty + s);
+            const int u_done = cur.u;
+            if (cur.next(p)) {  // the unit is complete: its lists are final
+                flush(u_done);
+                fresh = true;
+            }
         }
-        if (ok && rb_cur >= 0) flush();
     }
 
     fence_before_sync();
@@ -273,16 +308,12 @@ __global__ void __launch_bounds__(kKThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-// Per row: the lists of every (CTA, half) that saw part of it, merged on (key, index).
+// Per row: the lists of every (unit, part) of its row block, merged on (key, index).
 template <int K>
 __global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_t* __restrict__ indices) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.N) return;
     const int rb = (int)(i / kKBM), lr = (int)(i % kKBM);
-    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
-    auto start = [&](int c) { return (p.T * c) / p.G; };
-    // the CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1)
-    auto cta_of = [&](int64_t t) { return (int)(((int64_t)p.G * (t + 1) - 1) / p.T); };
     float kv[K];
     int ki[K];
 #pragma unroll
@@ -290,11 +321,9 @@ __global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_
         kv[t] = pinf<float>();
         ki[t] = 0x7fffffff;
     }
-    const int c_lo = cta_of(t0), c_hi = cta_of(t1);
-    for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - (int)(start(c) / p.CT);
-        for (int h = 0; h < 2; ++h) {
-            const size_t base = (((size_t)c * p.smax + seg) * 2 + h) * K * kKBM;
+    for (int u = rb * p.H; u < (rb + 1) * p.H; ++u) {
+        for (int h = 0; h < p.parts; ++h) {
+            const size_t base = ((size_t)u * kKLists + h) * K * kKBM;
             for (int t = 0; t < p.k; ++t)
                 topk_insert_lex<float, K>(kv, ki, p.pv[base + (size_t)t * kKBM + lr], p.pi[base + (size_t)t * kKBM + lr]);
         }
@@ -330,8 +359,7 @@ __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int 
 }
 
 struct TopkTcPlan {
-    int64_t T;
-    int CT, G, smax, DP, KB;
+    int CT, G, DP, KB, H, U, chunk;
     size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, off_err, bytes;
 };
 
@@ -341,10 +369,13 @@ inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     pl.KB = topk_bucket(k);
     const int64_t RB = (N + kKBM - 1) / kKBM;
     pl.CT = (int)((M + kKBN - 1) / kKBN);
-    pl.T = RB * pl.CT;
-    pl.G = (int)(pl.T < kKGrid ? pl.T : kKGrid);
-    const int64_t per = (pl.T + pl.G - 1) / pl.G;
-    pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
+    // column chunks per row block: enough units for about four per CTA (balance), none empty
+    const int64_t want = (4 * kKGrid + RB - 1) / RB;
+    const int h0 = (int)(want < 1 ? 1 : (want > pl.CT ? pl.CT : want));
+    pl.chunk = (pl.CT + h0 - 1) / h0;
+    pl.H = (pl.CT + pl.chunk - 1) / pl.chunk;
+    pl.U = (int)(RB * pl.H);
+    pl.G = pl.U < kKGrid ? pl.U : kKGrid;
     size_t o = 0;
     pl.off_xh = o; o += al256((size_t)N * pl.DP * 4);
     pl.off_xl = o; o += al256((size_t)N * pl.DP * 4);
@@ -357,7 +388,7 @@ inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     }
     pl.off_xn = o; o += al256((size_t)N * 4);
     pl.off_yn = o; o += al256((size_t)pl.CT * kKBN * 4);
-    const size_t lists = (size_t)pl.G * pl.smax * 2 * pl.KB * kKBM;
+    const size_t lists = (size_t)pl.U * kKLists * pl.KB * kKBM;
     pl.off_pv = o; o += al256(lists * 4);
     pl.off_pi = o; o += al256(lists * 4);
     pl.off_err = o; o += 256;
@@ -404,10 +435,12 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     TopkTcParams p;
     p.N = a.nP;
     p.M = a.nQ;
-    p.T = pl.T;
     p.CT = pl.CT;
     p.G = pl.G;
-    p.smax = pl.smax;
+    p.H = pl.H;
+    p.U = pl.U;
+    p.chunk = pl.chunk;
+    p.parts = sel_warps(pl.DP, pl.KB) / 4;
     p.k = a.k;
     p.metric = a.metric;
     p.apply_exp = a.apply_exp;
@@ -422,11 +455,11 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     auto go = [&](auto kernel, size_t smem) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         HookScope h("topk_tc", s);
-        kernel<<<pl.G, kKThreads, smem, s>>>(mxh, mxl, myh, myl, p);
+        kernel<<<pl.G, 32 * (2 + sel_warps(pl.DP, pl.KB)), smem, s>>>(mxh, mxl, myh, myl, p);
     };
     auto with_metric = [&](auto dp, auto kk) {
         constexpr int DP = decltype(dp)::value, KB = decltype(kk)::value;
-        constexpr size_t sm = TopkTcShape<DP>::kSmem;
+        constexpr size_t sm = TopkTcShape<DP, sel_warps(DP, KB)>::kSmem;
         const bool ex = a.apply_exp != 0;
         if (a.metric == kLinear) ex ? go(topk_tc<DP, KB, kLinear, true>, sm) : go(topk_tc<DP, KB, kLinear, false>, sm);
         else if (a.metric == kSqeuclidean)
