@@ -648,10 +648,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_commit(dz_full);
                 return true;
             };
+            // S(i + 2) goes in before the wait for tile i's kappa: its buffer last held kappa(i - 1), read by
+            // dZ(i - 1), already issued; so the tensor pipe works on it while the epilogue finishes tile i
             for (int64_t j = 0; j < n && j < 2 && ok; ++j) ok = issue_s(j);
             for (int64_t i = 0; i < n && ok; ++i) {
-                ok = issue_dz(i);
-                if (ok && i + 2 < n) ok = issue_s(i + 2);
+                if (i + 2 < n) ok = issue_s(i + 2);
+                if (ok) ok = issue_dz(i);
             }
         }
     } else {
