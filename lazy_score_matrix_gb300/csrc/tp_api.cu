@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <string>
 #include <type_traits>
 #include <utility>
@@ -27,6 +28,9 @@ size_t lse_bwd_tc_workspace(int64_t N);                                       //
 int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s);                // tp_tc_lse.cu
 size_t topk_tc_workspace(int64_t N, int64_t M, int D, int k, bool same);                        // tp_tc_topk.cu
 int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same, cudaStream_t s);  // tp_tc_topk.cu
+size_t attn_tc_workspace(int64_t N, int64_t M, bool backward);                  // tp_tc_attn.cu
+int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s);                    // tp_tc_attn.cu
+int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s);                    // tp_tc_attn.cu
 }  // namespace tp
 
 namespace {
@@ -207,6 +211,19 @@ bool lse_tc_eligible(const tp_pairs* p, const tp_score* s) {
            aligned(p->X, 16) && aligned(p->Y, 16);
 }
 
+// Tensor-core attention: softmax_matmul and its backward for fp32, D = C = 64, a linear score without
+// exp or row/column parameters, 16-byte aligned rows.
+constexpr bool kTcAttention = true;
+bool attn_tc_shape(const tp_pairs* p, int64_t C) { return p->dtype == TP_F32 && p->D == 64 && C == 64; }
+bool attn_tc_eligible(const tp_pairs* p, const tp_score* s, int64_t C, std::initializer_list<const void*> rows) {
+    if (!kTcAttention || force_simt() || !attn_tc_shape(p, C) || s->metric != TP_LINEAR || s->apply_exp || s->row_bias ||
+        s->col_bias || s->row_weight || s->col_weight || !aligned(p->X, 16) || !aligned(p->Y, 16))
+        return false;
+    for (const void* q : rows)
+        if (q && !aligned(q, 16)) return false;
+    return true;
+}
+
 // The tensor-core top-k covers fp32, D <= 64, k <= 32, no row/column parameters.
 bool topk_tc_shape(const tp_pairs* p, int k) { return p->dtype == TP_F32 && p->D <= 64 && k >= 1 && k <= kTopkMax; }
 bool topk_tc_eligible(const tp_pairs* p, const tp_score* s, int k) {
@@ -336,7 +353,12 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     const bool needC = e.find("matmul") != std::string::npos;
     if (needC && (C < 1 || C > 64)) return (size_t)-1;
     if (e == "pairwise_matmul") return partial_bytes(r, fwd_width(kMatmul, D, (int)C), es);
-    if (e == "pairwise_softmax_matmul") return partial_bytes(r, fwd_width(kSoftmax, D, (int)C), es);
+    if (e == "pairwise_softmax_matmul") {
+        const size_t simt = partial_bytes(r, fwd_width(kSoftmax, D, (int)C), es);
+        if (!(kTcAttention && attn_tc_shape(p, C))) return simt;
+        return std::max(simt, lse_tc_workspace(p->N, p->M, p->X == p->Y && p->N == p->M) +
+                                  attn_tc_workspace(p->N, p->M, false));
+    }
     if (e == "pairwise_logsumexp") {
         const size_t simt = partial_bytes(r, fwd_width(kLse, D, 0), es);
         return lse_tc_shape(p) ? std::max(simt, lse_tc_workspace(p->N, p->M, p->X == p->Y)) : simt;
@@ -350,7 +372,10 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
         return kTcTopk && topk_tc_shape(p, k) ? std::max(simt, topk_tc_workspace(p->N, p->M, D, k, p->X == p->Y)) : simt;
     }
     if (e == "pairwise_matmul_backward") return bwd_ws(p, kBMatmul, C, 0);
-    if (e == "pairwise_softmax_matmul_backward") return bwd_ws(p, kBSoftmax, C, align_up(p->N * es));
+    if (e == "pairwise_softmax_matmul_backward") {
+        const size_t simt = bwd_ws(p, kBSoftmax, C, align_up(p->N * es));
+        return kTcAttention && attn_tc_shape(p, C) ? std::max(simt, attn_tc_workspace(p->N, p->M, true)) : simt;
+    }
     if (e == "pairwise_logsumexp_backward") {
         const size_t simt = bwd_ws(p, kBLse, 0, 0);
         const bool sym = p->X == p->Y && p->N == p->M;
@@ -657,6 +682,25 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
     a.out2 = lse;
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (attn_tc_eligible(pr, sc, C, {V, out, lse})) {
+        // the row log-sum-exp first, then P V with P = exp(S - lse): no running rescale of the output
+        const bool same = pr->X == pr->Y && pr->N == pr->M;
+        const int n1 = launch_lse_tc(a, lse, same, st);
+        if (n1 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        AttnTcArgs t{};
+        t.Q = static_cast<const float*>(pr->X);
+        t.K = static_cast<const float*>(pr->Y);
+        t.V = static_cast<const float*>(V);
+        t.N = pr->N;
+        t.M = pr->M;
+        t.scale = sc->scale;
+        t.lse = static_cast<const float*>(lse);
+        t.out = static_cast<float*>(out);
+        t.ws = static_cast<char*>(ws) + lse_tc_workspace(pr->N, pr->M, same);
+        const int n2 = launch_attn_fwd_tc(t, st);
+        if (n2 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        return launched(n1 + n2);
+    }
     return by_dtype(pr->dtype, [&](auto t) { return launched(run_fwd_vals<decltype(t), kSoftmax>(a, st)); });
 }
 
@@ -838,6 +882,25 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
                          ws, ws_bytes));
     const size_t need = ws_size("pairwise_softmax_matmul_backward", pr, C, 0);
     TP_CHECK(check_ws(ws, ws_bytes, need));
+    if (attn_tc_eligible(pr, sc, C, {V, out, lse, grad_out, dX, dY, dV}) && !(dX && dX == dY)) {
+        AttnTcArgs t{};
+        t.Q = static_cast<const float*>(pr->X);
+        t.K = static_cast<const float*>(pr->Y);
+        t.V = static_cast<const float*>(V);
+        t.N = pr->N;
+        t.M = pr->M;
+        t.scale = sc->scale;
+        t.lse = static_cast<const float*>(lse);
+        t.O = static_cast<const float*>(out);
+        t.dO = static_cast<const float*>(grad_out);
+        t.dQ = static_cast<float*>(dX);
+        t.dK = static_cast<float*>(dY);
+        t.dV = static_cast<float*>(dV);
+        t.ws = ws;
+        const int n = launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream));
+        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        return launched(n);
+    }
     // workspace: delta [N] first, partial states after it
     void* delta = ws;
     void* part = static_cast<char*>(ws) + align_up(pr->N * es);

@@ -39,6 +39,19 @@ struct SweepArgs {
     int k, largest;
 };
 
+// Tensor-core attention (fp32, D = C = 64, linear score times `scale`): out = softmax(scale Q K^T) V.
+// Q [N, 64], K [M, 64], V [M, 64]; lse [N] the natural-log row log-sum-exp of the scores.
+struct AttnTcArgs {
+    const float *Q, *K, *V;
+    int64_t N, M;
+    double scale;
+    const float* lse;
+    const float *O, *dO;     // backward: the forward output and its upstream gradient [N, 64]
+    float* out;              // forward output [N, 64]
+    float *dQ, *dK, *dV;     // backward outputs (null: not wanted)
+    void* ws;
+};
+
 enum FwdMode : int { kMatmul = 0, kSoftmax = 1, kLse = 2, kDisp = 3, kSvgd = 4 };
 
 // kBLseSym: logsumexp backward when X and Y are the same points and the score is symmetric (no

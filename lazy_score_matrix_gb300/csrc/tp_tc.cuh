@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -131,6 +132,29 @@ struct TileCursor {
         }
     }
 };
+
+// Persistent schedules: the tiles t = rb * CT + ct are cut into G contiguous ranges, one per CTA.
+// First tile of CTA c: floor(T c / G). 32-bit division whenever T G fits (every practical size).
+__host__ __device__ inline int64_t range_start(int64_t T, int G, int c) {
+    if ((unsigned long long)T * (unsigned)G < (1ull << 32)) return (int64_t)((uint32_t)T * (uint32_t)c / (uint32_t)G);
+    return (T * c) / G;
+}
+// The CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1).
+__host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) {
+    if ((unsigned long long)T * (unsigned)G < (1ull << 32))
+        return (int)(((uint32_t)G * (uint32_t)(t + 1) - 1u) / (uint32_t)T);
+    return (int)(((int64_t)G * (t + 1) - 1) / T);
+}
+// Row block of tile t (t < T).
+__host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
+    return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
+}
+
+// Pack two floats into fp16x2 (a in the low half), rounded to nearest.
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
 
 // Instruction descriptor: kind::tf32, fp32 accumulate, both operands K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {

@@ -1,0 +1,727 @@
+// Pairwise attention out = softmax(scale Q K^T) V and its replay backward on the Blackwell tensor
+// cores (fp32 data, D = C = 64, linear score without exp or row/column parameters): torchpairwise
+// guide "Using Torchpairwise in Models", Task Map (attention: softmax_matmul(V) on lazy(Q, K, "linear")
+// times a scale), and the introduction ("First derivatives replay the tiles").
+//
+// Operands use the scaled fp16 split of the log-sum-exp kernels: every point row x is multiplied by a
+// power of two 2^e of its own (max|x| 2^e in [2^14, 2^15)) and split into hi = fp16(x 2^e) and
+// lo = fp16(x 2^e - hi); a dot product is (xh.yh + (xh.yl + xl.yh)) 2^-(e_x + e_y), with hi*hi in TMEM
+// columns of its own.
+//
+// Forward: the row log-sum-exp first (lse_fwd_tc), then one sweep that forms P_ij = exp(S_ij - lse_i)
+// tile by tile and accumulates P V on the tensor core. With lse known, the output needs no running
+// rescale. Backward, with dO = d loss / d out, delta_i = dO_i . out_i, dP_ij = dO_i . V_j and
+// dS_ij = P_ij (dP_ij - delta_i):
+//   row sweep     dQ_i = scale sum_j dS_ij K_j
+//   column sweep  dK_j = scale sum_i dS_ij Q_i,   dV_j = sum_i P_ij dO_i
+// All three sweeps are one kernel template. A 128 x 64 tile's S (and dP) go into TMEM; the epilogue
+// turns them into coefficient rows kappa (one per output), scales each row by a power of two that the
+// four warps sharing the row agree on, splits kappa into fp16 hi/lo and stores it back into TMEM as
+// the A operand of the output MMA. The output MMA's B operand is the tile's own streamed points read
+// MN-major, so no transposed copy of any matrix exists: the column sweep streams Q and dO and holds K
+// and V as its row block. Each tile's output block is added, unscaled, into per-row registers
+// (two-level accumulation); a CTA writes one partial per row block it touched, and the last CTA to
+// finish a row block adds the partials in CTA order (deterministic, no atomics on the data).
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "tp_args.h"
+#include "tp_device.cuh"
+#include "tp_launch.h"
+#include "tp_tc.cuh"
+#include "tp_tc_host.h"
+
+namespace tp {
+namespace tc {
+namespace attn {
+
+constexpr int kBM = 128;                      // rows per tile (TMEM lanes)
+constexpr int kBN = 64;                       // streamed points per tile
+constexpr int kRowB = 128;                    // one point: 64 fp16 features
+constexpr int kHalf = kBM * kRowB;            // 128 rows of hi (or lo): 16 KB
+constexpr int kTile = kBN * kRowB;            // 64 rows of hi (or lo): 8 KB
+constexpr int kStage = 4 * kTile;             // [B1 hi | B1 lo | B2 hi | B2 lo]: 32 KB
+constexpr int kStages = 4;
+constexpr int kABytes = 4 * kHalf;            // [A1 hi | A1 lo | A2 hi | A2 lo]: 64 KB
+constexpr int kEpi = 16;                      // epilogue warps: 4 per TMEM lane quarter
+constexpr int kParts = kEpi / 4;              // warps per lane quarter, each owning 16 tile columns
+constexpr int kCols = kBN / kParts;           // 16: one K step of the output MMA
+constexpr int kThreads = 32 * (2 + kEpi);
+constexpr int kGrid = 152;                    // persistent CTAs: one per GB300 SM
+constexpr size_t kSmem = (size_t)kABytes + (size_t)kStage * kStages + (size_t)kStages * kBN * 16 +
+                         2 * 4 * kParts * 32 * 8 + 512 + 1024;
+static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
+static_assert(kCols == 16, "one output K step per epilogue warp");
+
+enum Mode : int { kFwd = 0, kRowSweep = 1, kColSweep = 2 };
+
+// Per mode: the row block holds A1 (for S) and, for the backward, A2 (for dP); a stage holds B1 (the
+// other side of S) and B2 (the other side of dP, or V in the forward).
+//   kFwd:      rows Q, A1 = Q;          stream B1 = K, B2 = V;   out0 = O  <- kappa0 B2
+//   kRowSweep: rows Q, A1 = Q, A2 = dO; stream B1 = K, B2 = V;   out0 = dQ <- kappa0 B1
+//   kColSweep: rows K, A1 = K, A2 = V;  stream B1 = Q, B2 = dO;  out0 = dK <- kappa0 B1, out1 = dV <- kappa1 B2
+template <int MODE>
+struct Shape {
+    static constexpr bool kDP = MODE != kFwd;                       // dP = A2 B2^T is formed
+    static constexpr int kOuts = MODE == kColSweep ? 2 : 1;
+    static constexpr int kRegion = kDP ? 256 : 128;                 // TMEM columns of one S (+ dP) buffer
+    static constexpr int kBuf = (512 - 128 * kOuts) / kRegion;      // 3, 1, 1
+    static constexpr uint32_t kAcc = (uint32_t)(kBuf * kRegion);     // first output accumulator
+    static constexpr int kF = 64 * kOuts;                           // features of one partial row
+    // the stage part that is the B operand of output o
+    __host__ __device__ static constexpr uint32_t out_b(int o) { return MODE == kRowSweep ? 0u : (o == 0 && MODE == kColSweep ? 0u : 2u * kTile); }
+    // outputs whose coefficients leave out the score's scale (dQ, dK)
+    __host__ __device__ static constexpr bool out_scaled(int o) { return MODE != kFwd && o == 0; }
+};
+
+struct Params {
+    int64_t R;             // rows of the sweep (queries; keys for the column sweep)
+    int64_t C;             // streamed points (keys; queries for the column sweep)
+    int64_t T;             // tiles: row blocks x column tiles
+    int CT, G, smax;
+    float scale;
+    const float4* rstat;   // [rows padded to 128] the row side's stats
+    const float4* cstat;   // [CT * 64 or more] the streamed side's stats
+    float* part;           // [G][smax][F][128] per-CTA partials, row-minor
+    int* cnt;              // [row blocks] CTAs done with each row block (zeroed by the pre-pass)
+    float* out0;           // [R][64] (null: not wanted)
+    float* out1;
+    int* err;
+};
+
+// Output features [FG fg, FG fg + FG) of row lr of row block rb: the partials of every CTA that saw the
+// row block, added in CTA order.
+template <int MODE>
+__device__ __noinline__ void merge_row(const Params& p, int rb, int lr, int fg) {
+    using SH = Shape<MODE>;
+    constexpr int FG = SH::kF / 4;
+    const int64_t row = (int64_t)rb * kBM + lr;
+    if (row >= p.R) return;
+    const int fb = fg * FG;
+    float* dst = fb < 64 ? p.out0 : p.out1;
+    if (!dst) return;
+    const int64_t t0 = (int64_t)rb * p.CT;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t0 + p.CT - 1);
+    float acc[FG];
+#pragma unroll
+    for (int f = 0; f < FG; ++f) acc[f] = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
+        const float* o = p.part + (size_t)(c * p.smax + seg) * SH::kF * kBM + lr;
+#pragma unroll
+        for (int f = 0; f < FG; ++f) acc[f] += __ldcg(o + (size_t)(fb + f) * kBM);
+    }
+    float4* d4 = reinterpret_cast<float4*>(dst + row * 64 + (fb & 63));
+#pragma unroll
+    for (int f4 = 0; f4 < FG / 4; ++f4) d4[f4] = make_float4(acc[4 * f4], acc[4 * f4 + 1], acc[4 * f4 + 2], acc[4 * f4 + 3]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc(const __grid_constant__ CUtensorMap mA1h, const __grid_constant__ CUtensorMap mA1l,
+            const __grid_constant__ CUtensorMap mA2h, const __grid_constant__ CUtensorMap mA2l,
+            const __grid_constant__ CUtensorMap mB1h, const __grid_constant__ CUtensorMap mB1l,
+            const __grid_constant__ CUtensorMap mB2h, const __grid_constant__ CUtensorMap mB2l, const Params p) {
+    using SH = Shape<MODE>;
+    constexpr float kL2E = 1.4426950408889634f;
+    constexpr int NB = SH::kBuf;
+    constexpr int NO = SH::kOuts;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = sm;
+    unsigned char* sB = sm + kABytes;
+    float4* sStat = reinterpret_cast<float4*>(sB + (size_t)kStage * kStages);   // [stage][64]
+    float2* sMax = reinterpret_cast<float2*>(sStat + kStages * kBN);             // [parity][quarter][part][lane]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sMax + 2 * 4 * kParts * 32);
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* bs_full = bars + 2;              // [kStages]
+    uint64_t* bs_empty = bs_full + kStages;    // [kStages]
+    uint64_t* s_full = bs_empty + kStages;     // [NB] S (and dP) of a buffer are in TMEM
+    uint64_t* w_full = s_full + NB;            // [NB] the epilogue stored the buffer's kappa
+    uint64_t* o_full = w_full + NB;            // the output MMAs of a tile finished
+    uint64_t* o_empty = o_full + 1;            // the epilogue read the output block
+    uint64_t* xch = o_empty + 1;               // [quarter][parity]: the row-maximum exchange
+    uint64_t* fl_bar = xch + 8;                // the epilogue wrote its partials of a row block
+    uint64_t* dec_bar = fl_bar + 1;            // the CTA knows whether it merges that row block
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
+    volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
+    const int64_t n = t_end - t_begin;
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bs_full + s, 1);
+            mbar_init(bs_empty + s, 1);
+        }
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(s_full + b, 1);
+            mbar_init(w_full + b, 32 * kEpi);
+        }
+        mbar_init(o_full, 1);
+        mbar_init(o_empty, 32 * kEpi);
+        for (int x = 0; x < 8; ++x) mbar_init(xch + x, 32 * kParts);
+        mbar_init(fl_bar, 32 * kEpi);
+        mbar_init(dec_bar, 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer: row blocks and operand stages in tile order
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
+                const int rb = cur.rb, ct = cur.ct;
+                if (rb != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 41);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, SH::kDP ? 4 * kHalf : 2 * kHalf);
+                    tma_load_2d(sA, &mA1h, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kHalf, &mA1l, 0, rb * kBM, a_full);
+                    if (SH::kDP) {
+                        tma_load_2d(sA + 2 * kHalf, &mA2h, 0, rb * kBM, a_full);
+                        tma_load_2d(sA + 3 * kHalf, &mA2l, 0, rb * kBM, a_full);
+                    }
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStages), r = (int)(i / kStages);
+                if (r >= 1) ok = mbar_wait(bs_empty + s, (r - 1) & 1, p.err, 42);
+                if (!ok) break;
+                unsigned char* dst = sB + (size_t)s * kStage;
+                mbar_expect_tx(bs_full + s, kStage + kBN * 16);
+                tma_load_2d(dst, &mB1h, 0, ct * kBN, bs_full + s);
+                tma_load_2d(dst + kTile, &mB1l, 0, ct * kBN, bs_full + s);
+                tma_load_2d(dst + 2 * kTile, &mB2h, 0, ct * kBN, bs_full + s);
+                tma_load_2d(dst + 3 * kTile, &mB2l, 0, ct * kBN, bs_full + s);
+                bulk_load(sStat + s * kBN, p.cstat + (size_t)ct * kBN, kBN * 16, bs_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            constexpr uint32_t idS2 = idesc_f16(kBM, 2 * kBN, false);  // A_hi [B_hi; B_lo]: N 128
+            constexpr uint32_t idS = idesc_f16(kBM, kBN, false);       // A_lo B_hi: N 64
+            constexpr uint32_t idO2 = idesc_f16(kBM, 128, true);       // kappa_hi [B_hi | B_lo] (MN-major): N 128
+            constexpr uint32_t idO = idesc_f16(kBM, 64, true);         // kappa_lo B_hi (MN-major): N 64
+            int a_uses = 0, rb_cur = -1;
+            bool ok = true;
+            TileCursor cur(t_begin, p.CT);
+            // S (and dP) of tile j into buffer j % NB: its previous kappa was read by the output MMAs of
+            // tile j - NB, issued earlier (the tensor core runs one thread's MMAs in order)
+            auto issue_s = [&](int64_t j) -> bool {
+                const int rb = cur.rb;
+                cur.next();
+                if (rb != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);  // the old row block is free once its MMAs finish
+                    if (!mbar_wait(a_full, a_uses & 1, p.err, 43)) return false;
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(j % kStages), r = (int)(j / kStages), b = (int)(j % NB);
+                if (!mbar_wait(bs_full + s, r & 1, p.err, 44)) return false;
+                fence_after_sync();
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kStage);
+                const uint32_t d = tmem + (uint32_t)(b * SH::kRegion);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = (uint32_t)(ks * 32);
+                    mma_f16(d, desc_sw128(a0 + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), idS2, ks > 0 ? 1u : 0u);
+                    mma_f16(d + 64, desc_sw128(a0 + kHalf + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), idS, 1u);
+                }
+                if (SH::kDP) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t ko = (uint32_t)(ks * 32);
+                        mma_f16(d + 128, desc_sw128(a0 + 2 * kHalf + ko, 16, 1024),
+                                desc_sw128(b0 + 2 * kTile + ko, 16, 1024), idS2, ks > 0 ? 1u : 0u);
+                        mma_f16(d + 192, desc_sw128(a0 + 3 * kHalf + ko, 16, 1024),
+                                desc_sw128(b0 + 2 * kTile + ko, 16, 1024), idS, 1u);
+                    }
+                }
+                mma_commit(s_full + b);
+                return true;
+            };
+            // the output blocks of tile i, kappa from TMEM: once its epilogue stored kappa and drained the
+            // previous tile's outputs
+            auto issue_out = [&](int64_t i) -> bool {
+                const int b = (int)(i % NB), s = (int)(i % kStages);
+                if (!mbar_wait(w_full + b, (uint32_t)((i / NB) & 1), p.err, 45)) return false;
+                if (i >= 1 && !mbar_wait(o_empty, (uint32_t)((i - 1) & 1), p.err, 46)) return false;
+                fence_after_sync();
+                const uint32_t b0 = smem_u32(sB + (size_t)s * kStage);
+#pragma unroll
+                for (int o = 0; o < NO; ++o) {
+                    const uint32_t kh = tmem + (uint32_t)(b * SH::kRegion + 64 * o), kl = kh + 32;
+                    const uint32_t acc = tmem + SH::kAcc + (uint32_t)(128 * o);
+                    const uint32_t bb = b0 + SH::out_b(o);
+                    // per 16 streamed points (one epilogue part): hi and lo feature blocks kTile apart
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t bo = bb + (uint32_t)(ks * 16 * kRowB);
+                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO2, ks > 0 ? 1u : 0u);
+                        mma_f16_ta(acc + 64, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
+                    }
+                }
+                mma_commit(bs_empty + s);  // the stage fed S, dP and the outputs
+                mma_commit(o_full);
+                return true;
+            };
+            constexpr int L = NB - 1;  // S runs L tiles ahead of the outputs
+            for (int64_t j = 0; j < n && j < L && ok; ++j) ok = issue_s(j);
+            for (int64_t i = 0; i < n && ok; ++i) {
+                if (i + L < n) ok = issue_s(i + L);
+                if (ok) ok = issue_out(i);
+            }
+        }
+    } else {
+        // ---------------- epilogue: four warps per TMEM lane quarter; part p owns tile columns
+        // [16 p, 16 p + 16) (one output K step) and output features [16 p, 16 p + 16)
+        const int q = warp & 3;
+        const int part = (warp - 2) >> 2;
+        const int lr = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int seg = 0;
+        float4 rst = make_float4(0.f, 0.f, 0.f, 0.f);
+        float rsl = 0.f;
+        float acc[NO][kCols];
+#pragma unroll
+        for (int o = 0; o < NO; ++o)
+#pragma unroll
+            for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
+        bool ok = true;
+        // add this part of tile j's output blocks, scaled back, into the row accumulators
+        auto drain = [&](int64_t j, const float (&inv)[NO]) -> bool {
+            if (!mbar_wait(o_full, (uint32_t)(j & 1), p.err, 47)) return false;
+            fence_after_sync();
+#pragma unroll
+            for (int o = 0; o < NO; ++o) {
+                const uint32_t a = tmem + SH::kAcc + (uint32_t)(128 * o) + lane_off + (uint32_t)(part * kCols);
+                float v[kCols], w[kCols];
+                tmem_ld16x2(a, a + 64, v, w);
+#pragma unroll
+                for (int u = 0; u < kCols; ++u) acc[o][u] += (v[u] + w[u]) * inv[o];
+            }
+            fence_before_sync();
+            mbar_arrive(o_empty);
+            return true;
+        };
+        int rb_cur = -1;
+        const int etid = threadIdx.x - 64;  // 0 .. 32 kEpi - 1
+        // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
+        // of the CTAs whose tile ranges meet it to count itself in) merges it into the outputs.
+        auto write_partial = [&]() {
+            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * SH::kF * kBM;
+#pragma unroll
+            for (int oo = 0; oo < NO; ++oo)
+#pragma unroll
+                for (int f = 0; f < kCols; ++f) o[(size_t)(oo * 64 + part * kCols + f) * kBM + lr] = acc[oo][f];
+            __threadfence();
+            mbar_arrive(fl_bar);
+            if (etid == 0) {
+                int last = 0;
+                if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 48)) {
+                    const int64_t t0 = (int64_t)rb_cur * p.CT;
+                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
+                    __threadfence();
+                }
+                *sflag = last;
+                mbar_arrive(dec_bar);
+            }
+            if (mbar_wait(dec_bar, (uint32_t)(seg & 1), p.err, 49) && *sflag) merge_row<MODE>(p, rb_cur, etid % kBM, etid / kBM);
+            ++seg;
+        };
+        // with a single S buffer the tensor core idles while the epilogue works on a tile, so the previous
+        // tile's outputs are drained before it (during that tile's S); with several, after it
+        constexpr bool kDrainFirst = NB == 1;
+        int64_t pending = -1;
+        float pinv[NO];
+#pragma unroll
+        for (int o = 0; o < NO; ++o) pinv[o] = 0.f;
+        TileCursor cur(t_begin, p.CT);
+        for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
+            const int rb = cur.rb, ct = cur.ct;
+            if (rb != rb_cur) {
+                if (pending >= 0) {
+                    ok = drain(pending, pinv);
+                    pending = -1;
+                    if (!ok) break;
+                }
+                if (rb_cur >= 0) write_partial();
+                rb_cur = rb;
+#pragma unroll
+                for (int o = 0; o < NO; ++o)
+#pragma unroll
+                    for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
+                rst = p.rstat[(int64_t)rb * kBM + lr];  // the row stats are padded to whole row blocks
+                // base-2 score factor of the row: scale log2(e) 2^-e of the row's S operand
+                rsl = (MODE == kColSweep ? rst.x : rst.z) * p.scale * kL2E;
+            }
+            if (kDrainFirst && pending >= 0) {
+                ok = drain(pending, pinv);
+                pending = -1;
+                if (!ok) break;
+            }
+            const int b = (int)(i % NB), s = (int)(i % kStages);
+            ok = mbar_wait(s_full + b, (uint32_t)((i / NB) & 1), p.err, 50) &&
+                 mbar_wait(bs_full + s, (uint32_t)((i / kStages) & 1), p.err, 51);  // the tile's column stats
+            if (!ok) break;
+            fence_after_sync();
+            const float4* st = sStat + s * kBN + part * kCols;
+            const uint32_t reg = tmem + lane_off + (uint32_t)(b * SH::kRegion + part * kCols);
+            float k0[kCols], k1[kCols];
+            float pm0 = 0.f, pm1 = 0.f;
+            {
+                float v[kCols], w[kCols];
+                tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
+                if (MODE == kFwd) {
+                    // O: kappa_ij = P_ij 2^-e_Vj (the stage's V rows are V_j 2^e_Vj)
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) {
+                        const float4 cs = st[u];  // key stats (2^-e_K, 2^-e_V, 0, 0); zeros for padding keys
+                        const float s2 = (v[u] + w[u]) * cs.x * rsl;
+                        const float kp = ExpTraits<float>::bexp(s2 - rst.x) * cs.y;
+                        k0[u] = kp;
+                        pm0 = fmaxf(pm0, kp);
+                    }
+                } else {
+                    float pr[kCols];
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) {
+                        const float4 cs = st[u];
+                        const float s2 = (v[u] + w[u]) * (MODE == kColSweep ? cs.z : cs.x) * rsl;
+                        pr[u] = ExpTraits<float>::bexp(s2 - (MODE == kColSweep ? cs.x : rst.x));
+                    }
+                    tmem_ld16x2(reg + 128, reg + 192, v, w);  // dP: hi*hi, hi*lo + lo*hi
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) {
+                        const float4 cs = st[u];
+                        if (MODE == kRowSweep) {
+                            // row = query i (lse2, delta, 2^-e_Q, 2^-e_dO); column = key j (2^-e_K, 2^-e_V, 0, 0)
+                            const float dp = (v[u] + w[u]) * cs.y * rst.w;
+                            const float kp = pr[u] * (dp - rst.y) * cs.x;  // dS_ij 2^-e_Kj
+                            k0[u] = kp;
+                            pm0 = fmaxf(pm0, fabsf(kp));
+                        } else {
+                            // row = key j (2^-e_K, 2^-e_V, 0, 0); column = query i (lse2, delta, 2^-e_Q, 2^-e_dO)
+                            const float dp = (v[u] + w[u]) * cs.w * rst.y;
+                            const float kp = pr[u] * (dp - cs.y) * cs.z;   // dS_ij 2^-e_Qi
+                            const float kv = pr[u] * cs.w;                 // P_ij 2^-e_dOi
+                            k0[u] = kp;
+                            k1[u] = kv;
+                            pm0 = fmaxf(pm0, fabsf(kp));
+                            pm1 = fmaxf(pm1, kv);
+                        }
+                    }
+                }
+            }
+            // Streamed points past the end (keys of the last tile) have S = 0 and zero stats, but their P may
+            // overflow (a row whose lse is below the float range of exp): give them no weight. The column
+            // sweep's padding queries carry lse = +inf, so their P is exactly 0 there.
+            if (MODE != kColSweep) {
+                const int lim = (int)(p.C - (int64_t)ct * kBN) - part * kCols;  // columns u >= lim are padding
+                if (lim < kCols) {
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) k0[u] = u < lim ? k0[u] : 0.f;
+                }
+            }
+            // the row's largest |kappa| over the tile: the four parts of the quarter exchange theirs (this
+            // also tells each part that the others have read S and dP, which the stores below overwrite)
+            const int par = (int)(i & 1);
+            float2* xm = sMax + (size_t)((par * 4 + q) * kParts) * 32;
+            xm[part * 32 + lane] = make_float2(pm0, pm1);
+            fence_before_sync();
+            mbar_arrive(xch + q * 2 + par);
+            ok = mbar_wait(xch + q * 2 + par, (uint32_t)((i >> 1) & 1), p.err, 52);
+            if (!ok) break;
+            fence_after_sync();
+            float2 mx = xm[lane];
+#pragma unroll
+            for (int pp = 1; pp < kParts; ++pp) {
+                const float2 t = xm[pp * 32 + lane];
+                mx.x = fmaxf(mx.x, t.x);
+                mx.y = fmaxf(mx.y, t.y);
+            }
+            float ninv[NO];  // 2^-e per output: undoes this tile's row scale when its outputs are drained
+#pragma unroll
+            for (int o = 0; o < NO; ++o) {
+                const int e = f16_row_exponent(o == 0 ? mx.x : mx.y);
+                ninv[o] = SH::out_scaled(o) ? pow2i(-e) * p.scale : pow2i(-e);
+                const float f = pow2i(e);
+                uint32_t hw[kCols / 2], lw[kCols / 2];
+#pragma unroll
+                for (int k = 0; k < kCols / 2; ++k) {
+                    const float a = (o == 0 ? k0[2 * k] : k1[2 * k]) * f, c = (o == 0 ? k0[2 * k + 1] : k1[2 * k + 1]) * f;
+                    const __half2 h = __floats2half2_rn(a, c);
+                    const float2 hf = __half22float2(h);
+                    hw[k] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[k] = pack_f16x2(a - hf.x, c - hf.y);
+                }
+                // kappa_hi of points [16 part, 16 part + 16) in columns 64 o + 8 part .. +8, kappa_lo 32 further
+                tmem_st8(tmem + lane_off + (uint32_t)(b * SH::kRegion + 64 * o + part * 8), hw);
+                tmem_st8(tmem + lane_off + (uint32_t)(b * SH::kRegion + 64 * o + 32 + part * 8), lw);
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            mbar_arrive(w_full + b);
+            if (!kDrainFirst && pending >= 0) {
+                ok = drain(pending, pinv);
+                if (!ok) break;
+            }
+            pending = i;
+#pragma unroll
+            for (int o = 0; o < NO; ++o) pinv[o] = ninv[o];
+        }
+        if (ok && pending >= 0) ok = drain(pending, pinv);
+        if (ok && rb_cur >= 0) write_partial();
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Pre-pass, one warp per row over rows_pad rows (two features per lane): the fp16 hi/lo split of A 2^eA
+// (and B 2^eB) and the row's stats.
+//   QUERY: stat = (lse log2 e, delta = B . O, 2^-eA, 2^-eB), padding rows (+inf, 0, 0, 0)
+//   keys:  stat = (2^-eA, 2^-eB, 0, 0), padding rows zeros
+// B, O, lse may be null (their entries are then 0). cnt: ncnt counters zeroed for the sweep that follows.
+template <bool QUERY>
+__global__ void __launch_bounds__(256) attn_prep(const float* __restrict__ A, const float* __restrict__ B,
+                                                 const float* __restrict__ O, const float* __restrict__ lse,
+                                                 int64_t rows, int64_t rows_pad, __half2* __restrict__ Ah,
+                                                 __half2* __restrict__ Al, __half2* __restrict__ Bh,
+                                                 __half2* __restrict__ Bl, float4* __restrict__ stat,
+                                                 int* __restrict__ cnt, int64_t ncnt) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && r < ncnt) cnt[r] = 0;
+    if (r >= rows_pad) return;
+    const __half2 z2 = __floats2half2_rn(0.f, 0.f);
+    if (r >= rows) {
+        Ah[r * 32 + lane] = z2;
+        Al[r * 32 + lane] = z2;
+        if (B) {
+            Bh[r * 32 + lane] = z2;
+            Bl[r * 32 + lane] = z2;
+        }
+        if (lane == 0) stat[r] = QUERY ? make_float4(__int_as_float(0x7f800000), 0.f, 0.f, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    // split one row of X into hi/lo of X 2^e; returns 2^-e
+    auto split = [&](const float* X, __half2* hi, __half2* lo, float2& v) -> float {
+        v = reinterpret_cast<const float2*>(X + r * 64)[lane];
+        float m = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const int e = f16_row_exponent(m);
+        const float f = pow2i(e);
+        const float a = v.x * f, b = v.y * f;
+        const __half2 h = __floats2half2_rn(a, b);
+        const float2 hf = __half22float2(h);
+        hi[r * 32 + lane] = h;
+        lo[r * 32 + lane] = __floats2half2_rn(a - hf.x, b - hf.y);
+        return pow2i(-e);
+    };
+    float2 va, vb = make_float2(0.f, 0.f);
+    const float ia = split(A, Ah, Al, va);
+    const float ib = B ? split(B, Bh, Bl, vb) : 0.f;
+    float delta = 0.f;
+    if (QUERY && B && O) {
+        const float2 o = reinterpret_cast<const float2*>(O + r * 64)[lane];
+        delta = fmaf(vb.x, o.x, vb.y * o.y);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+    }
+    if (lane == 0)
+        stat[r] = QUERY ? make_float4(lse ? lse[r] * 1.4426950408889634f : 0.f, delta, ia, ib) : make_float4(ia, ib, 0.f, 0.f);
+}
+
+struct Plan {
+    int64_t Npad, Mpad;
+    size_t off_qh, off_ql, off_dh, off_dl, off_qst, off_kh, off_kl, off_vh, off_vl, off_kst, off_part, off_cntq,
+        off_cntk, off_err, bytes;
+};
+
+struct Sweep {
+    int64_t T;
+    int CT, G, smax;
+};
+
+static Sweep sweep_of(int64_t R, int64_t C) {
+    Sweep w;
+    const int64_t RB = (R + kBM - 1) / kBM;
+    w.CT = (int)((C + kBN - 1) / kBN);
+    w.T = RB * w.CT;
+    w.G = (int)(w.T < kGrid ? w.T : kGrid);
+    const int64_t per = (w.T + w.G - 1) / w.G;
+    w.smax = (int)((per + w.CT - 1) / w.CT + 1);
+    return w;
+}
+
+static Plan plan_of(int64_t N, int64_t M, bool backward) {
+    Plan pl;
+    pl.Npad = (N + kBM - 1) / kBM * kBM;
+    pl.Mpad = (M + kBM - 1) / kBM * kBM;
+    const size_t qb = (size_t)pl.Npad * kRowB, kb = (size_t)pl.Mpad * kRowB;
+    size_t o = 0;
+    pl.off_qh = o; o += al256(qb);
+    pl.off_ql = o; o += al256(qb);
+    pl.off_dh = o; o += backward ? al256(qb) : 0;
+    pl.off_dl = o; o += backward ? al256(qb) : 0;
+    pl.off_qst = o; o += al256((size_t)pl.Npad * 16);
+    pl.off_kh = o; o += al256(kb);
+    pl.off_kl = o; o += al256(kb);
+    pl.off_vh = o; o += al256(kb);
+    pl.off_vl = o; o += al256(kb);
+    pl.off_kst = o; o += al256((size_t)pl.Mpad * 16);
+    const Sweep a = sweep_of(N, M);
+    size_t part = (size_t)a.G * a.smax * 64 * kBM * 4;
+    if (backward) {
+        const Sweep c = sweep_of(M, N);
+        const size_t pc = (size_t)c.G * c.smax * 128 * kBM * 4;
+        part = part > pc ? part : pc;
+    }
+    pl.off_part = o; o += al256(part);
+    pl.off_cntq = o; o += al256((size_t)(pl.Npad / kBM) * 4);
+    pl.off_cntk = o; o += al256((size_t)(pl.Mpad / kBM) * 4);
+    pl.off_err = o; o += 256;
+    pl.bytes = o;
+    return pl;
+}
+
+template <int MODE>
+static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
+                      const float4* cstat, float* part, int* cnt, float* out0, float* out1, int* err, const char* name,
+                      cudaStream_t s) {
+    const Sweep w = sweep_of(R, C);
+    Params p;
+    p.R = R;
+    p.C = C;
+    p.T = w.T;
+    p.CT = w.CT;
+    p.G = w.G;
+    p.smax = w.smax;
+    p.scale = scale;
+    p.rstat = rstat;
+    p.cstat = cstat;
+    p.part = part;
+    p.cnt = cnt;
+    p.out0 = out0;
+    p.out1 = out1;
+    p.err = err;
+    cudaFuncSetAttribute(attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    HookScope h(name, s);
+    attn_tc<MODE><<<w.G, kThreads, kSmem, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p);
+}
+
+}  // namespace attn
+}  // namespace tc
+
+size_t attn_tc_workspace(int64_t N, int64_t M, bool backward) { return tc::attn::plan_of(N, M, backward).bytes; }
+
+// Forward: a.lse holds the row log-sum-exp (already computed on the stream); writes a.out.
+int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
+    using namespace tc;
+    using namespace tc::attn;
+    const Plan pl = plan_of(a.N, a.M, false);
+    char* ws = static_cast<char*>(a.ws);
+    __half2* qh = reinterpret_cast<__half2*>(ws + pl.off_qh);
+    __half2* ql = reinterpret_cast<__half2*>(ws + pl.off_ql);
+    __half2* kh = reinterpret_cast<__half2*>(ws + pl.off_kh);
+    __half2* kl = reinterpret_cast<__half2*>(ws + pl.off_kl);
+    __half2* vh = reinterpret_cast<__half2*>(ws + pl.off_vh);
+    __half2* vl = reinterpret_cast<__half2*>(ws + pl.off_vl);
+    float4* qst = reinterpret_cast<float4*>(ws + pl.off_qst);
+    float4* kst = reinterpret_cast<float4*>(ws + pl.off_kst);
+    int* cntq = reinterpret_cast<int*>(ws + pl.off_cntq);
+    CUtensorMap m[8];
+    if (!make_map_f16(&m[0], qh, pl.Npad, kBM) || !make_map_f16(&m[1], ql, pl.Npad, kBM) ||
+        !make_map_f16(&m[4], kh, pl.Mpad, kBN) || !make_map_f16(&m[5], kl, pl.Mpad, kBN) ||
+        !make_map_f16(&m[6], vh, pl.Mpad, kBN) || !make_map_f16(&m[7], vl, pl.Mpad, kBN))
+        return -1;
+    m[2] = m[0];  // no second row operand in the forward
+    m[3] = m[1];
+    {
+        HookScope h("attn_prep", s);
+        attn_prep<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, nullptr, nullptr, a.lse, a.N, pl.Npad, qh, ql,
+                                                               nullptr, nullptr, qst, cntq, pl.Npad / kBM);
+    }
+    {
+        HookScope h("attn_prep", s);
+        attn_prep<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, kh, kl, vh,
+                                                                vl, kst, nullptr, 0);
+    }
+    run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, reinterpret_cast<float*>(ws + pl.off_part), cntq, a.out,
+                    nullptr, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
+    return 3;
+}
+
+// Backward: dQ (row sweep) and dK, dV (column sweep); null outputs are not written (a sweep none of whose
+// outputs is wanted does not run).
+int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
+    using namespace tc;
+    using namespace tc::attn;
+    const Plan pl = plan_of(a.N, a.M, true);
+    char* ws = static_cast<char*>(a.ws);
+    __half2* qh = reinterpret_cast<__half2*>(ws + pl.off_qh);
+    __half2* ql = reinterpret_cast<__half2*>(ws + pl.off_ql);
+    __half2* dh = reinterpret_cast<__half2*>(ws + pl.off_dh);
+    __half2* dl = reinterpret_cast<__half2*>(ws + pl.off_dl);
+    __half2* kh = reinterpret_cast<__half2*>(ws + pl.off_kh);
+    __half2* kl = reinterpret_cast<__half2*>(ws + pl.off_kl);
+    __half2* vh = reinterpret_cast<__half2*>(ws + pl.off_vh);
+    __half2* vl = reinterpret_cast<__half2*>(ws + pl.off_vl);
+    float4* qst = reinterpret_cast<float4*>(ws + pl.off_qst);
+    float4* kst = reinterpret_cast<float4*>(ws + pl.off_kst);
+    int* cntq = reinterpret_cast<int*>(ws + pl.off_cntq);
+    int* cntk = reinterpret_cast<int*>(ws + pl.off_cntk);
+    float* part = reinterpret_cast<float*>(ws + pl.off_part);
+    int* err = reinterpret_cast<int*>(ws + pl.off_err);
+    // row sweep maps: A = (Q, dO) in 128-row boxes, B = (K, V) in 64-row boxes; column sweep the reverse
+    CUtensorMap mr[8], mc[8];
+    if (!make_map_f16(&mr[0], qh, pl.Npad, kBM) || !make_map_f16(&mr[1], ql, pl.Npad, kBM) ||
+        !make_map_f16(&mr[2], dh, pl.Npad, kBM) || !make_map_f16(&mr[3], dl, pl.Npad, kBM) ||
+        !make_map_f16(&mr[4], kh, pl.Mpad, kBN) || !make_map_f16(&mr[5], kl, pl.Mpad, kBN) ||
+        !make_map_f16(&mr[6], vh, pl.Mpad, kBN) || !make_map_f16(&mr[7], vl, pl.Mpad, kBN) ||
+        !make_map_f16(&mc[0], kh, pl.Mpad, kBM) || !make_map_f16(&mc[1], kl, pl.Mpad, kBM) ||
+        !make_map_f16(&mc[2], vh, pl.Mpad, kBM) || !make_map_f16(&mc[3], vl, pl.Mpad, kBM) ||
+        !make_map_f16(&mc[4], qh, pl.Npad, kBN) || !make_map_f16(&mc[5], ql, pl.Npad, kBN) ||
+        !make_map_f16(&mc[6], dh, pl.Npad, kBN) || !make_map_f16(&mc[7], dl, pl.Npad, kBN))
+        return -1;
+    int n = 0;
+    {
+        HookScope h("attn_prep", s);
+        attn_prep<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, a.dO, a.O, a.lse, a.N, pl.Npad, qh, ql, dh, dl,
+                                                               qst, cntq, pl.Npad / kBM);
+        ++n;
+    }
+    {
+        HookScope h("attn_prep", s);
+        attn_prep<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, kh, kl, vh,
+                                                                vl, kst, cntk, pl.Mpad / kBM);
+        ++n;
+    }
+    if (a.dQ) {
+        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, part, cntq, a.dQ, nullptr, err, "attn_bwd_row_tc", s);
+        ++n;
+    }
+    if (a.dK || a.dV) {
+        run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, part, cntk, a.dK, a.dV, err, "attn_bwd_col_tc", s);
+        ++n;
+    }
+    return n;
+}
+
+}  // namespace tp

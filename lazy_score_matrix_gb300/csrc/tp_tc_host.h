@@ -63,6 +63,12 @@ inline bool make_map_f16(CUtensorMap* m, const void* base, int64_t rows, int box
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp16 hi/lo split of x 2^e per point row (the pre-pass of the kind::f16 kernels, tp_tc_lse.cu): hi and lo
+// [rows][64] fp16, inv_scale = 2^-e and norm = |x|^2 for rows_pad rows (zeros past rows); cnt (optional):
+// ncnt counters zeroed for the kernel that follows.
+void launch_split16(const float* x, int64_t rows, int64_t rows_pad, void* hi, void* lo, float* inv_scale, float* norm,
+                    int* cnt, int64_t ncnt, cudaStream_t s);
+
 inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace tc

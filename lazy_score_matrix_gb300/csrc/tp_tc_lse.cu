@@ -38,22 +38,6 @@ constexpr int kEpi = 16;                    // epilogue warps: 4 per TMEM lane q
 constexpr int kTcThreads = 32 * (2 + kEpi);
 constexpr int kGrid = 152;                  // persistent CTAs: one per GB300 SM
 
-// First tile of CTA c: floor(T c / G). 32-bit division whenever T G fits (every practical size).
-__host__ __device__ inline int64_t range_start(int64_t T, int G, int c) {
-    if ((unsigned long long)T * (unsigned)G < (1ull << 32)) return (int64_t)((uint32_t)T * (uint32_t)c / (uint32_t)G);
-    return (T * c) / G;
-}
-// The CTA whose range holds tile t: the largest c with floor(T c / G) <= t, i.e. T c < G (t + 1).
-__host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) {
-    if ((unsigned long long)T * (unsigned)G < (1ull << 32))
-        return (int)(((uint32_t)G * (uint32_t)(t + 1) - 1u) / (uint32_t)T);
-    return (int)(((int64_t)G * (t + 1) - 1) / T);
-}
-// Row block of tile t (t < T).
-__host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
-    return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
-}
-
 // Base-2 score of one element from its dot product (metric, scale, exp).
 template <int METRIC, bool EXP>
 __device__ __forceinline__ float score2(float dot, float xn, float yn, float scale, float neg_gamma_log2) {
@@ -68,12 +52,6 @@ __device__ __forceinline__ float score2(float dot, float xn, float yn, float sca
     const float t = scale * base;
     const float S = EXP ? ExpTraits<float>::bexp(t * kL2E) : t;
     return S * kL2E;
-}
-
-// Pack two floats into fp16x2 (a in the low half), rounded to nearest.
-__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Per point row: the fp16 hi/lo split of x 2^e, 2^-e, and |x|^2. One warp per row, two features per
@@ -112,6 +90,13 @@ __global__ void __launch_bounds__(256) tc_split16(const float* __restrict__ x, i
         inv_scale[r] = pow2i(-e);
         norm[r] = ss;
     }
+}
+
+void launch_split16(const float* x, int64_t rows, int64_t rows_pad, void* hi, void* lo, float* inv_scale, float* norm,
+                    int* cnt, int64_t ncnt, cudaStream_t s) {
+    HookScope h("tc_split16", s);
+    tc_split16<<<(unsigned)((rows_pad + 7) / 8), 256, 0, s>>>(x, rows, rows_pad, static_cast<__half2*>(hi),
+                                                             static_cast<__half2*>(lo), inv_scale, norm, cnt, ncnt);
 }
 
 // ------------------------------------------------------------------------------------------------
