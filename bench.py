@@ -322,11 +322,18 @@ class Attention(Workload):
         self.h2d = sum(v.numel() * 4 for v in self.host.values())
         self.d2h = (self.N * self.C + (self.N + self.M) * self.D + self.M * self.C) * 4
         D, C = self.D, self.C
-        # fwd 2D + 2C + 3; bwd: S 2D, dV 2C, dP 2C, dS 2, dQ 2D, dK 2D (dQ row sweep: S, dP, dS, dQ)
+        # fwd 2D + 2C + 3; bwd: S 2D, dV 2C, dP 2C, dS 2, dQ 2D, dK 2D (dQ row sweep: S, dP, dS, dQ).
+        # Tensor-core path: the forward's S and exp go to the log-sum-exp pass and P V (2C) to the second
+        # pass (its replay of S is not credited); the row sweep as above, the column sweep dK + dV (its
+        # replay of S and dP not credited), against the fp16 tensor peak.
         self.flops_per_pair = {"fwd_sweep_softmax": (2 * D + 2 * C + 3, "alu"),
                                "bwd_sweep_softmax_row": (2 * D + 2 * C + 2 + 2 * D, "alu"),
                                "bwd_sweep_softmax_col": (2 * D, "alu"),
-                               "bwd_sweep_softmax_col_dv": (2 * C, "alu")}
+                               "bwd_sweep_softmax_col_dv": (2 * C, "alu"),
+                               "lse_fwd_tc": (2 * D + 3, "tensor-f16"),
+                               "attn_fwd_tc": (2 * C, "tensor-f16"),
+                               "attn_bwd_row_tc": (2 * D + 2 * C + 2 + 2 * D, "tensor-f16"),
+                               "attn_bwd_col_tc": (2 * D + 2 * C, "tensor-f16")}
         self.step_flops_per_pair = (2 * D + 2 * C + 3) + (2 * D + 2 * C + 2 * C + 2 + 2 * D + 2 * D)
 
     def step(self):

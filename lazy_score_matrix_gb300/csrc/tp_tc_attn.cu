@@ -65,15 +65,31 @@ template <int MODE>
 struct Shape {
     static constexpr bool kDP = MODE != kFwd;                       // dP = A2 B2^T is formed
     static constexpr int kOuts = MODE == kColSweep ? 2 : 1;
+    // Forward: three S buffers of 128 TMEM columns, kappa stored over the buffer's S, the output at 384.
+    // Backward (kSep): one S + dP region (256 columns) that the MMA refills as soon as the epilogue has
+    // read it into registers, kappa in columns of its own (64 per output), the outputs after them.
+    static constexpr bool kSep = MODE != kFwd;
     static constexpr int kRegion = kDP ? 256 : 128;                 // TMEM columns of one S (+ dP) buffer
-    static constexpr int kBuf = (512 - 128 * kOuts) / kRegion;      // 3, 1, 1
-    static constexpr uint32_t kAcc = (uint32_t)(kBuf * kRegion);     // first output accumulator
+    static constexpr int kBuf = kSep ? 1 : 3;
     static constexpr int kF = 64 * kOuts;                           // features of one partial row
+    // TMEM column of output o's kappa (hi in +0..31, lo in +32..63) for S buffer b
+    __host__ __device__ static constexpr uint32_t kap(int b, int o) {
+        return kSep ? (uint32_t)(kRegion + 64 * o) : (uint32_t)(b * kRegion + 64 * o);
+    }
+    // TMEM column of output o's accumulator (64 columns, one fp32 accumulator)
+    __host__ __device__ static constexpr uint32_t acc(int o) {
+        return kSep ? (uint32_t)(kRegion + 64 * kOuts + 64 * o) : (uint32_t)(kBuf * kRegion + 64 * o);
+    }
     // the stage part that is the B operand of output o
-    __host__ __device__ static constexpr uint32_t out_b(int o) { return MODE == kRowSweep ? 0u : (o == 0 && MODE == kColSweep ? 0u : 2u * kTile); }
+    __host__ __device__ static constexpr uint32_t out_b(int o) {
+        return MODE == kRowSweep ? 0u : (o == 0 && MODE == kColSweep ? 0u : 2u * kTile);
+    }
     // outputs whose coefficients leave out the score's scale (dQ, dK)
     __host__ __device__ static constexpr bool out_scaled(int o) { return MODE != kFwd && o == 0; }
 };
+static_assert(Shape<kColSweep>::acc(1) + 64 <= 512 && Shape<kRowSweep>::acc(0) + 64 <= 512 &&
+                  Shape<kFwd>::acc(0) + 64 <= 512,
+              "TMEM columns");
 
 struct Params {
     int64_t R;             // rows of the sweep (queries; keys for the column sweep)
@@ -127,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr float kL2E = 1.4426950408889634f;
     constexpr int NB = SH::kBuf;
     constexpr int NO = SH::kOuts;
+    constexpr bool SEP = SH::kSep;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;
@@ -139,9 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bs_full = bars + 2;              // [kStages]
     uint64_t* bs_empty = bs_full + kStages;    // [kStages]
     uint64_t* s_full = bs_empty + kStages;     // [NB] S (and dP) of a buffer are in TMEM
-    uint64_t* w_full = s_full + NB;            // [NB] the epilogue stored the buffer's kappa
-    uint64_t* o_full = w_full + NB;            // the output MMAs of a tile finished
-    uint64_t* o_empty = o_full + 1;            // the epilogue read the output block
+    uint64_t* w_full = s_full + NB;            // [NB] the epilogue stored the tile's kappa
+    uint64_t* s_free = w_full + NB;            // (backward) the epilogue has read S and dP into registers
+    uint64_t* o_full = s_free + 1;             // the output MMAs of a tile finished
+    uint64_t* o_empty = o_full + 1;            // (forward) the epilogue read the output block
     uint64_t* xch = o_empty + 1;               // [quarter][parity]: the row-maximum exchange
     uint64_t* fl_bar = xch + 8;                // the epilogue wrote its partials of a row block
     uint64_t* dec_bar = fl_bar + 1;            // the CTA knows whether it merges that row block
@@ -163,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(s_full + b, 1);
             mbar_init(w_full + b, 32 * kEpi);
         }
+        mbar_init(s_free, 32 * kEpi);
         mbar_init(o_full, 1);
         mbar_init(o_empty, 32 * kEpi);
         for (int x = 0; x < 8; ++x) mbar_init(xch + x, 32 * kParts);
@@ -212,13 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idS2 = idesc_f16(kBM, 2 * kBN, false);  // A_hi [B_hi; B_lo]: N 128
             constexpr uint32_t idS = idesc_f16(kBM, kBN, false);       // A_lo B_hi: N 64
-            constexpr uint32_t idO2 = idesc_f16(kBM, 128, true);       // kappa_hi [B_hi | B_lo] (MN-major): N 128
-            constexpr uint32_t idO = idesc_f16(kBM, 64, true);         // kappa_lo B_hi (MN-major): N 64
+            constexpr uint32_t idO = idesc_f16(kBM, 64, true);         // kappa B (MN-major): N 64
             int a_uses = 0, rb_cur = -1;
             bool ok = true;
             TileCursor cur(t_begin, p.CT);
-            // S (and dP) of tile j into buffer j % NB: its previous kappa was read by the output MMAs of
-            // tile j - NB, issued earlier (the tensor core runs one thread's MMAs in order)
+            // S (and dP) of tile j into buffer j % NB
             auto issue_s = [&](int64_t j) -> bool {
                 const int rb = cur.rb;
                 cur.next();
@@ -252,36 +269,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(s_full + b);
                 return true;
             };
-            // the output blocks of tile i, kappa from TMEM: once its epilogue stored kappa and drained the
-            // previous tile's outputs
+            // the output blocks of tile i from its kappa in TMEM: kappa_lo B_hi, kappa_hi B_lo, kappa_hi B_hi
+            // into one accumulator per output (the epilogue drains it every tile). The forward waits for the
+            // previous tile's drain; the backward's epilogue drains it before storing this tile's kappa.
             auto issue_out = [&](int64_t i) -> bool {
                 const int b = (int)(i % NB), s = (int)(i % kStages);
                 if (!mbar_wait(w_full + b, (uint32_t)((i / NB) & 1), p.err, 45)) return false;
-                if (i >= 1 && !mbar_wait(o_empty, (uint32_t)((i - 1) & 1), p.err, 46)) return false;
+                if (!SEP && i >= 1 && !mbar_wait(o_empty, (uint32_t)((i - 1) & 1), p.err, 46)) return false;
                 fence_after_sync();
                 const uint32_t b0 = smem_u32(sB + (size_t)s * kStage);
 #pragma unroll
                 for (int o = 0; o < NO; ++o) {
-                    const uint32_t kh = tmem + (uint32_t)(b * SH::kRegion + 64 * o), kl = kh + 32;
-                    const uint32_t acc = tmem + SH::kAcc + (uint32_t)(128 * o);
+                    const uint32_t kh = tmem + SH::kap(b, o), kl = kh + 32;
+                    const uint32_t acc = tmem + SH::acc(o);
                     const uint32_t bb = b0 + SH::out_b(o);
-                    // per 16 streamed points (one epilogue part): hi and lo feature blocks kTile apart
+                    // per 16 streamed points (one epilogue part): the stage's hi and lo feature blocks, MN-major
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t bo = bb + (uint32_t)(ks * 16 * kRowB);
-                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO2, ks > 0 ? 1u : 0u);
-                        mma_f16_ta(acc + 64, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
+                        mma_f16_ta(acc, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, ks > 0 ? 1u : 0u);
+                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo + kTile, kTile, 1024), idO, 1u);
+                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
                     }
                 }
                 mma_commit(bs_empty + s);  // the stage fed S, dP and the outputs
                 mma_commit(o_full);
                 return true;
             };
-            constexpr int L = NB - 1;  // S runs L tiles ahead of the outputs
-            for (int64_t j = 0; j < n && j < L && ok; ++j) ok = issue_s(j);
-            for (int64_t i = 0; i < n && ok; ++i) {
-                if (i + L < n) ok = issue_s(i + L);
-                if (ok) ok = issue_out(i);
+            if (SEP) {
+                // S and dP of tile i + 1 go in as soon as the epilogue has read tile i's, before its outputs
+                if (n > 0) ok = issue_s(0);
+                for (int64_t i = 0; i < n && ok; ++i) {
+                    if (i + 1 < n) {
+                        ok = mbar_wait(s_free, (uint32_t)(i & 1), p.err, 53);
+                        if (ok) ok = issue_s(i + 1);
+                    }
+                    if (ok) ok = issue_out(i);
+                }
+            } else {
+                // S runs two tiles ahead of the outputs: buffer (i + 2) % 3 held kappa(i - 1), read by the
+                // outputs of tile i - 1, issued earlier (the tensor core runs one thread's MMAs in order)
+                constexpr int L = NB - 1;
+                for (int64_t j = 0; j < n && j < L && ok; ++j) ok = issue_s(j);
+                for (int64_t i = 0; i < n && ok; ++i) {
+                    if (i + L < n) ok = issue_s(i + L);
+                    if (ok) ok = issue_out(i);
+                }
             }
         }
     } else {
@@ -300,20 +333,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
         bool ok = true;
-        // add this part of tile j's output blocks, scaled back, into the row accumulators
-        auto drain = [&](int64_t j, const float (&inv)[NO]) -> bool {
+        // tile j's output MMAs have finished (its kappa is no longer read)
+        auto wait_out = [&](int64_t j) -> bool {
             if (!mbar_wait(o_full, (uint32_t)(j & 1), p.err, 47)) return false;
             fence_after_sync();
+            return true;
+        };
+        // add this part of the finished output blocks, scaled back, into the row accumulators
+        auto add_out = [&](const float (&inv)[NO]) {
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
-                const uint32_t a = tmem + SH::kAcc + (uint32_t)(128 * o) + lane_off + (uint32_t)(part * kCols);
-                float v[kCols], w[kCols];
-                tmem_ld16x2(a, a + 64, v, w);
+                float v[kCols];
+                tmem_ld16(tmem + SH::acc(o) + lane_off + (uint32_t)(part * kCols), v);
 #pragma unroll
-                for (int u = 0; u < kCols; ++u) acc[o][u] += (v[u] + w[u]) * inv[o];
+                for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u], inv[o], acc[o][u]);
             }
-            fence_before_sync();
-            mbar_arrive(o_empty);
+        };
+        auto drain = [&](int64_t j, const float (&inv)[NO]) -> bool {
+            if (!wait_out(j)) return false;
+            add_out(inv);
+            if (!SEP) {
+                fence_before_sync();
+                mbar_arrive(o_empty);
+            }
             return true;
         };
         int rb_cur = -1;
@@ -342,9 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mbar_wait(dec_bar, (uint32_t)(seg & 1), p.err, 49) && *sflag) merge_row<MODE>(p, rb_cur, etid % kBM, etid / kBM);
             ++seg;
         };
-        // with a single S buffer the tensor core idles while the epilogue works on a tile, so the previous
-        // tile's outputs are drained before it (during that tile's S); with several, after it
-        constexpr bool kDrainFirst = NB == 1;
         int64_t pending = -1;
         float pinv[NO];
 #pragma unroll
@@ -368,11 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // base-2 score factor of the row: scale log2(e) 2^-e of the row's S operand
                 rsl = (MODE == kColSweep ? rst.x : rst.z) * p.scale * kL2E;
             }
-            if (kDrainFirst && pending >= 0) {
-                ok = drain(pending, pinv);
-                pending = -1;
-                if (!ok) break;
-            }
             const int b = (int)(i % NB), s = (int)(i % kStages);
             ok = mbar_wait(s_full + b, (uint32_t)((i / NB) & 1), p.err, 50) &&
                  mbar_wait(bs_full + s, (uint32_t)((i / kStages) & 1), p.err, 51);  // the tile's column stats
@@ -382,47 +416,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t reg = tmem + lane_off + (uint32_t)(b * SH::kRegion + part * kCols);
             float k0[kCols], k1[kCols];
             float pm0 = 0.f, pm1 = 0.f;
-            {
+            if (MODE == kFwd) {
                 float v[kCols], w[kCols];
                 tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
-                if (MODE == kFwd) {
-                    // O: kappa_ij = P_ij 2^-e_Vj (the stage's V rows are V_j 2^e_Vj)
+                // O: kappa_ij = P_ij 2^-e_Vj (the stage's V rows are V_j 2^e_Vj)
+#pragma unroll
+                for (int u = 0; u < kCols; ++u) {
+                    const float4 cs = st[u];  // key stats (2^-e_K, 2^-e_V, 0, 0); zeros for padding keys
+                    const float kp = ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.x * rsl, -rst.x)) * cs.y;
+                    k0[u] = kp;
+                    pm0 = fmaxf(pm0, kp);
+                }
+            } else {
+                // row sweep: row = query i (lse2, delta, 2^-e_Q, 2^-e_dO), column = key j (2^-e_K, 2^-e_V, 0, 0);
+                // column sweep: row = key j (2^-e_K, 2^-e_V, 0, 0), column = query i (lse2, delta, 2^-e_Q, 2^-e_dO)
+                float pr[kCols];
+                {
+                    float v[kCols], w[kCols];
+                    tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
 #pragma unroll
                     for (int u = 0; u < kCols; ++u) {
-                        const float4 cs = st[u];  // key stats (2^-e_K, 2^-e_V, 0, 0); zeros for padding keys
-                        const float s2 = (v[u] + w[u]) * cs.x * rsl;
-                        const float kp = ExpTraits<float>::bexp(s2 - rst.x) * cs.y;
+                        const float4 cs = st[u];
+                        pr[u] = MODE == kRowSweep ? ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.x * rsl, -rst.x))
+                                                  : ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.z * rsl, -cs.x));
+                    }
+                }
+                float a[kCols], c[kCols];
+                tmem_ld16x2(reg + 128, reg + 192, a, c);  // dP: hi*hi, hi*lo + lo*hi
+                // S and dP are in registers: the MMA may refill the region with the next tile's
+                fence_before_sync();
+                mbar_arrive(s_free);
+#pragma unroll
+                for (int u = 0; u < kCols; ++u) {
+                    const float4 cs = st[u];
+                    if (MODE == kRowSweep) {
+                        const float kp = pr[u] * cs.x * fmaf(a[u] + c[u], cs.y * rst.w, -rst.y);  // dS_ij 2^-e_Kj
                         k0[u] = kp;
-                        pm0 = fmaxf(pm0, kp);
-                    }
-                } else {
-                    float pr[kCols];
-#pragma unroll
-                    for (int u = 0; u < kCols; ++u) {
-                        const float4 cs = st[u];
-                        const float s2 = (v[u] + w[u]) * (MODE == kColSweep ? cs.z : cs.x) * rsl;
-                        pr[u] = ExpTraits<float>::bexp(s2 - (MODE == kColSweep ? cs.x : rst.x));
-                    }
-                    tmem_ld16x2(reg + 128, reg + 192, v, w);  // dP: hi*hi, hi*lo + lo*hi
-#pragma unroll
-                    for (int u = 0; u < kCols; ++u) {
-                        const float4 cs = st[u];
-                        if (MODE == kRowSweep) {
-                            // row = query i (lse2, delta, 2^-e_Q, 2^-e_dO); column = key j (2^-e_K, 2^-e_V, 0, 0)
-                            const float dp = (v[u] + w[u]) * cs.y * rst.w;
-                            const float kp = pr[u] * (dp - rst.y) * cs.x;  // dS_ij 2^-e_Kj
-                            k0[u] = kp;
-                            pm0 = fmaxf(pm0, fabsf(kp));
-                        } else {
-                            // row = key j (2^-e_K, 2^-e_V, 0, 0); column = query i (lse2, delta, 2^-e_Q, 2^-e_dO)
-                            const float dp = (v[u] + w[u]) * cs.w * rst.y;
-                            const float kp = pr[u] * (dp - cs.y) * cs.z;   // dS_ij 2^-e_Qi
-                            const float kv = pr[u] * cs.w;                 // P_ij 2^-e_dOi
-                            k0[u] = kp;
-                            k1[u] = kv;
-                            pm0 = fmaxf(pm0, fabsf(kp));
-                            pm1 = fmaxf(pm1, kv);
-                        }
+                        pm0 = fmaxf(pm0, fabsf(kp));
+                    } else {
+                        const float kp = pr[u] * cs.z * fmaf(a[u] + c[u], cs.w * rst.y, -cs.y);  // dS_ij 2^-e_Qi
+                        const float kv = pr[u] * cs.w;                                              // P_ij 2^-e_dOi
+                        k0[u] = kp;
+                        k1[u] = kv;
+                        pm0 = fmaxf(pm0, fabsf(kp));
+                        pm1 = fmaxf(pm1, kv);
                     }
                 }
             }
@@ -436,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < kCols; ++u) k0[u] = u < lim ? k0[u] : 0.f;
                 }
             }
-            // the row's largest |kappa| over the tile: the four parts of the quarter exchange theirs (this
-            // also tells each part that the others have read S and dP, which the stores below overwrite)
+            // the row's largest |kappa| over the tile: the four parts of the quarter exchange theirs (in the
+            // forward this also tells each part that the others have read S, which the stores overwrite)
             const int par = (int)(i & 1);
             float2* xm = sMax + (size_t)((par * 4 + q) * kParts) * 32;
             xm[part * 32 + lane] = make_float2(pm0, pm1);
@@ -453,29 +490,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx.x = fmaxf(mx.x, t.x);
                 mx.y = fmaxf(mx.y, t.y);
             }
+            // backward: the previous tile's output MMAs have read their kappa before this tile's is stored,
+            // and the epilogue takes their result out of the accumulators before it hands them over again
+            if (SEP && pending >= 0) {
+                ok = wait_out(pending);
+                if (!ok) break;
+            }
             float ninv[NO];  // 2^-e per output: undoes this tile's row scale when its outputs are drained
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
                 const int e = f16_row_exponent(o == 0 ? mx.x : mx.y);
-                ninv[o] = SH::out_scaled(o) ? pow2i(-e) * p.scale : pow2i(-e);
                 const float f = pow2i(e);
+                ninv[o] = SH::out_scaled(o) ? pow2i(-e) * p.scale : pow2i(-e);
                 uint32_t hw[kCols / 2], lw[kCols / 2];
 #pragma unroll
                 for (int k = 0; k < kCols / 2; ++k) {
-                    const float a = (o == 0 ? k0[2 * k] : k1[2 * k]) * f, c = (o == 0 ? k0[2 * k + 1] : k1[2 * k + 1]) * f;
-                    const __half2 h = __floats2half2_rn(a, c);
+                    const float x0 = (o == 0 ? k0[2 * k] : k1[2 * k]) * f, x1 = (o == 0 ? k0[2 * k + 1] : k1[2 * k + 1]) * f;
+                    const __half2 h = __floats2half2_rn(x0, x1);
                     const float2 hf = __half22float2(h);
                     hw[k] = *reinterpret_cast<const uint32_t*>(&h);
-                    lw[k] = pack_f16x2(a - hf.x, c - hf.y);
+                    lw[k] = pack_f16x2(x0 - hf.x, x1 - hf.y);
                 }
-                // kappa_hi of points [16 part, 16 part + 16) in columns 64 o + 8 part .. +8, kappa_lo 32 further
-                tmem_st8(tmem + lane_off + (uint32_t)(b * SH::kRegion + 64 * o + part * 8), hw);
-                tmem_st8(tmem + lane_off + (uint32_t)(b * SH::kRegion + 64 * o + 32 + part * 8), lw);
+                // kappa_hi of points [16 part, 16 part + 16) in columns kap + 8 part .. +8, kappa_lo 32 further
+                tmem_st8(tmem + lane_off + SH::kap(b, o) + (uint32_t)(part * 8), hw);
+                tmem_st8(tmem + lane_off + SH::kap(b, o) + (uint32_t)(32 + part * 8), lw);
             }
             tmem_st_wait();
+            if (SEP && pending >= 0) add_out(pinv);
             fence_before_sync();
             mbar_arrive(w_full + b);
-            if (!kDrainFirst && pending >= 0) {
+            if (!SEP && pending >= 0) {
                 ok = drain(pending, pinv);
                 if (!ok) break;
             }
