@@ -882,7 +882,7 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
                          ws, ws_bytes));
     const size_t need = ws_size("pairwise_softmax_matmul_backward", pr, C, 0);
     TP_CHECK(check_ws(ws, ws_bytes, need));
-    if (attn_tc_eligible(pr, sc, C, {V, out, lse, grad_out, dX, dY, dV}) && !(dX && dX == dY)) {
+    if (attn_tc_eligible(pr, sc, C, {V, out, lse, grad_out, dX, dY, dV})) {
         AttnTcArgs t{};
         t.Q = static_cast<const float*>(pr->X);
         t.K = static_cast<const float*>(pr->Y);
@@ -896,6 +896,7 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
         t.dQ = static_cast<float*>(dX);
         t.dK = static_cast<float*>(dY);
         t.dV = static_cast<float*>(dV);
+        t.accumulate_dK = dX && dX == dY ? 1 : 0;  // same points: the column sweep adds dK onto dQ
         t.ws = ws;
         const int n = launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream));
         if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");

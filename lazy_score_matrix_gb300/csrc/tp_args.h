@@ -49,6 +49,7 @@ struct AttnTcArgs {
     const float *O, *dO;     // backward: the forward output and its upstream gradient [N, 64]
     float* out;              // forward output [N, 64]
     float *dQ, *dK, *dV;     // backward outputs (null: not wanted)
+    int accumulate_dK;       // add dK into its buffer (dQ and dK of the same points summed in one buffer)
     void* ws;
 };
 

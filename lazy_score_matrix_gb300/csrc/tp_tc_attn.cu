@@ -3,10 +3,11 @@
 // guide "Using Torchpairwise in Models", Task Map (attention: softmax_matmul(V) on lazy(Q, K, "linear")
 // times a scale), and the introduction ("First derivatives replay the tiles").
 //
-// Operands use the scaled fp16 split of the log-sum-exp kernels: every point row x is multiplied by a
-// power of two 2^e of its own (max|x| 2^e in [2^14, 2^15)) and split into hi = fp16(x 2^e) and
-// lo = fp16(x 2^e - hi); a dot product is (xh.yh + (xh.yl + xl.yh)) 2^-(e_x + e_y), with hi*hi in TMEM
-// columns of its own.
+// Operands. Each of Q, K, V and dO is multiplied by one power of two of its own (its largest |element|
+// brought into [2^14, 2^15)) and split into hi = fp16(x 2^e) and lo = fp16(x 2^e - hi), both rounded to
+// nearest: 22 significant bits for every element within 2^17 of the matrix's largest, the same as a
+// per-row power of two gives within a row, and the unscale factors of S and dP become constants. A dot
+// product is (xh.yh + (xh.yl + xl.yh)) 2^-(e_x + e_y), with hi*hi in TMEM columns of its own.
 //
 // Forward: the row log-sum-exp first (lse_fwd_tc), then one sweep that forms P_ij = exp(S_ij - lse_i)
 // tile by tile and accumulates P V on the tensor core. With lse known, the output needs no running
@@ -15,13 +16,15 @@
 //   row sweep     dQ_i = scale sum_j dS_ij K_j
 //   column sweep  dK_j = scale sum_i dS_ij Q_i,   dV_j = sum_i P_ij dO_i
 // All three sweeps are one kernel template. A 128 x 64 tile's S (and dP) go into TMEM; the epilogue
-// turns them into coefficient rows kappa (one per output), scales each row by a power of two that the
-// four warps sharing the row agree on, splits kappa into fp16 hi/lo and stores it back into TMEM as
-// the A operand of the output MMA. The output MMA's B operand is the tile's own streamed points read
-// MN-major, so no transposed copy of any matrix exists: the column sweep streams Q and dO and holds K
-// and V as its row block. Each tile's output block is added, unscaled, into per-row registers
-// (two-level accumulation); a CTA writes one partial per row block it touched, and the last CTA to
-// finish a row block adds the partials in CTA order (deterministic, no atomics on the data).
+// reads them into registers (after which the MMA refills the buffer with a later tile) and turns them
+// into coefficient rows kappa, one per output, each row scaled by a power of two fixed in advance from a
+// bound (P <= 1 and |dP_ij - delta_i| <= |dO_i| |V_j| + |delta_i|): P 2^14 for the P V products, and
+// dS 2^E with E from the bound for the dS products, the power of two folded into the exp. kappa is
+// split into fp16 hi/lo and stored into TMEM as the A operand of the output MMA, whose B operand is the
+// tile's own streamed points read MN-major: no transposed copy of any matrix exists (the column sweep
+// streams Q and dO and holds K and V as its row block). Each tile's output block is added into per-row
+// registers (two-level accumulation); a CTA writes one partial per row block it touched, and the last
+// CTA to finish a row block adds the partials in CTA order (deterministic, no atomics on the data).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -49,10 +52,14 @@ constexpr int kParts = kEpi / 4;              // warps per lane quarter, each ow
 constexpr int kCols = kBN / kParts;           // 16: one K step of the output MMA
 constexpr int kThreads = 32 * (2 + kEpi);
 constexpr int kGrid = 152;                    // persistent CTAs: one per GB300 SM
-constexpr size_t kSmem = (size_t)kABytes + (size_t)kStage * kStages + (size_t)kStages * kBN * 16 +
-                         2 * 4 * kParts * 32 * 8 + 512 + 1024;
+constexpr size_t kSmem = (size_t)kABytes + (size_t)kStage * kStages + (size_t)kStages * kBN * 16 + 512 + 1024;
 static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 static_assert(kCols == 16, "one output K step per epilogue warp");
+constexpr float kL2E = 1.4426950408889634f;
+
+// Slots of the global maxima (float bits of non-negative values, combined with atomicMax on int):
+// |Q|, |K|, |V|, |dO| elementwise, the largest row norms of V and dO, the largest |delta_i|.
+enum Slot : int { gQ = 0, gK, gV, gD, gVn, gDn, gDelta, kSlots };
 
 enum Mode : int { kFwd = 0, kRowSweep = 1, kColSweep = 2 };
 
@@ -65,27 +72,17 @@ template <int MODE>
 struct Shape {
     static constexpr bool kDP = MODE != kFwd;                       // dP = A2 B2^T is formed
     static constexpr int kOuts = MODE == kColSweep ? 2 : 1;
-    // Forward: three S buffers of 128 TMEM columns, kappa stored over the buffer's S, the output at 384.
-    // Backward (kSep): one S + dP region (256 columns) that the MMA refills as soon as the epilogue has
-    // read it into registers, kappa in columns of its own (64 per output), the outputs after them.
-    static constexpr bool kSep = MODE != kFwd;
     static constexpr int kRegion = kDP ? 256 : 128;                 // TMEM columns of one S (+ dP) buffer
-    static constexpr int kBuf = kSep ? 1 : 3;
+    static constexpr int kBuf = kDP ? 1 : 3;                        // S (+ dP) buffers
+    static constexpr bool kColStats = MODE == kColSweep;            // the stage carries per-column stats
     static constexpr int kF = 64 * kOuts;                           // features of one partial row
-    // TMEM column of output o's kappa (hi in +0..31, lo in +32..63) for S buffer b
-    __host__ __device__ static constexpr uint32_t kap(int b, int o) {
-        return kSep ? (uint32_t)(kRegion + 64 * o) : (uint32_t)(b * kRegion + 64 * o);
-    }
-    // TMEM column of output o's accumulator (64 columns, one fp32 accumulator)
-    __host__ __device__ static constexpr uint32_t acc(int o) {
-        return kSep ? (uint32_t)(kRegion + 64 * kOuts + 64 * o) : (uint32_t)(kBuf * kRegion + 64 * o);
-    }
+    // TMEM column of output o's kappa (hi in +0..31, lo in +32..63) and accumulator (64 columns)
+    __host__ __device__ static constexpr uint32_t kap(int o) { return (uint32_t)(kBuf * kRegion + 64 * o); }
+    __host__ __device__ static constexpr uint32_t acc(int o) { return (uint32_t)(kBuf * kRegion + 64 * kOuts + 64 * o); }
     // the stage part that is the B operand of output o
     __host__ __device__ static constexpr uint32_t out_b(int o) {
         return MODE == kRowSweep ? 0u : (o == 0 && MODE == kColSweep ? 0u : 2u * kTile);
     }
-    // outputs whose coefficients leave out the score's scale (dQ, dK)
-    __host__ __device__ static constexpr bool out_scaled(int o) { return MODE != kFwd && o == 0; }
 };
 static_assert(Shape<kColSweep>::acc(1) + 64 <= 512 && Shape<kRowSweep>::acc(0) + 64 <= 512 &&
                   Shape<kFwd>::acc(0) + 64 <= 512,
@@ -98,13 +95,18 @@ struct Params {
     int CT, G, smax;
     float scale;
     const float4* rstat;   // [rows padded to 128] the row side's stats
-    const float4* cstat;   // [CT * 64 or more] the streamed side's stats
+    const float4* cstat;   // [CT * 64 or more] the streamed side's stats (column sweep)
+    const int* gmax;       // [kSlots] the global maxima
     float* part;           // [G][smax][F][128] per-CTA partials, row-minor
     int* cnt;              // [row blocks] CTAs done with each row block (zeroed by the pre-pass)
     float* out0;           // [R][64] (null: not wanted)
     float* out1;
+    int acc0;              // add output 0 into out0 instead of writing it
     int* err;
 };
+
+// The power of two of a matrix from its largest |element| (the same rule as per row elsewhere).
+__device__ __forceinline__ int gexp(const int* gm, int slot) { return f16_row_exponent(__int_as_float(__ldg(gm + slot))); }
 
 // Output features [FG fg, FG fg + FG) of row lr of row block rb: the partials of every CTA that saw the
 // row block, added in CTA order.
@@ -129,8 +131,16 @@ __device__ __noinline__ void merge_row(const Params& p, int rb, int lr, int fg) 
         for (int f = 0; f < FG; ++f) acc[f] += __ldcg(o + (size_t)(fb + f) * kBM);
     }
     float4* d4 = reinterpret_cast<float4*>(dst + row * 64 + (fb & 63));
+    const bool add = p.acc0 && fb < 64;
 #pragma unroll
-    for (int f4 = 0; f4 < FG / 4; ++f4) d4[f4] = make_float4(acc[4 * f4], acc[4 * f4 + 1], acc[4 * f4 + 2], acc[4 * f4 + 3]);
+    for (int f4 = 0; f4 < FG / 4; ++f4) {
+        float4 v = make_float4(acc[4 * f4], acc[4 * f4 + 1], acc[4 * f4 + 2], acc[4 * f4 + 3]);
+        if (add) {
+            const float4 o = d4[f4];
+            v = make_float4(o.x + v.x, o.y + v.y, o.z + v.z, o.w + v.w);
+        }
+        d4[f4] = v;
+    }
 }
 
 template <int MODE>
@@ -140,28 +150,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __grid_constant__ CUtensorMap mB1h, const __grid_constant__ CUtensorMap mB1l,
             const __grid_constant__ CUtensorMap mB2h, const __grid_constant__ CUtensorMap mB2l, const Params p) {
     using SH = Shape<MODE>;
-    constexpr float kL2E = 1.4426950408889634f;
     constexpr int NB = SH::kBuf;
     constexpr int NO = SH::kOuts;
-    constexpr bool SEP = SH::kSep;
+    constexpr bool CST = SH::kColStats;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;
     unsigned char* sB = sm + kABytes;
     float4* sStat = reinterpret_cast<float4*>(sB + (size_t)kStage * kStages);   // [stage][64]
-    float2* sMax = reinterpret_cast<float2*>(sStat + kStages * kBN);             // [parity][quarter][part][lane]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sMax + 2 * 4 * kParts * 32);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStages * kBN);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
     uint64_t* bs_full = bars + 2;              // [kStages]
     uint64_t* bs_empty = bs_full + kStages;    // [kStages]
     uint64_t* s_full = bs_empty + kStages;     // [NB] S (and dP) of a buffer are in TMEM
-    uint64_t* w_full = s_full + NB;            // [NB] the epilogue stored the tile's kappa
-    uint64_t* s_free = w_full + NB;            // (backward) the epilogue has read S and dP into registers
-    uint64_t* o_full = s_free + 1;             // the output MMAs of a tile finished
-    uint64_t* o_empty = o_full + 1;            // (forward) the epilogue read the output block
-    uint64_t* xch = o_empty + 1;               // [quarter][parity]: the row-maximum exchange
-    uint64_t* fl_bar = xch + 8;                // the epilogue wrote its partials of a row block
+    uint64_t* s_free = s_full + NB;            // [NB] the epilogue has read the buffer into registers
+    uint64_t* w_full = s_free + NB;            // the epilogue stored the tile's kappa
+    uint64_t* o_full = w_full + 1;             // the output MMAs of a tile finished
+    uint64_t* fl_bar = o_full + 1;             // the epilogue wrote its partials of a row block
     uint64_t* dec_bar = fl_bar + 1;            // the CTA knows whether it merges that row block
     uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
     volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -179,12 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(s_full + b, 1);
-            mbar_init(w_full + b, 32 * kEpi);
+            mbar_init(s_free + b, 32 * kEpi);
         }
-        mbar_init(s_free, 32 * kEpi);
+        mbar_init(w_full, 32 * kEpi);
         mbar_init(o_full, 1);
-        mbar_init(o_empty, 32 * kEpi);
-        for (int x = 0; x < 8; ++x) mbar_init(xch + x, 32 * kParts);
         mbar_init(fl_bar, 32 * kEpi);
         mbar_init(dec_bar, 1);
         mbar_fence_init();
@@ -219,12 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (r >= 1) ok = mbar_wait(bs_empty + s, (r - 1) & 1, p.err, 42);
                 if (!ok) break;
                 unsigned char* dst = sB + (size_t)s * kStage;
-                mbar_expect_tx(bs_full + s, kStage + kBN * 16);
+                mbar_expect_tx(bs_full + s, kStage + (CST ? kBN * 16 : 0));
                 tma_load_2d(dst, &mB1h, 0, ct * kBN, bs_full + s);
                 tma_load_2d(dst + kTile, &mB1l, 0, ct * kBN, bs_full + s);
                 tma_load_2d(dst + 2 * kTile, &mB2h, 0, ct * kBN, bs_full + s);
                 tma_load_2d(dst + 3 * kTile, &mB2l, 0, ct * kBN, bs_full + s);
-                bulk_load(sStat + s * kBN, p.cstat + (size_t)ct * kBN, kBN * 16, bs_full + s);
+                if (CST) bulk_load(sStat + s * kBN, p.cstat + (size_t)ct * kBN, kBN * 16, bs_full + s);
             }
         }
     } else if (warp == 1) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int a_uses = 0, rb_cur = -1;
             bool ok = true;
             TileCursor cur(t_begin, p.CT);
-            // S (and dP) of tile j into buffer j % NB
+            // S (and dP) of tile j into buffer j % NB, once the epilogue has read tile j - NB out of it
             auto issue_s = [&](int64_t j) -> bool {
                 const int rb = cur.rb;
                 cur.next();
@@ -246,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rb_cur = rb;
                 }
                 const int s = (int)(j % kStages), r = (int)(j / kStages), b = (int)(j % NB);
+                if (j >= NB && !mbar_wait(s_free + b, (uint32_t)((j / NB - 1) & 1), p.err, 53)) return false;
                 if (!mbar_wait(bs_full + s, r & 1, p.err, 44)) return false;
                 fence_after_sync();
                 const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kStage);
@@ -270,17 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             // the output blocks of tile i from its kappa in TMEM: kappa_lo B_hi, kappa_hi B_lo, kappa_hi B_hi
-            // into one accumulator per output (the epilogue drains it every tile). The forward waits for the
-            // previous tile's drain; the backward's epilogue drains it before storing this tile's kappa.
+            // into one accumulator per output. The epilogue stores kappa (w_full) only after it has taken the
+            // previous tile's outputs out of the accumulators.
             auto issue_out = [&](int64_t i) -> bool {
-                const int b = (int)(i % NB), s = (int)(i % kStages);
-                if (!mbar_wait(w_full + b, (uint32_t)((i / NB) & 1), p.err, 45)) return false;
-                if (!SEP && i >= 1 && !mbar_wait(o_empty, (uint32_t)((i - 1) & 1), p.err, 46)) return false;
+                const int s = (int)(i % kStages);
+                if (!mbar_wait(w_full, (uint32_t)(i & 1), p.err, 45)) return false;
                 fence_after_sync();
                 const uint32_t b0 = smem_u32(sB + (size_t)s * kStage);
 #pragma unroll
                 for (int o = 0; o < NO; ++o) {
-                    const uint32_t kh = tmem + SH::kap(b, o), kl = kh + 32;
+                    const uint32_t kh = tmem + SH::kap(o), kl = kh + 32;
                     const uint32_t acc = tmem + SH::acc(o);
                     const uint32_t bb = b0 + SH::out_b(o);
                     // per 16 streamed points (one epilogue part): the stage's hi and lo feature blocks, MN-major
@@ -296,25 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(o_full);
                 return true;
             };
-            if (SEP) {
-                // S and dP of tile i + 1 go in as soon as the epilogue has read tile i's, before its outputs
-                if (n > 0) ok = issue_s(0);
-                for (int64_t i = 0; i < n && ok; ++i) {
-                    if (i + 1 < n) {
-                        ok = mbar_wait(s_free, (uint32_t)(i & 1), p.err, 53);
-                        if (ok) ok = issue_s(i + 1);
-                    }
-                    if (ok) ok = issue_out(i);
-                }
-            } else {
-                // S runs two tiles ahead of the outputs: buffer (i + 2) % 3 held kappa(i - 1), read by the
-                // outputs of tile i - 1, issued earlier (the tensor core runs one thread's MMAs in order)
-                constexpr int L = NB - 1;
-                for (int64_t j = 0; j < n && j < L && ok; ++j) ok = issue_s(j);
-                for (int64_t i = 0; i < n && ok; ++i) {
-                    if (i + L < n) ok = issue_s(i + L);
-                    if (ok) ok = issue_out(i);
-                }
+            // S (and dP) run NB tiles ahead: tile i + NB goes in as soon as the epilogue has read tile i
+            for (int64_t j = 0; j < n && j < NB && ok; ++j) ok = issue_s(j);
+            for (int64_t i = 0; i < n && ok; ++i) {
+                if (i + NB < n) ok = issue_s(i + NB);
+                if (ok) ok = issue_out(i);
             }
         }
     } else {
@@ -324,14 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int part = (warp - 2) >> 2;
         const int lr = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        // constants: the unscale factors of S (base 2, with the score's scale) and dP
+        const int eQ = gexp(p.gmax, gQ), eK = gexp(p.gmax, gK), eV = gexp(p.gmax, gV), eD = gexp(p.gmax, gD);
+        const float cS = pow2i(-eQ) * pow2i(-eK) * p.scale * kL2E;
+        const float cP = pow2i(-eD) * pow2i(-eV);
         int seg = 0;
         float4 rst = make_float4(0.f, 0.f, 0.f, 0.f);
-        float rsl = 0.f;
+        float inv[NO];  // per output: the row's factor from the accumulator to the result
         float acc[NO][kCols];
 #pragma unroll
-        for (int o = 0; o < NO; ++o)
+        for (int o = 0; o < NO; ++o) {
+            inv[o] = 0.f;
 #pragma unroll
             for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
+        }
         bool ok = true;
         // tile j's output MMAs have finished (its kappa is no longer read)
         auto wait_out = [&](int64_t j) -> bool {
@@ -339,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_after_sync();
             return true;
         };
-        // add this part of the finished output blocks, scaled back, into the row accumulators
-        auto add_out = [&](const float (&inv)[NO]) {
+        // add this part of the finished output blocks into the row accumulators
+        auto add_out = [&]() {
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
                 float v[kCols];
@@ -348,15 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u], inv[o], acc[o][u]);
             }
-        };
-        auto drain = [&](int64_t j, const float (&inv)[NO]) -> bool {
-            if (!wait_out(j)) return false;
-            add_out(inv);
-            if (!SEP) {
-                fence_before_sync();
-                mbar_arrive(o_empty);
-            }
-            return true;
         };
         int rb_cur = -1;
         const int etid = threadIdx.x - 64;  // 0 .. 32 kEpi - 1
@@ -385,17 +372,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++seg;
         };
         int64_t pending = -1;
-        float pinv[NO];
-#pragma unroll
-        for (int o = 0; o < NO; ++o) pinv[o] = 0.f;
         TileCursor cur(t_begin, p.CT);
         for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
             const int rb = cur.rb, ct = cur.ct;
             if (rb != rb_cur) {
                 if (pending >= 0) {
-                    ok = drain(pending, pinv);
-                    pending = -1;
+                    ok = wait_out(pending);
                     if (!ok) break;
+                    add_out();
+                    pending = -1;
                 }
                 if (rb_cur >= 0) write_partial();
                 rb_cur = rb;
@@ -403,69 +388,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int o = 0; o < NO; ++o)
 #pragma unroll
                     for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
-                rst = p.rstat[(int64_t)rb * kBM + lr];  // the row stats are padded to whole row blocks
-                // base-2 score factor of the row: scale log2(e) 2^-e of the row's S operand
-                rsl = (MODE == kColSweep ? rst.x : rst.z) * p.scale * kL2E;
+                // row stats, padded to whole row blocks: queries (14 - lse_i log2 e, delta_i, E_i - lse_i log2 e,
+                // 2^-E_i), keys (2^(E_j - 14), 2^-E_j, 0, 0)
+                rst = p.rstat[(int64_t)rb * kBM + lr];
+                if (MODE == kFwd) inv[0] = pow2i(-14) * pow2i(-eV);
+                if (MODE == kRowSweep) inv[0] = rst.w * pow2i(-eK) * p.scale;
+                if (MODE == kColSweep) {
+                    inv[0] = rst.y * pow2i(-eQ) * p.scale;
+                    inv[NO - 1] = pow2i(-14) * pow2i(-eD);
+                }
             }
             const int b = (int)(i % NB), s = (int)(i % kStages);
-            ok = mbar_wait(s_full + b, (uint32_t)((i / NB) & 1), p.err, 50) &&
-                 mbar_wait(bs_full + s, (uint32_t)((i / kStages) & 1), p.err, 51);  // the tile's column stats
+            ok = mbar_wait(s_full + b, (uint32_t)((i / NB) & 1), p.err, 50);
+            if (ok && CST) ok = mbar_wait(bs_full + s, (uint32_t)((i / kStages) & 1), p.err, 51);  // column stats
             if (!ok) break;
             fence_after_sync();
             const float4* st = sStat + s * kBN + part * kCols;
             const uint32_t reg = tmem + lane_off + (uint32_t)(b * SH::kRegion + part * kCols);
             float k0[kCols], k1[kCols];
-            float pm0 = 0.f, pm1 = 0.f;
             if (MODE == kFwd) {
+                // O: kappa = P 2^14 = 2^(s2 + 14 - lse2)
                 float v[kCols], w[kCols];
                 tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
-                // O: kappa_ij = P_ij 2^-e_Vj (the stage's V rows are V_j 2^e_Vj)
+                fence_before_sync();
+                mbar_arrive(s_free + b);
 #pragma unroll
-                for (int u = 0; u < kCols; ++u) {
-                    const float4 cs = st[u];  // key stats (2^-e_K, 2^-e_V, 0, 0); zeros for padding keys
-                    const float kp = ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.x * rsl, -rst.x)) * cs.y;
-                    k0[u] = kp;
-                    pm0 = fmaxf(pm0, kp);
-                }
+                for (int u = 0; u < kCols; ++u) k0[u] = ExpTraits<float>::bexp(fmaf(v[u] + w[u], cS, rst.x));
             } else {
-                // row sweep: row = query i (lse2, delta, 2^-e_Q, 2^-e_dO), column = key j (2^-e_K, 2^-e_V, 0, 0);
-                // column sweep: row = key j (2^-e_K, 2^-e_V, 0, 0), column = query i (lse2, delta, 2^-e_Q, 2^-e_dO)
+                // P (with the row's or the column's power of two) from S, then dP
                 float pr[kCols];
                 {
                     float v[kCols], w[kCols];
-                    tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
+                    tmem_ld16x2(reg, reg + 64, v, w);
 #pragma unroll
-                    for (int u = 0; u < kCols; ++u) {
-                        const float4 cs = st[u];
-                        pr[u] = MODE == kRowSweep ? ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.x * rsl, -rst.x))
-                                                  : ExpTraits<float>::bexp(fmaf(v[u] + w[u], cs.z * rsl, -cs.x));
-                    }
+                    for (int u = 0; u < kCols; ++u)
+                        pr[u] = ExpTraits<float>::bexp(fmaf(v[u] + w[u], cS, MODE == kRowSweep ? rst.z : st[u].x));
                 }
                 float a[kCols], c[kCols];
                 tmem_ld16x2(reg + 128, reg + 192, a, c);  // dP: hi*hi, hi*lo + lo*hi
-                // S and dP are in registers: the MMA may refill the region with the next tile's
                 fence_before_sync();
-                mbar_arrive(s_free);
+                mbar_arrive(s_free + b);
 #pragma unroll
                 for (int u = 0; u < kCols; ++u) {
-                    const float4 cs = st[u];
                     if (MODE == kRowSweep) {
-                        const float kp = pr[u] * cs.x * fmaf(a[u] + c[u], cs.y * rst.w, -rst.y);  // dS_ij 2^-e_Kj
-                        k0[u] = kp;
-                        pm0 = fmaxf(pm0, fabsf(kp));
+                        k0[u] = pr[u] * fmaf(a[u] + c[u], cP, -rst.y);  // dS_ij 2^E_i
                     } else {
-                        const float kp = pr[u] * cs.z * fmaf(a[u] + c[u], cs.w * rst.y, -cs.y);  // dS_ij 2^-e_Qi
-                        const float kv = pr[u] * cs.w;                                              // P_ij 2^-e_dOi
-                        k0[u] = kp;
-                        k1[u] = kv;
-                        pm0 = fmaxf(pm0, fabsf(kp));
-                        pm1 = fmaxf(pm1, kv);
+                        k1[u] = pr[u];                                          // P_ij 2^14
+                        k0[u] = pr[u] * rst.x * fmaf(a[u] + c[u], cP, -st[u].y);  // dS_ij 2^E_j
                     }
                 }
             }
-            // Streamed points past the end (keys of the last tile) have S = 0 and zero stats, but their P may
-            // overflow (a row whose lse is below the float range of exp): give them no weight. The column
-            // sweep's padding queries carry lse = +inf, so their P is exactly 0 there.
+            // Streamed points past the end (keys of the last tile) have S = 0 but their P is not 0: give
+            // them no weight. The column sweep's padding queries carry -inf in place of 14 - lse2.
             if (MODE != kColSweep) {
                 const int lim = (int)(p.C - (int64_t)ct * kBN) - part * kCols;  // columns u >= lim are padding
                 if (lim < kCols) {
@@ -473,61 +447,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < kCols; ++u) k0[u] = u < lim ? k0[u] : 0.f;
                 }
             }
-            // the row's largest |kappa| over the tile: the four parts of the quarter exchange theirs (in the
-            // forward this also tells each part that the others have read S, which the stores overwrite)
-            const int par = (int)(i & 1);
-            float2* xm = sMax + (size_t)((par * 4 + q) * kParts) * 32;
-            xm[part * 32 + lane] = make_float2(pm0, pm1);
-            fence_before_sync();
-            mbar_arrive(xch + q * 2 + par);
-            ok = mbar_wait(xch + q * 2 + par, (uint32_t)((i >> 1) & 1), p.err, 52);
-            if (!ok) break;
-            fence_after_sync();
-            float2 mx = xm[lane];
-#pragma unroll
-            for (int pp = 1; pp < kParts; ++pp) {
-                const float2 t = xm[pp * 32 + lane];
-                mx.x = fmaxf(mx.x, t.x);
-                mx.y = fmaxf(mx.y, t.y);
-            }
-            // backward: the previous tile's output MMAs have read their kappa before this tile's is stored,
-            // and the epilogue takes their result out of the accumulators before it hands them over again
-            if (SEP && pending >= 0) {
+            // the previous tile's output MMAs have read their kappa before this tile's is stored, and the
+            // epilogue takes their result out of the accumulators before it hands them over again
+            if (pending >= 0) {
                 ok = wait_out(pending);
                 if (!ok) break;
             }
-            float ninv[NO];  // 2^-e per output: undoes this tile's row scale when its outputs are drained
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
-                const int e = f16_row_exponent(o == 0 ? mx.x : mx.y);
-                const float f = pow2i(e);
-                ninv[o] = SH::out_scaled(o) ? pow2i(-e) * p.scale : pow2i(-e);
                 uint32_t hw[kCols / 2], lw[kCols / 2];
 #pragma unroll
                 for (int k = 0; k < kCols / 2; ++k) {
-                    const float x0 = (o == 0 ? k0[2 * k] : k1[2 * k]) * f, x1 = (o == 0 ? k0[2 * k + 1] : k1[2 * k + 1]) * f;
+                    const float x0 = o == 0 ? k0[2 * k] : k1[2 * k], x1 = o == 0 ? k0[2 * k + 1] : k1[2 * k + 1];
                     const __half2 h = __floats2half2_rn(x0, x1);
                     const float2 hf = __half22float2(h);
                     hw[k] = *reinterpret_cast<const uint32_t*>(&h);
                     lw[k] = pack_f16x2(x0 - hf.x, x1 - hf.y);
                 }
                 // kappa_hi of points [16 part, 16 part + 16) in columns kap + 8 part .. +8, kappa_lo 32 further
-                tmem_st8(tmem + lane_off + SH::kap(b, o) + (uint32_t)(part * 8), hw);
-                tmem_st8(tmem + lane_off + SH::kap(b, o) + (uint32_t)(32 + part * 8), lw);
+                tmem_st8(tmem + lane_off + SH::kap(o) + (uint32_t)(part * 8), hw);
+                tmem_st8(tmem + lane_off + SH::kap(o) + (uint32_t)(32 + part * 8), lw);
             }
             tmem_st_wait();
-            if (SEP && pending >= 0) add_out(pinv);
+            if (pending >= 0) add_out();
             fence_before_sync();
-            mbar_arrive(w_full + b);
-            if (!SEP && pending >= 0) {
-                ok = drain(pending, pinv);
-                if (!ok) break;
-            }
+            mbar_arrive(w_full);
             pending = i;
-#pragma unroll
-            for (int o = 0; o < NO; ++o) pinv[o] = ninv[o];
         }
-        if (ok && pending >= 0) ok = drain(pending, pinv);
+        if (ok && pending >= 0) {
+            ok = wait_out(pending);
+            if (ok) add_out();
+        }
         if (ok && rb_cur >= 0) write_partial();
     }
 
@@ -536,18 +486,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// Global maxima for the powers of two and the kappa bounds: one warp per row (grid-stride), the block's
+// maxima combined in shared memory, one atomicMax per block and quantity (the values are non-negative,
+// so their float bits order like integers). A: max|A| into slot sa. B (optional): max|B| into sb, the
+// largest row norm |B_r| into sbn. O (optional, with B): the largest |B_r . O_r| into sdel.
+__global__ void __launch_bounds__(256) attn_reduce(const float* __restrict__ A, const float* __restrict__ B,
+                                                   const float* __restrict__ O, int64_t rows, int* __restrict__ gm,
+                                                   int sa, int sb, int sbn, int sdel) {
+    __shared__ float red[4][8];
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float ma = 0.f, mb = 0.f, mbn = 0.f, md = 0.f;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + wib; r < rows; r += (int64_t)gridDim.x * 8) {
+        const float2 a = reinterpret_cast<const float2*>(A + r * 64)[lane];
+        ma = fmaxf(ma, fmaxf(fabsf(a.x), fabsf(a.y)));
+        if (B) {
+            const float2 b = reinterpret_cast<const float2*>(B + r * 64)[lane];
+            mb = fmaxf(mb, fmaxf(fabsf(b.x), fabsf(b.y)));
+            float ss = fmaf(b.x, b.x, b.y * b.y);
+            float d = 0.f;
+            if (O) {
+                const float2 o = reinterpret_cast<const float2*>(O + r * 64)[lane];
+                d = fmaf(b.x, o.x, b.y * o.y);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                d += __shfl_xor_sync(0xffffffffu, d, off);
+            }
+            mbn = fmaxf(mbn, sqrtf(ss));
+            md = fmaxf(md, fabsf(d));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+    }
+    if (lane == 0) {
+        red[0][wib] = ma;
+        red[1][wib] = mb;
+        red[2][wib] = mbn;
+        red[3][wib] = md;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+        float m = 0.f;
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, red[threadIdx.x][w]);
+        const int slot = threadIdx.x == 0 ? sa : threadIdx.x == 1 ? sb : threadIdx.x == 2 ? sbn : sdel;
+        if (slot >= 0) atomicMax(gm + slot, __float_as_int(m));
+    }
+}
+
 // Pre-pass, one warp per row over rows_pad rows (two features per lane): the fp16 hi/lo split of A 2^eA
-// (and B 2^eB) and the row's stats.
-//   QUERY: stat = (lse log2 e, delta = B . O, 2^-eA, 2^-eB), padding rows (+inf, 0, 0, 0)
-//   keys:  stat = (2^-eA, 2^-eB, 0, 0), padding rows zeros
-// B, O, lse may be null (their entries are then 0). cnt: ncnt counters zeroed for the sweep that follows.
+// (and B 2^eB), with the powers of two of the whole matrices (slots sa, sb), and the row's stats:
+//   QUERY: (14 - lse log2 e, delta = B . O, E - lse log2 e, 2^-E) with E the power of two that brings the
+//          bound |B_r| max_j |V_j| + |delta| of this row's |dP - delta| into [2^14, 2^15) (backward, B and O
+//          given), (14 - lse log2 e, 0, 0, 0) otherwise; padding rows (-inf, 0, -inf, 0)
+//   keys:  (2^(E - 14), 2^-E, 0, 0) with E from the bound |B_r| max_i |dO_i| + max_i |delta_i| (bounds),
+//          zeros otherwise and for padding rows
+// B, O, lse may be null. cnt: ncnt counters zeroed for the sweep that follows.
 template <bool QUERY>
-__global__ void __launch_bounds__(256) attn_prep(const float* __restrict__ A, const float* __restrict__ B,
-                                                 const float* __restrict__ O, const float* __restrict__ lse,
-                                                 int64_t rows, int64_t rows_pad, __half2* __restrict__ Ah,
-                                                 __half2* __restrict__ Al, __half2* __restrict__ Bh,
-                                                 __half2* __restrict__ Bl, float4* __restrict__ stat,
-                                                 int* __restrict__ cnt, int64_t ncnt) {
+__global__ void __launch_bounds__(256) attn_split(const float* __restrict__ A, const float* __restrict__ B,
+                                                  const float* __restrict__ O, const float* __restrict__ lse,
+                                                  int64_t rows, int64_t rows_pad, const int* __restrict__ gm, int sa,
+                                                  int sb, int bounds, __half2* __restrict__ Ah,
+                                                  __half2* __restrict__ Al, __half2* __restrict__ Bh,
+                                                  __half2* __restrict__ Bl, float4* __restrict__ stat,
+                                                  int* __restrict__ cnt, int64_t ncnt) {
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (lane == 0 && r < ncnt) cnt[r] = 0;
@@ -560,42 +565,59 @@ __global__ void __launch_bounds__(256) attn_prep(const float* __restrict__ A, co
             Bh[r * 32 + lane] = z2;
             Bl[r * 32 + lane] = z2;
         }
-        if (lane == 0) stat[r] = QUERY ? make_float4(__int_as_float(0x7f800000), 0.f, 0.f, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float ninf = __int_as_float(0xff800000);
+        if (lane == 0) stat[r] = QUERY ? make_float4(ninf, 0.f, ninf, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    // split one row of X into hi/lo of X 2^e; returns 2^-e
-    auto split = [&](const float* X, __half2* hi, __half2* lo, float2& v) -> float {
-        v = reinterpret_cast<const float2*>(X + r * 64)[lane];
-        float m = fmaxf(fabsf(v.x), fabsf(v.y));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const int e = f16_row_exponent(m);
-        const float f = pow2i(e);
+    auto split = [&](const float* X, int slot, __half2* hi, __half2* lo) -> float2 {
+        const float2 v = reinterpret_cast<const float2*>(X + r * 64)[lane];
+        const float f = pow2i(f16_row_exponent(__int_as_float(__ldg(gm + slot))));
         const float a = v.x * f, b = v.y * f;
         const __half2 h = __floats2half2_rn(a, b);
         const float2 hf = __half22float2(h);
         hi[r * 32 + lane] = h;
         lo[r * 32 + lane] = __floats2half2_rn(a - hf.x, b - hf.y);
-        return pow2i(-e);
+        return v;
     };
-    float2 va, vb = make_float2(0.f, 0.f);
-    const float ia = split(A, Ah, Al, va);
-    const float ib = B ? split(B, Bh, Bl, vb) : 0.f;
-    float delta = 0.f;
-    if (QUERY && B && O) {
-        const float2 o = reinterpret_cast<const float2*>(O + r * 64)[lane];
-        delta = fmaf(vb.x, o.x, vb.y * o.y);
+    split(A, sa, Ah, Al);
+    float ss = 0.f, d = 0.f;
+    if (B) {
+        const float2 b = split(B, sb, Bh, Bl);
+        ss = fmaf(b.x, b.x, b.y * b.y);
+        if (O) {
+            const float2 o = reinterpret_cast<const float2*>(O + r * 64)[lane];
+            d = fmaf(b.x, o.x, b.y * o.y);
+        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) delta += __shfl_xor_sync(0xffffffffu, delta, off);
+        for (int off = 16; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            d += __shfl_xor_sync(0xffffffffu, d, off);
+        }
     }
-    if (lane == 0)
-        stat[r] = QUERY ? make_float4(lse ? lse[r] * 1.4426950408889634f : 0.f, delta, ia, ib) : make_float4(ia, ib, 0.f, 0.f);
+    if (lane != 0) return;
+    if (QUERY) {
+        const float l2 = lse[r] * kL2E;
+        if (bounds) {
+            const int E = f16_row_exponent(fmaf(sqrtf(ss), __int_as_float(__ldg(gm + gVn)), fabsf(d)));
+            stat[r] = make_float4(14.f - l2, d, (float)E - l2, pow2i(-E));
+        } else {
+            stat[r] = make_float4(14.f - l2, 0.f, 0.f, 0.f);
+        }
+    } else {
+        if (bounds) {
+            const int E = f16_row_exponent(
+                fmaf(sqrtf(ss), __int_as_float(__ldg(gm + gDn)), __int_as_float(__ldg(gm + gDelta))));
+            stat[r] = make_float4(pow2i(E) * pow2i(-14), pow2i(-E), 0.f, 0.f);
+        } else {
+            stat[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
 }
 
 struct Plan {
     int64_t Npad, Mpad;
     size_t off_qh, off_ql, off_dh, off_dl, off_qst, off_kh, off_kl, off_vh, off_vl, off_kst, off_part, off_cntq,
-        off_cntk, off_err, bytes;
+        off_cntk, off_gmax, off_err, bytes;
 };
 
 struct Sweep {
@@ -640,6 +662,7 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
     pl.off_part = o; o += al256(part);
     pl.off_cntq = o; o += al256((size_t)(pl.Npad / kBM) * 4);
     pl.off_cntk = o; o += al256((size_t)(pl.Mpad / kBM) * 4);
+    pl.off_gmax = o; o += 256;
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -647,8 +670,8 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
 
 template <int MODE>
 static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
-                      const float4* cstat, float* part, int* cnt, float* out0, float* out1, int* err, const char* name,
-                      cudaStream_t s) {
+                      const float4* cstat, const int* gmax, float* part, int* cnt, float* out0, float* out1, int acc0,
+                      int* err, const char* name, cudaStream_t s) {
     const Sweep w = sweep_of(R, C);
     Params p;
     p.R = R;
@@ -660,14 +683,21 @@ static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float sca
     p.scale = scale;
     p.rstat = rstat;
     p.cstat = cstat;
+    p.gmax = gmax;
     p.part = part;
     p.cnt = cnt;
     p.out0 = out0;
     p.out1 = out1;
+    p.acc0 = acc0;
     p.err = err;
     cudaFuncSetAttribute(attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     HookScope h(name, s);
     attn_tc<MODE><<<w.G, kThreads, kSmem, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p);
+}
+
+static unsigned reduce_grid(int64_t rows) {
+    const int64_t b = (rows + 7) / 8;
+    return (unsigned)(b < 4 * kGrid ? b : 4 * kGrid);
 }
 
 }  // namespace attn
@@ -675,7 +705,8 @@ static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float sca
 
 size_t attn_tc_workspace(int64_t N, int64_t M, bool backward) { return tc::attn::plan_of(N, M, backward).bytes; }
 
-// Forward: a.lse holds the row log-sum-exp (already computed on the stream); writes a.out.
+// Forward: a.lse holds the row log-sum-exp (already computed on the stream); writes a.out. Returns the
+// number of kernels launched, or -1 if a tensor map could not be encoded.
 int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     using namespace tc;
     using namespace tc::attn;
@@ -690,6 +721,7 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     float4* qst = reinterpret_cast<float4*>(ws + pl.off_qst);
     float4* kst = reinterpret_cast<float4*>(ws + pl.off_kst);
     int* cntq = reinterpret_cast<int*>(ws + pl.off_cntq);
+    int* gm = reinterpret_cast<int*>(ws + pl.off_gmax);
     CUtensorMap m[8];
     if (!make_map_f16(&m[0], qh, pl.Npad, kBM) || !make_map_f16(&m[1], ql, pl.Npad, kBM) ||
         !make_map_f16(&m[4], kh, pl.Mpad, kBN) || !make_map_f16(&m[5], kl, pl.Mpad, kBN) ||
@@ -697,23 +729,34 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
         return -1;
     m[2] = m[0];  // no second row operand in the forward
     m[3] = m[1];
+    cudaMemsetAsync(gm, 0, kSlots * sizeof(int), s);
     {
-        HookScope h("attn_prep", s);
-        attn_prep<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, nullptr, nullptr, a.lse, a.N, pl.Npad, qh, ql,
-                                                               nullptr, nullptr, qst, cntq, pl.Npad / kBM);
+        HookScope h("attn_reduce", s);
+        attn_reduce<<<reduce_grid(a.N), 256, 0, s>>>(a.Q, nullptr, nullptr, a.N, gm, gQ, -1, -1, -1);
     }
     {
-        HookScope h("attn_prep", s);
-        attn_prep<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, kh, kl, vh,
-                                                                vl, kst, nullptr, 0);
+        HookScope h("attn_reduce", s);
+        attn_reduce<<<reduce_grid(a.M), 256, 0, s>>>(a.K, a.V, nullptr, a.M, gm, gK, gV, gVn, -1);
     }
-    run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, reinterpret_cast<float*>(ws + pl.off_part), cntq, a.out,
-                    nullptr, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
-    return 3;
+    {
+        HookScope h("attn_split", s);
+        attn_split<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, nullptr, nullptr, a.lse, a.N, pl.Npad, gm, gQ, -1,
+                                                                0, qh, ql, nullptr, nullptr, qst, cntq, pl.Npad / kBM);
+    }
+    {
+        HookScope h("attn_split", s);
+        attn_split<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, gm, gK, gV,
+                                                                 0, kh, kl, vh, vl, kst, nullptr, 0);
+    }
+    run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part), cntq,
+                    a.out, nullptr, 0, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
+    return 5;
 }
 
 // Backward: dQ (row sweep) and dK, dV (column sweep); null outputs are not written (a sweep none of whose
-// outputs is wanted does not run).
+// outputs is wanted does not run). With accumulate_dK the column sweep adds dK into its buffer, which
+// then holds dQ from the row sweep (same points on both sides, one summed gradient). Returns the number
+// of kernels launched, or -1 as above.
 int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     using namespace tc;
     using namespace tc::attn;
@@ -731,6 +774,7 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     float4* kst = reinterpret_cast<float4*>(ws + pl.off_kst);
     int* cntq = reinterpret_cast<int*>(ws + pl.off_cntq);
     int* cntk = reinterpret_cast<int*>(ws + pl.off_cntk);
+    int* gm = reinterpret_cast<int*>(ws + pl.off_gmax);
     float* part = reinterpret_cast<float*>(ws + pl.off_part);
     int* err = reinterpret_cast<int*>(ws + pl.off_err);
     // row sweep maps: A = (Q, dO) in 128-row boxes, B = (K, V) in 64-row boxes; column sweep the reverse
@@ -744,25 +788,34 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
         !make_map_f16(&mc[4], qh, pl.Npad, kBN) || !make_map_f16(&mc[5], ql, pl.Npad, kBN) ||
         !make_map_f16(&mc[6], dh, pl.Npad, kBN) || !make_map_f16(&mc[7], dl, pl.Npad, kBN))
         return -1;
-    int n = 0;
+    cudaMemsetAsync(gm, 0, kSlots * sizeof(int), s);
     {
-        HookScope h("attn_prep", s);
-        attn_prep<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, a.dO, a.O, a.lse, a.N, pl.Npad, qh, ql, dh, dl,
-                                                               qst, cntq, pl.Npad / kBM);
-        ++n;
+        HookScope h("attn_reduce", s);
+        attn_reduce<<<reduce_grid(a.N), 256, 0, s>>>(a.Q, a.dO, a.O, a.N, gm, gQ, gD, gDn, gDelta);
     }
     {
-        HookScope h("attn_prep", s);
-        attn_prep<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, kh, kl, vh,
-                                                                vl, kst, cntk, pl.Mpad / kBM);
-        ++n;
+        HookScope h("attn_reduce", s);
+        attn_reduce<<<reduce_grid(a.M), 256, 0, s>>>(a.K, a.V, nullptr, a.M, gm, gK, gV, gVn, -1);
     }
+    {
+        HookScope h("attn_split", s);
+        attn_split<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, a.dO, a.O, a.lse, a.N, pl.Npad, gm, gQ, gD, 1,
+                                                                qh, ql, dh, dl, qst, cntq, pl.Npad / kBM);
+    }
+    {
+        HookScope h("attn_split", s);
+        attn_split<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, gm, gK, gV,
+                                                                 1, kh, kl, vh, vl, kst, cntk, pl.Mpad / kBM);
+    }
+    int n = 4;
     if (a.dQ) {
-        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, part, cntq, a.dQ, nullptr, err, "attn_bwd_row_tc", s);
+        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, gm, part, cntq, a.dQ, nullptr, 0, err,
+                             "attn_bwd_row_tc", s);
         ++n;
     }
     if (a.dK || a.dV) {
-        run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, part, cntk, a.dK, a.dV, err, "attn_bwd_col_tc", s);
+        run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, gm, part, cntk, a.dK, a.dV, a.accumulate_dK,
+                             err, "attn_bwd_col_tc", s);
         ++n;
     }
     return n;
