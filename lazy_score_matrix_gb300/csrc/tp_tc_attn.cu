@@ -73,19 +73,24 @@ struct Shape {
     static constexpr bool kDP = MODE != kFwd;                       // dP = A2 B2^T is formed
     static constexpr int kOuts = MODE == kColSweep ? 2 : 1;
     static constexpr int kRegion = kDP ? 256 : 128;                 // TMEM columns of one S (+ dP) buffer
-    static constexpr int kBuf = kDP ? 1 : 3;                        // S (+ dP) buffers
+    static constexpr int kBuf = kDP ? 1 : 2;                        // S (+ dP) buffers
     static constexpr bool kColStats = MODE == kColSweep;            // the stage carries per-column stats
     static constexpr int kF = 64 * kOuts;                           // features of one partial row
-    // TMEM column of output o's kappa (hi in +0..31, lo in +32..63) and accumulator (64 columns)
+    // One output: kappa_hi [B_hi | B_lo] (N 128, hi*hi and hi*lo in 128 accumulator columns) and
+    // kappa_lo B_hi (N 64) into the hi*lo half. Two outputs (column sweep): TMEM holds one 64-column
+    // accumulator each, fed by three N 64 MMAs.
+    static constexpr bool kWide = kOuts == 1;
+    static constexpr int kAccW = kWide ? 128 : 64;
+    // TMEM column of output o's kappa (hi in +0..31, lo in +32..63) and accumulator
     __host__ __device__ static constexpr uint32_t kap(int o) { return (uint32_t)(kBuf * kRegion + 64 * o); }
-    __host__ __device__ static constexpr uint32_t acc(int o) { return (uint32_t)(kBuf * kRegion + 64 * kOuts + 64 * o); }
+    __host__ __device__ static constexpr uint32_t acc(int o) { return (uint32_t)(kBuf * kRegion + 64 * kOuts + kAccW * o); }
     // the stage part that is the B operand of output o
     __host__ __device__ static constexpr uint32_t out_b(int o) {
         return MODE == kRowSweep ? 0u : (o == 0 && MODE == kColSweep ? 0u : 2u * kTile);
     }
 };
-static_assert(Shape<kColSweep>::acc(1) + 64 <= 512 && Shape<kRowSweep>::acc(0) + 64 <= 512 &&
-                  Shape<kFwd>::acc(0) + 64 <= 512,
+static_assert(Shape<kColSweep>::acc(1) + 64 <= 512 && Shape<kRowSweep>::acc(0) + 128 <= 512 &&
+                  Shape<kFwd>::acc(0) + 128 <= 512,
               "TMEM columns");
 
 struct Params {
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idS2 = idesc_f16(kBM, 2 * kBN, false);  // A_hi [B_hi; B_lo]: N 128
             constexpr uint32_t idS = idesc_f16(kBM, kBN, false);       // A_lo B_hi: N 64
             constexpr uint32_t idO = idesc_f16(kBM, 64, true);         // kappa B (MN-major): N 64
+            constexpr uint32_t idO2 = idesc_f16(kBM, 128, true);       // kappa_hi [B_hi | B_lo] (MN-major): N 128
             int a_uses = 0, rb_cur = -1;
             bool ok = true;
             TileCursor cur(t_begin, p.CT);
@@ -274,9 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(s_full + b);
                 return true;
             };
-            // the output blocks of tile i from its kappa in TMEM: kappa_lo B_hi, kappa_hi B_lo, kappa_hi B_hi
-            // into one accumulator per output. The epilogue stores kappa (w_full) only after it has taken the
-            // previous tile's outputs out of the accumulators.
+            // the output blocks of tile i from its kappa in TMEM. The epilogue stores kappa (w_full) only after
+            // it has taken the previous tile's outputs out of the accumulators.
             auto issue_out = [&](int64_t i) -> bool {
                 const int s = (int)(i % kStages);
                 if (!mbar_wait(w_full, (uint32_t)(i & 1), p.err, 45)) return false;
@@ -291,9 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t bo = bb + (uint32_t)(ks * 16 * kRowB);
-                        mma_f16_ta(acc, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, ks > 0 ? 1u : 0u);
-                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo + kTile, kTile, 1024), idO, 1u);
-                        mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
+                        if (SH::kWide) {
+                            mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO2, ks > 0 ? 1u : 0u);
+                            mma_f16_ta(acc + 64, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
+                        } else {
+                            mma_f16_ta(acc, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, ks > 0 ? 1u : 0u);
+                            mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo + kTile, kTile, 1024), idO, 1u);
+                            mma_f16_ta(acc, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTile, 1024), idO, 1u);
+                        }
                     }
                 }
                 mma_commit(bs_empty + s);  // the stage fed S, dP and the outputs
@@ -339,10 +349,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto add_out = [&]() {
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
-                float v[kCols];
-                tmem_ld16(tmem + SH::acc(o) + lane_off + (uint32_t)(part * kCols), v);
+                const uint32_t a = tmem + SH::acc(o) + lane_off + (uint32_t)(part * kCols);
+                if (SH::kWide) {
+                    float v[kCols], w[kCols];
+                    tmem_ld16x2(a, a + 64, v, w);  // hi*hi, hi*lo + lo*hi
 #pragma unroll
-                for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u], inv[o], acc[o][u]);
+                    for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u] + w[u], inv[o], acc[o][u]);
+                } else {
+                    float v[kCols];
+                    tmem_ld16(a, v);
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u], inv[o], acc[o][u]);
+                }
             }
         };
         int rb_cur = -1;
