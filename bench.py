@@ -490,7 +490,7 @@ def gpu_arm(args, rank, world):
         roof = {"kernel": dname, "bound": "tensor" if bound.startswith("tensor") else bound,
                 "operands": bound[len("tensor-"):] if bound.startswith("tensor") else "fp32",
                 "achieved": round(ach, 3), "peak": round(peak, 2),
-                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname),
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname, wl.name),
                 "peak_source": src, "flop_per_pair": fpp}
     step_tflops = wl.step_flops_per_pair * wl.pairs / (ms_step / 1e3) / 1e12
     line = {
@@ -516,16 +516,17 @@ def gpu_arm(args, rank, world):
     return line
 
 
-def traffic_for(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary (lines
+    `kernel workload bytes src=<hash>`), if taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     cur = source_hash()
     for l in open(path):
         parts = l.split()
-        if len(parts) >= 3 and parts[0] == kernel and parts[2] == f"src={cur}":
-            return float(parts[1])
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[3] == f"src={cur}":
+            return float(parts[2])
     return None
 
 
