@@ -423,6 +423,29 @@ def time_steps(fn, steps, flush):
     return total  # ms
 
 
+def capture_step(wl):
+    """The step captured once in a CUDA graph (its launches replayed without the host in between), or None
+    if the capture fails (the step then runs eagerly)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            wl.step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g):
+            wl.step()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+
+
 def gpu_arm(args, rank, world):
     from lazy_score_matrix_gb300 import _lib
 
@@ -440,12 +463,18 @@ def gpu_arm(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    _lib.launch_count(reset=True)
+    # The timed steps: replays of the step captured in a CUDA graph, nothing recorded between its launches.
+    graph = capture_step(wl)
     clocks.t0 = time.time()
+    ms = time_steps(graph.replay if graph is not None else wl.step, args.steps, flush)
+    clocks.t1 = time.time()
+    torch.cuda.synchronize()
+    # Kernel durations for the roofline: the same steps again, eagerly, with CUDA events around every
+    # launch on its stream (events between launches would add gaps to the timed steps above).
+    _lib.launch_count(reset=True)
     timer = KernelTimer(capacity=64 * args.steps + 64)
     with timer:
-        ms = time_steps(wl.step, args.steps, flush)
-    clocks.t1 = time.time()
+        time_steps(wl.step, args.steps, flush)
     launches = _lib.launch_count()
     torch.cuda.synchronize()
     if world > 1:
@@ -499,6 +528,9 @@ def gpu_arm(args, rank, world):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the workload)",
         "config": {"workload": wl.name, "N": wl.N, "M": getattr(wl, "M", wl.N), "D": wl.D, "pairs_per_step": wl.pairs,
                    "l2": "flushed before every timed step (256 MB write, untimed)",
+                   "launch": ("step captured once in a CUDA graph, replayed per timed step" if graph is not None
+                              else "eager"),
+                   "kernel_times": "CUDA events around every launch, in a second pass of the same steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "impl": "libtp",
         "roofline": roof,

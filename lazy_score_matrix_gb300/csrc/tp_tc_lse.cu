@@ -458,8 +458,17 @@ struct LseBwdTcParams {
     int* cnt;             // [RB] CTAs done with each row block (zeroed by the pre-pass)
     const float* z;       // [N][64] the points (distance metrics subtract z_k sum_j kappa_kj)
     float* grad;          // [N][64] output: z.grad
+    const int* gmax;      // linear score without exp: (max|z|, max|g|) as float bits
     int* err;
 };
+
+// Linear score without exp: z carries one power of two e (max|z| 2^e in [2^14, 2^15)), and kappa one
+// power of two E fixed from the bound |kappa_kj| = |scale| |g_k P_kj + g_j P_jk| <= 2 |scale| max|g|
+// (P <= 1 off the diagonal), so both are constants of the whole sweep.
+__device__ __forceinline__ int lin_z_exp(const int* gm) { return f16_row_exponent(__int_as_float(__ldg(gm))); }
+__device__ __forceinline__ int lin_kappa_exp(const int* gm, float scale) {
+    return f16_row_exponent(2.f * fabsf(scale) * __int_as_float(__ldg(gm + 1)));
+}
 
 // z.grad for features [16 fg, 16 fg + 16) of row lr of row block rb from the partials of every CTA that
 // saw the row block, added in CTA order: dZ - [distance metric] z sum kappa.
@@ -502,6 +511,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
                    const LseBwdTcParams p) {
     constexpr float kL2E = 1.4426950408889634f;
+    // linear score without exp: powers of two fixed for the whole sweep (no per-tile exchange); each part
+    // stores its kappa over its own hi*hi S columns ([16 part, +8) hi, [16 part + 8, +8) lo), which it has
+    // already read, so the four parts of a lane quarter need not wait for one another
+    constexpr bool GLOB = METRIC == kLinear && !EXP;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                        // row block: [hi 128 rows | lo 128 rows]
@@ -620,14 +633,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (i >= 1 && !mbar_wait(dz_empty, (uint32_t)((i - 1) & 1), p.err, 26)) return false;
                 fence_after_sync();
                 const uint32_t b0 = smem_u32(sB + (size_t)s * kStageB);
-                const uint32_t kh = tmem + (uint32_t)(b * 128), kl = kh + 32;  // packed kappa_hi, kappa_lo
+                const uint32_t kb = tmem + (uint32_t)(b * 128);  // packed kappa_hi, kappa_lo of the buffer
                 // per 16 points (one epilogue part): the stage read MN-major, rows of 16 points, hi and lo
                 // feature blocks kTileB apart
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t bo = b0 + (uint32_t)(ks * 16 * kRowBytes);
-                    mma_f16_ta(tDZ, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTileB, 1024), idZ2, ks > 0 ? 1u : 0u);
-                    mma_f16_ta(tDZ + 64, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTileB, 1024), idZ, 1u);
+                    const uint32_t kh = GLOB ? kb + (uint32_t)(ks * 16) : kb + (uint32_t)(ks * 8);
+                    const uint32_t kl = GLOB ? kh + 8 : kh + 32;
+                    mma_f16_ta(tDZ, kh, desc_sw128(bo, kTileB, 1024), idZ2, ks > 0 ? 1u : 0u);
+                    mma_f16_ta(tDZ + 64, kl, desc_sw128(bo, kTileB, 1024), idZ, 1u);
                 }
                 mma_commit(bs_empty + s);  // the stage fed both S and dZ
                 mma_commit(dz_full);
@@ -694,6 +709,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         int64_t pending = -1;
         float pend_inv = 0.f;
+        float gcS = 0.f, gInv = 0.f;  // GLOB: the S factor (base 2) and the factor from a dZ block to z.grad
+        if (GLOB) {
+            const int ez = lin_z_exp(p.gmax), E = lin_kappa_exp(p.gmax, p.scale);
+            gcS = pow2i(-ez) * pow2i(-ez) * p.scale * kL2E;
+            gInv = pow2i(-E) * pow2i(-ez);
+        }
         TileCursor cur(t_begin, p.CT);
         for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
             const int rb = cur.rb, ct = cur.ct;
@@ -710,7 +731,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int f = 0; f < kColsB; ++f) dacc[f] = 0.f;
                 const bool live = row < N32;
-                const float4 st = live ? p.stat[row] : make_float4(__int_as_float(0x7f800000), 0.f, 0.f, 0.f);
+                // rows past the stats (the last row block may pass N by more than the padding): no weight
+                const float4 st = live ? p.stat[row]
+                                       : make_float4(__int_as_float(GLOB ? 0xff800000 : 0x7f800000), 0.f, 0.f, 0.f);
                 lse2k = st.x;
                 gk = st.y;
                 rs_k = st.z;
@@ -730,6 +753,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t col = (uint32_t)(b * 128 + part * kColsB);
             float v[kColsB], w[kColsB];
             tmem_ld16x2(tmem + lane_off + col, tmem + lane_off + col + 64, v, w);  // hi*hi, hi*lo + lo*hi
+            if constexpr (GLOB) {
+                // kappa 2^E = a_k 2^(s2 + E - lse2_k) + a_j 2^(s2 + E - lse2_j) with a = scale g; the stats of
+                // rows and columns are the same (E - lse2, a); s2 = (x.y 2^2e) cS
+#pragma unroll
+                for (int u = 0; u < kColsB; ++u) {
+                    const float2 c = *reinterpret_cast<const float2*>(st + u);
+                    const float t = v[u] + w[u];
+                    v[u] = fmaf(gk, ExpTraits<float>::bexp(fmaf(t, gcS, lse2k)), c.y * ExpTraits<float>::bexp(fmaf(t, gcS, c.x)));
+                }
+                // padding columns and, with exclude_self, the pair (row, row) carry no weight
+                const bool dead_any = lim < kColsB || (dead_self >= 0 && dead_self < kColsB);
+                if (__any_sync(0xffffffffu, dead_any)) {
+#pragma unroll
+                    for (int u = 0; u < kColsB; ++u) v[u] = (u >= lim || u == dead_self) ? 0.f : v[u];
+                }
+                uint32_t hw[kColsB / 2], lw[kColsB / 2];
+#pragma unroll
+                for (int k = 0; k < kColsB / 2; ++k) {
+                    const __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+                    const float2 hf = __half22float2(h);
+                    hw[k] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[k] = pack_f16x2(v[2 * k] - hf.x, v[2 * k + 1] - hf.y);
+                }
+                tmem_st8(tmem + lane_off + col, hw);
+                tmem_st8(tmem + lane_off + col + 8, lw);
+                tmem_st_wait();
+                fence_before_sync();
+                mbar_arrive(w_full + b);
+                if (pending >= 0) {
+                    ok = drain(pending, gInv);
+                    if (!ok) break;
+                }
+                pending = i;
+                pend_inv = gInv;
+                continue;
+            }
             float ksum = 0.f, pm = 0.f;
             // columns that need care in this warp: padding past N, or the pair (row, row)
             const bool edge = lim < kColsB || (self >= 0 && self < kColsB && (p.exclude_self || METRIC != kLinear));
@@ -853,6 +912,71 @@ __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ 
     }
 }
 
+// Linear score without exp: the largest |z| and |g| (float bits, combined with atomicMax; both are
+// non-negative) for the sweep's two powers of two. One warp per row, grid-stride; one atomic per block.
+__global__ void __launch_bounds__(256) lse_bwd_reduce(const float* __restrict__ z, const float* __restrict__ g,
+                                                      int64_t N, int* __restrict__ gm) {
+    __shared__ float red[2][8];
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float mz = 0.f, mg = 0.f;
+    const int64_t stride = (int64_t)gridDim.x * 8;
+    // eight rows' loads in flight per warp before any is used (the data comes from DRAM)
+    for (int64_t r0 = (int64_t)blockIdx.x * 8 + wib; r0 < N; r0 += 8 * stride) {
+        float2 v[8];
+        float gg[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t r = r0 + k * stride;
+            v[k] = r < N ? reinterpret_cast<const float2*>(z + r * 64)[lane] : make_float2(0.f, 0.f);
+            gg[k] = r < N && lane == 0 ? g[r] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            mz = fmaxf(mz, fmaxf(fabsf(v[k].x), fabsf(v[k].y)));
+            mg = fmaxf(mg, fabsf(gg[k]));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mz = fmaxf(mz, __shfl_xor_sync(0xffffffffu, mz, off));
+    if (lane == 0) {
+        red[0][wib] = mz;
+        red[1][wib] = mg;
+    }
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        float m = 0.f;
+        for (int w = 0; w < 8; ++w) m = fmaxf(m, red[threadIdx.x][w]);
+        atomicMax(gm + threadIdx.x, __float_as_int(m));
+    }
+}
+
+// Linear score without exp: one warp per row over the padded rows, the fp16 hi/lo split of z 2^e with
+// the matrix's power of two e, and the stats (E - lse_j log2 e, scale g_j) shared by rows and columns
+// (E the kappa's power of two), (-inf, 0) for padding rows.
+__global__ void __launch_bounds__(256) lse_bwd_prep_lin(const float* __restrict__ z, const float* __restrict__ lse,
+                                                        const float* __restrict__ g, float scale, int64_t N,
+                                                        int64_t Npad, const int* __restrict__ gm,
+                                                        __half2* __restrict__ hi, __half2* __restrict__ lo,
+                                                        float4* __restrict__ stat, int* __restrict__ cnt, int64_t ncnt) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
+    if (r >= Npad) return;
+    if (r >= N) {
+        if (lane == 0) stat[r] = make_float4(__int_as_float(0xff800000), 0.f, 0.f, 0.f);
+        return;
+    }
+    const float f = pow2i(lin_z_exp(gm));
+    const float2 v = reinterpret_cast<const float2*>(z + r * 64)[lane];
+    const float a = v.x * f, b = v.y * f;
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    hi[r * 32 + lane] = h;
+    lo[r * 32 + lane] = __floats2half2_rn(a - hf.x, b - hf.y);
+    if (lane == 0)
+        stat[r] = make_float4((float)lin_kappa_exp(gm, scale) - lse[r] * 1.4426950408889634f, scale * g[r], 0.f, 0.f);
+}
+
 struct LseTcPlan {
     int64_t T, Xpad, Ypad;
     int CT, G, smax;
@@ -895,7 +1019,7 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
 struct LseBwdTcPlan {
     int64_t T, Npad;
     int CT, G, smax;
-    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_cnt, off_err, bytes;
+    size_t off_zh, off_zl, off_zn, off_stat, off_part, off_cnt, off_gmax, off_err, bytes;
 };
 
 static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
@@ -914,6 +1038,7 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     pl.off_stat = o; o += al256((size_t)pl.Npad * 16);
     pl.off_part = o; o += al256((size_t)pl.G * pl.smax * kPartRowsB * kBM * 4);
     pl.off_cnt = o; o += al256((size_t)RB * 4);
+    pl.off_gmax = o; o += 256;
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -1004,7 +1129,23 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         !make_map_f16(&mbh, zh, a.nP, kBNb) || !make_map_f16(&mbl, zl, a.nP, kBNb))
         return -1;
     int n = 0;
-    {
+    int* gm = reinterpret_cast<int*>(ws + pl.off_gmax);
+    const bool glob = a.metric == kLinear && !a.apply_exp;
+    if (glob) {
+        cudaMemsetAsync(gm, 0, 2 * sizeof(int), s);
+        {
+            HookScope h("lse_bwd_reduce", s);
+            const int64_t blocks = (a.nP + 7) / 8;  // one block per SM at most: few atomics on the two slots
+            lse_bwd_reduce<<<(unsigned)(blocks < kGrid ? blocks : kGrid), 256, 0, s>>>(
+                static_cast<const float*>(a.P), static_cast<const float*>(a.glse), a.nP, gm);
+            ++n;
+        }
+        HookScope h("lse_bwd_prep", s);
+        lse_bwd_prep_lin<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
+            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
+            (float)a.scale, a.nP, pl.Npad, gm, zh, zl, stat, cnt, (a.nP + kBM - 1) / kBM);
+        ++n;
+    } else {
         HookScope h("lse_bwd_prep", s);
         lse_bwd_prep16<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
             static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
@@ -1029,6 +1170,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     p.cnt = cnt;
     p.z = static_cast<const float*>(a.P);
     p.grad = static_cast<float*>(a.gP);
+    p.gmax = gm;
     p.err = reinterpret_cast<int*>(ws + pl.off_err);
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemB);
