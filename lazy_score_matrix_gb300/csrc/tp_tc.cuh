@@ -56,6 +56,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// One arrival per warp (the barrier counts warps): the warp synchronises, so every lane's earlier
+// tcgen05 operations (after its tcgen05.fence::before_thread_sync) and memory accesses are ordered before
+// lane 0's arrival. 512 per-thread arrivals on one barrier are as many serialised shared-memory atomics.
+// All 32 lanes must reach the call.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+// mbar_wait whose outcome all lanes of the warp share (so that control flow stays warp-uniform).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* err, int code) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, code));
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }

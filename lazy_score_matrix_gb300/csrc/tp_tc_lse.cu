@@ -190,9 +190,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 32 * kEpi);
+            mbar_init(acc_empty + b, kEpi);  // one arrival per epilogue warp
         }
-        mbar_init(fl_bar, 32 * kEpi);
+        mbar_init(fl_bar, kEpi);
         mbar_init(dec_bar, 1);
         mbar_fence_init();
     }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             o[lr] = m;
             o[kBM + lr] = l;
             __threadfence();
-            mbar_arrive(fl_bar);
+            mbar_arrive_warp(fl_bar);
             if (etid == 0) {
                 int last = 0;
                 if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 17)) {
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 c1r = p.scale * kL2E * xs;
             }
             const int b = (int)(i & 1), rr = (int)(i >> 1);
-            ok = mbar_wait(acc_full + b, rr & 1, p.err, 16);
+            ok = mbar_wait_warp(acc_full + b, rr & 1, p.err, 16);
             if (!ok) break;
             fence_after_sync();
             float v[32];  // hi*hi + (hi*lo + lo*hi), 16 columns at a time to bound live registers
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int u = 0; u < 16; ++u) v[hlf * 16 + u] = t0[u] + t1[u];
             }
             fence_before_sync();
-            mbar_arrive(acc_empty + b);  // the values are in registers: the MMA may reuse the buffer
+            mbar_arrive_warp(acc_empty + b);  // the values are in registers: the MMA may reuse the buffer
             const int64_t j0 = (int64_t)ct * kBN + sub * 32;
             const bool diag = row >= j0 && row < j0 + 32;
             const bool masked = p.M - j0 < 32 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
@@ -877,6 +877,326 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Symmetric backward, linear score without exp: the epilogue is two groups of eight warps (two per TMEM
+// lane quarter) that take alternate tiles, each group with an S buffer and a dZ accumulator of its own
+// in TMEM. One group's TMEM loads, stores and drains then overlap the other group's arithmetic, and the
+// tensor core runs the S and dZ MMAs of the two groups back to back. A warp covers 32 of the tile's 64
+// columns (two K steps of the dZ MMA) and 32 of the 64 dZ features. Both groups flush a partial for every
+// row block of the CTA's range, in order (zeros where a group had no tile), so the row-block completion
+// protocol sees both; the merge adds the two groups' slices.
+// ------------------------------------------------------------------------------------------------
+constexpr int kGrpW = kEpi / 2;             // warps per epilogue group
+constexpr int kPartRowsL = 128;             // rows of one partial: 64 dZ features per group
+
+// z.grad for features [16 fg, 16 fg + 16) of row lr of row block rb: both groups' slices of the partials
+// of every CTA that saw the row block, added in CTA order.
+__device__ __noinline__ void lin_merge_row(const LseBwdTcParams& p, int rb, int lr, int fg) {
+    const int64_t row = (int64_t)rb * kBM + lr;
+    if (row >= p.N) return;
+    const int64_t t0 = (int64_t)rb * p.CT;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t0 + p.CT - 1);
+    float acc[16];
+#pragma unroll
+    for (int f = 0; f < 16; ++f) acc[f] = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
+        const float* o = p.part + (size_t)(c * p.smax + seg) * kPartRowsL * kBM + lr;
+#pragma unroll
+        for (int f = 0; f < 16; ++f)
+            acc[f] += __ldcg(o + (size_t)(fg * 16 + f) * kBM) + __ldcg(o + (size_t)(64 + fg * 16 + f) * kBM);
+    }
+    float4* g4 = reinterpret_cast<float4*>(p.grad + row * 64 + fg * 16);
+#pragma unroll
+    for (int f4 = 0; f4 < 4; ++f4) g4[f4] = make_float4(acc[4 * f4], acc[4 * f4 + 1], acc[4 * f4 + 2], acc[4 * f4 + 3]);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    lse_bwd_lin_tc(const __grid_constant__ CUtensorMap mAh, const __grid_constant__ CUtensorMap mAl,
+                   const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
+                   const LseBwdTcParams p) {
+    constexpr float kL2E = 1.4426950408889634f;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sA = sm;                                        // row block: [hi 128 rows | lo 128 rows]
+    unsigned char* sB = sm + kPairF;                               // stage s: [hi 64 points | lo 64 points]
+    float4* sStat = reinterpret_cast<float4*>(sB + (size_t)kStageB * kStagesS);  // [stage][64]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStagesS * kBNb);
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* bs_full = bars + 2;                // [kStagesS]
+    uint64_t* bs_empty = bs_full + kStagesS;     // [kStagesS]
+    uint64_t* s_full = bs_empty + kStagesS;      // [2] per group: S of its tile is in its buffer
+    uint64_t* w_full = s_full + 2;               // [2] the group stored its tile's kappa
+    uint64_t* dz_full = w_full + 2;              // [2] the group's dZ block is complete
+    uint64_t* dz_empty = dz_full + 2;            // [2] the group read its dZ block
+    uint64_t* fl_bar = dz_empty + 2;             // the epilogue wrote its partials of a row block
+    uint64_t* dec_bar = fl_bar + 1;              // the CTA knows whether it merges that row block
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
+    volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
+    const int64_t n = t_end - t_begin;
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < kStagesS; ++s) {
+            mbar_init(bs_full + s, 1);
+            mbar_init(bs_empty + s, 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(s_full + g, 1);
+            mbar_init(w_full + g, kGrpW);  // one arrival per warp of the group
+            mbar_init(dz_full + g, 1);
+            mbar_init(dz_empty + g, kGrpW);
+        }
+        mbar_init(fl_bar, kEpi);
+        mbar_init(dec_bar, 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    // group g: S buffer at column 128 g (hi*hi 0..63, hi*lo + lo*hi 64..127), dZ at 256 + 128 g
+    auto tS = [&](int g) { return tmem + (uint32_t)(128 * g); };
+    auto tD = [&](int g) { return tmem + (uint32_t)(256 + 128 * g); };
+
+    if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer: operand stages in tile order
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            TileCursor cur(t_begin, p.CT);
+            for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
+                const int rb = cur.rb, ct = cur.ct;
+                if (rb != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 61);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, kPairF);
+                    tma_load_2d(sA, &mAh, 0, rb * kBM, a_full);
+                    tma_load_2d(sA + kHalfTile, &mAl, 0, rb * kBM, a_full);
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(i % kStagesS), r = (int)(i / kStagesS);
+                if (r >= 1) ok = mbar_wait(bs_empty + s, (r - 1) & 1, p.err, 62);
+                if (!ok) break;
+                unsigned char* dst = sB + (size_t)s * kStageB;
+                mbar_expect_tx(bs_full + s, kStageB + kBNb * 16);
+                tma_load_2d(dst, &mBh, 0, ct * kBNb, bs_full + s);
+                tma_load_2d(dst + kTileB, &mBl, 0, ct * kBNb, bs_full + s);
+                bulk_load(sStat + s * kBNb, p.stat + (size_t)ct * kBNb, kBNb * 16, bs_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer
+            constexpr uint32_t idS2 = idesc_f16(kBM, 2 * kBNb, false);  // Zh [Zth; Ztl]: N 128
+            constexpr uint32_t idS = idesc_f16(kBM, kBNb, false);       // Zl Zth: N 64
+            constexpr uint32_t idZ2 = idesc_f16(kBM, 128, true);        // kappa_hi [Zh | Zl] (MN-major): N 128
+            constexpr uint32_t idZ = idesc_f16(kBM, 64, true);          // kappa_lo Zh (MN-major): N 64
+            int a_uses = 0, rb_cur = -1;
+            bool ok = true;
+            TileCursor cur(t_begin, p.CT);
+            // S of tile j into its group's buffer (whose kappa(j - 2) was read by dZ(j - 2), issued before)
+            auto issue_s = [&](int64_t j) -> bool {
+                const int rb = cur.rb;
+                cur.next();
+                if (rb != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);  // the old A is free once its MMAs finish
+                    if (!mbar_wait(a_full, a_uses & 1, p.err, 63)) return false;
+                    ++a_uses;
+                    rb_cur = rb;
+                }
+                const int s = (int)(j % kStagesS), r = (int)(j / kStagesS), g = (int)(j & 1);
+                if (!mbar_wait(bs_full + s, r & 1, p.err, 64)) return false;
+                fence_after_sync();
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kStageB);
+                const uint32_t d = tS(g);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = (uint32_t)(ks * 32);
+                    mma_f16(d, desc_sw128(a0 + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), idS2, ks > 0 ? 1u : 0u);
+                    mma_f16(d + 64, desc_sw128(a0 + kHalfTile + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), idS, 1u);
+                }
+                mma_commit(s_full + g);
+                return true;
+            };
+            // dZ of tile i from its kappa (stored by its group over the hi*hi S columns, K step ks at 16 ks)
+            auto issue_dz = [&](int64_t i) -> bool {
+                const int g = (int)(i & 1), s = (int)(i % kStagesS);
+                if (!mbar_wait(w_full + g, (uint32_t)((i >> 1) & 1), p.err, 65)) return false;
+                if (i >= 2 && !mbar_wait(dz_empty + g, (uint32_t)(((i >> 1) - 1) & 1), p.err, 66)) return false;
+                fence_after_sync();
+                const uint32_t b0 = smem_u32(sB + (size_t)s * kStageB);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t bo = b0 + (uint32_t)(ks * 16 * kRowBytes);
+                    const uint32_t kh = tS(g) + (uint32_t)(ks * 16), kl = kh + 8;
+                    mma_f16_ta(tD(g), kh, desc_sw128(bo, kTileB, 1024), idZ2, ks > 0 ? 1u : 0u);
+                    mma_f16_ta(tD(g) + 64, kl, desc_sw128(bo, kTileB, 1024), idZ, 1u);
+                }
+                mma_commit(bs_empty + s);  // the stage fed both S and dZ
+                mma_commit(dz_full + g);
+                return true;
+            };
+            for (int64_t j = 0; j < n && j < 2 && ok; ++j) ok = issue_s(j);
+            for (int64_t i = 0; i < n && ok; ++i) {
+                ok = issue_dz(i);
+                if (ok && i + 2 < n) ok = issue_s(i + 2);
+            }
+        }
+    } else {
+        // ---------------- epilogue: group grp takes the tiles i with i % 2 == grp; within it, half h of a lane
+        // quarter owns tile columns [32 h, 32 h + 32) (dZ K steps 2h, 2h + 1) and dZ features [32 h, 32 h + 32)
+        const int etid = threadIdx.x - 64;  // 0 .. 32 kEpi - 1
+        const int grp = etid >> 8;
+        const int q = warp & 3;
+        const int half = ((warp - 2) >> 2) & 1;
+        const int lr = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int N32 = (int)p.N;
+        const int ez = lin_z_exp(p.gmax), E = lin_kappa_exp(p.gmax, p.scale);
+        const float cS = pow2i(-ez) * pow2i(-ez) * p.scale * kL2E;  // s2 = (x.y 2^2e) cS
+        const float inv = pow2i(-E) * pow2i(-ez);                  // a dZ block back to z.grad units
+        const int rb_first = rb_of_tile(t_begin, p.CT);
+        const int rb_last = n > 0 ? rb_of_tile(t_end - 1, p.CT) : rb_first - 1;
+        float dacc[32];
+#pragma unroll
+        for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
+        float lse2k = 0.f, gk = 0.f;
+        int rb_cur = rb_first, row = rb_first * kBM + lr;
+        auto load_row = [&]() {
+            row = rb_cur * kBM + lr;
+            // rows past the stats (the last row block may pass N by more than the padding): no weight
+            const float4 st = row < N32 ? p.stat[row] : make_float4(__int_as_float(0xff800000), 0.f, 0.f, 0.f);
+            lse2k = st.x;
+            gk = st.y;
+        };
+        load_row();
+        bool ok = true;
+        // add this warp's 32 features of the group's finished dZ block of tile j into the accumulator
+        auto drain = [&](int64_t j) -> bool {
+            if (!mbar_wait_warp(dz_full + grp, (uint32_t)((j >> 1) & 1), p.err, 67)) return false;
+            fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v[16], w[16];
+                const uint32_t a = tD(grp) + lane_off + (uint32_t)(32 * half + 16 * c);
+                tmem_ld16x2(a, a + 64, v, w);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) dacc[16 * c + u] = fmaf(v[u] + w[u], inv, dacc[16 * c + u]);
+            }
+            fence_before_sync();
+            mbar_arrive_warp(dz_empty + grp);
+            return true;
+        };
+        // Write this thread's partial of row block rb_cur (both groups, every row block of the range in
+        // order); the CTA that completes the row block merges it into z.grad.
+        auto flush = [&]() {
+            const int seg = rb_cur - rb_first;
+            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * kPartRowsL * kBM;
+#pragma unroll
+            for (int f = 0; f < 32; ++f) o[(size_t)(grp * 64 + 32 * half + f) * kBM + lr] = dacc[f];
+            __threadfence();
+            mbar_arrive_warp(fl_bar);
+            if (etid == 0) {
+                int last = 0;
+                if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 68)) {
+                    const int64_t t0 = (int64_t)rb_cur * p.CT;
+                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
+                    __threadfence();
+                }
+                *sflag = last;
+                mbar_arrive(dec_bar);
+            }
+            if (mbar_wait_warp(dec_bar, (uint32_t)(seg & 1), p.err, 69) && *sflag)
+                lin_merge_row(p, rb_cur, etid % kBM, etid / kBM);
+#pragma unroll
+            for (int f = 0; f < 32; ++f) dacc[f] = 0.f;
+        };
+        int64_t pending = -1;
+        TileCursor cur(t_begin, p.CT);
+        if (grp == 1 && n > 0) cur.next();
+        for (int64_t i = grp; i < n && ok; i += 2, cur.next(), cur.next()) {
+            const int rb = cur.rb, ct = cur.ct;
+            if (rb != rb_cur) {
+                if (pending >= 0) {
+                    ok = drain(pending);
+                    pending = -1;
+                    if (!ok) break;
+                }
+                while (rb_cur < rb) {
+                    flush();
+                    ++rb_cur;
+                }
+                load_row();
+            }
+            const int s = (int)(i % kStagesS);
+            ok = mbar_wait_warp(s_full + grp, (uint32_t)((i >> 1) & 1), p.err, 70) &&
+                 mbar_wait_warp(bs_full + s, (uint32_t)((i / kStagesS) & 1), p.err, 71);  // the tile's column stats
+            if (!ok) break;
+            fence_after_sync();
+            const int dead_self = p.exclude_self ? row : -1;  // the pair (row, row)
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                const int ks = 2 * half + c;
+                const uint32_t col = tS(grp) + lane_off + (uint32_t)(16 * ks);
+                float v[16], w[16];
+                tmem_ld16x2(col, col + 64, v, w);  // hi*hi, hi*lo + lo*hi
+                const float4* st = sStat + s * kBNb + 16 * ks;
+                // kappa 2^E = a_k 2^(s2 + E - lse2_k) + a_j 2^(s2 + E - lse2_j), a = scale g; row and column
+                // stats alike are (E - lse2, a)
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float2 cc = *reinterpret_cast<const float2*>(st + u);
+                    const float t = v[u] + w[u];
+                    v[u] = fmaf(gk, ExpTraits<float>::bexp(fmaf(t, cS, lse2k)), cc.y * ExpTraits<float>::bexp(fmaf(t, cS, cc.x)));
+                }
+                const int j0 = ct * kBNb + 16 * ks;
+                const int lim = N32 - j0, self = dead_self - j0;  // columns u >= lim are padding
+                if (__any_sync(0xffffffffu, lim < 16 || (self >= 0 && self < 16))) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) v[u] = (u >= lim || u == self) ? 0.f : v[u];
+                }
+                uint32_t hw[8], lw[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+                    const float2 hf = __half22float2(h);
+                    hw[k] = *reinterpret_cast<const uint32_t*>(&h);
+                    lw[k] = pack_f16x2(v[2 * k] - hf.x, v[2 * k + 1] - hf.y);
+                }
+                // kappa of K step ks over this warp's own hi*hi columns [16 ks, 16 ks + 16), read above
+                tmem_st8(col, hw);
+                tmem_st8(col + 8, lw);
+            }
+            tmem_st_wait();
+            fence_before_sync();
+            mbar_arrive_warp(w_full + grp);
+            if (pending >= 0) {
+                ok = drain(pending);
+                if (!ok) break;
+            }
+            pending = i;
+        }
+        if (ok && pending >= 0) ok = drain(pending);
+        if (ok) {
+            while (rb_cur <= rb_last) {
+                flush();
+                ++rb_cur;
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
 // Backward pre-pass, one warp per row over the padded rows: the fp16 hi/lo split of z 2^e, |z|^2 and the
 // column stats (lse_j log2 e, g_j, 2^-e_j, scale 2^-e_j), (+inf, 0, 0, 0) for padding rows.
 __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ z, const float* __restrict__ lse,
@@ -1036,7 +1356,7 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     pl.off_zl = o; o += al256((size_t)N * kRowBytes);
     pl.off_zn = o; o += al256((size_t)N * 4);
     pl.off_stat = o; o += al256((size_t)pl.Npad * 16);
-    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * kPartRowsB * kBM * 4);
+    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * (kPartRowsB > kPartRowsL ? kPartRowsB : kPartRowsL) * kBM * 4);
     pl.off_cnt = o; o += al256((size_t)RB * 4);
     pl.off_gmax = o; o += 256;
     pl.off_err = o; o += 256;
@@ -1178,7 +1498,8 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         kernel<<<pl.G, kTcThreads, kSmemB, s>>>(mah, mal, mbh, mbl, p);
     };
     const bool ex = a.apply_exp != 0;
-    if (a.metric == kLinear) ex ? go(lse_bwd_sym_tc<kLinear, true>) : go(lse_bwd_sym_tc<kLinear, false>);
+    if (glob) go(lse_bwd_lin_tc);
+    else if (a.metric == kLinear) go(lse_bwd_sym_tc<kLinear, true>);
     else if (a.metric == kSqeuclidean) ex ? go(lse_bwd_sym_tc<kSqeuclidean, true>) : go(lse_bwd_sym_tc<kSqeuclidean, false>);
     else ex ? go(lse_bwd_sym_tc<kRbf, true>) : go(lse_bwd_sym_tc<kRbf, false>);
     ++n;
