@@ -511,10 +511,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const __grid_constant__ CUtensorMap mBh, const __grid_constant__ CUtensorMap mBl,
                    const LseBwdTcParams p) {
     constexpr float kL2E = 1.4426950408889634f;
-    // linear score without exp: powers of two fixed for the whole sweep (no per-tile exchange); each part
-    // stores its kappa over its own hi*hi S columns ([16 part, +8) hi, [16 part + 8, +8) lo), which it has
-    // already read, so the four parts of a lane quarter need not wait for one another
-    constexpr bool GLOB = METRIC == kLinear && !EXP;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                        // row block: [hi 128 rows | lo 128 rows]
@@ -633,16 +629,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (i >= 1 && !mbar_wait(dz_empty, (uint32_t)((i - 1) & 1), p.err, 26)) return false;
                 fence_after_sync();
                 const uint32_t b0 = smem_u32(sB + (size_t)s * kStageB);
-                const uint32_t kb = tmem + (uint32_t)(b * 128);  // packed kappa_hi, kappa_lo of the buffer
+                const uint32_t kh = tmem + (uint32_t)(b * 128), kl = kh + 32;  // packed kappa_hi, kappa_lo
                 // per 16 points (one epilogue part): the stage read MN-major, rows of 16 points, hi and lo
                 // feature blocks kTileB apart
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t bo = b0 + (uint32_t)(ks * 16 * kRowBytes);
-                    const uint32_t kh = GLOB ? kb + (uint32_t)(ks * 16) : kb + (uint32_t)(ks * 8);
-                    const uint32_t kl = GLOB ? kh + 8 : kh + 32;
-                    mma_f16_ta(tDZ, kh, desc_sw128(bo, kTileB, 1024), idZ2, ks > 0 ? 1u : 0u);
-                    mma_f16_ta(tDZ + 64, kl, desc_sw128(bo, kTileB, 1024), idZ, 1u);
+                    mma_f16_ta(tDZ, kh + (uint32_t)(ks * 8), desc_sw128(bo, kTileB, 1024), idZ2, ks > 0 ? 1u : 0u);
+                    mma_f16_ta(tDZ + 64, kl + (uint32_t)(ks * 8), desc_sw128(bo, kTileB, 1024), idZ, 1u);
                 }
                 mma_commit(bs_empty + s);  // the stage fed both S and dZ
                 mma_commit(dz_full);
@@ -709,12 +703,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         int64_t pending = -1;
         float pend_inv = 0.f;
-        float gcS = 0.f, gInv = 0.f;  // GLOB: the S factor (base 2) and the factor from a dZ block to z.grad
-        if (GLOB) {
-            const int ez = lin_z_exp(p.gmax), E = lin_kappa_exp(p.gmax, p.scale);
-            gcS = pow2i(-ez) * pow2i(-ez) * p.scale * kL2E;
-            gInv = pow2i(-E) * pow2i(-ez);
-        }
         TileCursor cur(t_begin, p.CT);
         for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
             const int rb = cur.rb, ct = cur.ct;
@@ -731,9 +719,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int f = 0; f < kColsB; ++f) dacc[f] = 0.f;
                 const bool live = row < N32;
-                // rows past the stats (the last row block may pass N by more than the padding): no weight
-                const float4 st = live ? p.stat[row]
-                                       : make_float4(__int_as_float(GLOB ? 0xff800000 : 0x7f800000), 0.f, 0.f, 0.f);
+                const float4 st = live ? p.stat[row] : make_float4(__int_as_float(0x7f800000), 0.f, 0.f, 0.f);
                 lse2k = st.x;
                 gk = st.y;
                 rs_k = st.z;
@@ -753,42 +739,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t col = (uint32_t)(b * 128 + part * kColsB);
             float v[kColsB], w[kColsB];
             tmem_ld16x2(tmem + lane_off + col, tmem + lane_off + col + 64, v, w);  // hi*hi, hi*lo + lo*hi
-            if constexpr (GLOB) {
-                // kappa 2^E = a_k 2^(s2 + E - lse2_k) + a_j 2^(s2 + E - lse2_j) with a = scale g; the stats of
-                // rows and columns are the same (E - lse2, a); s2 = (x.y 2^2e) cS
-#pragma unroll
-                for (int u = 0; u < kColsB; ++u) {
-                    const float2 c = *reinterpret_cast<const float2*>(st + u);
-                    const float t = v[u] + w[u];
-                    v[u] = fmaf(gk, ExpTraits<float>::bexp(fmaf(t, gcS, lse2k)), c.y * ExpTraits<float>::bexp(fmaf(t, gcS, c.x)));
-                }
-                // padding columns and, with exclude_self, the pair (row, row) carry no weight
-                const bool dead_any = lim < kColsB || (dead_self >= 0 && dead_self < kColsB);
-                if (__any_sync(0xffffffffu, dead_any)) {
-#pragma unroll
-                    for (int u = 0; u < kColsB; ++u) v[u] = (u >= lim || u == dead_self) ? 0.f : v[u];
-                }
-                uint32_t hw[kColsB / 2], lw[kColsB / 2];
-#pragma unroll
-                for (int k = 0; k < kColsB / 2; ++k) {
-                    const __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
-                    const float2 hf = __half22float2(h);
-                    hw[k] = *reinterpret_cast<const uint32_t*>(&h);
-                    lw[k] = pack_f16x2(v[2 * k] - hf.x, v[2 * k + 1] - hf.y);
-                }
-                tmem_st8(tmem + lane_off + col, hw);
-                tmem_st8(tmem + lane_off + col + 8, lw);
-                tmem_st_wait();
-                fence_before_sync();
-                mbar_arrive(w_full + b);
-                if (pending >= 0) {
-                    ok = drain(pending, gInv);
-                    if (!ok) break;
-                }
-                pending = i;
-                pend_inv = gInv;
-                continue;
-            }
             float ksum = 0.f, pm = 0.f;
             // columns that need care in this warp: padding past N, or the pair (row, row)
             const bool edge = lim < kColsB || (self >= 0 && self < kColsB && (p.exclude_self || METRIC != kLinear));
@@ -1450,6 +1400,9 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         return -1;
     int n = 0;
     int* gm = reinterpret_cast<int*>(ws + pl.off_gmax);
+    // linear score without exp: one power of two for z and one for kappa, fixed for the whole sweep (a
+    // reduction finds max|z| and max|g|), and the two-group kernel lse_bwd_lin_tc; otherwise per-row powers
+    // of two and lse_bwd_sym_tc with its per-tile row-maximum exchange
     const bool glob = a.metric == kLinear && !a.apply_exp;
     if (glob) {
         cudaMemsetAsync(gm, 0, 2 * sizeof(int), s);
