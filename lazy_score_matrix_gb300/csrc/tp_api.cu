@@ -199,8 +199,8 @@ bool force_simt() {
 }
 
 // The tensor-core symmetric backward (fp32, D = 64, X = Y, no row/column parameters) and the
-// tensor-core top-k (fp32, D <= 64, k <= 32): both pass every parity test on the GPU and are faster
-// than the SIMT sweeps they replace (InfoNCE backward 168 us vs 0.8 ms; k-NN 43 ms vs 130 ms).
+// tensor-core top-k (fp32, D <= 64, k <= 32): both pass every parity test on the GPU and are several
+// times faster than the SIMT sweeps they replace on the InfoNCE and k-NN workloads.
 constexpr bool kTcBackward = true;
 constexpr bool kTcTopk = true;
 

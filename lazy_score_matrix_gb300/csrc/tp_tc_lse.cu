@@ -16,8 +16,8 @@
 // and cut into equal contiguous ranges, one per CTA. Warp 0 lane 0 loads tiles with TMA (128-byte
 // swizzle), warp 1 owns the TMEM allocation and its lane 0 issues the MMAs, the other warps are the
 // epilogue (one row per thread, four warps per TMEM lane quarter). A CTA writes a partial per row for
-// each row block it touched; a merge kernel combines the partials of each row in CTA order, so
-// results are deterministic.
+// each row block it touched; the last CTA to finish a row block (an atomic count per row block) adds
+// the partials of its rows in CTA order, so results are deterministic.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -424,8 +424,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // contractions. Each tile's dZ (128 x 64) lands in a TMEM block of its own and the epilogue adds it,
 // unscaled, into a per-row register accumulator: the tensor core's accumulation never spans more
 // than one tile, and the rows' sums are two-level like everywhere else. At the end of the CTA's
-// share of a row block the accumulator is written as a partial; a merge kernel adds the partials
-// of each row in CTA order.
+// share of a row block the accumulator is written as a partial; the last CTA to finish the row block
+// adds the partials of each row in CTA order.
 //
 // Order of the MMAs: S runs two tiles ahead of dZ (three S buffers in TMEM), so the S of tile i+1 is
 // ready when the epilogue finishes tile i.
