@@ -76,15 +76,27 @@ typedef enum { TP_F32 = 0, TP_F64 = 1 } tp_dtype;
 
 typedef enum { TP_SQEUCLIDEAN = 0, TP_LINEAR = 1, TP_RBF = 2 } tp_metric;
 
+/* Pair masks, torchpairwise guide "Using Torchpairwise in Models", Score Expressions and Task Map
+ * (tp.masks: causal, band, same_group). A masked pair leaves the consumer's reduction: it adds no term
+ * to K@V, a log-sum-exp, a softmax or a displacement, top-k never selects it, and it gets no gradient.
+ * A softmax row with every pair masked returns 0 (its log-sum-exp is -inf). TP_PAIRS_CAUSAL keeps
+ * j <= i, TP_PAIRS_BAND keeps |i - j| <= band, TP_PAIRS_SAME_GROUP keeps row_group[i] ==
+ * col_group[j]. These run in the streamed sweeps (the pages run them on materialised tiles). */
+typedef enum { TP_PAIRS_ALL = 0, TP_PAIRS_CAUSAL = 1, TP_PAIRS_BAND = 2, TP_PAIRS_SAME_GROUP = 3 } tp_pair_mask;
+
 /* The canonical score (see the file comment). Bias and weight pointers are device arrays of the
  * problem's dtype, [N] for rows and [M] for columns, or NULL when absent. gamma is used by TP_RBF
- * only. */
+ * only. pair_mask selects a pair mask (above); band (>= 0) is read by TP_PAIRS_BAND only; row_group
+ * [N] and col_group [M] are int32 device arrays read by TP_PAIRS_SAME_GROUP only (NULL otherwise). */
 typedef struct {
     tp_metric metric;
     double gamma;
     double scale;
     int apply_exp;
     const void *row_bias, *col_bias, *row_weight, *col_weight;
+    tp_pair_mask pair_mask;
+    int64_t band;
+    const int32_t *row_group, *col_group;
 } tp_score;
 
 /* The two point sets: X [N,D] and Y [M,D], device, row-major, contiguous. */

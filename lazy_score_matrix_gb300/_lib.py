@@ -18,11 +18,16 @@ TP_F32, TP_F64 = 0, 1
 METRICS = {"sqeuclidean": 0, "linear": 1, "rbf": 2}
 
 
+PAIR_MASKS = {"all": 0, "causal": 1, "band": 2, "same_group": 3}
+
+
 class tp_score(ctypes.Structure):
     _fields_ = [("metric", ctypes.c_int), ("gamma", ctypes.c_double), ("scale", ctypes.c_double),
                 ("apply_exp", ctypes.c_int),
                 ("row_bias", ctypes.c_void_p), ("col_bias", ctypes.c_void_p),
-                ("row_weight", ctypes.c_void_p), ("col_weight", ctypes.c_void_p)]
+                ("row_weight", ctypes.c_void_p), ("col_weight", ctypes.c_void_p),
+                ("pair_mask", ctypes.c_int), ("band", ctypes.c_int64),
+                ("row_group", ctypes.c_void_p), ("col_group", ctypes.c_void_p)]
 
 
 class tp_pairs(ctypes.Structure):

@@ -132,6 +132,19 @@ tp_status check_score(const tp_score* s, const tp_pairs* p) {
     const size_t es = esize(p->dtype);
     for (const void* q : {s->row_bias, s->col_bias, s->row_weight, s->col_weight})
         if (q && !aligned(q, es)) return fail(TP_ERR_INVALID_ARG, "bias/weight not aligned to the element size");
+    switch (s->pair_mask) {
+        case TP_PAIRS_ALL:
+        case TP_PAIRS_CAUSAL: break;
+        case TP_PAIRS_BAND:
+            if (s->band < 0) return fail(TP_ERR_INVALID_ARG, "band must be >= 0");
+            break;
+        case TP_PAIRS_SAME_GROUP:
+            if (!s->row_group || !s->col_group) return fail(TP_ERR_INVALID_ARG, "same-group mask needs row_group and col_group");
+            if (!aligned(s->row_group, 4) || !aligned(s->col_group, 4))
+                return fail(TP_ERR_INVALID_ARG, "row_group/col_group not aligned to 4 bytes");
+            break;
+        default: return fail(TP_ERR_INVALID_ARG, "unknown pair mask");
+    }
     return TP_OK;
 }
 
@@ -158,10 +171,13 @@ tp_status check_ws(const void* ws, size_t have, size_t need) {
 
 std::vector<Span> score_spans(const tp_score* s, const tp_pairs* p) {
     const size_t es = esize(p->dtype);
+    const bool groups = s->pair_mask == TP_PAIRS_SAME_GROUP;
     return {{s->row_bias, p->N * es, "row_bias"},
             {s->col_bias, p->M * es, "col_bias"},
             {s->row_weight, p->N * es, "row_weight"},
-            {s->col_weight, p->M * es, "col_weight"}};
+            {s->col_weight, p->M * es, "col_weight"},
+            {groups ? s->row_group : nullptr, (size_t)p->N * 4, "row_group"},
+            {groups ? s->col_group : nullptr, (size_t)p->M * 4, "col_group"}};
 }
 
 // Row-side (P = X) or column-side (P = Y) arguments of a sweep.
@@ -182,6 +198,13 @@ SweepArgs side_args(const tp_pairs* p, const tp_score* s, bool col) {
     a.pw = col ? s->col_weight : s->row_weight;
     a.qw = col ? s->row_weight : s->col_weight;
     a.affine = (s->row_bias || s->col_bias || s->row_weight || s->col_weight) ? 1 : 0;
+    a.pm = (int)s->pair_mask;
+    a.pcol = col ? 1 : 0;
+    a.band = s->band;
+    if (s->pair_mask == TP_PAIRS_SAME_GROUP) {
+        a.pg = col ? s->col_group : s->row_group;
+        a.qg = col ? s->row_group : s->col_group;
+    }
     const Plan pl = plan_split(a.nP, a.nQ);
     a.splits = pl.splits;
     a.cps = pl.cps;
@@ -208,7 +231,7 @@ constexpr bool kTcTopk = true;
 bool lse_tc_shape(const tp_pairs* p) { return p->dtype == TP_F32 && p->D == 64; }
 bool lse_tc_eligible(const tp_pairs* p, const tp_score* s) {
     return !force_simt() && lse_tc_shape(p) && !s->row_bias && !s->col_bias && !s->row_weight && !s->col_weight &&
-           aligned(p->X, 16) && aligned(p->Y, 16);
+           s->pair_mask == TP_PAIRS_ALL && aligned(p->X, 16) && aligned(p->Y, 16);
 }
 
 // Tensor-core attention: softmax_matmul and its backward for fp32, D = C = 64, a linear score without
@@ -217,7 +240,8 @@ constexpr bool kTcAttention = true;
 bool attn_tc_shape(const tp_pairs* p, int64_t C) { return p->dtype == TP_F32 && p->D == 64 && C == 64; }
 bool attn_tc_eligible(const tp_pairs* p, const tp_score* s, int64_t C, std::initializer_list<const void*> rows) {
     if (!kTcAttention || force_simt() || !attn_tc_shape(p, C) || s->metric != TP_LINEAR || s->apply_exp || s->row_bias ||
-        s->col_bias || s->row_weight || s->col_weight || !aligned(p->X, 16) || !aligned(p->Y, 16))
+        s->col_bias || s->row_weight || s->col_weight || s->pair_mask != TP_PAIRS_ALL || !aligned(p->X, 16) ||
+        !aligned(p->Y, 16))
         return false;
     for (const void* q : rows)
         if (q && !aligned(q, 16)) return false;
@@ -227,7 +251,8 @@ bool attn_tc_eligible(const tp_pairs* p, const tp_score* s, int64_t C, std::init
 // The tensor-core top-k covers fp32, D <= 64, k <= 32, no row/column parameters.
 bool topk_tc_shape(const tp_pairs* p, int k) { return p->dtype == TP_F32 && p->D <= 64 && k >= 1 && k <= kTopkMax; }
 bool topk_tc_eligible(const tp_pairs* p, const tp_score* s, int k) {
-    return kTcTopk && !force_simt() && topk_tc_shape(p, k) && !s->row_bias && !s->col_bias && !s->row_weight && !s->col_weight;
+    return kTcTopk && !force_simt() && topk_tc_shape(p, k) && !s->row_bias && !s->col_bias && !s->row_weight &&
+           !s->col_weight && s->pair_mask == TP_PAIRS_ALL;
 }
 
 tp_status launched(int n) {
@@ -842,7 +867,7 @@ tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pr, const tp_score* sc,
     // Same points, summed gradient wanted, no row/column parameters: the score is symmetric and one
     // sweep gives sum_j (H_kj + H_jk) dt_kj/dz_k, each pair evaluated once.
     const bool symmetric = dX && dX == dY && pr->X == pr->Y && pr->N == pr->M && !sc->row_bias && !sc->col_bias &&
-                           !sc->row_weight && !sc->col_weight;
+                           !sc->row_weight && !sc->col_weight && sc->pair_mask == TP_PAIRS_ALL;
     if (symmetric) {
         row.gP = dX;
         if (kTcBackward && lse_tc_eligible(pr, sc)) {

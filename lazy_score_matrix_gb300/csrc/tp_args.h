@@ -24,6 +24,12 @@ struct SweepArgs {
     const void* glse;               // [rows] upstream gradient of lse
     const void* delta;              // [rows] softmax: dO_i . out_i
     int exclude_self;
+    // pair mask (tp_pair_mask): 0 none, 1 causal (j <= i), 2 band (|i - j| <= band), 3 same group. The
+    // sweep's own points are the rows i, or the columns j when pcol (a column sweep); pg / qg are the own
+    // and the streamed side's group ids.
+    int pm, pcol;
+    int64_t band;
+    const int *pg, *qg;
     int splits;
     int64_t cps;  // streamed points per split (multiple of kTile)
     void* out;

@@ -15,11 +15,26 @@
 // displacement and the SVGD direction).
 #pragma once
 
+#include <type_traits>
+
 #include "tp_args.h"
 #include "tp_device.cuh"
 #include "tp_launch.h"
 
 namespace tp {
+
+// Whether the pair of own point pi and streamed point qj stays in the consumer's reduction under the
+// sweep's pair mask (torchpairwise guide "Using Torchpairwise in Models", Score Expressions: tp.masks
+// causal, band, same_group). og: the own point's group id (same-group masks only).
+__device__ __forceinline__ bool pair_kept(const SweepArgs& a, int64_t pi, int64_t qj, int og) {
+    const int64_t i = a.pcol ? qj : pi, j = a.pcol ? pi : qj;
+    switch (a.pm) {
+        case 1: return j <= i;
+        case 2: return (i > j ? i - j : j - i) <= a.band;
+        case 3: return __ldg(a.qg + qj) == og;
+        default: return true;
+    }
+}
 
 // ------------------------------------------------------------------------------------------------
 // two-level accumulation
@@ -155,6 +170,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
         if (pvalid && a.pw) A *= static_cast<const T*>(a.pw)[pi];
         if (pvalid && a.pb) Cp = static_cast<const T*>(a.pb)[pi];
     }
+    const int og = (a.pm == 3 && pvalid) ? a.pg[pi] : 0;
 
     // tile accumulators (registers); running accumulators (shared memory / scalars)
     T acc[NACC];
@@ -173,69 +189,76 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
     zero_smem(sq, kTile * DP);
     if constexpr (HAS_V) zero_smem(sv, kTile * VW);
 
-    for (int64_t j0 = jb; j0 < je; j0 += kTile) {
-        const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
-        __syncthreads();
-        stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
-        if constexpr (HAS_V)
-            stage_rows<T, VW>(sv, static_cast<const T*>(a.Vq), j0, cnt, MODE == kSvgd ? a.D : a.C, a.vecV);
-        if constexpr (AFFINE) {
-            stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
-            stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
-        }
-        __syncthreads();
-        if (a.metric != kLinear) {
-            stage_norms<T, DP>(sn, sq, cnt);
+    // the tile loop, compiled once without and once with the pair mask test (chosen per launch)
+    auto sweep = [&](auto masked) {
+        for (int64_t j0 = jb; j0 < je; j0 += kTile) {
+            const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
             __syncthreads();
-        }
-        const T m0 = m;  // the running state is relative to the max at the start of the tile
-#pragma unroll 2
-        for (int jj = 0; jj < cnt; ++jj) {
-            const T* q = sq + jj * DP;
-            const T dot = dot_regs_smem<T, DP>(p, q);
-            const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
-            T t;
-            if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
-            else t = A * base;
-            const T S = a.apply_exp ? E::exp(t) : t;
-            if constexpr (MODE == kMatmul) {
-                axpy_smem<T, CP>(acc, S, sv + jj * CP);
-            } else if constexpr (MODE == kLse || MODE == kSoftmax) {
-                if (MODE == kLse && a.exclude_self && j0 + jj == pi) continue;
-                const T s = S * E::kLogB;
-                if (s > m) {
-                    const T r = E::bexp(m - s);
-                    l.tile *= r;
-                    if constexpr (MODE == kSoftmax) {
-#pragma unroll
-                        for (int c = 0; c < CP; ++c) acc[c] *= r;
+            stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
+            if constexpr (HAS_V)
+                stage_rows<T, VW>(sv, static_cast<const T*>(a.Vq), j0, cnt, MODE == kSvgd ? a.D : a.C, a.vecV);
+            if constexpr (AFFINE) {
+                stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
+                stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
+            }
+            __syncthreads();
+            if (a.metric != kLinear) {
+                stage_norms<T, DP>(sn, sq, cnt);
+                __syncthreads();
+            }
+            const T m0 = m;  // the running state is relative to the max at the start of the tile
+    #pragma unroll 2
+            for (int jj = 0; jj < cnt; ++jj) {
+                if constexpr (decltype(masked)::value)
+                    if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair adds nothing
+                const T* q = sq + jj * DP;
+                const T dot = dot_regs_smem<T, DP>(p, q);
+                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                T t;
+                if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
+                else t = A * base;
+                const T S = a.apply_exp ? E::exp(t) : t;
+                if constexpr (MODE == kMatmul) {
+                    axpy_smem<T, CP>(acc, S, sv + jj * CP);
+                } else if constexpr (MODE == kLse || MODE == kSoftmax) {
+                    if (MODE == kLse && a.exclude_self && j0 + jj == pi) continue;
+                    const T s = S * E::kLogB;
+                    if (s > m) {
+                        const T r = E::bexp(m - s);
+                        l.tile *= r;
+                        if constexpr (MODE == kSoftmax) {
+    #pragma unroll
+                            for (int c = 0; c < CP; ++c) acc[c] *= r;
+                        }
+                        m = s;
                     }
-                    m = s;
+                    const T pr = s > ninf<T>() ? E::bexp(s - m) : T(0);  // an empty element (-inf) adds 0, not NaN
+                    l.tile += pr;
+                    if constexpr (MODE == kSoftmax) axpy_smem<T, CP>(acc, pr, sv + jj * CP);
+                } else if constexpr (MODE == kDisp) {
+                    axpy_smem<T, DP>(acc, S, q);
+                    mass.tile += S;
+                } else {  // kSvgd: S is the bare rbf kernel value k_ij
+                    axpy_smem<T, DP>(acc, S, sv + jj * DP);
+                    axpy_smem<T, DP>(acc2, S, q);
+                    mass.tile += S;
                 }
-                const T pr = s > ninf<T>() ? E::bexp(s - m) : T(0);  // an empty element (-inf) adds 0, not NaN
-                l.tile += pr;
-                if constexpr (MODE == kSoftmax) axpy_smem<T, CP>(acc, pr, sv + jj * CP);
-            } else if constexpr (MODE == kDisp) {
-                axpy_smem<T, DP>(acc, S, q);
-                mass.tile += S;
-            } else {  // kSvgd: S is the bare rbf kernel value k_ij
-                axpy_smem<T, DP>(acc, S, sv + jj * DP);
-                axpy_smem<T, DP>(acc2, S, q);
-                mass.tile += S;
+            }
+            if constexpr (MODE == kLse || MODE == kSoftmax) {
+                // 0 while the running state is empty (m0 = -inf); 1 when the max did not move (this also
+                // covers a tile with no admitted pair, where both are -inf)
+                const T r = m0 == m ? T(1) : E::bexp(m0 - m);
+                l.flush(r);
+                if constexpr (MODE == kSoftmax) run1.flush(acc, r);
+            } else {
+                if constexpr (VEC_RUN) run1.flush(acc);
+                if constexpr (MODE == kSvgd) run2.flush(acc2);
+                mass.flush();
             }
         }
-        if constexpr (MODE == kLse || MODE == kSoftmax) {
-            // 0 while the running state is empty (m0 = -inf); 1 when the max did not move (this also
-            // covers a tile with no admitted pair, where both are -inf)
-            const T r = m0 == m ? T(1) : E::bexp(m0 - m);
-            l.flush(r);
-            if constexpr (MODE == kSoftmax) run1.flush(acc, r);
-        } else {
-            if constexpr (VEC_RUN) run1.flush(acc);
-            if constexpr (MODE == kSvgd) run2.flush(acc2);
-            mass.flush();
-        }
-    }
+    };
+    if (a.pm) sweep(std::true_type{});
+    else sweep(std::false_type{});
     if (!pvalid) return;
     const T L = l.run, MASS = mass.run;
 
@@ -279,7 +302,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
         for (int c = 0; c < CP; ++c)
             if (c < a.C) out[pi * a.C + c] = run1.get(c);
     } else if constexpr (MODE == kSoftmax) {
-        const T inv = T(1) / L;
+        const T inv = L > T(0) ? T(1) / L : T(0);  // a row with every pair masked returns 0
 #pragma unroll
         for (int c = 0; c < CP; ++c)
             if (c < a.C) out[pi * a.C + c] = run1.get(c) * inv;
@@ -327,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const SweepArgs a) {
             out[pi] = lse;
         } else {
             static_cast<T*>(a.out2)[pi] = lse;
-            const T inv = T(1) / l;
+            const T inv = l > T(0) ? T(1) / l : T(0);  // a row with every pair masked returns 0
             for (int c = 0; c < a.C; ++c) {
                 T s = T(0);
                 for (int sp = 0; sp < a.splits; ++sp) {
@@ -387,6 +410,7 @@ __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
         if (pvalid && a.pb) Cp = static_cast<const T*>(a.pb)[pi];
     }
     const T sgn = a.largest ? T(-1) : T(1);
+    const int og = (a.pm == 3 && pvalid) ? a.pg[pi] : 0;
 
     T kv[K];
     int ki[K];
@@ -396,30 +420,37 @@ __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
         ki[t] = kNoIndex;
     }
     zero_smem(sq, kTile * DP);
-    for (int64_t j0 = jb; j0 < je; j0 += kTile) {
-        const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
-        __syncthreads();
-        stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
-        if constexpr (AFFINE) {
-            stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
-            stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
-        }
-        __syncthreads();
-        if (a.metric != kLinear) {
-            stage_norms<T, DP>(sn, sq, cnt);
+    // the tile loop, compiled once without and once with the pair mask test (chosen per launch)
+    auto sweep = [&](auto masked) {
+        for (int64_t j0 = jb; j0 < je; j0 += kTile) {
+            const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
             __syncthreads();
+            stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
+            if constexpr (AFFINE) {
+                stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
+                stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
+            }
+            __syncthreads();
+            if (a.metric != kLinear) {
+                stage_norms<T, DP>(sn, sq, cnt);
+                __syncthreads();
+            }
+    #pragma unroll 4
+            for (int jj = 0; jj < cnt; ++jj) {
+                if constexpr (decltype(masked)::value)
+                    if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair is never selected
+                const T dot = dot_regs_smem<T, DP>(p, sq + jj * DP);
+                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                T t;
+                if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
+                else t = A * base;
+                const T S = a.apply_exp ? E::exp(t) : t;
+                topk_insert<T, K>(kv, ki, sgn * S, (int)(j0 + jj));
+            }
         }
-#pragma unroll 4
-        for (int jj = 0; jj < cnt; ++jj) {
-            const T dot = dot_regs_smem<T, DP>(p, sq + jj * DP);
-            const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
-            T t;
-            if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
-            else t = A * base;
-            const T S = a.apply_exp ? E::exp(t) : t;
-            topk_insert<T, K>(kv, ki, sgn * S, (int)(j0 + jj));
-        }
-    }
+    };
+    if (a.pm) sweep(std::true_type{});
+    else sweep(std::false_type{});
     if (!pvalid) return;
     if (a.splits > 1) {
         T* wv = static_cast<T*>(a.ws);
@@ -440,7 +471,7 @@ __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
     for (int t = 0; t < K; ++t)
         if (t < a.k) {
             vals[pi * a.k + t] = sgn * kv[t];
-            idx[pi * a.k + t] = ki[t];
+            idx[pi * a.k + t] = ki[t] == kNoIndex ? -1 : ki[t];  // fewer than k kept pairs: (+-inf, -1)
         }
 }
 
@@ -469,7 +500,7 @@ __global__ void __launch_bounds__(kThreads) topk_merge(const SweepArgs a) {
     for (int t = 0; t < K; ++t)
         if (t < a.k) {
             vals[pi * a.k + t] = sgn * kv[t];
-            idx[pi * a.k + t] = ki[t];
+            idx[pi * a.k + t] = ki[t] == kNoIndex ? -1 : ki[t];  // fewer than k kept pairs: (+-inf, -1)
         }
 }
 
@@ -543,6 +574,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
     T wp = T(1), bp = T(0);
     if (pvalid && a.pw) wp = static_cast<const T*>(a.pw)[pi];
     if (pvalid && a.pb) bp = static_cast<const T*>(a.pb)[pi];
+    const int og = (a.pm == 3 && pvalid) ? a.pg[pi] : 0;
     const T A = scale * wp;
     const bool affine = a.affine != 0;
 
@@ -589,92 +621,99 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
     zero_smem(sq, kTile * DP);
     if constexpr (HAS_QV) zero_smem(sv, kTile * QVW);
 
-    for (int64_t j0 = jb; j0 < je; j0 += kTile) {
-        const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
-        __syncthreads();
-        stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
-        if constexpr (HAS_QV)
-            stage_rows<T, QVW>(sv, static_cast<const T*>(a.Vq), j0, cnt, MODE == kBDisp ? a.D : a.C, a.vecV);
-        stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
-        stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
-        if constexpr (QSTAT) {
-            for (int e = threadIdx.x; e < cnt; e += kThreads) {
-                s1[e] = static_cast<const T*>(a.lse)[j0 + e] * E::kLogB;
-                s2[e] = MODE == kBSoftmax ? static_cast<const T*>(a.delta)[j0 + e]
-                                          : static_cast<const T*>(a.glse)[j0 + e];
+    // the tile loop, compiled once without and once with the pair mask test (chosen per launch)
+    auto sweep = [&](auto masked) {
+        for (int64_t j0 = jb; j0 < je; j0 += kTile) {
+            const int cnt = (int)(je - j0 < (int64_t)kTile ? je - j0 : (int64_t)kTile);
+            __syncthreads();
+            stage_rows<T, DP>(sq, Q, j0, cnt, a.D, a.vecQ);
+            if constexpr (HAS_QV)
+                stage_rows<T, QVW>(sv, static_cast<const T*>(a.Vq), j0, cnt, MODE == kBDisp ? a.D : a.C, a.vecV);
+            stage_scalar<T>(sw, static_cast<const T*>(a.qw), j0, cnt, T(1));
+            stage_scalar<T>(sb, static_cast<const T*>(a.qb), j0, cnt, T(0));
+            if constexpr (QSTAT) {
+                for (int e = threadIdx.x; e < cnt; e += kThreads) {
+                    s1[e] = static_cast<const T*>(a.lse)[j0 + e] * E::kLogB;
+                    s2[e] = MODE == kBSoftmax ? static_cast<const T*>(a.delta)[j0 + e]
+                                              : static_cast<const T*>(a.glse)[j0 + e];
+                }
             }
-        }
-        __syncthreads();
-        if (a.metric != kLinear) stage_norms<T, DP>(sn, sq, cnt);
-        if constexpr (SIDE == kCol && MODE == kBDisp) {
-            for (int r = threadIdx.x; r < cnt; r += kThreads) {
-                T c0 = T(0);
-                for (int d = 0; d < DP; ++d) c0 = fma(sv[r * QVW + d], sq[r * DP + d], c0);
-                s1[r] = c0;
+            __syncthreads();
+            if (a.metric != kLinear) stage_norms<T, DP>(sn, sq, cnt);
+            if constexpr (SIDE == kCol && MODE == kBDisp) {
+                for (int r = threadIdx.x; r < cnt; r += kThreads) {
+                    T c0 = T(0);
+                    for (int d = 0; d < DP; ++d) c0 = fma(sv[r * QVW + d], sq[r * DP + d], c0);
+                    s1[r] = c0;
+                }
             }
-        }
-        __syncthreads();
-#pragma unroll 2
-        for (int jj = 0; jj < cnt; ++jj) {
-            const T* q = sq + jj * DP;
-            const T dot = dot_regs_smem<T, DP>(p, q);
-            const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
-            const T wq = sw[jj];
-            const T t = affine ? fma(A * wq, base, bp + sb[jj]) : A * base;
-            const T S = a.apply_exp ? E::exp(t) : t;
-            T G = T(0), Pw = S;
-            if constexpr (MODE == kBMatmul) {
-                if constexpr (DO_G) G = dot_regs_smem<T, CP>(pv, sv + jj * CP);
-            } else if constexpr (MODE == kBSoftmax) {
-                const T lse_b = SIDE == kRow ? plse : s1[jj];
-                Pw = E::bexp(S * E::kLogB - lse_b);
+            __syncthreads();
+    #pragma unroll 2
+            for (int jj = 0; jj < cnt; ++jj) {
+                if constexpr (decltype(masked)::value)
+                    if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair has no gradient
+                const T* q = sq + jj * DP;
+                const T dot = dot_regs_smem<T, DP>(p, q);
+                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                const T wq = sw[jj];
+                const T t = affine ? fma(A * wq, base, bp + sb[jj]) : A * base;
+                const T S = a.apply_exp ? E::exp(t) : t;
+                T G = T(0), Pw = S;
+                if constexpr (MODE == kBMatmul) {
+                    if constexpr (DO_G) G = dot_regs_smem<T, CP>(pv, sv + jj * CP);
+                } else if constexpr (MODE == kBSoftmax) {
+                    const T lse_b = SIDE == kRow ? plse : s1[jj];
+                    Pw = E::bexp(S * E::kLogB - lse_b);
+                    if constexpr (DO_G) {
+                        const T dl = SIDE == kRow ? pstat : s2[jj];
+                        G = Pw * (dot_regs_smem<T, CP>(pv, sv + jj * CP) - dl);
+                    }
+                } else if constexpr (MODE == kBLse) {
+                    const T lse_b = SIDE == kRow ? plse : s1[jj];
+                    const T g = SIDE == kRow ? pstat : s2[jj];
+                    const bool excluded = a.exclude_self && (j0 + jj == pi);
+                    G = (excluded || !(lse_b > ninf<T>())) ? T(0) : g * E::bexp(S * E::kLogB - lse_b);
+                } else if constexpr (MODE == kBLseSym) {
+                    // the pair seen from row k (this thread) and from row j (the streamed point)
+                    const bool excluded = a.exclude_self && (j0 + jj == pi);
+                    const T sb2 = S * E::kLogB;
+                    const T gk = plse > ninf<T>() ? pstat * E::bexp(sb2 - plse) : T(0);
+                    const T gj = s1[jj] > ninf<T>() ? s2[jj] * E::bexp(sb2 - s1[jj]) : T(0);
+                    G = excluded ? T(0) : gk + gj;
+                } else {  // kBDisp
+                    if constexpr (SIDE == kRow) {
+                        G = dot_regs_smem<T, DP>(pv, q) - pstat;
+                        sumS.tile += S;
+                    } else {
+                        const T* dO = sv + jj * DP;
+                        G = dot_regs_smem<T, DP>(p, dO) - s1[jj];
+                        axpy_smem<T, DP>(Kd, S, dO);
+                    }
+                }
+                if constexpr (DO_V) axpy_smem<T, CP>(KdV, Pw, sv + jj * CP);
                 if constexpr (DO_G) {
-                    const T dl = SIDE == kRow ? pstat : s2[jj];
-                    G = Pw * (dot_regs_smem<T, CP>(pv, sv + jj * CP) - dl);
-                }
-            } else if constexpr (MODE == kBLse) {
-                const T lse_b = SIDE == kRow ? plse : s1[jj];
-                const T g = SIDE == kRow ? pstat : s2[jj];
-                const bool excluded = a.exclude_self && (j0 + jj == pi);
-                G = (excluded || !(lse_b > ninf<T>())) ? T(0) : g * E::bexp(S * E::kLogB - lse_b);
-            } else if constexpr (MODE == kBLseSym) {
-                // the pair seen from row k (this thread) and from row j (the streamed point)
-                const bool excluded = a.exclude_self && (j0 + jj == pi);
-                const T sb2 = S * E::kLogB;
-                const T gk = plse > ninf<T>() ? pstat * E::bexp(sb2 - plse) : T(0);
-                const T gj = s1[jj] > ninf<T>() ? s2[jj] * E::bexp(sb2 - s1[jj]) : T(0);
-                G = excluded ? T(0) : gk + gj;
-            } else {  // kBDisp
-                if constexpr (SIDE == kRow) {
-                    G = dot_regs_smem<T, DP>(pv, q) - pstat;
-                    sumS.tile += S;
-                } else {
-                    const T* dO = sv + jj * DP;
-                    G = dot_regs_smem<T, DP>(p, dO) - s1[jj];
-                    axpy_smem<T, DP>(Kd, S, dO);
+                    const T H = a.apply_exp ? G * S : G;
+                    sumH.tile += H;
+                    if (affine) sumHw.tile = fma(H * scale * wq, base, sumHw.tile);
+                    const T Ev = H * A * wq;
+                    const T kappa = a.metric == kLinear ? Ev : (a.metric == kSqeuclidean ? T(-2) * Ev : T(-2) * neg_gamma * Ev * base);
+                    K0.tile += kappa;
+                    axpy_smem<T, DP>(K1, kappa, q);
                 }
             }
-            if constexpr (DO_V) axpy_smem<T, CP>(KdV, Pw, sv + jj * CP);
             if constexpr (DO_G) {
-                const T H = a.apply_exp ? G * S : G;
-                sumH.tile += H;
-                if (affine) sumHw.tile = fma(H * scale * wq, base, sumHw.tile);
-                const T Ev = H * A * wq;
-                const T kappa = a.metric == kLinear ? Ev : (a.metric == kSqeuclidean ? T(-2) * Ev : T(-2) * neg_gamma * Ev * base);
-                K0.tile += kappa;
-                axpy_smem<T, DP>(K1, kappa, q);
+                rK1.flush(K1);
+                K0.flush();
+                sumH.flush();
+                sumHw.flush();
+                sumS.flush();
             }
+            if constexpr (SM::NKD > 0) rKd.flush(Kd);
+            if constexpr (DO_V) rKV.flush(KdV);
         }
-        if constexpr (DO_G) {
-            rK1.flush(K1);
-            K0.flush();
-            sumH.flush();
-            sumHw.flush();
-            sumS.flush();
-        }
-        if constexpr (SM::NKD > 0) rKd.flush(Kd);
-        if constexpr (DO_V) rKV.flush(KdV);
-    }
+    };
+    if (a.pm) sweep(std::true_type{});
+    else sweep(std::false_type{});
     if (!pvalid) return;
 
     if (a.splits > 1) {

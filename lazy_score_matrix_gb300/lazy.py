@@ -21,6 +21,7 @@ from typing import Optional
 import torch
 
 from . import ops
+from .masks import PairMask
 from .ops import Score
 
 TopK = namedtuple("TopK", ["values", "indices"])
@@ -32,9 +33,13 @@ class _Meta:
     gamma: float
     scale: float
     apply_exp: bool
+    pair: Optional[PairMask] = None
 
     def score(self, rb, cb, rw, cw) -> Score:
-        return Score(self.metric, self.gamma, self.scale, self.apply_exp, rb, cb, rw, cw)
+        if self.pair is None:
+            return Score(self.metric, self.gamma, self.scale, self.apply_exp, rb, cb, rw, cw)
+        return Score(self.metric, self.gamma, self.scale, self.apply_exp, rb, cb, rw, cw, self.pair.kind,
+                     self.pair.width, self.pair.row_group, self.pair.col_group)
 
 
 def _unsupported(what: str):
@@ -124,8 +129,19 @@ class LazyScores:
         points; the row and column parameters trade places."""
         o = self._with(row_bias=self.col_bias, col_bias=self.row_bias, row_weight=self.col_weight,
                        col_weight=self.row_weight)
+        if self._meta.pair is not None:
+            o._meta = replace(self._meta, pair=self._meta.pair.transposed())
         o.X, o.Y = self.Y, self.X
         return o
+
+    def mask_pairs(self, mask: PairMask) -> "LazyScores":
+        """Remove the pairs a pair mask (``masks.causal()``, ``masks.band(w)``, ``masks.same_group(g)``)
+        masks from every consumer of this score (Task Map: softmax_matmul with mask=...)."""
+        if not isinstance(mask, PairMask):
+            raise TypeError("mask_pairs expects a masks.PairMask")
+        if self._meta.pair is not None:
+            _unsupported("a second pair mask")
+        return self._with(meta=replace(self._meta, pair=mask))
 
     def mask_columns(self, keep: torch.Tensor) -> "LazyScores":
         """Boolean column mask ("Score Expressions": boolean row/column masks stay fused): columns with
@@ -220,9 +236,9 @@ class LazyScores:
         return _LseFn.apply(e.X, e.Y, *e._params(), e._meta, bool(exclude_self))
 
     def softmax_matmul(self, V: torch.Tensor, mask=None) -> torch.Tensor:
-        """out_i = sum_j softmax_j(S_ij) V_j ("Task Map", attention; fused without a pair mask)."""
+        """out_i = sum_j softmax_j(S_ij) V_j ("Task Map", attention), over the pairs a pair mask keeps."""
         if mask is not None:
-            _unsupported("a pair mask")
+            return self.mask_pairs(mask).softmax_matmul(V)
         e = self._masked("lse")
         return _SoftmaxFn.apply(e.X, e.Y, V, *e._params(), e._meta)
 

@@ -20,7 +20,9 @@ _DT = {torch.float32: _lib.TP_F32, torch.float64: _lib.TP_F64}
 @dataclass
 class Score:
     """The canonical score: base (metric), then scale * w_row * w_col * base + b_row + b_col, then
-    an optional exp (torchpairwise guide "Score Expressions")."""
+    an optional exp (torchpairwise guide "Score Expressions"); optionally a pair mask ("all",
+    "causal": j <= i, "band": |i - j| <= band, "same_group": row_group[i] == col_group[j], int32 ids)
+    whose masked pairs leave the consumer's reduction."""
     metric: str = "linear"
     gamma: float = 1.0
     scale: float = 1.0
@@ -29,6 +31,10 @@ class Score:
     col_bias: Optional[torch.Tensor] = None
     row_weight: Optional[torch.Tensor] = None
     col_weight: Optional[torch.Tensor] = None
+    pair_mask: str = "all"
+    band: int = 0
+    row_group: Optional[torch.Tensor] = None
+    col_group: Optional[torch.Tensor] = None
 
     def params(self):
         return (self.row_bias, self.col_bias, self.row_weight, self.col_weight)
@@ -79,13 +85,21 @@ class _Call:
         self.cb = _contig(score.col_bias, self.dtype, "col_bias", (self.M,))
         self.rw = _contig(score.row_weight, self.dtype, "row_weight", (self.N,))
         self.cw = _contig(score.col_weight, self.dtype, "col_weight", (self.M,))
-        self.device = _need_cuda(self.X, self.Y, self.rb, self.cb, self.rw, self.cw)
+        if score.pair_mask not in _lib.PAIR_MASKS:
+            raise ValueError(f"unknown pair mask {score.pair_mask!r}")
+        groups = score.pair_mask == "same_group"
+        self.rg = _contig(score.row_group, torch.int32, "row_group", (self.N,)) if groups else None
+        self.cg = _contig(score.col_group, torch.int32, "col_group", (self.M,)) if groups else None
+        if groups and (self.rg is None or self.cg is None):
+            raise ValueError("a same_group mask needs row_group [N] and col_group [M]")
+        self.device = _need_cuda(self.X, self.Y, self.rb, self.cb, self.rw, self.cw, self.rg, self.cg)
         if score.metric not in _lib.METRICS:
             raise ValueError(f"unknown metric {score.metric!r}")
         self.pairs = _lib.tp_pairs(_DT[self.dtype], self.N, self.M, self.D, self.X.data_ptr(), self.Y.data_ptr())
         self.score = _lib.tp_score(_lib.METRICS[score.metric], float(score.gamma), float(score.scale),
                                    int(bool(score.apply_exp)), _ptr(self.rb), _ptr(self.cb), _ptr(self.rw),
-                                   _ptr(self.cw))
+                                   _ptr(self.cw), _lib.PAIR_MASKS[score.pair_mask], int(score.band),
+                                   _ptr(self.rg), _ptr(self.cg))
         self.gamma = float(score.gamma)
         self.lib = _lib.load()
         self.stream = ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)

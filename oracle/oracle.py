@@ -46,7 +46,12 @@ class _Score(ctypes.Structure):
     _fields_ = [("metric", ctypes.c_int), ("gamma", ctypes.c_double), ("scale", ctypes.c_double),
                 ("apply_exp", ctypes.c_int),
                 ("row_bias", ctypes.c_void_p), ("col_bias", ctypes.c_void_p),
-                ("row_weight", ctypes.c_void_p), ("col_weight", ctypes.c_void_p)]
+                ("row_weight", ctypes.c_void_p), ("col_weight", ctypes.c_void_p),
+                ("pair_mask", ctypes.c_int), ("band", ctypes.c_int64),
+                ("row_group", ctypes.c_void_p), ("col_group", ctypes.c_void_p)]
+
+
+PAIR_MASKS = {"all": 0, "causal": 1, "band": 2, "same_group": 3}
 
 
 class _Pairs(ctypes.Structure):
@@ -112,7 +117,8 @@ class Problem:
     """fp64 copies of X, Y and the score parameters, kept alive for the C calls."""
 
     def __init__(self, X, Y, metric="linear", gamma=1.0, scale=1.0, apply_exp=False,
-                 row_bias=None, col_bias=None, row_weight=None, col_weight=None):
+                 row_bias=None, col_bias=None, row_weight=None, col_weight=None,
+                 pair_mask="all", band=0, row_group=None, col_group=None):
         self.X = _f64(X)
         self.Y = _f64(Y)
         if self.X.ndim != 2 or self.Y.ndim != 2 or self.X.shape[1] != self.Y.shape[1]:
@@ -121,8 +127,15 @@ class Problem:
         self.M = self.Y.shape[0]
         self.rb, self.cb = _f64(row_bias), _f64(col_bias)
         self.rw, self.cw = _f64(row_weight), _f64(col_weight)
+        # pair masks ("Score Expressions": tp.masks causal, band, same_group), group ids as int32
+        self.rg = None if row_group is None else np.ascontiguousarray(np.asarray(row_group), dtype=np.int32)
+        self.cg = None if col_group is None else np.ascontiguousarray(np.asarray(col_group), dtype=np.int32)
+        if pair_mask == "same_group" and (self.rg is None or self.cg is None):
+            raise ValueError("same_group needs row_group and col_group")
+        gp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
         self.score = _Score(METRICS[metric], float(gamma), float(scale), int(bool(apply_exp)),
-                            _ptr(self.rb), _ptr(self.cb), _ptr(self.rw), _ptr(self.cw))
+                            _ptr(self.rb), _ptr(self.cb), _ptr(self.rw), _ptr(self.cw),
+                            PAIR_MASKS[pair_mask], int(band), gp(self.rg), gp(self.cg))
         self.pairs = _Pairs(_ptr(self.X), _ptr(self.Y), self.N, self.M, self.D)
 
     def _args(self):
@@ -179,9 +192,10 @@ def svgd_direction(x, score, gamma, y=None):
 def topk(pb: Problem, k, largest=False):
     vals = np.zeros((pb.N, k))
     idx = np.zeros((pb.N, k), dtype=np.int64)
-    _check(_load().or_topk(*pb._args(), int(k), int(bool(largest)), _ptr(vals), _ptr(idx)), "topk")
-    if (idx < 0).any():
+    rc = _load().or_topk(*pb._args(), int(k), int(bool(largest)), _ptr(vals), _ptr(idx))
+    if rc == 2:
         raise MemoryError("oracle topk ran out of host memory")
+    _check(rc, "topk")
     return vals, idx
 
 

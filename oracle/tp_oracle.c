@@ -14,6 +14,10 @@
  *     with exclude_self (InfoNCE row), topk(k, largest=False) with exact tie order (k-NN row).
  *   - "Stein Variational Gradient Descent": the rbf kernel exp(-gamma |x-y|^2), its displacement
  *     sum_j k_ij (x_j - x_i), and the SVGD direction.
+ *   - "Score Expressions" and "Task Map": pair masks tp.masks causal, band, same_group. Read here as
+ *     removing the masked pairs from the consumer: no term in a sum, log-sum-exp or softmax, never
+ *     selected by top-k (a row with fewer than k kept pairs pads with value +-inf and index -1), no
+ *     gradient; a softmax row with no kept pair is 0.
  *
  * Score, in one fixed order (the reading adopted for the expression nodes the guide calls fused):
  *   base = |x-y|^2 (sqeuclidean) | x.y (linear) | exp(-gamma |x-y|^2) (rbf)
@@ -42,13 +46,31 @@
 #define OR_LINEAR 1
 #define OR_RBF 2
 
+#define OR_PAIRS_ALL 0
+#define OR_PAIRS_CAUSAL 1     /* keep j <= i */
+#define OR_PAIRS_BAND 2       /* keep |i - j| <= band */
+#define OR_PAIRS_SAME_GROUP 3 /* keep row_group[i] == col_group[j] */
+
 typedef struct {
     int metric;
     double gamma;
     double scale;
     int apply_exp;
     const double *row_bias, *col_bias, *row_weight, *col_weight; /* [N] / [M] or NULL */
+    int pair_mask;
+    int64_t band;
+    const int32_t *row_group, *col_group; /* [N] / [M], same-group masks only */
 } or_score;
+
+/* whether the pair (i, j) stays in the consumer under the score's pair mask */
+static int pair_kept(const or_score *s, int64_t i, int64_t j) {
+    switch (s->pair_mask) {
+    case OR_PAIRS_CAUSAL: return j <= i;
+    case OR_PAIRS_BAND: return llabs(i - j) <= s->band;
+    case OR_PAIRS_SAME_GROUP: return s->row_group[i] == s->col_group[j];
+    default: return 1;
+    }
+}
 
 typedef struct {
     const double *X, *Y; /* [N,D], [M,D] row-major */
@@ -203,6 +225,7 @@ typedef struct {
     int exclude_self;
     int k, largest;
     int64_t *idx;
+    volatile int failed;
     const double *aux0, *aux1, *aux2, *aux3;
     double *g0, *g1, *g2, *g3, *g4;
 } or_ctx;
@@ -213,6 +236,7 @@ static void matmul_row(void *c_, int64_t i) {
     double *o = c->out + i * c->C;
     for (int64_t cc = 0; cc < c->C; ++cc) o[cc] = 0.0;
     for (int64_t j = 0; j < c->p->M; ++j) {
+        if (!pair_kept(c->s, i, j)) continue;
         double S = pair_eval(c->s, c->p, i, j).S;
         for (int64_t cc = 0; cc < c->C; ++cc) o[cc] += S * c->V[j * c->C + cc];
     }
@@ -229,14 +253,14 @@ int or_matmul(const or_pairs *p, const or_score *s, const double *V, int64_t C, 
 static double row_lse(const or_score *s, const or_pairs *p, int64_t i, int exclude_self) {
     double m = -INFINITY;
     for (int64_t j = 0; j < p->M; ++j) {
-        if (exclude_self && j == i) continue;
+        if ((exclude_self && j == i) || !pair_kept(s, i, j)) continue;
         double S = pair_eval(s, p, i, j).S;
         if (S > m) m = S;
     }
     if (m == -INFINITY) return -INFINITY;
     double sum = 0.0;
     for (int64_t j = 0; j < p->M; ++j) {
-        if (exclude_self && j == i) continue;
+        if ((exclude_self && j == i) || !pair_kept(s, i, j)) continue;
         sum += exp(pair_eval(s, p, i, j).S - m);
     }
     return m + log(sum);
@@ -262,7 +286,8 @@ static void softmax_row(void *c_, int64_t i) {
     double l = row_lse(c->s, c->p, i, 0);
     double *o = c->out + i * c->C;
     for (int64_t cc = 0; cc < c->C; ++cc) o[cc] = 0.0;
-    for (int64_t j = 0; j < c->p->M; ++j) {
+    for (int64_t j = 0; j < c->p->M && l > -INFINITY; ++j) {
+        if (!pair_kept(c->s, i, j)) continue;
         double P = exp(pair_eval(c->s, c->p, i, j).S - l);
         for (int64_t cc = 0; cc < c->C; ++cc) o[cc] += P * c->V[j * c->C + cc];
     }
@@ -284,6 +309,7 @@ static void disp_row(void *c_, int64_t i) {
     double *o = c->out + i * p->D;
     for (int64_t d = 0; d < p->D; ++d) o[d] = 0.0;
     for (int64_t j = 0; j < p->M; ++j) {
+        if (!pair_kept(c->s, i, j)) continue;
         double S = pair_eval(c->s, p, i, j).S;
         for (int64_t d = 0; d < p->D; ++d) o[d] += S * (p->Y[j * p->D + d] - p->X[i * p->D + d]);
     }
@@ -350,19 +376,27 @@ static void topk_row(void *c_, int64_t i) {
     or_ctx *c = (or_ctx *)c_;
     const or_pairs *p = c->p;
     or_kv *buf = (or_kv *)malloc(sizeof(or_kv) * (size_t)p->M);
-    if (!buf) { /* out of host memory: mark the row so the caller sees it */
-        for (int t = 0; t < c->k; ++t) c->idx[i * c->k + t] = -1;
+    if (!buf) { /* out of host memory: the caller sees the flag */
+        c->failed = 1;
         return;
     }
+    int64_t n = 0;
     for (int64_t j = 0; j < p->M; ++j) {
+        if (!pair_kept(c->s, i, j)) continue;
         double S = pair_eval(c->s, p, i, j).S;
-        buf[j].key = c->largest ? -S : S;
-        buf[j].j = j;
+        buf[n].key = c->largest ? -S : S;
+        buf[n].j = j;
+        ++n;
     }
-    qsort(buf, (size_t)p->M, sizeof(or_kv), kv_cmp);
+    qsort(buf, (size_t)n, sizeof(or_kv), kv_cmp);
     for (int t = 0; t < c->k; ++t) {
-        c->out[i * c->k + t] = c->largest ? -buf[t].key : buf[t].key;
-        c->idx[i * c->k + t] = buf[t].j;
+        if (t < n) {
+            c->out[i * c->k + t] = c->largest ? -buf[t].key : buf[t].key;
+            c->idx[i * c->k + t] = buf[t].j;
+        } else { /* fewer kept pairs than k */
+            c->out[i * c->k + t] = c->largest ? -INFINITY : INFINITY;
+            c->idx[i * c->k + t] = -1;
+        }
     }
     free(buf);
 }
@@ -373,7 +407,7 @@ int or_topk(const or_pairs *p, const or_score *s, int k, int largest, double *va
     or_ctx c = {0};
     c.p = p; c.s = s; c.k = k; c.largest = largest; c.out = values; c.idx = indices;
     or_parallel_for(p->N, topk_row, &c);
-    return 0;
+    return c.failed ? 2 : 0;
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -434,6 +468,7 @@ static void bwd_row(void *b_, int64_t i) {
     if (gx)
         for (int64_t d = 0; d < p->D; ++d) gx[d] = 0.0;
     for (int64_t j = 0; j < p->M; ++j) {
+        if (!pair_kept(b->s, i, j)) continue;
         or_pair_val v = pair_eval(b->s, p, i, j);
         double G = consumer_G(b, i, j, v.S);
         pair_chain(b->s, p, i, j, v, G, gx, NULL, &gbr, &gwr, NULL, NULL);
@@ -455,6 +490,7 @@ static void bwd_col(void *b_, int64_t j) {
     if (gv)
         for (int64_t c = 0; c < b->C; ++c) gv[c] = 0.0;
     for (int64_t i = 0; i < p->N; ++i) {
+        if (!pair_kept(b->s, i, j)) continue;
         or_pair_val v = pair_eval(b->s, p, i, j);
         double G = consumer_G(b, i, j, v.S);
         pair_chain(b->s, p, i, j, v, G, NULL, gy, NULL, NULL, &gbc, &gwc);
@@ -555,6 +591,7 @@ int or_topk_backward(const or_pairs *p, const or_score *s, int k, const int64_t 
     for (int64_t i = 0; i < p->N; ++i) {
         for (int t = 0; t < k; ++t) {
             int64_t j = indices[i * k + t];
+            if (j == -1) continue; /* a padding place (fewer kept pairs than k): no gradient */
             if (j < 0 || j >= p->M) return 1;
             or_pair_val v = pair_eval(s, p, i, j);
             pair_chain(s, p, i, j, v, grad_values[i * k + t], dX ? dX + i * p->D : NULL,

@@ -1,0 +1,146 @@
+"""GPU parity of pair masks (causal, band, same_group) on every consumer, forward and backward, against
+the oracle (torchpairwise guide "Using Torchpairwise in Models", Score Expressions and Task Map:
+softmax_matmul(V, mask=tp.masks.causal()), band, same_group). Masked pairs leave the reduction; the
+masks run inside the streamed sweeps."""
+import numpy as np
+import pytest
+import torch
+
+import lazy_score_matrix_gb300 as tp
+from lazy_score_matrix_gb300 import ops
+from lazy_score_matrix_gb300.ops import Score
+from tests._util import STRESS_FLOOR, TOL_F32_FWD, TOL_F32_GRAD, TOL_F64, assert_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+SHAPES = {"split": (300, 517, 16, 8), "square": (260, 260, 7, 5), "one_split": (130, 40, 16, 5)}
+MASKS = ["causal", "band", "same_group"]
+
+
+def _gen(seed, shape, dtype):
+    return torch.randn(*shape, generator=torch.Generator().manual_seed(seed), dtype=dtype)
+
+
+def _setup(shape, dtype, kind, metric="linear", seed=0):
+    N, M, D, C = SHAPES[shape]
+    X, Y, V = _gen(seed + 1, (N, D), dtype), _gen(seed + 2, (M, D), dtype), _gen(seed + 3, (M, C), dtype)
+    g = torch.Generator().manual_seed(seed + 4)
+    rg = torch.randint(0, 5, (N,), generator=g, dtype=torch.int32)
+    cg = torch.randint(0, 5, (M,), generator=g, dtype=torch.int32)
+    rg[3] = 9  # a row no column shares a group with
+    scale = (-0.5 if metric == "sqeuclidean" else 0.5) / D ** 0.5
+    sc = dict(metric=metric, gamma=0.5 / D, scale=scale if metric != "rbf" else 0.8)
+    mask = dict(pair_mask=kind, band=17)
+    gpu = Score(**sc, **mask, row_group=rg.to(DEV) if kind == "same_group" else None,
+                col_group=cg.to(DEV) if kind == "same_group" else None)
+    pb_kw = dict(**sc, **mask, row_group=rg.numpy(), col_group=cg.numpy())
+    return X, Y, V, gpu, pb_kw
+
+
+def _tols(dtype):
+    return (TOL_F64, TOL_F64) if dtype == torch.float64 else (TOL_F32_FWD, TOL_F32_GRAD)
+
+
+def _grads(got, want, tol, what):
+    for k in ("dX", "dY", "dV"):
+        if got.get(k) is not None and want.get(k) is not None:
+            assert_close(got[k], want[k], tol, f"{what} {k}", STRESS_FLOOR)
+
+
+CASES = [(s, d, k) for s in SHAPES for d in (torch.float32, torch.float64) for k in MASKS]
+
+
+def _id(c):
+    return f"{c[0]}-{str(c[1])[6:]}-{c[2]}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_masked_logsumexp_and_softmax(oracle, case):
+    shape, dt, kind = case
+    X, Y, V, sc, kw = _setup(shape, dt, kind)
+    ftol, gtol = _tols(dt)
+    pb = oracle.Problem(X, Y, **kw)
+    Xd, Yd, Vd = X.to(DEV), Y.to(DEV), V.to(DEV)
+    lse = ops.pairwise_logsumexp(Xd, Yd, sc)
+    assert_close(lse, oracle.logsumexp(pb), ftol, "lse", STRESS_FLOOR)
+    gl = _gen(7, (X.shape[0],), dt)
+    g = ops.pairwise_logsumexp_backward(Xd, Yd, sc, lse, gl.to(DEV))
+    _grads(g, oracle.logsumexp_backward(pb, lse.double().cpu().numpy(), gl), gtol, "lse")
+    out, l2 = ops.pairwise_softmax_matmul(Xd, Yd, Vd, sc)
+    oo, ol = oracle.softmax_matmul(pb, V)
+    assert_close(out, oo, ftol, "softmax out", STRESS_FLOOR)
+    G = _gen(8, out.shape, dt)
+    g = ops.pairwise_softmax_matmul_backward(Xd, Yd, Vd, sc, out, l2, G.to(DEV))
+    _grads(g, oracle.softmax_matmul_backward(pb, V, out.double().cpu().numpy(), l2.double().cpu().numpy(), G),
+           gtol, "softmax")
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_masked_matmul_and_displacement(oracle, case):
+    shape, dt, kind = case
+    X, Y, V, sc, kw = _setup(shape, dt, kind, metric="rbf")
+    ftol, gtol = _tols(dt)
+    pb = oracle.Problem(X, Y, **kw)
+    Xd, Yd, Vd = X.to(DEV), Y.to(DEV), V.to(DEV)
+    assert_close(ops.pairwise_matmul(Xd, Yd, Vd, sc), oracle.matmul(pb, V), ftol, "K@V", STRESS_FLOOR)
+    G = _gen(9, (X.shape[0], V.shape[1]), dt)
+    _grads(ops.pairwise_matmul_backward(Xd, Yd, Vd, sc, G.to(DEV)), oracle.matmul_backward(pb, V, G), gtol, "K@V")
+    assert_close(ops.pairwise_displacement(Xd, Yd, sc), oracle.displacement(pb), ftol, "disp", STRESS_FLOOR)
+    Gd = _gen(10, X.shape, dt)
+    _grads(ops.pairwise_displacement_backward(Xd, Yd, sc, Gd.to(DEV)), oracle.displacement_backward(pb, Gd),
+           gtol, "disp")
+
+
+@pytest.mark.parametrize("kind", MASKS)
+@pytest.mark.parametrize("shape", ["split", "square"])
+def test_masked_topk_exact(oracle, kind, shape):
+    N, M, D, _ = SHAPES[shape]
+    g = torch.Generator().manual_seed(11)
+    X = torch.randint(-4, 5, (N, D), generator=g).float()
+    Y = torch.randint(-4, 5, (M, D), generator=g).float()
+    _, _, _, sc, kw = _setup(shape, torch.float32, kind, metric="sqeuclidean")
+    sc.scale, kw["scale"] = 1.0, 1.0
+    v, i = ops.pairwise_topk(X.to(DEV), Y.to(DEV), sc, 24, False)
+    ov, oi = oracle.topk(oracle.Problem(X, Y, **kw), 24, False)
+    assert np.array_equal(i.cpu().numpy(), oi)
+    assert np.array_equal(v.cpu().double().numpy(), ov)
+
+
+def test_causal_self_attention_lazy_autograd(oracle):
+    # attention shape (D = C = 64, fp32): a pair mask routes it to the streamed SIMT sweeps
+    X0, V0 = _gen(21, (200, 64), torch.float32), _gen(22, (200, 64), torch.float32)
+    X = X0.to(DEV).requires_grad_()
+    V = V0.to(DEV).requires_grad_()
+    out = (tp.lazy(X, X, "linear") * 0.125).softmax_matmul(V, mask=tp.masks.causal())
+    G = _gen(23, out.shape, torch.float32)
+    (out * G.to(DEV)).sum().backward()
+    pb = oracle.Problem(X0, X0, metric="linear", scale=0.125, pair_mask="causal")
+    oo, _ = oracle.softmax_matmul(pb, V0)
+    assert_close(out, oo, TOL_F32_FWD, "out")
+    # the backward's inputs as the lazy forward saved them (the entry is deterministic)
+    o2, l2 = ops.pairwise_softmax_matmul(X.detach(), X.detach(), V.detach(),
+                                         Score("linear", scale=0.125, pair_mask="causal"))
+    assert torch.equal(o2, out.detach())
+    og = oracle.softmax_matmul_backward(pb, V0, o2.double().cpu().numpy(), l2.double().cpu().numpy(), G)
+    # the same points on both sides put |x|^2/8 ~ 8 on the diagonal against ~N(0, 1) off it, so the
+    # early causal rows hold nearly all their mass on the self pair and dS = P (dP - delta) cancels to
+    # ~1e-3 of its terms there: fp32 arithmetic with per-pair dot products on these exact inputs reaches
+    # 4.7e-4 at the 1e-3 floor (6.1e-4 without the mask) and 9e-5 at the 1e-2 floor, which this uses
+    assert_close(X.grad, og["dX"] + og["dY"], TOL_F32_GRAD, "dX summed", floor_frac=STRESS_FLOOR)
+    assert_close(V.grad, og["dV"], TOL_F32_GRAD, "dV")
+
+
+def test_same_group_lazy_and_empty_rows():
+    X = _gen(31, (90, 6), torch.float32).to(DEV)
+    Y = _gen(32, (70, 6), torch.float32).to(DEV)
+    rg = torch.arange(90) % 4
+    rg[0] = 11
+    cg = torch.arange(70) % 4
+    L = tp.lazy(X, Y, "linear").mask_pairs(tp.masks.same_group(rg.to(DEV), cg.to(DEV)))
+    lse = L.logsumexp(-1)
+    assert lse[0].item() == float("-inf") and torch.isfinite(lse[1:]).all()
+    out = L.softmax_matmul(torch.ones(70, 2, device=DEV))
+    assert torch.all(out[0] == 0) and torch.allclose(out[1:], torch.ones_like(out[1:]), atol=1e-5)
+    with pytest.raises(NotImplementedError):
+        tp.lazy(X, Y).mask_pairs(tp.masks.causal()).T
