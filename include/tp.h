@@ -148,7 +148,8 @@ TP_API tp_status tp_svgd_direction(const tp_pairs* pairs, double gamma, const vo
 
 /* Row top-k: the k smallest S_ij of each row (largest != 0: the k largest), values [N,k] and
  * indices [N,k] (int64), sorted by value (ascending; descending for largest) and, among equal
- * values, by ascending column index. 1 <= k <= min(M, 128).
+ * values, by ascending column index. 1 <= k <= min(M, 128). Under a pair mask a row with fewer than
+ * k kept pairs fills its tail with value +inf (-inf for largest) and index -1.
  * Guide "Task Map", k-NN / retrieval row: lazy(X, R, "sqeuclidean").topk(k, largest=False), fused,
  * exact tie order; argmin and min are k = 1. */
 TP_API tp_status tp_pairwise_topk(const tp_pairs* pairs, const tp_score* score, int k, int largest,
