@@ -354,6 +354,17 @@ class Attention(Workload):
             h.copy_(g[k], non_blocking=True)
 
 
+class CausalAttention(Attention):
+    """Workload 6: workload 4 under the causal mask (key j <= query i), the attention of the Task Map's
+    softmax_matmul(V, mask=tp.masks.causal()). Pairs are the kept ones, N (N + 1) / 2."""
+
+    def __init__(self, dev):
+        super().__init__(dev)
+        self.name = "causal_attention_softmax_matmul_f32_QKV16384x64_fwd+bwd"
+        self.score = self.ops.Score("linear", scale=self.score.scale, pair_mask="causal")
+        self.pairs = self.N * (self.N + 1) // 2
+
+
 class Svgd(Workload):
     """Workload 5: SVGD direction fp64, x [131072,8], score = -x, rbf gamma 0.1, one fused sweep."""
     dtype = "f64"
@@ -388,7 +399,7 @@ class Svgd(Workload):
         self.phi_h.copy_(phi, non_blocking=True)
 
 
-WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd}
+WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd, 6: CausalAttention}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:

@@ -235,12 +235,13 @@ bool lse_tc_eligible(const tp_pairs* p, const tp_score* s) {
 }
 
 // Tensor-core attention: softmax_matmul and its backward for fp32, D = C = 64, a linear score without
-// exp or row/column parameters, 16-byte aligned rows.
+// exp or row/column parameters, 16-byte aligned rows, no pair mask or an index mask (causal, band: the
+// epilogues test the pair's indices; same-group masks stay on the streamed sweeps).
 constexpr bool kTcAttention = true;
 bool attn_tc_shape(const tp_pairs* p, int64_t C) { return p->dtype == TP_F32 && p->D == 64 && C == 64; }
 bool attn_tc_eligible(const tp_pairs* p, const tp_score* s, int64_t C, std::initializer_list<const void*> rows) {
     if (!kTcAttention || force_simt() || !attn_tc_shape(p, C) || s->metric != TP_LINEAR || s->apply_exp || s->row_bias ||
-        s->col_bias || s->row_weight || s->col_weight || s->pair_mask != TP_PAIRS_ALL || !aligned(p->X, 16) ||
+        s->col_bias || s->row_weight || s->col_weight || s->pair_mask == TP_PAIRS_SAME_GROUP || !aligned(p->X, 16) ||
         !aligned(p->Y, 16))
         return false;
     for (const void* q : rows)
@@ -721,6 +722,8 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
         t.scale = sc->scale;
         t.lse = static_cast<const float*>(lse);
         t.out = static_cast<float*>(out);
+        t.pm = (int)sc->pair_mask;
+        t.band = sc->band;
         t.ws = static_cast<char*>(ws) + lse_tc_workspace(pr->N, pr->M, same);
         const int n2 = launch_attn_fwd_tc(t, st);
         if (n2 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
@@ -922,6 +925,8 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
         t.dK = static_cast<float*>(dY);
         t.dV = static_cast<float*>(dV);
         t.accumulate_dK = dX && dX == dY ? 1 : 0;  // same points: the column sweep adds dK onto dQ
+        t.pm = (int)sc->pair_mask;
+        t.band = sc->band;
         t.ws = ws;
         const int n = launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream));
         if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");

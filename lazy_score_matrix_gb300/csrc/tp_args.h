@@ -56,6 +56,8 @@ struct AttnTcArgs {
     float* out;              // forward output [N, 64]
     float *dQ, *dK, *dV;     // backward outputs (null: not wanted)
     int accumulate_dK;       // add dK into its buffer (dQ and dK of the same points summed in one buffer)
+    int pm;                  // pair mask: 0 none, 1 causal (j <= i), 2 band (|i - j| <= band)
+    int64_t band;
     void* ws;
 };
 

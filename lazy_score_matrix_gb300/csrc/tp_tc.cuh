@@ -162,6 +162,15 @@ __host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
     return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
 }
 
+// Index pair masks of the tensor-core kernels (torchpairwise guide, Score Expressions: tp.masks causal
+// and band): pm 1 keeps the column points j <= i of row i, pm 2 keeps |i - j| <= band, 0 keeps all.
+constexpr int kPairsCausal = 1, kPairsBand = 2;
+__device__ __forceinline__ bool pair_in(int pm, int64_t band, int64_t i, int64_t j) {
+    if (pm == kPairsCausal) return j <= i;
+    if (pm == kPairsBand) return (i > j ? i - j : j - i) <= band;
+    return true;
+}
+
 // Pack two floats into fp16x2 (a in the low half), rounded to nearest.
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);

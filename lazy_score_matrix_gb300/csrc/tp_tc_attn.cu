@@ -107,6 +107,8 @@ struct Params {
     float* out0;           // [R][64] (null: not wanted)
     float* out1;
     int acc0;              // add output 0 into out0 instead of writing it
+    int pm;                // index pair mask (pair_in): 0 none, kPairsCausal, kPairsBand
+    int64_t band;
     int* err;
 };
 
@@ -457,12 +459,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Streamed points past the end (keys of the last tile) have S = 0 but their P is not 0: give
-            // them no weight. The column sweep's padding queries carry -inf in place of 14 - lse2.
-            if (MODE != kColSweep) {
-                const int lim = (int)(p.C - (int64_t)ct * kBN) - part * kCols;  // columns u >= lim are padding
-                if (lim < kCols) {
+            // them no weight. The column sweep's padding queries carry -inf in place of 14 - lse2. A pair
+            // mask keeps an interval of the slice's columns too: lo <= u < hi. The masked kappa is replaced,
+            // not scaled (its P may exceed 1 or be infinite: lse leaves the pair out).
+            {
+                const int64_t base = (int64_t)ct * kBN + part * kCols;  // first streamed point of the slice
+                const int64_t me = (int64_t)rb * kBM + lr;               // this thread's row point
+                int64_t lo = 0, hi = kCols;
+                if (MODE != kColSweep) hi = p.C - base;
+                if (p.pm == kPairsCausal) {
+                    if (MODE == kColSweep) lo = me - base;      // queries i >= key j
+                    else hi = min(hi, me - base + 1);           // keys j <= query i
+                } else if (p.pm == kPairsBand) {
+                    lo = max(lo, me - p.band - base);
+                    hi = min(hi, me + p.band - base + 1);
+                }
+                if (lo > 0 || hi < kCols) {
+                    const int l = (int)min(max(lo, (int64_t)0), (int64_t)kCols);
+                    const int h = (int)max(min(hi, (int64_t)kCols), (int64_t)0);
 #pragma unroll
-                    for (int u = 0; u < kCols; ++u) k0[u] = u < lim ? k0[u] : 0.f;
+                    for (int u = 0; u < kCols; ++u) {
+                        const bool keep = u >= l && u < h;
+                        k0[u] = keep ? k0[u] : 0.f;
+                        if (MODE == kColSweep) k1[u] = keep ? k1[u] : 0.f;
+                    }
                 }
             }
             // the previous tile's output MMAs have read their kappa before this tile's is stored, and the
@@ -689,7 +709,7 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
 template <int MODE>
 static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
                       const float4* cstat, const int* gmax, float* part, int* cnt, float* out0, float* out1, int acc0,
-                      int* err, const char* name, cudaStream_t s) {
+                      int pm, int64_t band, int* err, const char* name, cudaStream_t s) {
     const Sweep w = sweep_of(R, C);
     Params p;
     p.R = R;
@@ -707,6 +727,8 @@ static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float sca
     p.out0 = out0;
     p.out1 = out1;
     p.acc0 = acc0;
+    p.pm = pm;
+    p.band = band;
     p.err = err;
     cudaFuncSetAttribute(attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     HookScope h(name, s);
@@ -767,7 +789,7 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
                                                                  0, kh, kl, vh, vl, kst, nullptr, 0);
     }
     run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part), cntq,
-                    a.out, nullptr, 0, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
+                    a.out, nullptr, 0, a.pm, a.band, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
     return 5;
 }
 
@@ -827,13 +849,13 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     }
     int n = 4;
     if (a.dQ) {
-        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, gm, part, cntq, a.dQ, nullptr, 0, err,
-                             "attn_bwd_row_tc", s);
+        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, gm, part, cntq, a.dQ, nullptr, 0, a.pm, a.band,
+                             err, "attn_bwd_row_tc", s);
         ++n;
     }
     if (a.dK || a.dV) {
         run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, gm, part, cntk, a.dK, a.dV, a.accumulate_dK,
-                             err, "attn_bwd_col_tc", s);
+                             a.pm, a.band, err, "attn_bwd_col_tc", s);
         ++n;
     }
     return n;

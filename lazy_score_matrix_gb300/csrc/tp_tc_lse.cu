@@ -117,6 +117,8 @@ struct LseTcParams {
     int G;       // CTAs
     int smax;    // partial slots per CTA
     int metric, apply_exp, exclude_self, same;
+    int pm;                // index pair mask (pair_in): 0 none, kPairsCausal, kPairsBand
+    int64_t band;
     float scale;
     float neg_gamma_log2;  // -gamma * log2(e)
     const float* xs;       // 2^-e of each row point
@@ -330,7 +332,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive_warp(acc_empty + b);  // the values are in registers: the MMA may reuse the buffer
             const int64_t j0 = (int64_t)ct * kBN + sub * 32;
             const bool diag = row >= j0 && row < j0 + 32;
-            const bool masked = p.M - j0 < 32 || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
+            // a pair mask cuts into these 32 columns (the first or the last of them is outside it)
+            const bool cut = p.pm != 0 && !(pair_in(p.pm, p.band, row, j0) && pair_in(p.pm, p.band, row, j0 + 31));
+            const bool masked = p.M - j0 < 32 || cut || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
             const float4* ys4 = reinterpret_cast<const float4*>(p.ys + j0);  // padded: 32 readable entries
             if (METRIC == kLinear && !EXP && !masked && c1r > 0.f) {
                 // common case: score c1r * (x.y 2^(e_x+e_y)) 2^-e_y with c1r = scale log2(e) 2^-e_x > 0. The
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (masked) {
                         const int64_t j = j0 + u;
-                        if (j >= p.M || (p.exclude_self && j == row)) sc = ninf<float>();
+                        if (j >= p.M || (p.exclude_self && j == row) || !pair_in(p.pm, p.band, row, j)) sc = ninf<float>();
                     }
                     v[u] = sc;
                 }
@@ -1360,6 +1364,8 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     p.apply_exp = a.apply_exp;
     p.exclude_self = a.exclude_self;
     p.same = same ? 1 : 0;
+    p.pm = a.pm;  // causal or band only: callers route same-group masks to the streamed sweeps
+    p.band = a.band;
     p.scale = (float)a.scale;
     p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
     p.xs = xs;
