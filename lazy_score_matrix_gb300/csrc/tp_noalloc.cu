@@ -34,8 +34,8 @@ namespace {
 
 // 16 MiB per device. The SIMT log-sum-exp needs at most about 1.2 MiB (fp32) or 2.4 MiB (fp64) for
 // any shape; the fp32 D = 64 tensor-core path needs the hi/lo split of the points (512 bytes per
-// distinct point) plus about 0.3 MiB, so it fits up to ~30000 distinct points. Larger problems are
-// rejected by the size check below.
+// distinct point) and 4 KiB of partials per row block of 128 points plus 0.6 MiB, so it fits up to
+// ~29000 distinct points. Larger problems are rejected by the size check below.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -145,6 +145,122 @@ struct TileCursor {
     }
 };
 
+// Index pair masks of the tensor-core kernels (torchpairwise guide, Score Expressions: tp.masks causal
+// and band): pm 1 keeps the column points j <= i of row i, pm 2 keeps |i - j| <= band, 0 keeps all.
+constexpr int kPairsCausal = 1, kPairsBand = 2;
+__device__ __forceinline__ bool pair_in(int pm, int64_t band, int64_t i, int64_t j) {
+    if (pm == kPairsCausal) return j <= i;
+    if (pm == kPairsBand) return (i > j ? i - j : j - i) <= band;
+    return true;
+}
+
+// Schedules of the sweeps. Dense: row block rb streams all CT column tiles, tile t = rb * CT + ct. Under
+// an index pair mask (pair_in) row block rb streams only the tiles [c0, c1) that hold a kept pair of its
+// rows (an interval: causal and band keep an interval of streamed points per row), numbered row block by
+// row block from pfx[rb]; a row block keeps at least one tile, so every row is written (a row that keeps
+// no pair still gets its -inf or 0 from the masked tile).
+struct Sched {
+    int pm;              // 0 dense, kPairsCausal, kPairsBand
+    int col;             // 1: the rows are the score's columns (keys), the stream its rows (queries)
+    int64_t band;
+    int64_t R, C;        // row points, streamed points
+    int lbm, lbn, CT;    // log2 of the rows per block and of the streamed points per tile; column tiles
+    int64_t RB;          // row blocks
+    const int64_t* pfx;  // [RB + 1] first tile of each row block (masked schedules; built by sched_prefix)
+};
+
+__host__ __device__ inline Sched make_sched(int pm, int col, int64_t band, int64_t R, int64_t C, int BM, int BN,
+                                            const int64_t* pfx) {
+    Sched s;
+    s.pm = pm;
+    s.col = col;
+    s.band = band;
+    s.R = R;
+    s.C = C;
+    s.lbm = 0;
+    while ((1 << s.lbm) < BM) ++s.lbm;
+    s.lbn = 0;
+    while ((1 << s.lbn) < BN) ++s.lbn;
+    s.CT = (int)((C + BN - 1) / BN);
+    s.RB = (R + BM - 1) / BM;
+    s.pfx = pfx;
+    return s;
+}
+
+// Column tiles [c0, c1) that row block rb (< RB) streams (BM and BN are powers of two: shifts, no division).
+__host__ __device__ inline void live_tiles(const Sched& s, int64_t rb, int& c0, int& c1) {
+    if (s.pm == 0) {
+        c0 = 0;
+        c1 = s.CT;
+        return;
+    }
+    const int64_t r0 = rb << s.lbm, r1 = (r0 + (1 << s.lbm) < s.R ? r0 + (1 << s.lbm) : s.R) - 1;
+    int64_t lo = 0, hi = s.C - 1;  // streamed points kept by some row of the block
+    if (s.pm == kPairsCausal) {
+        if (s.col) lo = r0;              // queries i >= key j
+        else hi = hi < r1 ? hi : r1;     // keys j <= query i
+    } else {
+        lo = r0 - s.band > 0 ? r0 - s.band : 0;
+        hi = r1 + s.band < hi ? r1 + s.band : hi;
+    }
+    if (lo <= hi) {  // 0 <= lo <= hi < C
+        c0 = (int)(lo >> s.lbn);
+        c1 = (int)(hi >> s.lbn) + 1;
+    } else {  // no kept pair: one tile, fully masked
+        const int64_t a = lo < s.C - 1 ? lo : s.C - 1;
+        c0 = (int)(a >> s.lbn);
+        c1 = c0 + 1;
+    }
+}
+
+__host__ __device__ inline int64_t sched_tiles(const Sched& s, int64_t rb) {
+    int c0, c1;
+    live_tiles(s, rb, c0, c1);
+    return c1 - c0;
+}
+
+// Tiles of the whole schedule (host: the grid and the ranges of the CTAs follow from it).
+inline int64_t sched_total(const Sched& s) {
+    if (!s.pm) return s.RB * s.CT;
+    int64_t T = 0;
+    for (int64_t rb = 0; rb < s.RB; ++rb) T += sched_tiles(s, rb);
+    return T;
+}
+
+// First tile of row block rb (rb <= RB; pfx[RB] is the tile count).
+__device__ __forceinline__ int64_t tile_start(const Sched& s, int64_t rb) {
+    return s.pm ? __ldg(s.pfx + rb) : rb * s.CT;
+}
+
+// Row block of tile t: the largest rb with tile_start(rb) <= t.
+__device__ inline int row_block_of(const Sched& s, int64_t t) {
+    if (!s.pm) return (int)(t / s.CT);
+    int64_t lo = 0, hi = s.RB;  // pfx[lo] <= t < pfx[hi]
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (__ldg(s.pfx + mid) <= t) lo = mid;
+        else hi = mid;
+    }
+    return (int)lo;
+}
+
+// (row block, column tile) of consecutive tiles of a schedule.
+struct SchedCursor {
+    int rb, ct, c1;
+    __device__ __forceinline__ SchedCursor(const Sched& s, int64_t t) {
+        rb = row_block_of(s, t);
+        int c0;
+        live_tiles(s, rb, c0, c1);
+        ct = c0 + (int)(t - tile_start(s, rb));
+    }
+    __device__ __forceinline__ void next(const Sched& s) {
+        if (++ct == c1) {
+            ++rb;
+            if (rb < s.RB) live_tiles(s, rb, ct, c1);
+        }
+    }
+};
+
 // Persistent schedules: the tiles t = rb * CT + ct are cut into G contiguous ranges, one per CTA.
 // First tile of CTA c: floor(T c / G). 32-bit division whenever T G fits (every practical size).
 __host__ __device__ inline int64_t range_start(int64_t T, int G, int c) {
@@ -160,15 +276,6 @@ __host__ __device__ inline int cta_of_tile(int64_t T, int G, int64_t t) {
 // Row block of tile t (t < T).
 __host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
     return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
-}
-
-// Index pair masks of the tensor-core kernels (torchpairwise guide, Score Expressions: tp.masks causal
-// and band): pm 1 keeps the column points j <= i of row i, pm 2 keeps |i - j| <= band, 0 keeps all.
-constexpr int kPairsCausal = 1, kPairsBand = 2;
-__device__ __forceinline__ bool pair_in(int pm, int64_t band, int64_t i, int64_t j) {
-    if (pm == kPairsCausal) return j <= i;
-    if (pm == kPairsBand) return (i > j ? i - j : j - i) <= band;
-    return true;
 }
 
 // Pack two floats into fp16x2 (a in the low half), rounded to nearest.

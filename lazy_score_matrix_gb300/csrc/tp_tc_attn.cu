@@ -96,19 +96,18 @@ static_assert(Shape<kColSweep>::acc(1) + 64 <= 512 && Shape<kRowSweep>::acc(0) +
 struct Params {
     int64_t R;             // rows of the sweep (queries; keys for the column sweep)
     int64_t C;             // streamed points (keys; queries for the column sweep)
-    int64_t T;             // tiles: row blocks x column tiles
-    int CT, G, smax;
+    Sched sc;              // the tiles each row block streams (all CT of them without a pair mask)
+    int64_t T;             // tiles
+    int G;
     float scale;
     const float4* rstat;   // [rows padded to 128] the row side's stats
     const float4* cstat;   // [CT * 64 or more] the streamed side's stats (column sweep)
     const int* gmax;       // [kSlots] the global maxima
-    float* part;           // [G][smax][F][128] per-CTA partials, row-minor
+    float* part;           // [RB + G][F][128] partials, slot rb + CTA, row-minor
     int* cnt;              // [row blocks] CTAs done with each row block (zeroed by the pre-pass)
     float* out0;           // [R][64] (null: not wanted)
     float* out1;
     int acc0;              // add output 0 into out0 instead of writing it
-    int pm;                // index pair mask (pair_in): 0 none, kPairsCausal, kPairsBand
-    int64_t band;
     int* err;
 };
 
@@ -126,14 +125,13 @@ __device__ __noinline__ void merge_row(const Params& p, int rb, int lr, int fg) 
     const int fb = fg * FG;
     float* dst = fb < 64 ? p.out0 : p.out1;
     if (!dst) return;
-    const int64_t t0 = (int64_t)rb * p.CT;
-    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t0 + p.CT - 1);
+    const int64_t t0 = tile_start(p.sc, rb), t1 = tile_start(p.sc, rb + 1) - 1;
+    const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float acc[FG];
 #pragma unroll
     for (int f = 0; f < FG; ++f) acc[f] = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
-        const float* o = p.part + (size_t)(c * p.smax + seg) * SH::kF * kBM + lr;
+        const float* o = p.part + (size_t)(rb + c) * SH::kF * kBM + lr;
 #pragma unroll
         for (int f = 0; f < FG; ++f) acc[f] += __ldcg(o + (size_t)(fb + f) * kBM);
     }
@@ -210,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {  // ---------------- TMA producer: row blocks and operand stages in tile order
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
-            for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
+            SchedCursor cur(p.sc, t_begin);
+            for (int64_t i = 0; i < n && ok; ++i, cur.next(p.sc)) {
                 const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
                     if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 41);
@@ -246,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idO2 = idesc_f16(kBM, 128, true);       // kappa_hi [B_hi | B_lo] (MN-major): N 128
             int a_uses = 0, rb_cur = -1;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
+            SchedCursor cur(p.sc, t_begin);
             // S (and dP) of tile j into buffer j % NB, once the epilogue has read tile j - NB out of it
             auto issue_s = [&](int64_t j) -> bool {
                 const int rb = cur.rb;
-                cur.next();
+                cur.next(p.sc);
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);  // the old row block is free once its MMAs finish
                     if (!mbar_wait(a_full, a_uses & 1, p.err, 43)) return false;
@@ -370,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
         // of the CTAs whose tile ranges meet it to count itself in) merges it into the outputs.
         auto write_partial = [&]() {
-            float* o = p.part + (size_t)(blockIdx.x * p.smax + seg) * SH::kF * kBM;
+            float* o = p.part + (size_t)(rb_cur + blockIdx.x) * SH::kF * kBM;
 #pragma unroll
             for (int oo = 0; oo < NO; ++oo)
 #pragma unroll
@@ -380,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (etid == 0) {
                 int last = 0;
                 if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 48)) {
-                    const int64_t t0 = (int64_t)rb_cur * p.CT;
-                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    const int64_t t0 = tile_start(p.sc, rb_cur), t1 = tile_start(p.sc, rb_cur + 1) - 1;
+                    const int need = cta_of_tile(p.T, p.G, t1) - cta_of_tile(p.T, p.G, t0) + 1;
                     last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
                     __threadfence();
                 }
@@ -392,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++seg;
         };
         int64_t pending = -1;
-        TileCursor cur(t_begin, p.CT);
-        for (int64_t i = 0; i < n && ok; ++i, cur.next()) {
+        SchedCursor cur(p.sc, t_begin);
+        for (int64_t i = 0; i < n && ok; ++i, cur.next(p.sc)) {
             const int rb = cur.rb, ct = cur.ct;
             if (rb != rb_cur) {
                 if (pending >= 0) {
@@ -467,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t me = (int64_t)rb * kBM + lr;               // this thread's row point
                 int64_t lo = 0, hi = kCols;
                 if (MODE != kColSweep) hi = p.C - base;
-                if (p.pm == kPairsCausal) {
+                if (p.sc.pm == kPairsCausal) {
                     if (MODE == kColSweep) lo = me - base;      // queries i >= key j
                     else hi = min(hi, me - base + 1);           // keys j <= query i
-                } else if (p.pm == kPairsBand) {
-                    lo = max(lo, me - p.band - base);
-                    hi = min(hi, me + p.band - base + 1);
+                } else if (p.sc.pm == kPairsBand) {
+                    lo = max(lo, me - p.sc.band - base);
+                    hi = min(hi, me + p.sc.band - base + 1);
                 }
                 if (lo > 0 || hi < kCols) {
                     const int l = (int)min(max(lo, (int64_t)0), (int64_t)kCols);
@@ -655,29 +653,14 @@ __global__ void __launch_bounds__(256) attn_split(const float* __restrict__ A, c
 struct Plan {
     int64_t Npad, Mpad;
     size_t off_qh, off_ql, off_dh, off_dl, off_qst, off_kh, off_kl, off_vh, off_vl, off_kst, off_part, off_cntq,
-        off_cntk, off_gmax, off_err, bytes;
+        off_cntk, off_pfxq, off_pfxk, off_gmax, off_err, bytes;
 };
-
-struct Sweep {
-    int64_t T;
-    int CT, G, smax;
-};
-
-static Sweep sweep_of(int64_t R, int64_t C) {
-    Sweep w;
-    const int64_t RB = (R + kBM - 1) / kBM;
-    w.CT = (int)((C + kBN - 1) / kBN);
-    w.T = RB * w.CT;
-    w.G = (int)(w.T < kGrid ? w.T : kGrid);
-    const int64_t per = (w.T + w.G - 1) / w.G;
-    w.smax = (int)((per + w.CT - 1) / w.CT + 1);
-    return w;
-}
 
 static Plan plan_of(int64_t N, int64_t M, bool backward) {
     Plan pl;
     pl.Npad = (N + kBM - 1) / kBM * kBM;
     pl.Mpad = (M + kBM - 1) / kBM * kBM;
+    const int64_t RBq = pl.Npad / kBM, RBk = pl.Mpad / kBM;
     const size_t qb = (size_t)pl.Npad * kRowB, kb = (size_t)pl.Mpad * kRowB;
     size_t o = 0;
     pl.off_qh = o; o += al256(qb);
@@ -690,34 +673,42 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
     pl.off_vh = o; o += al256(kb);
     pl.off_vl = o; o += al256(kb);
     pl.off_kst = o; o += al256((size_t)pl.Mpad * 16);
-    const Sweep a = sweep_of(N, M);
-    size_t part = (size_t)a.G * a.smax * 64 * kBM * 4;
+    // partial slots rb + CTA: at most RB + G (consecutive CTA ranges never go back a row block)
+    size_t part = (size_t)(RBq + kGrid) * 64 * kBM * 4;
     if (backward) {
-        const Sweep c = sweep_of(M, N);
-        const size_t pc = (size_t)c.G * c.smax * 128 * kBM * 4;
+        const size_t pc = (size_t)(RBk + kGrid) * 128 * kBM * 4;
         part = part > pc ? part : pc;
     }
     pl.off_part = o; o += al256(part);
-    pl.off_cntq = o; o += al256((size_t)(pl.Npad / kBM) * 4);
-    pl.off_cntk = o; o += al256((size_t)(pl.Mpad / kBM) * 4);
+    pl.off_cntq = o; o += al256((size_t)RBq * 4);
+    pl.off_cntk = o; o += al256((size_t)RBk * 4);
+    pl.off_pfxq = o; o += al256((size_t)(RBq + 1) * 8);
+    pl.off_pfxk = o; o += al256((size_t)(RBk + 1) * 8);
     pl.off_gmax = o; o += 256;
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
 }
 
+// One sweep over R rows and C streamed points; with a pair mask (causal, band) only the column tiles that
+// hold kept pairs, from the tile table built first into pfx. Returns the number of kernels launched.
 template <int MODE>
-static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
-                      const float4* cstat, const int* gmax, float* part, int* cnt, float* out0, float* out1, int acc0,
-                      int pm, int64_t band, int* err, const char* name, cudaStream_t s) {
-    const Sweep w = sweep_of(R, C);
+static int run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
+                     const float4* cstat, const int* gmax, float* part, int* cnt, float* out0, float* out1, int acc0,
+                     int pm, int64_t band, int64_t* pfx, int* err, const char* name, cudaStream_t s) {
+    const Sched sc = make_sched(pm, MODE == kColSweep ? 1 : 0, band, R, C, kBM, kBN, pm ? pfx : nullptr);
+    int n = 0;
+    if (pm) {
+        launch_sched_prefix(sc, pfx, s);
+        ++n;
+    }
+    const int64_t T = sched_total(sc);
     Params p;
     p.R = R;
     p.C = C;
-    p.T = w.T;
-    p.CT = w.CT;
-    p.G = w.G;
-    p.smax = w.smax;
+    p.sc = sc;
+    p.T = T;
+    p.G = (int)(T < kGrid ? T : kGrid);
     p.scale = scale;
     p.rstat = rstat;
     p.cstat = cstat;
@@ -727,12 +718,11 @@ static void run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float sca
     p.out0 = out0;
     p.out1 = out1;
     p.acc0 = acc0;
-    p.pm = pm;
-    p.band = band;
     p.err = err;
     cudaFuncSetAttribute(attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     HookScope h(name, s);
-    attn_tc<MODE><<<w.G, kThreads, kSmem, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p);
+    attn_tc<MODE><<<p.G, kThreads, kSmem, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], p);
+    return n + 1;
 }
 
 static unsigned reduce_grid(int64_t rows) {
@@ -788,9 +778,9 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
         attn_split<false><<<(unsigned)(pl.Mpad / 8), 256, 0, s>>>(a.K, a.V, nullptr, nullptr, a.M, pl.Mpad, gm, gK, gV,
                                                                  0, kh, kl, vh, vl, kst, nullptr, 0);
     }
-    run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part), cntq,
-                    a.out, nullptr, 0, a.pm, a.band, reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
-    return 5;
+    return 4 + run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part),
+                               cntq, a.out, nullptr, 0, a.pm, a.band, reinterpret_cast<int64_t*>(ws + pl.off_pfxq),
+                               reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
 }
 
 // Backward: dQ (row sweep) and dK, dV (column sweep); null outputs are not written (a sweep none of whose
@@ -849,14 +839,13 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     }
     int n = 4;
     if (a.dQ) {
-        run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, gm, part, cntq, a.dQ, nullptr, 0, a.pm, a.band,
-                             err, "attn_bwd_row_tc", s);
-        ++n;
+        n += run_sweep<kRowSweep>(mr, a.N, a.M, (float)a.scale, qst, kst, gm, part, cntq, a.dQ, nullptr, 0, a.pm,
+                                  a.band, reinterpret_cast<int64_t*>(ws + pl.off_pfxq), err, "attn_bwd_row_tc", s);
     }
     if (a.dK || a.dV) {
-        run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, gm, part, cntk, a.dK, a.dV, a.accumulate_dK,
-                             a.pm, a.band, err, "attn_bwd_col_tc", s);
-        ++n;
+        n += run_sweep<kColSweep>(mc, a.M, a.N, (float)a.scale, kst, qst, gm, part, cntk, a.dK, a.dV, a.accumulate_dK,
+                                  a.pm, a.band, reinterpret_cast<int64_t*>(ws + pl.off_pfxk), err, "attn_bwd_col_tc",
+                                  s);
     }
     return n;
 }

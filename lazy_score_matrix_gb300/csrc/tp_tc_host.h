@@ -69,6 +69,10 @@ inline bool make_map_f16(CUtensorMap* m, const void* base, int64_t rows, int box
 void launch_split16(const float* x, int64_t rows, int64_t rows_pad, void* hi, void* lo, float* inv_scale, float* norm,
                     int* cnt, int64_t ncnt, cudaStream_t s);
 
+// The tile table pfx [RB + 1] of a masked schedule (tp_tc.cuh, Sched), built on the stream (tp_tc_lse.cu).
+struct Sched;
+void launch_sched_prefix(const Sched& sc, int64_t* pfx, cudaStream_t s);
+
 inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace tc

@@ -112,20 +112,17 @@ static_assert(kSmemF <= 232448, "dynamic shared memory per CTA");
 
 struct LseTcParams {
     int64_t N, M;
-    int64_t T;   // total tiles = RB * CT
-    int CT;      // column tiles per row block
+    Sched sc;    // the tiles each row block streams (all CT of them without a pair mask)
+    int64_t T;   // total tiles
     int G;       // CTAs
-    int smax;    // partial slots per CTA
     int metric, apply_exp, exclude_self, same;
-    int pm;                // index pair mask (pair_in): 0 none, kPairsCausal, kPairsBand
-    int64_t band;
     float scale;
     float neg_gamma_log2;  // -gamma * log2(e)
     const float* xs;       // 2^-e of each row point
     const float* ys;       // 2^-e of each column point
     const float* xn;       // |x_i|^2 (distance metrics)
     const float* yn;       // |y_j|^2
-    float* part;           // [G][smax][4 column parts][2][128] partial (max, sum) in base 2
+    float* part;           // [RB + G][4 column parts][2][128] partial (max, sum) in base 2: slot rb + CTA
     int* cnt;              // [RB] CTAs done with each row block (zeroed by the split pre-pass)
     float* lse;            // [N] output
     int* err;
@@ -134,12 +131,11 @@ struct LseTcParams {
 // lse of row `row` of row block rb from the partials of every CTA that saw it, in CTA order (one
 // pass, combining the (max, sum) pairs online in a fixed order: the result does not depend on timing).
 __device__ __noinline__ float lse_merge_row(const LseTcParams& p, int rb, int lr) {
-    const int64_t t0 = (int64_t)rb * p.CT, t1 = t0 + p.CT - 1;
+    const int64_t t0 = tile_start(p.sc, rb), t1 = tile_start(p.sc, rb + 1) - 1;
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float m = ninf<float>(), l = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
-        const int seg = rb - rb_of_tile(range_start(p.T, p.G, c), p.CT);
-        const float* o = p.part + ((size_t)((c * p.smax + seg) * 4) * 2) * kBM + lr;
+        const float* o = p.part + ((size_t)((rb + c) * 4) * 2) * kBM + lr;
         float pm[4], pl[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -208,8 +204,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {  // ---------------- TMA producer
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
-            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+            SchedCursor cur(p.sc, t_begin);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next(p.sc)) {
                 const int64_t i = t - t_begin;
                 const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
@@ -236,8 +232,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr uint32_t id128 = idesc_f16(kBM, kBN, false);
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
-            TileCursor cur(t_begin, p.CT);
-            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+            SchedCursor cur(p.sc, t_begin);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next(p.sc)) {
                 const int64_t i = t - t_begin;
                 const int rb = cur.rb;
                 if (rb != rb_cur) {
@@ -278,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
         // of the CTAs whose tile ranges meet it to count itself in) merges its rows into lse.
         auto flush = [&]() {
-            float* o = p.part + ((size_t)((blockIdx.x * p.smax + seg) * 4 + sub) * 2) * kBM;
+            float* o = p.part + ((size_t)((rb_cur + blockIdx.x) * 4 + sub) * 2) * kBM;
             o[lr] = m;
             o[kBM + lr] = l;
             __threadfence();
@@ -286,8 +282,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (etid == 0) {
                 int last = 0;
                 if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 17)) {
-                    const int64_t t0 = (int64_t)rb_cur * p.CT;
-                    const int need = cta_of_tile(p.T, p.G, t0 + p.CT - 1) - cta_of_tile(p.T, p.G, t0) + 1;
+                    const int64_t t0 = tile_start(p.sc, rb_cur), t1 = tile_start(p.sc, rb_cur + 1) - 1;
+                    const int need = cta_of_tile(p.T, p.G, t1) - cta_of_tile(p.T, p.G, t0) + 1;
                     last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
                     __threadfence();
                 }
@@ -300,8 +296,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             ++seg;
         };
-        TileCursor cur(t_begin, p.CT);
-        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+        SchedCursor cur(p.sc, t_begin);
+        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next(p.sc)) {
             const int64_t i = t - t_begin;
             const int rb = cur.rb, ct = cur.ct;
             const int64_t row = (int64_t)rb * kBM + lr;
@@ -333,7 +329,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int64_t j0 = (int64_t)ct * kBN + sub * 32;
             const bool diag = row >= j0 && row < j0 + 32;
             // a pair mask cuts into these 32 columns (the first or the last of them is outside it)
-            const bool cut = p.pm != 0 && !(pair_in(p.pm, p.band, row, j0) && pair_in(p.pm, p.band, row, j0 + 31));
+            const bool cut = p.sc.pm != 0 &&
+                             !(pair_in(p.sc.pm, p.sc.band, row, j0) && pair_in(p.sc.pm, p.sc.band, row, j0 + 31));
             const bool masked = p.M - j0 < 32 || cut || (diag && (p.exclude_self || (p.same && METRIC != kLinear)));
             const float4* ys4 = reinterpret_cast<const float4*>(p.ys + j0);  // padded: 32 readable entries
             if (METRIC == kLinear && !EXP && !masked && c1r > 0.f) {
@@ -383,7 +380,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (masked) {
                         const int64_t j = j0 + u;
-                        if (j >= p.M || (p.exclude_self && j == row) || !pair_in(p.pm, p.band, row, j)) sc = ninf<float>();
+                        if (j >= p.M || (p.exclude_self && j == row) || !pair_in(p.sc.pm, p.sc.band, row, j))
+                            sc = ninf<float>();
                     }
                     v[u] = sc;
                 }
@@ -1251,20 +1249,46 @@ __global__ void __launch_bounds__(256) lse_bwd_prep_lin(const float* __restrict_
         stat[r] = make_float4((float)lin_kappa_exp(gm, scale) - lse[r] * 1.4426950408889634f, scale * g[r], 0.f, 0.f);
 }
 
+// pfx[rb] = tiles of the row blocks before rb of a masked schedule, pfx[RB] = all of them: one block,
+// each thread sums a run of consecutive row blocks, then an inclusive scan over the threads.
+__global__ void __launch_bounds__(1024) sched_prefix(const Sched sc, int64_t* __restrict__ pfx) {
+    __shared__ int64_t run[1024];
+    const int t = threadIdx.x;
+    const int64_t per = (sc.RB + 1023) / 1024;
+    const int64_t b = t * per, e = b + per < sc.RB ? b + per : sc.RB;
+    int64_t sum = 0;
+    for (int64_t rb = b; rb < e; ++rb) sum += sched_tiles(sc, rb);
+    run[t] = sum;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int64_t v = t >= off ? run[t - off] : 0;
+        __syncthreads();
+        run[t] += v;
+        __syncthreads();
+    }
+    int64_t acc = t > 0 ? run[t - 1] : 0;
+    for (int64_t rb = b; rb < e; ++rb) {
+        pfx[rb] = acc;
+        acc += sched_tiles(sc, rb);
+    }
+    if (t == 1023) pfx[sc.RB] = run[1023];
+}
+
+void launch_sched_prefix(const Sched& sc, int64_t* pfx, cudaStream_t s) {
+    HookScope h("sched_prefix", s);
+    sched_prefix<<<1, 1024, 0, s>>>(sc, pfx);
+}
+
 struct LseTcPlan {
-    int64_t T, Xpad, Ypad;
-    int CT, G, smax;
-    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_cnt, off_err, bytes;
+    int64_t Xpad, Ypad;
+    int CT;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_cnt, off_pfx, off_err, bytes;
 };
 
 static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
     LseTcPlan pl;
     const int64_t RB = (N + kBM - 1) / kBM;
     pl.CT = (int)((M + kBN - 1) / kBN);
-    pl.T = RB * pl.CT;
-    pl.G = (int)(pl.T < kGrid ? pl.T : kGrid);
-    const int64_t per = (pl.T + pl.G - 1) / pl.G;
-    pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
     pl.Xpad = RB * kBM;
     pl.Ypad = (int64_t)pl.CT * kBN;
     size_t o = 0;
@@ -1283,8 +1307,9 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
         pl.off_ys = o; o += al256((size_t)pl.Ypad * 4);
         pl.off_yn = o; o += al256((size_t)pl.Ypad * 4);
     }
-    pl.off_part = o; o += al256((size_t)pl.G * pl.smax * 4 * 2 * kBM * 4);
+    pl.off_part = o; o += al256((size_t)(RB + kGrid) * 4 * 2 * kBM * 4);  // slot rb + CTA
     pl.off_cnt = o; o += al256((size_t)RB * 4);
+    pl.off_pfx = o; o += al256((size_t)(RB + 1) * 8);
     pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
@@ -1353,19 +1378,26 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
                                                                 ys, yn, nullptr, 0);
         ++n;
     }
+    // causal or band only (callers route same-group masks to the streamed sweeps): the row blocks stream
+    // the column tiles that hold their kept pairs
+    int64_t* pfx = reinterpret_cast<int64_t*>(ws + pl.off_pfx);
+    const Sched sc = make_sched(a.pm, 0, a.band, a.nP, a.nQ, kBM, kBN, a.pm ? pfx : nullptr);
+    if (a.pm) {
+        launch_sched_prefix(sc, pfx, s);
+        ++n;
+    }
+    const int64_t T = sched_total(sc);
+    const int G = (int)(T < kGrid ? T : kGrid);
     LseTcParams p;
     p.N = a.nP;
     p.M = a.nQ;
-    p.T = pl.T;
-    p.CT = pl.CT;
-    p.G = pl.G;
-    p.smax = pl.smax;
+    p.sc = sc;
+    p.T = T;
+    p.G = G;
     p.metric = a.metric;
     p.apply_exp = a.apply_exp;
     p.exclude_self = a.exclude_self;
     p.same = same ? 1 : 0;
-    p.pm = a.pm;  // causal or band only: callers route same-group masks to the streamed sweeps
-    p.band = a.band;
     p.scale = (float)a.scale;
     p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
     p.xs = xs;
@@ -1379,7 +1411,7 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemF);
         HookScope h("lse_fwd_tc", s);
-        kernel<<<pl.G, kTcThreads, kSmemF, s>>>(mxh, mxl, myh, myl, p);
+        kernel<<<G, kTcThreads, kSmemF, s>>>(mxh, mxl, myh, myl, p);
     };
     const bool ex = a.apply_exp != 0;
     if (a.metric == kLinear) ex ? go(lse_fwd_tc<kLinear, true>) : go(lse_fwd_tc<kLinear, false>);

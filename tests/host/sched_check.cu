@@ -1,0 +1,102 @@
+// Host check of the tensor-core sweeps' persistent schedules (dense and under the causal and band pair
+// masks of the torchpairwise guide's Score Expressions): every tile that holds a kept pair is visited
+// exactly once, by the CTA ranges in order; every row block gets at least one tile; the partial slots
+// (row block + CTA) are distinct and below RB + G; the CTAs a merge reads are exactly those whose ranges
+// met the row block. The device-side table lookups (tile_start, row_block_of, SchedCursor) are restated
+// here over a host prefix table; the interval of each row block (live_tiles), the tile count
+// (sched_total) and the CTA ranges (range_start, cta_of_tile) are the header's own.
+#include <cstdio>
+#include <cstdlib>
+#include <set>
+#include <vector>
+
+#include "../../lazy_score_matrix_gb300/csrc/tp_tc.cuh"
+
+using namespace tp::tc;
+
+static int fails = 0;
+#define CHECK(c, ...)                                    \
+    do {                                                 \
+        if (!(c)) {                                      \
+            if (fails < 20) std::printf(__VA_ARGS__);    \
+            ++fails;                                     \
+        }                                                \
+    } while (0)
+
+static bool kept(int pm, long long band, int col, long long r, long long q) {
+    // r: a row point of the sweep, q: a streamed point; the score's (query i, key j) pair
+    const long long i = col ? q : r, j = col ? r : q;
+    if (pm == kPairsCausal) return j <= i;
+    if (pm == kPairsBand) return (i > j ? i - j : j - i) <= band;
+    return true;
+}
+
+static void run(int pm, int col, long long band, long long R, long long C, int BM, int BN, int grid) {
+    const Sched s = make_sched(pm, col, band, R, C, BM, BN, nullptr);
+    std::vector<long long> pfx(s.RB + 1, 0);
+    for (long long rb = 0; rb < s.RB; ++rb) pfx[rb + 1] = pfx[rb] + sched_tiles(s, rb);
+    const long long T = sched_total(s);
+    CHECK(T == pfx[s.RB], "total %lld != prefix %lld\n", T, pfx[s.RB]);
+    const int G = (int)(T < grid ? T : grid);
+    auto start = [&](long long rb) { return pm ? pfx[rb] : rb * s.CT; };
+    auto rb_of = [&](long long t) {
+        long long rb = 0;
+        while (rb + 1 <= s.RB && start(rb + 1) <= t) ++rb;
+        return rb;
+    };
+    std::set<std::pair<long long, int>> seen;
+    std::set<long long> slots;
+    std::vector<std::set<int>> touched(s.RB);
+    for (int c = 0; c < G; ++c) {
+        const long long tb = range_start(T, G, c), te = range_start(T, G, c + 1);
+        CHECK(te > tb, "empty range of CTA %d\n", c);
+        long long rb = rb_of(tb);
+        int c0, c1;
+        live_tiles(s, rb, c0, c1);
+        int ct = c0 + (int)(tb - start(rb));
+        for (long long t = tb; t < te; ++t) {
+            CHECK(rb < s.RB && ct >= c0 && ct < c1 && ct < s.CT, "tile %lld out of its row block\n", t);
+            CHECK(seen.insert({rb, ct}).second, "tile (%lld, %d) visited twice\n", rb, ct);
+            touched[rb].insert(c);
+            if (++ct == c1) {
+                ++rb;
+                if (rb < s.RB) live_tiles(s, rb, ct, c1), c0 = ct;
+            }
+        }
+    }
+    CHECK((long long)seen.size() == T, "%zu tiles visited of %lld\n", seen.size(), T);
+    for (long long rb = 0; rb < s.RB; ++rb) {
+        CHECK(!touched[rb].empty(), "row block %lld has no tile\n", rb);
+        for (int c : touched[rb]) CHECK(slots.insert(rb + c).second && rb + c < s.RB + G, "slot %lld\n", rb + c);
+        const int lo = cta_of_tile(T, G, start(rb)), hi = cta_of_tile(T, G, start(rb + 1) - 1);
+        CHECK((int)touched[rb].size() == hi - lo + 1 && *touched[rb].begin() == lo && *touched[rb].rbegin() == hi,
+              "merge CTAs of row block %lld\n", rb);
+        // every tile with a kept pair is in the schedule
+        for (int ct = 0; ct < s.CT; ++ct) {
+            bool any = false;
+            for (long long r = rb * BM; r < R && r < (rb + 1) * BM && !any; ++r)
+                for (long long q = (long long)ct * BN; q < C && q < (long long)(ct + 1) * BN && !any; ++q)
+                    any = kept(pm, band, col, r, q);
+            if (any) CHECK(seen.count({rb, ct}), "kept tile (%lld, %d) skipped (pm %d col %d R %lld C %lld)\n", rb, ct,
+                           pm, col, R, C);
+        }
+    }
+}
+
+int main() {
+    const long long sizes[] = {1, 5, 64, 127, 128, 129, 300, 517, 1000, 2049};
+    const long long bands[] = {0, 1, 17, 63, 64, 200, 5000};
+    int cases = 0;
+    for (int BN : {64, 128})
+        for (int grid : {3, 152})
+            for (long long R : sizes)
+                for (long long C : sizes)
+                    for (int col = 0; col < 2; ++col) {
+                        run(0, col, 0, R, C, 128, BN, grid);
+                        run(kPairsCausal, col, 0, R, C, 128, BN, grid);
+                        for (long long b : bands) run(kPairsBand, col, b, R, C, 128, BN, grid);
+                        cases += 9;
+                    }
+    std::printf("%d schedules, %d failures\n", cases, fails);
+    return fails ? 1 : 0;
+}
