@@ -156,9 +156,12 @@ __device__ __forceinline__ bool pair_in(int pm, int64_t band, int64_t i, int64_t
 
 // Schedules of the sweeps. Dense: row block rb streams all CT column tiles, tile t = rb * CT + ct. Under
 // an index pair mask (pair_in) row block rb streams only the tiles [c0, c1) that hold a kept pair of its
-// rows (an interval: causal and band keep an interval of streamed points per row), numbered row block by
-// row block from pfx[rb]; a row block keeps at least one tile, so every row is written (a row that keeps
-// no pair still gets its -inf or 0 from the masked tile).
+// rows (an interval: causal and band keep an interval of streamed points per row); a row block keeps at
+// least one tile, so every row is written (a row that keeps no pair still gets its -inf or 0 from the
+// masked tile). The row blocks are then visited in the order 0, RB-1, 1, RB-2, ... (position v holds row
+// block sched_rb(v)), which pairs a short row block of a causal mask with a long one, so that no CTA's
+// range is made of many short row blocks (each change of row block reloads the row operand); tiles are
+// numbered position by position from pfx[v].
 struct Sched {
     int pm;              // 0 dense, kPairsCausal, kPairsBand
     int col;             // 1: the rows are the score's columns (keys), the stream its rows (queries)
@@ -185,6 +188,16 @@ __host__ __device__ inline Sched make_sched(int pm, int col, int64_t band, int64
     s.RB = (R + BM - 1) / BM;
     s.pfx = pfx;
     return s;
+}
+
+// Row block at position v of the schedule, and the position of row block rb.
+__host__ __device__ inline int64_t sched_rb(const Sched& s, int64_t v) {
+    if (!s.pm) return v;
+    return (v & 1) ? s.RB - 1 - (v >> 1) : (v >> 1);
+}
+__host__ __device__ inline int64_t sched_pos(const Sched& s, int64_t rb) {
+    if (!s.pm) return rb;
+    return rb < ((s.RB + 1) >> 1) ? 2 * rb : 2 * (s.RB - 1 - rb) + 1;
 }
 
 // Column tiles [c0, c1) that row block rb (< RB) streams (BM and BN are powers of two: shifts, no division).
@@ -227,36 +240,41 @@ inline int64_t sched_total(const Sched& s) {
     return T;
 }
 
-// First tile of row block rb (rb <= RB; pfx[RB] is the tile count).
-__device__ __forceinline__ int64_t tile_start(const Sched& s, int64_t rb) {
-    return s.pm ? __ldg(s.pfx + rb) : rb * s.CT;
+// First tile of position v (v <= RB; pfx[RB] is the tile count).
+__device__ __forceinline__ int64_t tile_start(const Sched& s, int64_t v) {
+    return s.pm ? __ldg(s.pfx + v) : v * s.CT;
 }
 
-// Row block of tile t: the largest rb with tile_start(rb) <= t.
-__device__ inline int row_block_of(const Sched& s, int64_t t) {
-    if (!s.pm) return (int)(t / s.CT);
+// Position of tile t: the largest v with tile_start(v) <= t.
+__device__ inline int64_t pos_of_tile(const Sched& s, int64_t t) {
+    if (!s.pm) return t / s.CT;
     int64_t lo = 0, hi = s.RB;  // pfx[lo] <= t < pfx[hi]
     while (hi - lo > 1) {
         const int64_t mid = (lo + hi) >> 1;
         if (__ldg(s.pfx + mid) <= t) lo = mid;
         else hi = mid;
     }
-    return (int)lo;
+    return lo;
 }
 
 // (row block, column tile) of consecutive tiles of a schedule.
 struct SchedCursor {
+    int64_t v;  // position
     int rb, ct, c1;
     __device__ __forceinline__ SchedCursor(const Sched& s, int64_t t) {
-        rb = row_block_of(s, t);
+        v = pos_of_tile(s, t);
+        rb = (int)sched_rb(s, v);
         int c0;
         live_tiles(s, rb, c0, c1);
-        ct = c0 + (int)(t - tile_start(s, rb));
+        ct = c0 + (int)(t - tile_start(s, v));
     }
     __device__ __forceinline__ void next(const Sched& s) {
         if (++ct == c1) {
-            ++rb;
-            if (rb < s.RB) live_tiles(s, rb, ct, c1);
+            ++v;
+            if (v < s.RB) {
+                rb = (int)sched_rb(s, v);
+                live_tiles(s, rb, ct, c1);
+            }
         }
     }
 };

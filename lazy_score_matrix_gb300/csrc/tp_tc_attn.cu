@@ -103,7 +103,7 @@ struct Params {
     const float4* rstat;   // [rows padded to 128] the row side's stats
     const float4* cstat;   // [CT * 64 or more] the streamed side's stats (column sweep)
     const int* gmax;       // [kSlots] the global maxima
-    float* part;           // [RB + G][F][128] partials, slot rb + CTA, row-minor
+    float* part;           // [RB + G][F][128] partials, slot position + CTA, row-minor
     int* cnt;              // [row blocks] CTAs done with each row block (zeroed by the pre-pass)
     float* out0;           // [R][64] (null: not wanted)
     float* out1;
@@ -125,13 +125,13 @@ __device__ __noinline__ void merge_row(const Params& p, int rb, int lr, int fg) 
     const int fb = fg * FG;
     float* dst = fb < 64 ? p.out0 : p.out1;
     if (!dst) return;
-    const int64_t t0 = tile_start(p.sc, rb), t1 = tile_start(p.sc, rb + 1) - 1;
+    const int64_t v = sched_pos(p.sc, rb), t0 = tile_start(p.sc, v), t1 = tile_start(p.sc, v + 1) - 1;
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float acc[FG];
 #pragma unroll
     for (int f = 0; f < FG; ++f) acc[f] = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
-        const float* o = p.part + (size_t)(rb + c) * SH::kF * kBM + lr;
+        const float* o = p.part + (size_t)(v + c) * SH::kF * kBM + lr;
 #pragma unroll
         for (int f = 0; f < FG; ++f) acc[f] += __ldcg(o + (size_t)(fb + f) * kBM);
     }
@@ -368,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
         // of the CTAs whose tile ranges meet it to count itself in) merges it into the outputs.
         auto write_partial = [&]() {
-            float* o = p.part + (size_t)(rb_cur + blockIdx.x) * SH::kF * kBM;
+            const int64_t v = sched_pos(p.sc, rb_cur);
+            float* o = p.part + (size_t)(v + blockIdx.x) * SH::kF * kBM;
 #pragma unroll
             for (int oo = 0; oo < NO; ++oo)
 #pragma unroll
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (etid == 0) {
                 int last = 0;
                 if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 48)) {
-                    const int64_t t0 = tile_start(p.sc, rb_cur), t1 = tile_start(p.sc, rb_cur + 1) - 1;
+                    const int64_t t0 = tile_start(p.sc, v), t1 = tile_start(p.sc, v + 1) - 1;
                     const int need = cta_of_tile(p.T, p.G, t1) - cta_of_tile(p.T, p.G, t0) + 1;
                     last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
                     __threadfence();
@@ -673,7 +674,7 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
     pl.off_vh = o; o += al256(kb);
     pl.off_vl = o; o += al256(kb);
     pl.off_kst = o; o += al256((size_t)pl.Mpad * 16);
-    // partial slots rb + CTA: at most RB + G (consecutive CTA ranges never go back a row block)
+    // partial slots position + CTA: at most RB + G (consecutive CTA ranges never go back a position)
     size_t part = (size_t)(RBq + kGrid) * 64 * kBM * 4;
     if (backward) {
         const size_t pc = (size_t)(RBk + kGrid) * 128 * kBM * 4;

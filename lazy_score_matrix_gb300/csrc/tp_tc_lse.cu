@@ -122,7 +122,7 @@ struct LseTcParams {
     const float* ys;       // 2^-e of each column point
     const float* xn;       // |x_i|^2 (distance metrics)
     const float* yn;       // |y_j|^2
-    float* part;           // [RB + G][4 column parts][2][128] partial (max, sum) in base 2: slot rb + CTA
+    float* part;           // [RB + G][4 column parts][2][128] partial (max, sum) in base 2: slot position + CTA
     int* cnt;              // [RB] CTAs done with each row block (zeroed by the split pre-pass)
     float* lse;            // [N] output
     int* err;
@@ -131,11 +131,11 @@ struct LseTcParams {
 // lse of row `row` of row block rb from the partials of every CTA that saw it, in CTA order (one
 // pass, combining the (max, sum) pairs online in a fixed order: the result does not depend on timing).
 __device__ __noinline__ float lse_merge_row(const LseTcParams& p, int rb, int lr) {
-    const int64_t t0 = tile_start(p.sc, rb), t1 = tile_start(p.sc, rb + 1) - 1;
+    const int64_t v = sched_pos(p.sc, rb), t0 = tile_start(p.sc, v), t1 = tile_start(p.sc, v + 1) - 1;
     const int c_lo = cta_of_tile(p.T, p.G, t0), c_hi = cta_of_tile(p.T, p.G, t1);
     float m = ninf<float>(), l = 0.f;
     for (int c = c_lo; c <= c_hi; ++c) {
-        const float* o = p.part + ((size_t)((rb + c) * 4) * 2) * kBM + lr;
+        const float* o = p.part + ((size_t)((v + c) * 4) * 2) * kBM + lr;
         float pm[4], pl[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // Write this thread's partial of row block rb_cur. The CTA that completes the row block (the last
         // of the CTAs whose tile ranges meet it to count itself in) merges its rows into lse.
         auto flush = [&]() {
-            float* o = p.part + ((size_t)((rb_cur + blockIdx.x) * 4 + sub) * 2) * kBM;
+            const int64_t v = sched_pos(p.sc, rb_cur);
+            float* o = p.part + ((size_t)((v + blockIdx.x) * 4 + sub) * 2) * kBM;
             o[lr] = m;
             o[kBM + lr] = l;
             __threadfence();
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (etid == 0) {
                 int last = 0;
                 if (mbar_wait(fl_bar, (uint32_t)(seg & 1), p.err, 17)) {
-                    const int64_t t0 = tile_start(p.sc, rb_cur), t1 = tile_start(p.sc, rb_cur + 1) - 1;
+                    const int64_t t0 = tile_start(p.sc, v), t1 = tile_start(p.sc, v + 1) - 1;
                     const int need = cta_of_tile(p.T, p.G, t1) - cta_of_tile(p.T, p.G, t0) + 1;
                     last = atomicAdd(p.cnt + rb_cur, 1) + 1 == need;
                     __threadfence();
@@ -1249,15 +1250,15 @@ __global__ void __launch_bounds__(256) lse_bwd_prep_lin(const float* __restrict_
         stat[r] = make_float4((float)lin_kappa_exp(gm, scale) - lse[r] * 1.4426950408889634f, scale * g[r], 0.f, 0.f);
 }
 
-// pfx[rb] = tiles of the row blocks before rb of a masked schedule, pfx[RB] = all of them: one block,
-// each thread sums a run of consecutive row blocks, then an inclusive scan over the threads.
+// pfx[v] = tiles of the positions before v of a masked schedule, pfx[RB] = all of them: one block, each
+// thread sums a run of consecutive positions, then an inclusive scan over the threads.
 __global__ void __launch_bounds__(1024) sched_prefix(const Sched sc, int64_t* __restrict__ pfx) {
     __shared__ int64_t run[1024];
     const int t = threadIdx.x;
     const int64_t per = (sc.RB + 1023) / 1024;
     const int64_t b = t * per, e = b + per < sc.RB ? b + per : sc.RB;
     int64_t sum = 0;
-    for (int64_t rb = b; rb < e; ++rb) sum += sched_tiles(sc, rb);
+    for (int64_t v = b; v < e; ++v) sum += sched_tiles(sc, sched_rb(sc, v));
     run[t] = sum;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {
@@ -1267,9 +1268,9 @@ __global__ void __launch_bounds__(1024) sched_prefix(const Sched sc, int64_t* __
         __syncthreads();
     }
     int64_t acc = t > 0 ? run[t - 1] : 0;
-    for (int64_t rb = b; rb < e; ++rb) {
-        pfx[rb] = acc;
-        acc += sched_tiles(sc, rb);
+    for (int64_t v = b; v < e; ++v) {
+        pfx[v] = acc;
+        acc += sched_tiles(sc, sched_rb(sc, v));
     }
     if (t == 1023) pfx[sc.RB] = run[1023];
 }

@@ -1,10 +1,11 @@
 // Host check of the tensor-core sweeps' persistent schedules (dense and under the causal and band pair
 // masks of the torchpairwise guide's Score Expressions): every tile that holds a kept pair is visited
-// exactly once, by the CTA ranges in order; every row block gets at least one tile; the partial slots
-// (row block + CTA) are distinct and below RB + G; the CTAs a merge reads are exactly those whose ranges
-// met the row block. The device-side table lookups (tile_start, row_block_of, SchedCursor) are restated
-// here over a host prefix table; the interval of each row block (live_tiles), the tile count
-// (sched_total) and the CTA ranges (range_start, cta_of_tile) are the header's own.
+// exactly once, by the CTA ranges in order; every row block gets at least one tile; the order of the row
+// blocks (sched_rb, sched_pos) is a permutation; the partial slots (position + CTA) are distinct and below
+// RB + G; the CTAs a merge reads are exactly those whose ranges met the row block. The device-side table
+// lookups (tile_start, pos_of_tile, SchedCursor) are restated here over a host prefix table; the interval
+// of each row block (live_tiles), the order, the tile count (sched_total) and the CTA ranges
+// (range_start, cta_of_tile) are the header's own.
 #include <cstdio>
 #include <cstdlib>
 #include <set>
@@ -34,15 +35,20 @@ static bool kept(int pm, long long band, int col, long long r, long long q) {
 static void run(int pm, int col, long long band, long long R, long long C, int BM, int BN, int grid) {
     const Sched s = make_sched(pm, col, band, R, C, BM, BN, nullptr);
     std::vector<long long> pfx(s.RB + 1, 0);
-    for (long long rb = 0; rb < s.RB; ++rb) pfx[rb + 1] = pfx[rb] + sched_tiles(s, rb);
+    std::set<long long> order;
+    for (long long v = 0; v < s.RB; ++v) {
+        const long long rb = sched_rb(s, v);
+        CHECK(rb >= 0 && rb < s.RB && sched_pos(s, rb) == v && order.insert(rb).second, "order at %lld\n", v);
+        pfx[v + 1] = pfx[v] + sched_tiles(s, rb);
+    }
     const long long T = sched_total(s);
     CHECK(T == pfx[s.RB], "total %lld != prefix %lld\n", T, pfx[s.RB]);
     const int G = (int)(T < grid ? T : grid);
-    auto start = [&](long long rb) { return pm ? pfx[rb] : rb * s.CT; };
-    auto rb_of = [&](long long t) {
-        long long rb = 0;
-        while (rb + 1 <= s.RB && start(rb + 1) <= t) ++rb;
-        return rb;
+    auto start = [&](long long v) { return pm ? pfx[v] : v * s.CT; };
+    auto pos_of = [&](long long t) {
+        long long v = 0;
+        while (v + 1 <= s.RB && start(v + 1) <= t) ++v;
+        return v;
     };
     std::set<std::pair<long long, int>> seen;
     std::set<long long> slots;
@@ -50,25 +56,26 @@ static void run(int pm, int col, long long band, long long R, long long C, int B
     for (int c = 0; c < G; ++c) {
         const long long tb = range_start(T, G, c), te = range_start(T, G, c + 1);
         CHECK(te > tb, "empty range of CTA %d\n", c);
-        long long rb = rb_of(tb);
+        long long v = pos_of(tb), rb = sched_rb(s, v);
         int c0, c1;
         live_tiles(s, rb, c0, c1);
-        int ct = c0 + (int)(tb - start(rb));
+        int ct = c0 + (int)(tb - start(v));
         for (long long t = tb; t < te; ++t) {
-            CHECK(rb < s.RB && ct >= c0 && ct < c1 && ct < s.CT, "tile %lld out of its row block\n", t);
+            CHECK(v < s.RB && ct >= c0 && ct < c1 && ct < s.CT, "tile %lld out of its row block\n", t);
             CHECK(seen.insert({rb, ct}).second, "tile (%lld, %d) visited twice\n", rb, ct);
             touched[rb].insert(c);
             if (++ct == c1) {
-                ++rb;
-                if (rb < s.RB) live_tiles(s, rb, ct, c1), c0 = ct;
+                ++v;
+                if (v < s.RB) rb = sched_rb(s, v), live_tiles(s, rb, ct, c1), c0 = ct;
             }
         }
     }
     CHECK((long long)seen.size() == T, "%zu tiles visited of %lld\n", seen.size(), T);
     for (long long rb = 0; rb < s.RB; ++rb) {
         CHECK(!touched[rb].empty(), "row block %lld has no tile\n", rb);
-        for (int c : touched[rb]) CHECK(slots.insert(rb + c).second && rb + c < s.RB + G, "slot %lld\n", rb + c);
-        const int lo = cta_of_tile(T, G, start(rb)), hi = cta_of_tile(T, G, start(rb + 1) - 1);
+        const long long v = sched_pos(s, rb);
+        for (int c : touched[rb]) CHECK(slots.insert(v + c).second && v + c < s.RB + G, "slot %lld\n", v + c);
+        const int lo = cta_of_tile(T, G, start(v)), hi = cta_of_tile(T, G, start(v + 1) - 1);
         CHECK((int)touched[rb].size() == hi - lo + 1 && *touched[rb].begin() == lo && *touched[rb].rbegin() == hi,
               "merge CTAs of row block %lld\n", rb);
         // every tile with a kept pair is in the schedule
