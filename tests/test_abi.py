@@ -121,6 +121,29 @@ def test_invalid_arguments_rejected(lib, case):
     assert lib.tp_last_error()
 
 
+@pytest.mark.parametrize("case,msg", [("unknown", "unknown pair mask"), ("negative_band", "band must be >= 0"),
+                                      ("no_groups", "needs row_group and col_group"),
+                                      ("unaligned_groups", "not aligned to 4 bytes")])
+def test_pair_mask_arguments_rejected(lib, case, msg):
+    # the pair-mask fields of the score are checked on the host before anything is launched
+    s = score()
+    if case == "unknown":
+        s.pair_mask = 7
+    elif case == "negative_band":
+        s.pair_mask, s.band = _lib.PAIR_MASKS["band"], -1
+    elif case == "no_groups":
+        s.pair_mask, s.row_group = _lib.PAIR_MASKS["same_group"], FAKE + 0x700000
+    else:
+        s.pair_mask = _lib.PAIR_MASKS["same_group"]
+        s.row_group, s.col_group = FAKE + 0x700000, FAKE + 0x710002
+    p = pairs(N=12, M=12, D=64)
+    assert call_matmul(lib, p, s) == _lib.TP_ERR_INVALID_ARG
+    assert msg in lib.tp_last_error().decode()
+    assert lib.tp_pairwise_softmax_matmul(ctypes.byref(p), ctypes.byref(s), FAKE + 0x200000, 64, FAKE + 0x300000,
+                                          FAKE + 0x380000, None, 0, None) == _lib.TP_ERR_INVALID_ARG
+    assert msg in lib.tp_last_error().decode()
+
+
 def test_other_entries_reject(lib):
     p = pairs(N=10, M=12)
     s = score()
