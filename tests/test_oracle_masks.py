@@ -111,3 +111,35 @@ def test_masked_backward_matches_dense_autograd(kind):
     g2 = oracle.logsumexp_backward(pb, lse, gl.numpy())
     assert np.allclose(g2["dX"], X.grad.numpy(), rtol=1e-10, atol=1e-12)
     assert np.allclose(g2["dY"], Y.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_masks_that_keep_one_pair_per_row_are_closed_forms():
+    # band width 0 on N = M, and a same-group mask whose groups pair each row with one column: the
+    # softmax of a row over a single kept pair is 1, so lse_i = S_i,pi(i), out_i = V_pi(i), dS = 0 (no score
+    # gradient) and dV_pi(i) = dO_i; with causal, row 0 keeps column 0 alone
+    g = torch.Generator().manual_seed(5)
+    n = 17
+    X = torch.randn(n, D, generator=g, dtype=torch.float64)
+    Y = torch.randn(n, D, generator=g, dtype=torch.float64)
+    V = torch.randn(n, C, generator=g, dtype=torch.float64)
+    G = torch.randn(n, C, generator=g, dtype=torch.float64)
+    perm = torch.randperm(n, generator=g)
+    S = 0.3 * (X @ Y.T)
+    cases = [("band", dict(band=0), torch.arange(n)),
+             ("same_group", dict(row_group=torch.arange(n, dtype=torch.int32).numpy(),
+                                 col_group=torch.argsort(perm).to(torch.int32).numpy()), perm)]
+    for kind, kw, pick in cases:
+        pb = oracle.Problem(X, Y, metric="linear", scale=0.3, pair_mask=kind, **kw)
+        out, lse = oracle.softmax_matmul(pb, V)
+        np.testing.assert_allclose(lse, S[torch.arange(n), pick].numpy(), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(out, V[pick].numpy(), rtol=0, atol=1e-14)
+        gr = oracle.softmax_matmul_backward(pb, V, out, lse, G)
+        assert np.abs(gr["dX"]).max() < 1e-13 and np.abs(gr["dY"]).max() < 1e-13
+        dV = np.zeros((n, C))
+        dV[pick.numpy()] = G.numpy()
+        np.testing.assert_allclose(gr["dV"], dV, rtol=0, atol=1e-14)
+    pb = oracle.Problem(X, Y, metric="linear", scale=0.3, pair_mask="causal")
+    out, lse = oracle.softmax_matmul(pb, V)
+    assert abs(lse[0] - float(S[0, 0])) < 1e-14 and np.abs(out[0] - V[0].numpy()).max() < 1e-14
+    # row 1 keeps columns 0 and 1: a two-term log-sum-exp
+    assert abs(lse[1] - float(torch.logsumexp(S[1, :2], 0))) < 1e-13
