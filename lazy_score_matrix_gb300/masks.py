@@ -4,7 +4,8 @@
 A masked pair leaves the consumer's reduction: no term in K @ V, a log-sum-exp, a softmax or a
 displacement, never selected by top-k (rows with fewer than k kept pairs pad with value +-inf and
 index -1), no gradient; a softmax row with no kept pair returns 0. The masks run inside libtp's
-streamed sweeps (the guide runs them on materialised tiles).
+streamed sweeps; attention (fp32, D = C = 64) under a causal or band mask runs on its tensor-core kernels,
+which skip the tiles a mask removes whole (the guide runs pair masks on materialised tiles).
 """
 from __future__ import annotations
 
