@@ -573,11 +573,17 @@ def traffic_for(kernel, workload):
     return None
 
 
+# The sources the tensor-core kernels (the only ones with traffic entries) are compiled from: their
+# translation units and every header those include.
+TC_SOURCES = ("tp_args.h", "tp_device.cuh", "tp_launch.h", "tp_tc.cuh", "tp_tc_attn.cu", "tp_tc_host.h",
+              "tp_tc_lse.cu", "tp_tc_topk.cu")
+
+
 def source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lazy_score_matrix_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in TC_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:12]

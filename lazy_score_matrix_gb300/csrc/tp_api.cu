@@ -148,6 +148,13 @@ tp_status check_score(const tp_score* s, const tp_pairs* p) {
     return TP_OK;
 }
 
+// The band width the kernels read: a width of N + M or more keeps every pair, so wider ones are read as
+// N + M (the tensor-core schedule adds the width to point indices in 64-bit arithmetic).
+int64_t pair_band(const tp_score* s, const tp_pairs* p) {
+    const int64_t all = p->N + p->M;
+    return s->band < all ? s->band : all;
+}
+
 tp_status check_C(int64_t C, const void* V) {
     if (C < 1 || C > 64) return fail(TP_ERR_INVALID_ARG, "C must be in [1, 64]");
     if (!V) return fail(TP_ERR_INVALID_ARG, "V is NULL");
@@ -200,7 +207,7 @@ SweepArgs side_args(const tp_pairs* p, const tp_score* s, bool col) {
     a.affine = (s->row_bias || s->col_bias || s->row_weight || s->col_weight) ? 1 : 0;
     a.pm = (int)s->pair_mask;
     a.pcol = col ? 1 : 0;
-    a.band = s->band;
+    a.band = pair_band(s, p);
     if (s->pair_mask == TP_PAIRS_SAME_GROUP) {
         a.pg = col ? s->col_group : s->row_group;
         a.qg = col ? s->row_group : s->col_group;
@@ -723,7 +730,7 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
         t.lse = static_cast<const float*>(lse);
         t.out = static_cast<float*>(out);
         t.pm = (int)sc->pair_mask;
-        t.band = sc->band;
+        t.band = pair_band(sc, pr);
         t.ws = static_cast<char*>(ws) + lse_tc_workspace(pr->N, pr->M, same);
         const int n2 = launch_attn_fwd_tc(t, st);
         if (n2 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
@@ -926,7 +933,7 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
         t.dV = static_cast<float*>(dV);
         t.accumulate_dK = dX && dX == dY ? 1 : 0;  // same points: the column sweep adds dK onto dQ
         t.pm = (int)sc->pair_mask;
-        t.band = sc->band;
+        t.band = pair_band(sc, pr);
         t.ws = ws;
         const int n = launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream));
         if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");

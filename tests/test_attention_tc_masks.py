@@ -113,3 +113,16 @@ def test_index_masks_run_on_the_tensor_cores(mask, tc):
         lambda: ops.pairwise_softmax_matmul_backward(Q, K, V, sc, holder["o"], holder["l"], G))
     want = {"lse_fwd_tc", "attn_fwd_tc", "attn_bwd_row_tc", "attn_bwd_col_tc"}
     assert (want <= names) == tc, names
+
+
+@pytest.mark.parametrize("D", [64, 16])
+def test_band_wider_than_the_problem_keeps_every_pair(oracle, D):
+    # widths of N + M and far beyond (the tensor-core schedule adds the width to point indices): every
+    # pair is kept, on the tensor cores (D = 64) and on the streamed sweeps (D = 16)
+    N, M = 300, 517
+    C = 64 if D == 64 else 8
+    Q, K, V, G = _n(41, N, D), _n(42, M, D), _n(43, M, C), _n(44, N, C)
+    unmasked, _ = oracle.softmax_matmul(oracle.Problem(Q, K, metric="linear", scale=0.125), V)
+    for w in (N + M, 2 ** 40, 2 ** 62):
+        out, _, _ = _check(oracle, Q, K, V, G, "band", band=w, what=f"band {w} D {D}")
+        assert_close(out, unmasked, TOL_F32_FWD, f"band {w} D {D} vs unmasked", abs_floor=1e-3 * float(V.abs().max()))

@@ -1,0 +1,32 @@
+"""The DRAM-traffic figures bench.py reports are keyed to a hash of the sources the tensor-core kernels
+are compiled from (CPU only): that set must be the whole include closure of their translation units, so
+that a change to any file those kernels are built from voids the recorded figures."""
+import os
+import re
+
+import bench
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "lazy_score_matrix_gb300", "csrc")
+
+
+def test_traffic_hash_covers_every_source_of_the_tensor_core_kernels():
+    units = [f for f in os.listdir(CSRC) if f.startswith("tp_tc") and f.endswith(".cu")]
+    seen, todo = set(), list(units)
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        todo += re.findall(r'#include "([^"]+)"', open(os.path.join(CSRC, f)).read())
+    assert sorted(seen) == sorted(bench.TC_SOURCES)
+
+
+def test_bench_reports_only_traffic_taken_on_the_current_sources():
+    # every line of the committed summary carries the hash it was captured on: bench.py reports the lines
+    # on the current sources and null for the others
+    h = bench.source_hash()
+    lines = [l.split() for l in open(os.path.join(bench.ROOT, "profiles", "traffic.txt")) if not l.startswith("#")]
+    for kernel, workload, value, src in (l[:4] for l in lines if len(l) >= 4):
+        want = float(value) if src == f"src={h}" else None
+        if want is not None or not any(m[:2] == [kernel, workload] and m[3] == f"src={h}" for m in lines):
+            assert bench.traffic_for(kernel, workload) == want
