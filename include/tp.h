@@ -86,7 +86,8 @@ typedef enum { TP_PAIRS_ALL = 0, TP_PAIRS_CAUSAL = 1, TP_PAIRS_BAND = 2, TP_PAIR
 
 /* The canonical score (see the file comment). Bias and weight pointers are device arrays of the
  * problem's dtype, [N] for rows and [M] for columns, or NULL when absent. gamma is used by TP_RBF
- * only. pair_mask selects a pair mask (above); band (>= 0) is read by TP_PAIRS_BAND only; row_group
+ * only. pair_mask selects a pair mask (above); band (>= 0) is read by TP_PAIRS_BAND only (any width of
+ * N + M or more keeps every pair); row_group
  * [N] and col_group [M] are int32 device arrays read by TP_PAIRS_SAME_GROUP only (NULL otherwise). */
 typedef struct {
     tp_metric metric;
