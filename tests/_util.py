@@ -44,7 +44,22 @@ def rel_err(got, want, floor_frac=FLOOR, abs_floor=0.0):
     return float((np.abs(g - w) / (np.abs(w) + floor)).max())
 
 
+def other_errors(got, want):
+    """The two measures reported beside rel_err when a check fails: the normwise error |a - b| / |b| over
+    the finite entries and the elementwise relative error without a floor."""
+    g, w = to_np(got), to_np(want)
+    fin = np.isfinite(w) & np.isfinite(g)
+    g, w = g[fin], w[fin]
+    nw = float(np.linalg.norm(g - w) / np.linalg.norm(w)) if np.linalg.norm(w) > 0 else float(np.abs(g).max(initial=0))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ew = np.where(w != 0, np.abs(g - w) / np.abs(w), np.where(g == w, 0.0, np.inf))
+    return nw, float(ew.max(initial=0.0))
+
+
 def assert_close(got, want, tol, what="", floor_frac=FLOOR, abs_floor=0.0):
     e = rel_err(got, want, floor_frac, abs_floor)
-    assert e <= tol, f"{what}: max relative error {e:.3g} > {tol:g}"
+    if e > tol:
+        nw, ew = other_errors(got, want)
+        raise AssertionError(f"{what}: max relative error {e:.3g} > {tol:g} (normwise {nw:.3g}, elementwise "
+                             f"without a floor {ew:.3g})")
     return e
