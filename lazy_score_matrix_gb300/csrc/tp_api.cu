@@ -82,6 +82,11 @@ Plan plan_split(int64_t nP, int64_t nQ) {
 
 size_t esize(tp_dtype t) { return t == TP_F64 ? 8 : 4; }
 
+// X and Y are the same points: one pointer AND one count. A caller may pass Y = Z and X = Z[:N] with
+// N < M (the same pointer, fewer rows); the tensor-core paths then must not treat the two as one set,
+// since a workspace copy of X holds only N rows.
+bool same_points(const tp_pairs* p) { return p->X == p->Y && p->N == p->M; }
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Span {
@@ -389,12 +394,12 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     if (e == "pairwise_softmax_matmul") {
         const size_t simt = partial_bytes(r, fwd_width(kSoftmax, D, (int)C), es);
         if (!(kTcAttention && attn_tc_shape(p, C))) return simt;
-        return std::max(simt, lse_tc_workspace(p->N, p->M, p->X == p->Y && p->N == p->M) +
+        return std::max(simt, lse_tc_workspace(p->N, p->M, same_points(p)) +
                                   attn_tc_workspace(p->N, p->M, false));
     }
     if (e == "pairwise_logsumexp") {
         const size_t simt = partial_bytes(r, fwd_width(kLse, D, 0), es);
-        return lse_tc_shape(p) ? std::max(simt, lse_tc_workspace(p->N, p->M, p->X == p->Y)) : simt;
+        return lse_tc_shape(p) ? std::max(simt, lse_tc_workspace(p->N, p->M, same_points(p))) : simt;
     }
     if (e == "pairwise_displacement") return partial_bytes(r, fwd_width(kDisp, D, 0), es);
     if (e == "svgd_direction") return partial_bytes(r, fwd_width(kSvgd, D, 0), es);
@@ -402,7 +407,7 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
         if (k < 1 || k > p->M || k > kTopkMax) return (size_t)-1;
         const int K = topk_bucket(k);
         const size_t simt = r.splits > 1 ? align_up((size_t)r.splits * K * r.nP * (es + 4)) : 0;
-        return kTcTopk && topk_tc_shape(p, k) ? std::max(simt, topk_tc_workspace(p->N, p->M, D, k, p->X == p->Y)) : simt;
+        return kTcTopk && topk_tc_shape(p, k) ? std::max(simt, topk_tc_workspace(p->N, p->M, D, k, same_points(p))) : simt;
     }
     if (e == "pairwise_matmul_backward") return bwd_ws(p, kBMatmul, C, 0);
     if (e == "pairwise_softmax_matmul_backward") {
@@ -411,7 +416,7 @@ size_t ws_size(const char* entry, const tp_pairs* p, int64_t C, int k) {
     }
     if (e == "pairwise_logsumexp_backward") {
         const size_t simt = bwd_ws(p, kBLse, 0, 0);
-        const bool sym = p->X == p->Y && p->N == p->M;
+        const bool sym = same_points(p);
         return kTcBackward && lse_tc_shape(p) && sym ? std::max(simt, lse_bwd_tc_workspace(p->N)) : simt;
     }
     if (e == "pairwise_displacement_backward") return bwd_ws(p, kBDisp, 0, 0);
@@ -463,7 +468,7 @@ tp_status check_grads(const tp_pairs* pr, const tp_score* sc, const Grads& g, in
     if (g.dwc && !sc->col_weight)
         return fail(TP_ERR_INVALID_ARG, "d_col_weight given but the score has no column weight");
     const bool same = g.dX && g.dX == g.dY;
-    if (same && !(pr->X == pr->Y && pr->N == pr->M))
+    if (same && !same_points(pr))
         return fail(TP_ERR_INVALID_ARG, "dX and dY may only coincide when X and Y are the same points");
     std::vector<Span> sp = score_spans(sc, pr);
     in.insert(in.end(), sp.begin(), sp.end());
@@ -685,7 +690,7 @@ tp_status tp_pairwise_logsumexp(const tp_pairs* pr, const tp_score* sc, int excl
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (lse_tc_eligible(pr, sc)) {
-        const int n = launch_lse_tc(a, lse, pr->X == pr->Y, st);
+        const int n = launch_lse_tc(a, lse, same_points(pr), st);
         if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
         return launched(n);
     }
@@ -717,7 +722,7 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (attn_tc_eligible(pr, sc, C, {V, out, lse})) {
         // the row log-sum-exp first, then P V with P = exp(S - lse): no running rescale of the output
-        const bool same = pr->X == pr->Y && pr->N == pr->M;
+        const bool same = same_points(pr);
         const int n1 = launch_lse_tc(a, lse, same, st);
         if (n1 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
         AttnTcArgs t{};
@@ -805,7 +810,7 @@ tp_status tp_pairwise_topk(const tp_pairs* pr, const tp_score* sc, int k, int la
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (topk_tc_eligible(pr, sc, k)) {
-        const int n = launch_topk_tc(a, values, indices, pr->X == pr->Y, st);
+        const int n = launch_topk_tc(a, values, indices, same_points(pr), st);
         if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
         return launched(n);
     }
@@ -876,7 +881,7 @@ tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pr, const tp_score* sc,
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Same points, summed gradient wanted, no row/column parameters: the score is symmetric and one
     // sweep gives sum_j (H_kj + H_jk) dt_kj/dz_k, each pair evaluated once.
-    const bool symmetric = dX && dX == dY && pr->X == pr->Y && pr->N == pr->M && !sc->row_bias && !sc->col_bias &&
+    const bool symmetric = dX && dX == dY && same_points(pr) && !sc->row_bias && !sc->col_bias &&
                            !sc->row_weight && !sc->col_weight && sc->pair_mask == TP_PAIRS_ALL;
     if (symmetric) {
         row.gP = dX;
