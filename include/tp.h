@@ -37,8 +37,12 @@
  *                           with N != M, output aliasing an input or another output (except the
  *                           documented dX/dY alias), misaligned pointer, workspace too small.
  *       TP_ERR_UNSUPPORTED  a valid request this build has no kernel for.
- *       TP_ERR_CUDA         a CUDA launch error (the runtime's error text is in tp_last_error()).
- *     There is no CPU fallback.
+ *       TP_ERR_CUDA         a CUDA launch error (the runtime's error text is in tp_last_error()), or a
+ *                           fault injected before launch (TP_FAULT_INJECT, see tp_device_status).
+ *     Device-side conditions are not known when a call returns: the warps of the tensor-core kernels
+ *     wait on one another with bounded waits (2 s), and a wait that gives up records a code in a
+ *     per-device error word instead of trapping; tp_device_status reads it after the caller has
+ *     synchronised (TP_ERR_TIMEOUT). There is no CPU fallback.
  *   - Backward outputs are written, not accumulated. A NULL gradient output means "not requested";
  *     its work is skipped. When X and Y are the same points (X == Y, N == M), dY may be the same
  *     pointer as dX: the sum dX + dY is then written there.
@@ -69,7 +73,7 @@ typedef enum {
     TP_ERR_UNSUPPORTED = 2,
     TP_ERR_CUDA = 3,
     TP_ERR_WORKSPACE = 4, /* reserved: a too-small workspace is reported as TP_ERR_INVALID_ARG */
-    TP_ERR_TIMEOUT = 5    /* reserved: no kernel of this build waits on another block */
+    TP_ERR_TIMEOUT = 5    /* a bounded wait inside a kernel gave up (reported by tp_device_status) */
 } tp_status;
 
 typedef enum { TP_F32 = 0, TP_F64 = 1 } tp_dtype;
@@ -119,8 +123,8 @@ TP_API tp_status tp_pairwise_matmul(const tp_pairs* pairs, const tp_score* score
 
 /* Row log-sum-exp lse_i = log sum_j exp(S_ij), lse [N]; with exclude_self != 0 the pair j == i is
  * left out (requires N == M; a row with no pair left gives -inf).
- * Guide "Task Map", InfoNCE / NT-XEnt row: S.logsumexp(-1, exclude_self=True); "Score Expressions"
- * example -logits.logsumexp(-1).mean(). */
+ * Guide "Task Map", InfoNCE / NT-XEnt row (a log-sum-exp over the last axis with the self pair
+ * excluded); "Score Expressions" example (the loss is minus the mean of the row log-sum-exp). */
 TP_API tp_status tp_pairwise_logsumexp(const tp_pairs* pairs, const tp_score* score, int exclude_self,
                                 void* lse, void* ws, size_t ws_bytes, void* stream);
 
@@ -163,8 +167,10 @@ TP_API tp_status tp_pairwise_topk(const tp_pairs* pairs, const tp_score* score, 
  * There is no workspace argument: the scratch is a fixed 16 MiB array of device memory owned by this
  * library, held on every GPU that loads it until the process exits. A problem whose workspace
  * (tp_workspace_size("pairwise_logsumexp", ...)) exceeds 16 MiB is rejected with TP_ERR_INVALID_ARG
- * and a message in tp_last_error(): with fp32 and D = 64 that is beyond about 30000 distinct points
- * (N, plus M when Y is not X); other shapes need at most 2.4 MiB.
+ * and a message in tp_last_error(), before anything is launched. Only fp32 with D = 64 (the
+ * tensor-core path, which keeps an fp16 hi/lo copy of the points) can exceed it: beyond N = 54542 when
+ * Y is X (the same array and count), or beyond N + M of about 55000 when they differ. Every other shape
+ * needs at most 2 MiB.
  * The first call on a device looks up the array's address (with that device current); make that
  * first call before any stream capture. Every call shares the array and finds the previous call's
  * contents there; nothing in it needs clearing, but calls whose GPU work overlaps (different streams
@@ -174,7 +180,7 @@ TP_API tp_status tp_pairwise_logsumexp_noalloc(const tp_pairs* pairs, const tp_s
                                                void* lse, void* stream);
 
 /* ---------------------------------------------------------------------------------------------- */
-/* backward by replay (guide introduction: "First derivatives replay the tiles")                  */
+/* backward by replay (torchpairwise guide, "Using Torchpairwise in Models", introduction)       */
 /* Inputs are the forward's inputs plus the upstream gradient; outputs are gradients with the     */
 /* shapes of X [N,D], Y [M,D], V [M,C], row bias/weight [N], column bias/weight [M]. A gradient   */
 /* for a bias or weight that the score does not have must be NULL.                                */
@@ -265,6 +271,29 @@ TP_API void tp_set_launch_hook(tp_launch_hook hook, void* user);
 TP_API tp_status tp_timer_start(int64_t capacity);
 TP_API int64_t tp_timer_stop(void);
 TP_API tp_status tp_timer_read(int64_t index, const char** kernel, float* ms);
+
+/* Device-side status of the current device: TP_OK, or TP_ERR_TIMEOUT when a bounded wait inside one of
+ * this library's kernels gave up since the word was last reset (the message in tp_last_error() names the
+ * kernel and the wait's site code). The results of the call whose kernel gave up are invalid. The word is
+ * one per device and sticky: every kernel on every stream writes the same word, and the first code is
+ * kept until reset != 0 clears it. The read is synchronous (cudaMemcpy on the legacy default stream);
+ * call it after synchronising the streams whose work it should cover. TP_ERR_CUDA if the word cannot be
+ * read. The first call of any entry point on a device looks up the word's address (with that device
+ * current); make it before any stream capture.
+ * The method's "What to Check" section (torchpairwise guide) has solvers report a status beside their
+ * result; this is that convention for device-side waits.
+ * Host-side fault injection for tests: with TP_FAULT_INJECT=<entry> in the environment (the entry point's
+ * name without "tp_", e.g. "pairwise_logsumexp"), that entry returns TP_ERR_CUDA after validating its
+ * arguments and before launching anything. The variable is read on every call. */
+TP_API tp_status tp_device_status(int reset);
+
+/* Self-test of the device-side status path: launches on `stream` one block whose single mbarrier wait
+ * expects an arrival that never comes, bounded by limit_ns (1000 to 2e9 ns); the wait gives up, records
+ * its code in the error word and the kernel returns. Nothing else is in flight in that kernel (no copy,
+ * no tensor-core operation, no tensor memory), so giving up leaves the device usable. A following
+ * tp_device_status (after synchronising) reports TP_ERR_TIMEOUT. TP_ERR_INVALID_ARG for a limit outside
+ * the range. The guide has no counterpart; it exists to test the convention above. */
+TP_API tp_status tp_selftest_bounded_wait(int64_t limit_ns, void* stream);
 
 #ifdef __cplusplus
 }

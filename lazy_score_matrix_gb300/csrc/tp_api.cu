@@ -33,6 +33,11 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s);                    
 int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s);                    // tp_tc_attn.cu
 }  // namespace tp
 
+namespace tp {
+tp_status launched(int n);
+tp_status injected_fault(const char* entry);  // tp_status.cu: TP_FAULT_INJECT
+}  // namespace tp
+
 namespace {
 
 thread_local std::string g_err;
@@ -268,11 +273,12 @@ bool topk_tc_eligible(const tp_pairs* p, const tp_score* s, int k) {
            !s->col_weight && s->pair_mask == TP_PAIRS_ALL;
 }
 
-tp_status launched(int n) {
-    g_launches += n;
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(TP_ERR_CUDA, std::string("CUDA launch failed: ") + cudaGetErrorString(e));
-    return TP_OK;
+// A tensor-core launcher's result: kernels launched, or -1 (a TMA tensor map could not be encoded), or -3
+// (the device error word could not be looked up; the reason is already in tp_last_error).
+tp_status tc_launched(int n) {
+    if (n == -3) return TP_ERR_CUDA;
+    if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+    return launched(n);
 }
 
 template <int V>
@@ -555,6 +561,13 @@ int run_backward(const SweepArgs& row, const SweepArgs& col, const Grads& g, cud
 namespace tp {
 void set_last_error(const std::string& msg) { g_err = msg; }
 
+tp_status launched(int n) {
+    g_launches += n;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(TP_ERR_CUDA, std::string("CUDA launch failed: ") + cudaGetErrorString(e));
+    return TP_OK;
+}
+
 void launch_hook(const char* kernel, int phase, cudaStream_t s) {
     if (g_timer.on && g_timer.count < g_timer.capacity) {
         cudaEventRecord(g_timer.ev[2 * g_timer.count + phase], s);
@@ -665,6 +678,7 @@ tp_status tp_pairwise_matmul(const tp_pairs* pr, const tp_score* sc, const void*
     a.vecV = (cpad_bucket(a.C) == a.C && aligned(V, 16)) ? 1 : 0;
     a.out = out;
     a.ws = ws;
+    TP_CHECK(injected_fault("pairwise_matmul"));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return by_dtype(pr->dtype, [&](auto t) {
         using T = decltype(t);
@@ -684,15 +698,14 @@ tp_status tp_pairwise_logsumexp(const tp_pairs* pr, const tp_score* sc, int excl
     in.push_back({pr->Y, pr->M * pr->D * es, "Y"});
     TP_CHECK(check_alias(in, {{lse, pr->N * es, "lse"}, {ws, ws_bytes, "ws"}}));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_logsumexp", pr, 0, 0)));
+    TP_CHECK(injected_fault("pairwise_logsumexp"));
     SweepArgs a = side_args(pr, sc, false);
     a.exclude_self = exclude_self ? 1 : 0;
     a.out = lse;
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (lse_tc_eligible(pr, sc)) {
-        const int n = launch_lse_tc(a, lse, same_points(pr), st);
-        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
-        return launched(n);
+        return tc_launched(launch_lse_tc(a, lse, same_points(pr), st));
     }
     return by_dtype(pr->dtype, [&](auto t) { return launched(run_fwd_plain<decltype(t), kLse>(a, st)); });
 }
@@ -712,6 +725,7 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
     in.push_back({V, pr->M * C * es, "V"});
     TP_CHECK(check_alias(in, {{out, pr->N * C * es, "out"}, {lse, pr->N * es, "lse"}, {ws, ws_bytes, "ws"}}));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_softmax_matmul", pr, C, 0)));
+    TP_CHECK(injected_fault("pairwise_softmax_matmul"));
     SweepArgs a = side_args(pr, sc, false);
     a.C = (int)C;
     a.Vq = V;
@@ -724,7 +738,7 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
         // the row log-sum-exp first, then P V with P = exp(S - lse): no running rescale of the output
         const bool same = same_points(pr);
         const int n1 = launch_lse_tc(a, lse, same, st);
-        if (n1 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        if (n1 < 0) return tc_launched(n1);
         AttnTcArgs t{};
         t.Q = static_cast<const float*>(pr->X);
         t.K = static_cast<const float*>(pr->Y);
@@ -738,7 +752,10 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
         t.band = pair_band(sc, pr);
         t.ws = static_cast<char*>(ws) + lse_tc_workspace(pr->N, pr->M, same);
         const int n2 = launch_attn_fwd_tc(t, st);
-        if (n2 < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
+        if (n2 < 0) {
+            launched(n1);
+            return tc_launched(n2);
+        }
         return launched(n1 + n2);
     }
     return by_dtype(pr->dtype, [&](auto t) { return launched(run_fwd_vals<decltype(t), kSoftmax>(a, st)); });
@@ -755,6 +772,7 @@ tp_status tp_pairwise_displacement(const tp_pairs* pr, const tp_score* sc, void*
     in.push_back({pr->Y, pr->M * pr->D * es, "Y"});
     TP_CHECK(check_alias(in, {{out, pr->N * pr->D * es, "out"}, {ws, ws_bytes, "ws"}}));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_displacement", pr, 0, 0)));
+    TP_CHECK(injected_fault("pairwise_displacement"));
     SweepArgs a = side_args(pr, sc, false);
     a.out = out;
     a.ws = ws;
@@ -772,6 +790,7 @@ tp_status tp_svgd_direction(const tp_pairs* pr, double gamma, const void* score,
                             {score, pr->M * pr->D * es, "score"}};
     TP_CHECK(check_alias(in, {{phi, pr->N * pr->D * es, "phi"}, {ws, ws_bytes, "ws"}}));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("svgd_direction", pr, 0, 0)));
+    TP_CHECK(injected_fault("svgd_direction"));
     tp_score s;
     std::memset(&s, 0, sizeof s);
     s.metric = TP_RBF;
@@ -802,6 +821,7 @@ tp_status tp_pairwise_topk(const tp_pairs* pr, const tp_score* sc, int k, int la
     TP_CHECK(check_alias(in, {{values, (size_t)(pr->N * k) * es, "values"}, {indices, (size_t)(pr->N * k) * 8, "indices"},
                               {ws, ws_bytes, "ws"}}));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_topk", pr, 0, k)));
+    TP_CHECK(injected_fault("pairwise_topk"));
     SweepArgs a = side_args(pr, sc, false);
     a.k = k;
     a.largest = largest ? 1 : 0;
@@ -810,9 +830,7 @@ tp_status tp_pairwise_topk(const tp_pairs* pr, const tp_score* sc, int k, int la
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (topk_tc_eligible(pr, sc, k)) {
-        const int n = launch_topk_tc(a, values, indices, same_points(pr), st);
-        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
-        return launched(n);
+        return tc_launched(launch_topk_tc(a, values, indices, same_points(pr), st));
     }
     return by_dtype(pr->dtype, [&](auto t) {
         using T = decltype(t);
@@ -846,6 +864,7 @@ tp_status tp_pairwise_matmul_backward(const tp_pairs* pr, const tp_score* sc, co
     TP_CHECK(check_grads(pr, sc, g, C, {{V, pr->M * C * es, "V"}, {grad_out, pr->N * C * es, "grad_out"}}, ws,
                          ws_bytes));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_matmul_backward", pr, C, 0)));
+    TP_CHECK(injected_fault("pairwise_matmul_backward"));
     SweepArgs row = side_args(pr, sc, false), col = side_args(pr, sc, true);
     row.C = col.C = (int)C;
     row.Vp = grad_out;
@@ -873,6 +892,7 @@ tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pr, const tp_score* sc,
     TP_CHECK(check_grads(pr, sc, g, 1, {{lse, pr->N * es, "lse"}, {grad_lse, pr->N * es, "grad_lse"}}, ws,
                          ws_bytes));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_logsumexp_backward", pr, 0, 0)));
+    TP_CHECK(injected_fault("pairwise_logsumexp_backward"));
     SweepArgs row = side_args(pr, sc, false), col = side_args(pr, sc, true);
     row.lse = col.lse = lse;
     row.glse = col.glse = grad_lse;
@@ -886,9 +906,7 @@ tp_status tp_pairwise_logsumexp_backward(const tp_pairs* pr, const tp_score* sc,
     if (symmetric) {
         row.gP = dX;
         if (kTcBackward && lse_tc_eligible(pr, sc)) {
-            const int n = launch_lse_bwd_sym_tc(row, st);
-            if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
-            return launched(n);
+            return tc_launched(launch_lse_bwd_sym_tc(row, st));
         }
         return by_dtype(pr->dtype, [&](auto t) {
             using T = decltype(t);
@@ -922,6 +940,7 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
                          ws, ws_bytes));
     const size_t need = ws_size("pairwise_softmax_matmul_backward", pr, C, 0);
     TP_CHECK(check_ws(ws, ws_bytes, need));
+    TP_CHECK(injected_fault("pairwise_softmax_matmul_backward"));
     if (attn_tc_eligible(pr, sc, C, {V, out, lse, grad_out, dX, dY, dV})) {
         AttnTcArgs t{};
         t.Q = static_cast<const float*>(pr->X);
@@ -940,9 +959,7 @@ tp_status tp_pairwise_softmax_matmul_backward(const tp_pairs* pr, const tp_score
         t.pm = (int)sc->pair_mask;
         t.band = pair_band(sc, pr);
         t.ws = ws;
-        const int n = launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream));
-        if (n < 0) return fail(TP_ERR_CUDA, "could not encode the TMA tensor maps (cuTensorMapEncodeTiled)");
-        return launched(n);
+        return tc_launched(launch_attn_bwd_tc(t, static_cast<cudaStream_t>(stream)));
     }
     // workspace: delta [N] first, partial states after it
     void* delta = ws;
@@ -980,6 +997,7 @@ tp_status tp_pairwise_displacement_backward(const tp_pairs* pr, const tp_score* 
     const Grads g{dX, dY, nullptr, d_row_bias, d_col_bias, d_row_weight, d_col_weight};
     TP_CHECK(check_grads(pr, sc, g, 1, {{grad_out, pr->N * pr->D * es, "grad_out"}}, ws, ws_bytes));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_displacement_backward", pr, 0, 0)));
+    TP_CHECK(injected_fault("pairwise_displacement_backward"));
     SweepArgs row = side_args(pr, sc, false), col = side_args(pr, sc, true);
     row.Vp = grad_out;
     col.Vq = grad_out;
@@ -1005,6 +1023,7 @@ tp_status tp_pairwise_topk_backward(const tp_pairs* pr, const tp_score* sc, int 
                          {{indices, (size_t)(pr->N * k) * 8, "indices"}, {grad_values, (size_t)(pr->N * k) * es, "grad_values"}}, ws,
                          ws_bytes));
     TP_CHECK(check_ws(ws, ws_bytes, ws_size("pairwise_topk_backward", pr, 0, k)));
+    TP_CHECK(injected_fault("pairwise_topk_backward"));
     SweepArgs row = side_args(pr, sc, false), col = side_args(pr, sc, true);
     row.k = col.k = k;
     row.gP = dX;

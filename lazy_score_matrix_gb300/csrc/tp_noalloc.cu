@@ -32,10 +32,10 @@ void set_last_error(const std::string& msg);  // tp_api.cu: the text tp_last_err
 
 namespace {
 
-// 16 MiB per device. The SIMT log-sum-exp needs at most about 1.2 MiB (fp32) or 2.4 MiB (fp64) for
-// any shape; the fp32 D = 64 tensor-core path needs the hi/lo split of the points (512 bytes per
-// distinct point) and 4 KiB of partials per row block of 128 points plus 0.6 MiB, so it fits up to
-// ~29000 distinct points. Larger problems are rejected by the size check below.
+// 16 MiB per device. The streamed (SIMT) log-sum-exp needs at most 2 MiB for any shape; the fp32 D = 64
+// tensor-core path keeps an fp16 hi/lo copy of the points (256 bytes per point, once when Y is X) and
+// 4 KiB of partials per row block of 128 rows plus 0.6 MiB, so it fits up to N = 54542 when Y is X and
+// up to N + M of about 55000 when they differ. Larger problems are rejected by the size check below.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

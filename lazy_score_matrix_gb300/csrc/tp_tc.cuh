@@ -13,6 +13,9 @@ namespace tp {
 namespace tc {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait on an mbarrier gives up after 2 s
+// Site codes recorded by a wait that gives up: 1 the self-test (tp_status.cu), 11-18 lse_fwd_tc, 21-34
+// lse_bwd_sym_tc, 41-53 the attention sweeps, 61-71 lse_bwd_lin_tc, 81-86 topk_tc.
+constexpr int kSelfTestCode = 1;
 constexpr uint32_t kSuspendNs = 20000;                   // longest a single poll may sleep in hardware
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -41,15 +44,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-// Wait for the phase with the given parity to complete; false (and *err set) after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
+// Wait for the phase with the given parity to complete; false after limit_ns, with `code` recorded in
+// the library's device error word *err unless an earlier code is there (the first failure is kept;
+// tp_device_status reads it back on the host).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code,
+                                          unsigned long long limit_ns = kWaitNs) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitNs) break;
+        if (globaltimer_ns() - t0 > limit_ns) break;
     }
-    atomicExch(err, code);
+    atomicCAS(err, 0, code);
     return false;
 }
 

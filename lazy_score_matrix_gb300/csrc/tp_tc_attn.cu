@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(256) attn_split(const float* __restrict__ A, c
 struct Plan {
     int64_t Npad, Mpad;
     size_t off_qh, off_ql, off_dh, off_dl, off_qst, off_kh, off_kl, off_vh, off_vl, off_kst, off_part, off_cntq,
-        off_cntk, off_pfxq, off_pfxk, off_gmax, off_err, bytes;
+        off_cntk, off_pfxq, off_pfxk, off_gmax, bytes;
 };
 
 static Plan plan_of(int64_t N, int64_t M, bool backward) {
@@ -686,7 +686,6 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
     pl.off_pfxq = o; o += al256((size_t)(RBq + 1) * 8);
     pl.off_pfxk = o; o += al256((size_t)(RBk + 1) * 8);
     pl.off_gmax = o; o += 256;
-    pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
 }
@@ -742,6 +741,8 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     using namespace tc;
     using namespace tc::attn;
     const Plan pl = plan_of(a.N, a.M, false);
+    int* err = device_error_word();
+    if (!err) return -3;
     char* ws = static_cast<char*>(a.ws);
     __half2* qh = reinterpret_cast<__half2*>(ws + pl.off_qh);
     __half2* ql = reinterpret_cast<__half2*>(ws + pl.off_ql);
@@ -781,7 +782,7 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     }
     return 4 + run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part),
                                cntq, a.out, nullptr, 0, a.pm, a.band, reinterpret_cast<int64_t*>(ws + pl.off_pfxq),
-                               reinterpret_cast<int*>(ws + pl.off_err), "attn_fwd_tc", s);
+                               err, "attn_fwd_tc", s);
 }
 
 // Backward: dQ (row sweep) and dK, dV (column sweep); null outputs are not written (a sweep none of whose
@@ -792,6 +793,8 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     using namespace tc;
     using namespace tc::attn;
     const Plan pl = plan_of(a.N, a.M, true);
+    int* err = device_error_word();
+    if (!err) return -3;
     char* ws = static_cast<char*>(a.ws);
     __half2* qh = reinterpret_cast<__half2*>(ws + pl.off_qh);
     __half2* ql = reinterpret_cast<__half2*>(ws + pl.off_ql);
@@ -807,7 +810,6 @@ int launch_attn_bwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     int* cntk = reinterpret_cast<int*>(ws + pl.off_cntk);
     int* gm = reinterpret_cast<int*>(ws + pl.off_gmax);
     float* part = reinterpret_cast<float*>(ws + pl.off_part);
-    int* err = reinterpret_cast<int*>(ws + pl.off_err);
     // row sweep maps: A = (Q, dO) in 128-row boxes, B = (K, V) in 64-row boxes; column sweep the reverse
     CUtensorMap mr[8], mc[8];
     if (!make_map_f16(&mr[0], qh, pl.Npad, kBM) || !make_map_f16(&mr[1], ql, pl.Npad, kBM) ||

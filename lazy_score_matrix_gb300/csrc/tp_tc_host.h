@@ -8,6 +8,11 @@
 #include <mutex>
 
 namespace tp {
+
+// The library's device error word on the current device (tp_status.cu), written by a bounded wait that
+// gives up; nullptr (reason in tp_last_error) if its address cannot be looked up.
+int* device_error_word();
+
 namespace tc {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

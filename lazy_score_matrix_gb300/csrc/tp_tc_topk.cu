@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
             for (UnitCursor cur(p); cur.valid && ok; ++i, cur.next(p)) {
                 const int rb = cur.rb, ct = cur.ct;
                 if (rb != rb_cur) {
-                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 31);
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 81);
                     if (!ok) break;
                     mbar_expect_tx(a_full, SH::kPair);
                     for (int c = 0; c < SH::kChunks; ++c) {
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                     rb_cur = rb;
                 }
                 const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages);
-                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 32);
+                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 82);
                 if (!ok) break;
                 unsigned char* dst = sB + (size_t)s * SH::kPair;
                 mbar_expect_tx(b_full + s, SH::kPair + kKBN * 4);
@@ -187,14 +187,14 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 const int rb = cur.rb;
                 if (rb != rb_cur) {
                     if (a_uses > 0) mma_commit(a_empty);
-                    ok = mbar_wait(a_full, a_uses & 1, p.err, 33);
+                    ok = mbar_wait(a_full, a_uses & 1, p.err, 83);
                     if (!ok) break;
                     ++a_uses;
                     rb_cur = rb;
                 }
                 const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages), b = (int)(i & 1), rr = (int)(i >> 1);
-                ok = mbar_wait(b_full + s, r & 1, p.err, 34);
-                if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 35);
+                ok = mbar_wait(b_full + s, r & 1, p.err, 84);
+                if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 85);
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(b * kKBN);
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 fresh = false;
             }
             const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
-            ok = mbar_wait(acc_full + b, rr & 1, p.err, 36);
+            ok = mbar_wait(acc_full + b, rr & 1, p.err, 86);
             if (!ok) break;
             fence_after_sync();
             const int j0 = ct * kKBN + half * SH::kCols;
@@ -360,7 +360,7 @@ __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int 
 
 struct TopkTcPlan {
     int CT, G, DP, KB, H, U, chunk;
-    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, off_err, bytes;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, bytes;
 };
 
 inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
@@ -391,7 +391,6 @@ inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     const size_t lists = (size_t)pl.U * kKLists * pl.KB * kKBM;
     pl.off_pv = o; o += al256(lists * 4);
     pl.off_pi = o; o += al256(lists * 4);
-    pl.off_err = o; o += 256;
     pl.bytes = o;
     return pl;
 }
@@ -406,6 +405,8 @@ size_t topk_tc_workspace(int64_t N, int64_t M, int D, int k, bool same) {
 int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same, cudaStream_t s) {
     using namespace tc;
     const TopkTcPlan pl = topk_tc_plan(a.nP, a.nQ, a.D, a.k, same);
+    int* err = device_error_word();
+    if (!err) return -3;
     char* ws = static_cast<char*>(a.ws);
     float* xh = reinterpret_cast<float*>(ws + pl.off_xh);
     float* xl = reinterpret_cast<float*>(ws + pl.off_xl);
@@ -451,7 +452,7 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     p.yn = yn;
     p.pv = reinterpret_cast<float*>(ws + pl.off_pv);
     p.pi = reinterpret_cast<int*>(ws + pl.off_pi);
-    p.err = reinterpret_cast<int*>(ws + pl.off_err);
+    p.err = err;
     auto go = [&](auto kernel, size_t smem) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         HookScope h("topk_tc", s);

@@ -33,7 +33,7 @@ def score(metric=1, **kw):
 
 def test_exports_every_header_symbol(lib):
     declared = _lib.header_symbols()
-    assert len(declared) == 20, declared
+    assert len(declared) == 22, declared
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     missing = [s for s in declared if s not in exported]
@@ -190,3 +190,55 @@ def test_package_does_not_import_the_oracle():
         text = f.read_text()
         assert not re.search(r"^\s*(from|import)\s+oracle", text, flags=re.M), f
         assert "tp_oracle" not in text and "or_matmul" not in text, f
+
+
+def test_fault_injection_fails_the_named_entry_before_launch(lib, monkeypatch):
+    """TP_FAULT_INJECT=<entry>: that entry validates its arguments, then returns TP_ERR_CUDA without
+    launching anything (the fake device addresses are never touched); invalid arguments still win."""
+    p = pairs(10, 10, 3)
+    sc = score()
+    monkeypatch.setenv("TP_FAULT_INJECT", "pairwise_logsumexp")
+    _lib.launch_count(reset=True)
+    st = lib.tp_pairwise_logsumexp(ctypes.byref(p), ctypes.byref(sc), 0, FAKE + 0x200000, None, 0, None)
+    assert st == _lib.TP_ERR_CUDA
+    assert b"fault injected" in lib.tp_last_error()
+    assert _lib.launch_count() == 0
+    # validation runs first: a NULL output is still an invalid argument
+    assert lib.tp_pairwise_logsumexp(ctypes.byref(p), ctypes.byref(sc), 0, None, None, 0, None) == \
+        _lib.TP_ERR_INVALID_ARG
+    # the no-alloc entry point goes through the same entry (the shape needs no scratch here)
+    st = lib.tp_pairwise_logsumexp_noalloc(ctypes.byref(p), ctypes.byref(sc), 0, FAKE + 0x200000, None)
+    assert st == _lib.TP_ERR_CUDA and b"fault injected" in lib.tp_last_error()
+    for name, call in (
+            ("pairwise_matmul", lambda: lib.tp_pairwise_matmul(ctypes.byref(p), ctypes.byref(sc), FAKE + 0x300000, 4,
+                                                               FAKE + 0x400000, None, 0, None)),
+            ("pairwise_topk", lambda: lib.tp_pairwise_topk(ctypes.byref(p), ctypes.byref(sc), 3, 0, FAKE + 0x300000,
+                                                           FAKE + 0x400000, FAKE + 0x1000000, 1 << 30, None))):
+        monkeypatch.setenv("TP_FAULT_INJECT", name)
+        assert call() == _lib.TP_ERR_CUDA, name
+        assert b"fault injected" in lib.tp_last_error()
+    assert _lib.launch_count() == 0
+
+
+def test_selftest_limit_is_checked_on_the_host(lib):
+    assert lib.tp_selftest_bounded_wait(0, None) == _lib.TP_ERR_INVALID_ARG
+    assert lib.tp_selftest_bounded_wait(3 * 10 ** 9, None) == _lib.TP_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_problems_beyond_its_fixed_array(lib):
+    """The no-alloc entry point checks the scratch it needs against its fixed 16 MiB before anything
+    else: fp32 D = 64 beyond N = 54542 with Y the same array is rejected with a message, on the host."""
+    lim = 16 << 20
+    for N, same in ((54542, True), (54543, True), (30000, False)):
+        p = pairs(N, N, 64, X=FAKE, Y=FAKE if same else FAKE + (1 << 36))
+        need = ws(lib, "pairwise_logsumexp", p)
+        assert (need <= lim) == (N == 54542), (N, same, need)
+    for N, same in ((54543, True), (30000, False)):
+        p = pairs(N, N, 64, X=FAKE, Y=FAKE if same else FAKE + (1 << 36))
+        st = lib.tp_pairwise_logsumexp_noalloc(ctypes.byref(p), ctypes.byref(score()), 1, FAKE + (1 << 37), None)
+        assert st == _lib.TP_ERR_INVALID_ARG
+        assert b"fixed array" in lib.tp_last_error()
+    # any other shape fits: the streamed path needs at most 2 MiB
+    for D, dt in ((32, _lib.TP_F32), (64, _lib.TP_F64), (3, _lib.TP_F64)):
+        for N in (1000, 65536, 10 ** 6):
+            assert ws(lib, "pairwise_logsumexp", pairs(N, 10 ** 6, D, dtype=dt)) <= 2 << 20

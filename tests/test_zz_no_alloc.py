@@ -14,16 +14,17 @@ import pytest
 import torch
 
 from lazy_score_matrix_gb300 import _lib, ops, synth
-from tests._util import TOL_F32_FWD, assert_close
+from tests._util import TOL_F32_FWD, TOL_F64, assert_close
 
 pytestmark = pytest.mark.gpu
 
 
 def _call_noalloc(lib, z, scale, exclude_self):
     N, D = z.shape
-    pairs = _lib.tp_pairs(_lib.TP_F32, N, N, D, z.data_ptr(), z.data_ptr())
+    dt = _lib.TP_F64 if z.dtype == torch.float64 else _lib.TP_F32
+    pairs = _lib.tp_pairs(dt, N, N, D, z.data_ptr(), z.data_ptr())
     score = _lib.tp_score(_lib.METRICS["linear"], 1.0, scale, 0, None, None, None, None)
-    lse = torch.empty(N, dtype=torch.float32, device=z.device)
+    lse = torch.empty(N, dtype=z.dtype, device=z.device)
     stream = ctypes.c_void_p(torch.cuda.current_stream(z.device).cuda_stream)
     st = lib.tp_pairwise_logsumexp_noalloc(ctypes.byref(pairs), ctypes.byref(score), int(exclude_self),
                                            ctypes.c_void_p(lse.data_ptr()), stream)
@@ -46,3 +47,22 @@ def test_noalloc_matches_workspace_entry_twice(N):
     torch.cuda.synchronize()
     assert_close(first, ref, TOL_F32_FWD, "first call")
     assert_close(second, ref, TOL_F32_FWD, "second call")
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.float64, 64), (torch.float32, 16)])
+def test_noalloc_streamed_path_twice(dtype, D):
+    """Shapes the streamed (SIMT) log-sum-exp serves, whose split partial states use the fixed array."""
+    lib = _lib.load()
+    dev = torch.device("cuda:0")
+    N = 5000
+    g = torch.Generator().manual_seed(901 + D)
+    z = torch.nn.functional.normalize(torch.randn(N, D, generator=g, dtype=dtype), dim=1).to(dev)
+    ref = ops.pairwise_logsumexp(z, z, ops.Score("linear", scale=1 / 0.07), True)
+    assert lib.tp_workspace_size(b"pairwise_logsumexp", ctypes.byref(
+        _lib.tp_pairs(_lib.TP_F64 if dtype == torch.float64 else _lib.TP_F32, N, N, D, z.data_ptr(), z.data_ptr())),
+        0, 0) > 0
+    tol = TOL_F64 if dtype == torch.float64 else TOL_F32_FWD
+    for call in ("first", "second"):
+        got = _call_noalloc(lib, z, 1 / 0.07, True)
+        torch.cuda.synchronize()
+        assert_close(got, ref, tol, f"{call} call")
