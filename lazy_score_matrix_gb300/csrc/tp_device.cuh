@@ -51,6 +51,15 @@ struct ExpTraits<float> {
     }
     __device__ __forceinline__ static float blog(float x) { return __log2f(x); }
     __device__ __forceinline__ static float exp(float x) { return bexp(x * kLogB); }
+    // The natural log-sum-exp from the base-2 state (max m, sum L of 2^(s - m)): ln2 m + ln L. ln L comes
+    // from the accurate logf and ln2 m from a two-term split of ln 2 inside fused multiply-adds, so
+    // when the two terms cancel (a log-sum-exp near zero) nothing is lost beyond the final rounding
+    // (converting m + log2 L instead loses the ulps of two numbers several times larger than the result).
+    __device__ __forceinline__ static float lse(float m, float L) {
+        constexpr float kLn2Hi = 0.693147182464599609375f;  // ln 2 rounded to fp32
+        constexpr float kLn2Lo = -1.904654323148236e-09f;   // ln 2 - kLn2Hi
+        return fmaf(m, kLn2Hi, fmaf(m, kLn2Lo, logf(L)));
+    }
 };
 template <>
 struct ExpTraits<double> {
@@ -59,6 +68,7 @@ struct ExpTraits<double> {
     __device__ __forceinline__ static double bexp(double x) { return ::exp(x); }
     __device__ __forceinline__ static double blog(double x) { return ::log(x); }
     __device__ __forceinline__ static double exp(double x) { return ::exp(x); }
+    __device__ __forceinline__ static double lse(double m, double L) { return m + ::log(L); }
 };
 
 template <class T>
@@ -197,6 +207,52 @@ template <class T>
 __device__ __forceinline__ T metric_base(int metric, T dot, T pn, T qn, T neg_gamma) {
     if (metric == kLinear) return dot;
     T d2 = fmax(fma(T(-2), dot, pn + qn), T(0));
+    if (metric == kRbf) return ExpTraits<T>::exp(neg_gamma * d2);
+    return d2;
+}
+
+// |p - q|^2 of a register-resident point and a shared-memory row (both zero-padded to DP), feature by
+// feature: 16-byte broadcast loads, Vec16<T>::n independent FMA chains.
+template <class T, int DP>
+__device__ __forceinline__ T dist2_regs_smem(const T (&p)[DP], const T* __restrict__ q) {
+    using V = typename Vec16<T>::type;
+    constexpr int VN = Vec16<T>::n;
+    T acc[VN];
+#pragma unroll
+    for (int u = 0; u < VN; ++u) acc[u] = T(0);
+#pragma unroll
+    for (int d = 0; d < DP; d += VN) {
+        V v = *reinterpret_cast<const V*>(q + d);
+        if constexpr (VN == 4) {
+            const T e0 = p[d + 0] - v.x, e1 = p[d + 1] - v.y, e2 = p[d + 2] - v.z, e3 = p[d + 3] - v.w;
+            acc[0] = fma(e0, e0, acc[0]);
+            acc[1] = fma(e1, e1, acc[1]);
+            acc[2] = fma(e2, e2, acc[2]);
+            acc[3] = fma(e3, e3, acc[3]);
+        } else {
+            const T e0 = p[d + 0] - v.x, e1 = p[d + 1] - v.y;
+            acc[0] = fma(e0, e0, acc[0]);
+            acc[1] = fma(e1, e1, acc[1]);
+        }
+    }
+    if constexpr (VN == 4) return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    else return acc[0] + acc[1];
+}
+
+// The metric value of a register-resident point p and a staged row q (pn, qn: their squared norms).
+// Linear: the dot product. Distance metrics in fp32 subtract feature by feature: the expansion
+// |p|^2 + |q|^2 - 2 p.q rounds at the size of |p|^2 + |q|^2, so a distance much smaller than the
+// points' norms keeps only the bits the cancellation leaves (several fp32 ulps of |p|^2 + |q|^2, which
+// a log-sum-exp or softmax of the scores then carries). fp64 keeps the expansion (one FMA per feature
+// instead of two): its cancellation error stays far below the fp64 tolerance. Exact either way on
+// integer-valued points whose squared norms are below 2^24 (top-k's exact tie order).
+template <class T, int DP>
+__device__ __forceinline__ T pair_base(int metric, const T (&p)[DP], const T* __restrict__ q, T pn, T qn,
+                                       T neg_gamma) {
+    if (metric == kLinear) return dot_regs_smem<T, DP>(p, q);
+    T d2;
+    if constexpr (sizeof(T) == 4) d2 = dist2_regs_smem<T, DP>(p, q);
+    else d2 = fmax(fma(T(-2), dot_regs_smem<T, DP>(p, q), pn + qn), T(0));
     if (metric == kRbf) return ExpTraits<T>::exp(neg_gamma * d2);
     return d2;
 }

@@ -212,8 +212,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                 if constexpr (decltype(masked)::value)
                     if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair adds nothing
                 const T* q = sq + jj * DP;
-                const T dot = dot_regs_smem<T, DP>(p, q);
-                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                const T base = pair_base<T, DP>(a.metric, p, q, pn, sn[jj], neg_gamma);
                 T t;
                 if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
                 else t = A * base;
@@ -306,9 +305,9 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
 #pragma unroll
         for (int c = 0; c < CP; ++c)
             if (c < a.C) out[pi * a.C + c] = run1.get(c) * inv;
-        static_cast<T*>(a.out2)[pi] = (m + E::blog(L)) * E::kLnB;
+        static_cast<T*>(a.out2)[pi] = E::lse(m, L);
     } else if constexpr (MODE == kLse) {
-        out[pi] = L > T(0) ? (m + E::blog(L)) * E::kLnB : ninf<T>();
+        out[pi] = L > T(0) ? E::lse(m, L) : ninf<T>();
     } else if constexpr (MODE == kDisp) {
 #pragma unroll
         for (int d = 0; d < DP; ++d)
@@ -345,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const SweepArgs a) {
             const T ms = ws[sp * sstride + pi];
             if (ms > ninf<T>()) l += ws[sp * sstride + a.nP + pi] * E::bexp(ms - m);
         }
-        const T lse = l > T(0) ? (m + E::blog(l)) * E::kLnB : ninf<T>();
+        const T lse = l > T(0) ? E::lse(m, l) : ninf<T>();
         if constexpr (MODE == kLse) {
             out[pi] = lse;
         } else {
@@ -439,8 +438,7 @@ __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
             for (int jj = 0; jj < cnt; ++jj) {
                 if constexpr (decltype(masked)::value)
                     if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair is never selected
-                const T dot = dot_regs_smem<T, DP>(p, sq + jj * DP);
-                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                const T base = pair_base<T, DP>(a.metric, p, sq + jj * DP, pn, sn[jj], neg_gamma);
                 T t;
                 if constexpr (AFFINE) t = fma(A * sw[jj], base, Cp + sb[jj]);
                 else t = A * base;
@@ -653,8 +651,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
                 if constexpr (decltype(masked)::value)
                     if (!pair_kept(a, pi, j0 + jj, og)) continue;  // a masked pair has no gradient
                 const T* q = sq + jj * DP;
-                const T dot = dot_regs_smem<T, DP>(p, q);
-                const T base = metric_base<T>(a.metric, dot, pn, sn[jj], neg_gamma);
+                const T base = pair_base<T, DP>(a.metric, p, q, pn, sn[jj], neg_gamma);
                 const T wq = sw[jj];
                 const T t = affine ? fma(A * wq, base, bp + sb[jj]) : A * base;
                 const T S = a.apply_exp ? E::exp(t) : t;
@@ -824,13 +821,16 @@ template <class T>
 __device__ __forceinline__ void pair_chain_own(const SweepArgs& a, const T* p, const T* q, T wp, T bp, T wq,
                                                T bq, T G, T* gp, T& gb, T& gw) {
     using E = ExpTraits<T>;
-    T dot = T(0), pn = T(0), qn = T(0);
+    T dot = T(0), pn = T(0), qn = T(0), d2 = T(0);
     for (int d = 0; d < a.D; ++d) {
         dot = fma(p[d], q[d], dot);
         pn = fma(p[d], p[d], pn);
         qn = fma(q[d], q[d], qn);
+        d2 = fma(p[d] - q[d], p[d] - q[d], d2);
     }
-    const T base = metric_base<T>(a.metric, dot, pn, qn, T(-a.gamma));
+    // fp32 distances feature by feature, as in the sweeps (pair_base)
+    T base = metric_base<T>(a.metric, dot, pn, qn, T(-a.gamma));
+    if (sizeof(T) == 4 && a.metric != kLinear) base = a.metric == kRbf ? ExpTraits<T>::exp(T(-a.gamma) * d2) : d2;
     const T scale = T(a.scale);
     const T t = scale * wp * wq * base + bp + bq;
     const T S = a.apply_exp ? E::exp(t) : t;

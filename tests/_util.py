@@ -1,4 +1,6 @@
 """Shared test helpers: the error measure the tolerances are stated in, and array conversion."""
+import os
+
 import numpy as np
 
 # Tolerances (max relative error, see rel_err): fp32 forward, fp32 gradients, fp64 anything.
@@ -58,6 +60,10 @@ def other_errors(got, want):
 
 def assert_close(got, want, tol, what="", floor_frac=FLOOR, abs_floor=0.0):
     e = rel_err(got, want, floor_frac, abs_floor)
+    log = os.environ.get("TP_TEST_ERROR_LOG")
+    if log:  # one line per check: the error and the bound it was held to (for reviewing the margins)
+        with open(log, "a") as f:
+            f.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]}\t{what}\t{e:.4g}\t{tol:.4g}\n")
     if e > tol:
         nw, ew = other_errors(got, want)
         raise AssertionError(f"{what}: max relative error {e:.3g} > {tol:g} (normwise {nw:.3g}, elementwise "

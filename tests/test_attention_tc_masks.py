@@ -10,6 +10,7 @@ import torch
 
 from lazy_score_matrix_gb300 import _lib, ops
 from lazy_score_matrix_gb300.ops import Score
+from tests._plain import TC_SLACK, Plain, achievable
 from tests._util import TOL_F32_FWD, TOL_F32_GRAD, assert_close
 
 pytestmark = pytest.mark.gpu
@@ -45,17 +46,22 @@ def _check(oracle, Q, K, V, G, mask, band=0, what="", grad_floor=None, zero_rows
     g = ops.pairwise_softmax_matmul_backward(Q.to(DEV), K.to(DEV), V.to(DEV), sc, out, lse, G.to(DEV))
     pb = oracle.Problem(Q, K, metric="linear", scale=0.125, pair_mask=mask, band=band)
     oo, ol = oracle.softmax_matmul(pb, V)
-    # the output floor of the unmasked attention tests: 1e-3 of the largest |V|
-    assert_close(out, oo, TOL_F32_FWD, f"{what} out", abs_floor=1e-3 * float(V.abs().max()))
-    assert_close(lse, ol, TOL_F32_FWD, f"{what} lse")
+    # the fp32 tolerances, or twice what the plain dense fp32 evaluation reaches on these inputs where
+    # that is larger (tests/_plain.py), at the floor of 1e-3 of each output's largest magnitude
+    pl = Plain(Q, K, V=V, metric="linear", scale=0.125, pair_mask=mask, band=band)
+    p_out, p_lse = pl.softmax_matmul()
+    assert_close(out, oo, achievable(p_out.detach(), oo, TOL_F32_FWD, slack=TC_SLACK), f"{what} out")
+    assert_close(lse, ol, achievable(p_lse.detach(), ol, TOL_F32_FWD, slack=TC_SLACK), f"{what} lse")
     og = oracle.softmax_matmul_backward(pb, V, out.double().cpu().numpy(), lse.double().cpu().numpy(), G)
+    pg = pl.grads(p_out, G)
     for k in ("dX", "dY", "dV"):
-        got, want = g[k], og[k]
+        got, want, pk = g[k], og[k], pg[k].numpy()
         if k == "dX" and zero_rows:
             t = 0.125 * float(G.abs().max() * V.abs().max() * K.abs().max())
             assert_close(got[:zero_rows], want[:zero_rows], TOL_F32_GRAD, f"{what} dX (one key)", abs_floor=t)
-            got, want = got[zero_rows:], want[zero_rows:]
-        assert_close(got, want, TOL_F32_GRAD, f"{what} {k}", abs_floor=grad_floor.get(k, 0.0))
+            got, want, pk = got[zero_rows:], want[zero_rows:], pk[zero_rows:]
+        fl = grad_floor.get(k, 0.0)
+        assert_close(got, want, achievable(pk, want, TOL_F32_GRAD, abs_floor=fl, slack=TC_SLACK), f"{what} {k}", abs_floor=fl)
     return out, lse, g
 
 
@@ -83,19 +89,30 @@ def test_band_attention_tc_matches_oracle(oracle, N, M, w):
         assert torch.all(g["dY"][N + w:] == 0) and torch.all(g["dV"][N + w:] == 0)
 
 
-def test_causal_self_attention_tc_summed(oracle):
-    # the same points on both sides, |x|^2 / 8 ~ 1.3 on the diagonal (well inside fp32's conditioning)
-    X, V, G = _n(21, 390, 64, s=0.4), _n(22, 390, 64), _n(23, 390, 64)
+@pytest.mark.parametrize("s", [0.4, 1.0])
+def test_causal_self_attention_tc_summed(oracle, s):
+    # the same points on both sides. At unit scale |x|^2 / 8 ~ 8 sits on the diagonal against ~N(0, 1)
+    # off it: the early causal rows hold nearly all their mass on the self pair and dS = P (dP - delta)
+    # cancels far below its terms, which fp32 itself does not resolve to 5e-4; at 0.4 the diagonal is
+    # ~1.3, well inside fp32's conditioning
+    X, V, G = _n(21, 390, 64, s=s), _n(22, 390, 64), _n(23, 390, 64)
     Xd = X.to(DEV)
     sc = Score("linear", scale=0.125, pair_mask="causal")
     out, lse = ops.pairwise_softmax_matmul(Xd, Xd, V.to(DEV), sc)
     pb = oracle.Problem(X, X, metric="linear", scale=0.125, pair_mask="causal")
     oo, _ = oracle.softmax_matmul(pb, V)
-    assert_close(out, oo, TOL_F32_FWD, "self out", abs_floor=1e-3 * float(V.abs().max()))
+    pl = Plain(X, X, V=V, metric="linear", scale=0.125, pair_mask="causal", same=True)
+    p_out, _ = pl.softmax_matmul()
+    assert_close(out, oo, achievable(p_out.detach(), oo, TOL_F32_FWD, slack=TC_SLACK), "self out")
     og = oracle.softmax_matmul_backward(pb, V, out.double().cpu().numpy(), lse.double().cpu().numpy(), G)
     gs = ops.pairwise_softmax_matmul_backward(Xd, Xd, V.to(DEV), sc, out, lse, G.to(DEV), same=True)
-    assert_close(gs["dX"], og["dX"] + og["dY"], TOL_F32_GRAD, "self summed")
-    assert_close(gs["dV"], og["dV"], TOL_F32_GRAD, "self dV")
+    pg = pl.grads(p_out, G)
+    want = og["dX"] + og["dY"]
+    assert_close(gs["dX"], want, achievable(pg["dX"], want, TOL_F32_GRAD, slack=TC_SLACK), "self summed")
+    assert_close(gs["dV"], og["dV"], achievable(pg["dV"], og["dV"], TOL_F32_GRAD, slack=TC_SLACK), "self dV")
+    names = _kernels(lambda: ops.pairwise_softmax_matmul_backward(Xd, Xd, V.to(DEV), sc, out, lse, G.to(DEV),
+                                                                  same=True))
+    assert {"attn_bwd_row_tc", "attn_bwd_col_tc"} <= names
 
 
 @pytest.mark.parametrize("mask,tc", [("causal", True), ("band", True), ("same_group", False)])
@@ -125,4 +142,5 @@ def test_band_wider_than_the_problem_keeps_every_pair(oracle, D):
     unmasked, _ = oracle.softmax_matmul(oracle.Problem(Q, K, metric="linear", scale=0.125), V)
     for w in (N + M, 2 ** 40, 2 ** 62):
         out, _, _ = _check(oracle, Q, K, V, G, "band", band=w, what=f"band {w} D {D}")
-        assert_close(out, unmasked, TOL_F32_FWD, f"band {w} D {D} vs unmasked", abs_floor=1e-3 * float(V.abs().max()))
+        p_un, _ = Plain(Q, K, V=V, metric="linear", scale=0.125).softmax_matmul()
+        assert_close(out, unmasked, achievable(p_un.detach(), unmasked, TOL_F32_FWD, slack=TC_SLACK), f"band {w} D {D} vs unmasked")

@@ -2,11 +2,12 @@
 
 Shapes span several 128-point CTAs and 32-point tiles with ragged tails, with the split (workspace +
 merge) path and the single-split path both exercised, every metric, fp32 and fp64, with and without
-row/column biases and weights and the exp node. Tolerances: max relative error (tests/_util.rel_err)
-1e-4 for fp32 forward, 5e-4 for fp32 gradients, 1e-10 for fp64. This stress matrix is measured with
-the wider 1e-2 floor (STRESS_FLOOR, see tests/_util.py); the benchmark workloads' own shapes and
-distributions are checked with the 1e-3 floor in test_workloads.py. Top-k on integer-valued inputs is
-bit-exact in values and indices.
+row/column biases and weights and the exp node. Tolerances: max relative error (tests/_util.rel_err,
+floor 1e-3 of the largest magnitude) 1e-4 for fp32 forward, 5e-4 for fp32 gradients, 1e-10 for fp64,
+or twice what a plain dense evaluation in the same precision reaches on the same inputs where that is
+larger (tests/_plain.py: random biases, weights and exp build outputs that cancel far below their
+terms, where fp32 itself misses 1e-4 by up to ~3x). Top-k on integer-valued inputs is bit-exact in
+values and indices.
 """
 import ctypes
 import numpy as np
@@ -15,7 +16,8 @@ import torch
 
 from lazy_score_matrix_gb300 import _lib, ops
 from lazy_score_matrix_gb300.ops import Score
-from tests._util import STRESS_FLOOR, TOL_F32_FWD, TOL_F32_GRAD, TOL_F64, assert_close, to_np
+from tests._plain import Plain, achievable, svgd_direction as plain_svgd
+from tests._util import TOL_F32_FWD, TOL_F32_GRAD, TOL_F64, assert_close, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -69,15 +71,24 @@ def tols(dtype):
 GRAD_KEYS = ["dX", "dY", "dV", "d_row_bias", "d_col_bias", "d_row_weight", "d_col_weight"]
 
 
-def compare_grads(got, want, tol, what, floor=STRESS_FLOOR, zero_scale=None):
-    """zero_scale: {key: magnitude} for outputs that are zero by the mathematics (their floor is
-    that magnitude instead of a fraction of the, rounding-level, expected values)."""
+def check(got, want, plain, tol, what, abs_floor=0.0):
+    """got against the oracle's want, held to achievable(): the tolerance or twice the plain evaluation's
+    error in the working precision (plain: its result on the same inputs, or None)."""
+    bound = tol if plain is None else achievable(plain, want, tol, abs_floor=abs_floor)
+    return assert_close(got, want, bound, what, abs_floor=abs_floor)
+
+
+def compare_grads(got, want, tol, what, plain=None, zero_scale=None):
+    """plain: gradients of the plain evaluation (Plain.grads). zero_scale: {key: magnitude} for outputs
+    that are zero by the mathematics (their floor is that magnitude instead of a fraction of the,
+    rounding-level, expected values)."""
     zero_scale = zero_scale or {}
+    plain = plain or {}
     for k in GRAD_KEYS:
         if want.get(k) is None or got.get(k) is None:
             assert (want.get(k) is None) == (got.get(k) is None) or k == "dV", (what, k)
             continue
-        assert_close(got[k], want[k], tol, f"{what} {k}", floor, zero_scale.get(k, 0.0))
+        check(got[k], want[k], plain.get(k), tol, f"{what} {k}", zero_scale.get(k, 0.0))
 
 
 CASES = [(shape, dt, metric, affine, ex)
@@ -100,9 +111,11 @@ def test_matmul(oracle, case):
     ftol, gtol = tols(dt)
     out = ops.pairwise_matmul(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc))
     pb = oracle_problem(oracle, X, Y, sc)
-    assert_close(out, oracle.matmul(pb, V), ftol, "matmul out", STRESS_FLOOR)
+    pl = Plain(X, Y, dtype=dt, V=V, **sc)
+    p_out = pl.matmul()
+    check(out, oracle.matmul(pb, V), p_out.detach(), ftol, "matmul out")
     g = ops.pairwise_matmul_backward(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc), G.to(DEV))
-    compare_grads(g, oracle.matmul_backward(pb, V, G), gtol, "matmul")
+    compare_grads(g, oracle.matmul_backward(pb, V, G), gtol, "matmul", pl.grads(p_out, G))
 
 
 @pytest.mark.parametrize("case", CASES, ids=_id)
@@ -114,13 +127,16 @@ def test_softmax_matmul(oracle, case):
     out, lse = ops.pairwise_softmax_matmul(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc))
     pb = oracle_problem(oracle, X, Y, sc)
     o_out, o_lse = oracle.softmax_matmul(pb, V)
-    assert_close(out, o_out, ftol, "softmax out", STRESS_FLOOR)
-    assert_close(lse, o_lse, ftol, "softmax lse", STRESS_FLOOR)
+    pl = Plain(X, Y, dtype=dt, V=V, **sc)
+    p_out, p_lse = pl.softmax_matmul()
+    check(out, o_out, p_out.detach(), ftol, "softmax out")
+    check(lse, o_lse, p_lse.detach(), ftol, "softmax lse")
     g = ops.pairwise_softmax_matmul_backward(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc), out, lse, G.to(DEV))
     # a row bias shifts a whole row of scores: its softmax gradient is zero; measure it against the
     # size of the terms that cancel (|dO| |V|)
     zs = {"d_row_bias": float(G.abs().max() * V.abs().max())}
-    compare_grads(g, oracle.softmax_matmul_backward(pb, V, o_out, o_lse, G), gtol, "softmax", zero_scale=zs)
+    compare_grads(g, oracle.softmax_matmul_backward(pb, V, o_out, o_lse, G), gtol, "softmax", pl.grads(p_out, G),
+                  zero_scale=zs)
 
 
 @pytest.mark.parametrize("exclude_self", [False, True])
@@ -138,9 +154,11 @@ def test_logsumexp(oracle, case, exclude_self):
     lse = ops.pairwise_logsumexp(X.to(DEV), Y.to(DEV), gpu_score(sc), exclude_self)
     pb = oracle_problem(oracle, X, Y, sc)
     o_lse = oracle.logsumexp(pb, exclude_self)
-    assert_close(lse, o_lse, ftol, "lse", STRESS_FLOOR)
+    pl = Plain(X, Y, dtype=dt, **sc)
+    p_lse = pl.logsumexp(exclude_self)
+    check(lse, o_lse, p_lse.detach(), ftol, "lse")
     g = ops.pairwise_logsumexp_backward(X.to(DEV), Y.to(DEV), gpu_score(sc), lse, gl.to(DEV), exclude_self)
-    compare_grads(g, oracle.logsumexp_backward(pb, o_lse, gl, exclude_self), gtol, "lse")
+    compare_grads(g, oracle.logsumexp_backward(pb, o_lse, gl, exclude_self), gtol, "lse", pl.grads(p_lse, gl))
 
 
 @pytest.mark.parametrize("case", CASES, ids=_id)
@@ -151,9 +169,11 @@ def test_displacement(oracle, case):
     ftol, gtol = tols(dt)
     out = ops.pairwise_displacement(X.to(DEV), Y.to(DEV), gpu_score(sc))
     pb = oracle_problem(oracle, X, Y, sc)
-    assert_close(out, oracle.displacement(pb), ftol, "displacement", STRESS_FLOOR)
+    pl = Plain(X, Y, dtype=dt, **sc)
+    p_out = pl.displacement()
+    check(out, oracle.displacement(pb), p_out.detach(), ftol, "displacement")
     g = ops.pairwise_displacement_backward(X.to(DEV), Y.to(DEV), gpu_score(sc), G.to(DEV))
-    compare_grads(g, oracle.displacement_backward(pb, G), gtol, "displacement")
+    compare_grads(g, oracle.displacement_backward(pb, G), gtol, "displacement", pl.grads(p_out, G))
 
 
 @pytest.mark.parametrize("dt", [torch.float32, torch.float64])
@@ -164,7 +184,7 @@ def test_svgd_direction(oracle, shape, dt):
     s = -x + 0.1 * gen(32, (N, D), dt)
     gamma = 0.5 / D
     phi = ops.svgd_direction(x.to(DEV), s.to(DEV), gamma)
-    assert_close(phi, oracle.svgd_direction(x, s, gamma), tols(dt)[0], "svgd", STRESS_FLOOR)
+    check(phi, oracle.svgd_direction(x, s, gamma), plain_svgd(x, s, gamma, dt), tols(dt)[0], "svgd")
 
 
 # ------------------------------------------------------------------------------------------------
@@ -224,7 +244,9 @@ def test_topk_backward(oracle, metric, affine, dt):
     pb = oracle_problem(oracle, X, Y, sc)
     # the oracle differentiates through the same selected pairs (indices are not differentiated)
     want = oracle.topk_backward(pb, k, i.cpu().numpy(), gv)
-    compare_grads(g, want, tols(dt)[1], "topk")
+    pl = Plain(X, Y, dtype=dt, **sc)
+    sel = pl.scores().gather(1, i.cpu())
+    compare_grads(g, want, tols(dt)[1], "topk", pl.grads(sel, gv))
 
 
 # ------------------------------------------------------------------------------------------------
@@ -246,13 +268,20 @@ def test_edge_shapes(oracle, N, M, D, C):
     sc = dict(metric="rbf", gamma=0.3, scale=1.0, apply_exp=False)
     pb = oracle.Problem(X, Y, **sc)
     out = ops.pairwise_matmul(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc))
-    assert_close(out, oracle.matmul(pb, V), TOL_F32_FWD, "edge matmul", STRESS_FLOOR)
+    check(out, oracle.matmul(pb, V), Plain(X, Y, V=V, **sc).matmul().detach(), TOL_F32_FWD, "edge matmul")
     o, l = ops.pairwise_softmax_matmul(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc))
     oo, ol = oracle.softmax_matmul(pb, V)
-    assert_close(o, oo, TOL_F32_FWD, "edge softmax", STRESS_FLOOR)
+    pl = Plain(X, Y, V=V, **sc)
+    p_o, _ = pl.softmax_matmul()
+    check(o, oo, p_o.detach(), TOL_F32_FWD, "edge softmax")
     G = gen(64, (N, C), torch.float32)
     g = ops.pairwise_softmax_matmul_backward(X.to(DEV), Y.to(DEV), V.to(DEV), gpu_score(sc), o, l, G.to(DEV))
-    compare_grads(g, oracle.softmax_matmul_backward(pb, V, oo, ol, G), TOL_F32_GRAD, "edge softmax")
+    zero = {}
+    if M == 1:  # one column: P = 1, dS = dP - delta = 0, so dX = dY = 0 up to rounding (size of the terms)
+        t = float(G.abs().max() * V.abs().max()) * 2 * 0.3
+        zero = {"dX": t * float((X.abs().max() + Y.abs().max())), "dY": t * float((X.abs().max() + Y.abs().max()))}
+    compare_grads(g, oracle.softmax_matmul_backward(pb, V, oo, ol, G), TOL_F32_GRAD, "edge softmax",
+                  pl.grads(p_o, G), zero_scale=zero)
 
 
 def test_softmax_rows_sum_to_one_on_gpu():
@@ -352,5 +381,7 @@ def test_logsumexp_same_points_symmetric(oracle, ND, dt, metric, exclude_self, a
     ol = oracle.logsumexp(pb, exclude_self)
     og = oracle.logsumexp_backward(pb, ol, gl, exclude_self)
     ftol, gtol = tols(dt)
-    assert_close(lse, ol, ftol, "lse", STRESS_FLOOR)
-    assert_close(g["dX"], og["dX"] + og["dY"], gtol, "dX + dY", STRESS_FLOOR)
+    pl = Plain(X, X, dtype=dt, same=True, **sc)
+    p_lse = pl.logsumexp(exclude_self)
+    check(lse, ol, p_lse.detach(), ftol, "lse")
+    check(g["dX"], og["dX"] + og["dY"], pl.grads(p_lse, gl)["dX"], gtol, "dX + dY")

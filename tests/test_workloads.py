@@ -14,6 +14,7 @@ import torch
 
 from lazy_score_matrix_gb300 import ops, synth
 from lazy_score_matrix_gb300.ops import Score
+from tests._plain import TC_SLACK, achievable, attention_rows
 from tests._util import TOL_F32_FWD, TOL_F32_GRAD, TOL_F64, assert_close
 
 pytestmark = pytest.mark.gpu
@@ -110,11 +111,12 @@ def test_attention_softmax_matmul_full_sampled(oracle):
     torch.cuda.synchronize()
     pb = oracle.Problem(w["Q"], w["K"], metric="linear", scale=w["scale"])
     o_out, o_lse = oracle.softmax_matmul(pb, w["V"])
-    # every output entry is a convex combination of value rows and lands ~100x below them: floor the
-    # relative error at 1e-3 of the largest |V| (plain fp32 evaluation of S = q.k / 8 on the exact
-    # inputs misses the 1e-3 * max|out| floor by 1.5x; the absolute error is ~1e-8)
-    assert_close(out, o_out, TOL_F32_FWD, "out", abs_floor=1e-3 * float(w["V"].abs().max()))
-    assert_close(lse, o_lse, TOL_F32_FWD, "lse")
+    # every output entry is a convex combination of ~16K random-sign value rows and lands ~100x below
+    # them: the plain fp32 evaluation of softmax(Q K^T / 8) V on these inputs misses 1e-4 at the floor of
+    # 1e-3 max|out|; held to what it reaches there times the tensor cores' factor (22-bit operands), or 1e-4
+    p_out, p_lse = attention_rows(w["Q"], w["K"], w["V"], w["scale"])
+    assert_close(out, o_out, achievable(p_out, o_out, TOL_F32_FWD, slack=TC_SLACK), "out")
+    assert_close(lse, o_lse, achievable(p_lse, o_lse, TOL_F32_FWD, slack=TC_SLACK), "lse")
     rows = sample(16384, 48, 4)
     pr = oracle.Problem(w["Q"][rows], w["K"], metric="linear", scale=w["scale"])
     gr = oracle.softmax_matmul_backward(pr, w["V"], o_out[rows], o_lse[rows], w["grad_out"][rows])
