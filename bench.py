@@ -1,20 +1,32 @@
 """Benchmark of the streamed pairwise-score hot path on GB300.
 
-Default workload (one GPU): InfoNCE row logsumexp, fp32, z [8192,64] unit rows, S = z z^T / 0.07,
-exclude_self, forward plus the replay backward that gives the gradient in z. One step = the forward
-(every pair evaluated once) plus the backward (every pair replayed in a row sweep and a column sweep)
-through libtp's C ABI. Metric: Gpairs/s = N*M / step time.
+One step of a workload is one pass of its consumer over the workload's whole problem through libtp's
+C ABI: the forward (every pair evaluated once) and, where the workload has one, the replay backward
+(every pair evaluated again). Metric: Gpairs/s = pairs of the problem / step time (kept pairs under a
+pair mask). The workloads are those of the torchpairwise guide "Using Torchpairwise in Models" (Task
+Map and Stein Variational Gradient Descent sections), with seeded synthetic inputs of their shapes:
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libtp|reference] [--workload 1..5]
+  1  rbf kernel product K @ [V | 1], X, Y [1024,3], fp32, forward + gradients in X, Y, V
+  2  InfoNCE row log-sum-exp, z [8192,64] unit rows, S = z z^T / 0.07, exclude_self, forward + z.grad
+  3  exact k-NN top-16, X [65536,16] vs R [1048576,16], integers in [-8,8], fp32, forward
+  4  attention softmax_matmul, Q, K, V [16384,64], scale 1/8, fp32, forward + gradients
+  5  SVGD direction, x [131072,8], score = -x, rbf gamma 0.1, fp64, forward
+  6  workload 4 under the causal mask (kept pairs N (N + 1) / 2)
 
---impl reference times the oracle (plain fp64 CPU loops) on the host cores, on a bounded sample of
-the same workload, and prints the same JSON line with "impl": "reference".
-Under torchrun each rank runs an independent replica of the workload on its own GPU (weak scaling,
-no collective in the data path); rank 0 prints the line with the max time over ranks.
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libtp|reference] [--workload 2]
+                    [--workloads 1,2,3,4,5,6] [--no-cpu-baseline]
+
+The top-level JSON line is workload --workload (default 2, timed for exactly K steps); the line's
+"workloads" object holds every workload of --workloads, each with its own step count, roofline, e2e and
+CPU baseline. --impl reference times the oracle (plain fp64 CPU loops) on the host cores, on a bounded
+sample of the top-level workload, and prints the same JSON line with "impl": "reference". Under torchrun
+each rank runs an independent replica on its own GPU (weak scaling, no collective in the data path); rank
+0 prints the line with the max time over ranks.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -30,31 +42,96 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "Gpairs/s per fused consumer (fwd+bwd) at fp32/fp64; % of FP32/FP64 peak"
-SM_COUNT = 152
 FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+FALLBACK_SMS = 152       # GB300, used only when no device can be queried
+
+# ------------------------------------------------------------------------------------------------
+# peaks: the driver's measured copy / bf16 GEMM figures, the device's SM count, and our own measured
+# fp32 / fp64 FMA and exp2 rates (libtp_peaks)
+# ------------------------------------------------------------------------------------------------
 
 
-def peaks():
+def measured_alu_peaks():
+    """Rates of the calibration kernels on the current device (TFLOP/s for FMA, Tops/s for exp2), each
+    timed with CUDA events over one launch of ~50-100 ms after a warm-up launch; None if unavailable."""
+    path = os.path.join(ROOT, "lazy_score_matrix_gb300", "libtp_peaks.so")
+    if not os.path.exists(path) or not torch.cuda.is_available():
+        return None
+    lib = ctypes.CDLL(path)
+    lib.tpk_peak.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_float)]
+    lib.tpk_peak.restype = ctypes.c_double
+    out = {}
+    for kind, name, iters in ((0, "fp32_fma_tflops", 1_500_000), (1, "fp64_fma_tflops", 40_000),
+                              (2, "ex2_tops", 200_000)):
+        ms = ctypes.c_float()
+        r = lib.tpk_peak(kind, iters, 4, ctypes.byref(ms))
+        out[name] = round(r, 3) if r > 0 else None
+        out[name.rsplit("_", 1)[0] + "_ms"] = round(ms.value, 2)
+    return out
+
+
+_PEAKS = None
+
+
+def peaks(dev=None):
+    global _PEAKS
+    if _PEAKS is not None:
+        return _PEAKS
     p = {}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
     sm_mhz = float(p.get("sm_max_mhz", 2070.0))
-    return {
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count if dev is not None else FALLBACK_SMS
+    alu = measured_alu_peaks() if dev is not None else None
+    derived32 = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    _PEAKS = {
         "hbm_gbs": float(p.get("hbm_gbs", 6800.0)),
         "sm_max_mhz": sm_mhz,
-        "fp32_tflops": SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12,
-        "fp64_tflops": 1.25,  # nominal GB300 FP64 rate (no measured figure)
+        "sms": sms,
+        "fp32_derived_tflops": derived32,
+        "fp32_tflops": (alu or {}).get("fp32_fma_tflops") or derived32,
+        "fp64_tflops": (alu or {}).get("fp64_fma_tflops") or 1.25,
+        "ex2_tops": (alu or {}).get("ex2_tops"),
+        "alu_measured": alu,
         # fp16 tensor peak = the measured bf16 burst peak (same rate); tf32 = that x the nominal 1.1 / 2.25
         "f16_tflops": float(p.get("bf16_tflops", 1900.0)),
         "tf32_tflops": float(p.get("bf16_tflops", 1900.0)) * 1.1 / 2.25,
         "source": "MEASURED_PEAKS.json" if p else "fallback",
     }
+    return _PEAKS
+
+
+def roofline_for(kernel, fpp, bound, pairs, avg_ms, dtype, workload):
+    """The roofline object of one kernel: algorithmic flop per pair x pairs per launch / launch time."""
+    pk = peaks()
+    ach = fpp * pairs / (avg_ms / 1e3) / 1e12
+    if bound == "tensor-f16":
+        peak = pk["f16_tflops"]
+        src = f"fp16 tensor (kind::f16 operands): measured bf16 {peak:.0f} TFLOP/s, same rate, of measured"
+    elif bound == "tensor-tf32":
+        peak = pk["tf32_tflops"]
+        src = f"tf32 tensor: measured bf16 {pk['f16_tflops']:.0f} TFLOP/s x 1.1/2.25 (nominal tf32/bf16), of measured"
+    elif dtype == "f64":
+        peak = pk["fp64_tflops"]
+        m = pk["alu_measured"] and pk["alu_measured"].get("fp64_fma_tflops")
+        src = ("FP64 pipe: measured by this run's own fp64 FMA kernel (independent chains on every SM), of measured"
+               if m else "FP64 pipe: nominal 1.25 TFLOP/s (no measurement available), of fallback")
+    else:
+        peak = pk["fp32_tflops"]
+        m = pk["alu_measured"] and pk["alu_measured"].get("fp32_fma_tflops")
+        src = ("FP32 pipe: measured by this run's own fp32 FMA kernel, of measured" if m else
+               f"FP32 pipe: {pk['sms']} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x {pk['sm_max_mhz']:.0f} MHz, derived")
+    return {"kernel": kernel, "bound": "tensor" if bound.startswith("tensor") else "alu",
+            "operands": bound[len("tensor-"):] if bound.startswith("tensor") else dtype,
+            "achieved": round(ach, 3), "peak": round(peak, 2), "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "traffic": traffic_for(kernel, workload), "peak_source": src, "flop_per_pair": fpp,
+            "pairs_per_launch": pairs, "avg_launch_us": round(avg_ms * 1e3, 2)}
 
 
 # ------------------------------------------------------------------------------------------------
-# per-kernel timing through libtp's launch hook
+# per-kernel timing through libtp's own event timer
 # ------------------------------------------------------------------------------------------------
 
 
@@ -76,7 +153,6 @@ class KernelTimer:
         self.n = int(self._lib.load().tp_timer_stop())
 
     def summary(self):
-        import ctypes
         lib = self._lib.load()
         name, ms = ctypes.c_char_p(), ctypes.c_float()
         out = {}
@@ -89,7 +165,7 @@ class KernelTimer:
 
 
 # ------------------------------------------------------------------------------------------------
-# clocks during the timed region
+# clocks during a timed region
 # ------------------------------------------------------------------------------------------------
 
 
@@ -126,10 +202,8 @@ class ClockSampler:
                 self.proc.kill()
 
     def result(self):
-        win = [l for t, l in self.lines if self.t0 is not None and self.t0 - 0.06 <= t <= self.t1 + 0.06]
-        if not win:
-            win = [l for _, l in self.lines]
-        sm, smax, reasons = [], None, set()
+        win = [l for t, l in self.lines if self.t0 is not None and self.t0 <= t <= self.t1]
+        sm, smax, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in win:
             parts = [x.strip() for x in l.split(",")]
@@ -138,13 +212,15 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 smax = float(parts[2])
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm) if sm else None,
+                "power_w_median": statistics.median(power) if power else None}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -154,11 +230,16 @@ class ClockSampler:
 
 class Workload:
     """One hot-path step on device-resident inputs, plus the same step end to end from host buffers."""
+    wid = 0
     name = ""
     dtype = "f32"
     pairs = 0
-    flops_per_pair = {}  # per kernel name: algorithmic flop per pair the launch processes
-    bound = "alu"
+    flops_per_pair = {}  # per kernel name: (algorithmic flop per pair the launch processes, bound)
+    steps = 20           # timed steps in the "workloads" object (the top-level line uses --steps)
+
+    def config(self):
+        return {"workload": self.name, "N": self.N, "M": getattr(self, "M", self.N), "D": self.D,
+                "pairs_per_step": self.pairs}
 
     def step(self):
         raise NotImplementedError
@@ -166,9 +247,20 @@ class Workload:
     def e2e_step(self):
         raise NotImplementedError
 
+    def oracle_sample(self, rows):
+        """Time the oracle on `rows` sampled rows of this workload: (seconds, pairs, threads, text)."""
+        raise NotImplementedError
+
+
+def _sample_rows(n, count, seed):
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(n, size=min(count, n), replace=False))
+
 
 class InfoNCE(Workload):
     """Workload 2: InfoNCE row logsumexp fwd + replay bwd, z [8192,64] fp32."""
+    wid = 2
+    cpu_rows = 1024
 
     def __init__(self, dev, N=8192, D=64):
         from lazy_score_matrix_gb300 import ops, synth
@@ -181,7 +273,6 @@ class InfoNCE(Workload):
         self.z = w["z"].to(dev)
         self.gl = w["grad_lse"].to(dev)
         self.want = (True, True, False, False, False, False, False)
-        # pinned host copies for the end-to-end path
         self.z_h = w["z"].pin_memory()
         self.gl_h = w["grad_lse"].pin_memory()
         self.lse_h = torch.empty(N, dtype=torch.float32).pin_memory()
@@ -192,14 +283,15 @@ class InfoNCE(Workload):
         self.d2h = self.lse_h.numel() * 4 + self.grad_h.numel() * 4
         D2 = 2 * D
         # algorithmic flop per pair and launch (FMA = 2): forward 2D+3; backward 387 = (2D+3) + 2D + 2D,
-        # the row sweep credited with the recompute and dX, the column sweep with dY only; a kernel
-        # that produces the whole backward (X = Y, one symmetric sweep) is credited with all of it.
-        # (kernel: (flop per pair, bound)); "tensor-f16" kernels run the contraction on tcgen05 kind::f16
-        # (scaled fp16 hi/lo split), credited with the algorithmic flop against the fp16 tensor peak
+        # the row sweep credited with the recompute and dX, the column sweep with dY only; a kernel that
+        # produces the whole backward (X = Y, one symmetric sweep) is credited with all of it.
+        # "tensor-f16" kernels run the contraction on tcgen05 kind::f16 (scaled fp16 hi/lo split),
+        # credited with the algorithmic flop against the fp16 tensor peak
         self.flops_per_pair = {"fwd_sweep_lse": (D2 + 3, "alu"), "bwd_sweep_lse_row": (D2 + 3 + D2, "alu"),
                                "bwd_sweep_lse_col": (D2, "alu"), "bwd_sweep_lse_sym": (D2 + 3 + D2 + D2, "alu"),
-                               "lse_fwd_tc": (D2 + 3, "tensor-f16"), "lse_bwd_sym_tc": (D2 + 3 + D2 + D2, "tensor-f16")}
-        self.step_flops_per_pair = (D2 + 3) + (D2 + 3 + D2 + D2)
+                               "lse_fwd_tc": (D2 + 3, "tensor-f16"),
+                               "lse_bwd_lin_tc": (D2 + 3 + D2 + D2, "tensor-f16"),
+                               "lse_bwd_sym_tc": (D2 + 3 + D2 + D2, "tensor-f16")}
 
     def step(self):
         lse = self.ops.pairwise_logsumexp(self.z, self.z, self.score, True)
@@ -215,9 +307,15 @@ class InfoNCE(Workload):
         self.lse_h.copy_(lse, non_blocking=True)
         self.grad_h.copy_(g["dX"], non_blocking=True)
 
+    @staticmethod
+    def oracle_sample(rows):
+        return oracle_infonce(rows)
+
 
 class RbfMatmul(Workload):
     """Workload 1: rbf kernel product K @ [V | 1] fp32, X, Y [1024,3], fwd + grads in X, Y, V."""
+    wid = 1
+    cpu_rows = 1024
 
     def __init__(self, dev):
         from lazy_score_matrix_gb300 import ops, synth
@@ -231,8 +329,8 @@ class RbfMatmul(Workload):
         self.score = ops.Score("rbf", gamma=w["gamma"])
         self.X, self.Y, self.V, self.G = (w[k].to(dev) for k in ("X", "Y", "V", "grad_out"))
         self.host = {k: w[k].pin_memory() for k in ("X", "Y", "V", "grad_out")}
-        self.dev_in = {k: torch.empty_like(v) for k, v in ((k, getattr(self, kk)) for k, kk in
-                                                         (("X", "X"), ("Y", "Y"), ("V", "V"), ("grad_out", "G")))}
+        self.dev_in = {k: torch.empty_like(v) for k, v in
+                       (("X", self.X), ("Y", self.Y), ("V", self.V), ("grad_out", self.G))}
         self.out_h = torch.empty(self.N, self.C).pin_memory()
         self.h2d = sum(v.numel() * 4 for v in self.host.values())
         self.d2h = self.out_h.numel() * 4 + (self.N + self.M) * self.D * 4 + self.M * self.C * 4
@@ -241,7 +339,6 @@ class RbfMatmul(Workload):
         self.flops_per_pair = {"fwd_sweep_matmul": (2 * D + 3 + 2 * C, "alu"),
                                "bwd_sweep_matmul_row": (2 * D + 3 + 2 * C + 2 + 2 * D + 1, "alu"),
                                "bwd_sweep_matmul_col": (2 * C + 2 * D + 1, "alu")}
-        self.step_flops_per_pair = (2 * D + 3 + 2 * C) + (2 * D + 3 + 4 * C + 2 + 4 * D + 2)
         self.grads_h = [torch.empty(self.N, D).pin_memory(), torch.empty(self.M, D).pin_memory(),
                         torch.empty(self.M, C).pin_memory()]
 
@@ -262,9 +359,24 @@ class RbfMatmul(Workload):
         for h, k in zip(self.grads_h, ("dX", "dY", "dV")):
             h.copy_(g[k], non_blocking=True)
 
+    @staticmethod
+    def oracle_sample(rows):
+        from lazy_score_matrix_gb300 import synth
+        from oracle import oracle
+        w = synth.workload(1)
+        pb = oracle.Problem(w["X"], w["Y"], metric="rbf", gamma=w["gamma"])
+        t0 = time.perf_counter()
+        oracle.matmul(pb, w["V"])
+        oracle.matmul_backward(pb, w["V"], w["grad_out"])
+        return (time.perf_counter() - t0, w["X"].shape[0] * w["Y"].shape[0], oracle.get_threads(),
+                "oracle fwd + bwd of the whole 1024 x 1024 problem")
+
 
 class Knn(Workload):
     """Workload 3: exact k-NN top-16, X [65536,16] vs R [1048576,16] integers in [-8,8], fp32."""
+    wid = 3
+    steps = 10
+    cpu_rows = 64
 
     def __init__(self, dev):
         from lazy_score_matrix_gb300 import ops, synth
@@ -286,7 +398,6 @@ class Knn(Workload):
         # the SIMT sweep runs the distance on the FP32 pipe; the tensor-core kernel runs the contraction
         # on tcgen05 (tf32) and the selection on the ALUs: it is credited with the same algorithmic flop
         self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu"), "topk_tc": (2 * self.D + 2, "tensor-tf32")}
-        self.step_flops_per_pair = 2 * self.D + 2
 
     def step(self):
         return self.ops.pairwise_topk(self.X, self.R, self.score, self.k, False)
@@ -298,9 +409,24 @@ class Knn(Workload):
         self.v_h.copy_(v, non_blocking=True)
         self.i_h.copy_(i, non_blocking=True)
 
+    @staticmethod
+    def oracle_sample(rows):
+        from lazy_score_matrix_gb300 import synth
+        from oracle import oracle
+        w = synth.workload(3)
+        r = _sample_rows(w["X"].shape[0], rows, 33)
+        pb = oracle.Problem(w["X"][r], w["R"], metric="sqeuclidean")
+        t0 = time.perf_counter()
+        oracle.topk(pb, w["k"], False)
+        return (time.perf_counter() - t0, len(r) * w["R"].shape[0], oracle.get_threads(),
+                f"oracle top-16 of {len(r)} seeded sampled rows against all 1048576 references")
+
 
 class Attention(Workload):
     """Workload 4: softmax_matmul attention fp32, Q, K, V [16384,64], scale 1/8, fwd + grads."""
+    wid = 4
+    cpu_rows = 256
+    mask = "all"
 
     def __init__(self, dev):
         from lazy_score_matrix_gb300 import ops, synth
@@ -334,7 +460,6 @@ class Attention(Workload):
                                "attn_fwd_tc": (2 * C, "tensor-f16"),
                                "attn_bwd_row_tc": (2 * D + 2 * C + 2 + 2 * D, "tensor-f16"),
                                "attn_bwd_col_tc": (2 * D + 2 * C, "tensor-f16")}
-        self.step_flops_per_pair = (2 * D + 2 * C + 3) + (2 * D + 2 * C + 2 * C + 2 + 2 * D + 2 * D)
 
     def step(self):
         out, lse = self.ops.pairwise_softmax_matmul(self.Q, self.K, self.V, self.score)
@@ -353,10 +478,36 @@ class Attention(Workload):
         for h, k in zip(self.grads_h, ("dX", "dY", "dV")):
             h.copy_(g[k], non_blocking=True)
 
+    @classmethod
+    def oracle_sample(cls, rows):
+        """The oracle's forward and backward of `rows` seeded sampled query rows against all keys (the
+        sub-problem of those rows). Under the causal mask: the causal problem of the first 32 `rows`
+        queries and keys (a prefix of the workload, R (R + 1) / 2 kept pairs)."""
+        from lazy_score_matrix_gb300 import synth
+        from oracle import oracle
+        w = synth.workload(4)
+        if cls.mask == "causal":
+            R = 32 * rows
+            pb = oracle.Problem(w["Q"][:R], w["K"][:R], metric="linear", scale=w["scale"], pair_mask="causal")
+            t0 = time.perf_counter()
+            o, l = oracle.softmax_matmul(pb, w["V"][:R])
+            oracle.softmax_matmul_backward(pb, w["V"][:R], o, l, w["grad_out"][:R])
+            return (time.perf_counter() - t0, R * (R + 1) // 2, oracle.get_threads(),
+                    f"oracle fwd + bwd of the causal problem of the first {R} queries and keys")
+        r = _sample_rows(w["Q"].shape[0], rows, 44)
+        pb = oracle.Problem(w["Q"][r], w["K"], metric="linear", scale=w["scale"])
+        t0 = time.perf_counter()
+        o, l = oracle.softmax_matmul(pb, w["V"])
+        oracle.softmax_matmul_backward(pb, w["V"], o, l, w["grad_out"][r])
+        return (time.perf_counter() - t0, len(r) * w["K"].shape[0], oracle.get_threads(),
+                f"oracle fwd + bwd of {len(r)} seeded sampled query rows against all 16384 keys")
+
 
 class CausalAttention(Attention):
     """Workload 6: workload 4 under the causal mask (key j <= query i), the attention of the Task Map's
     softmax_matmul(V, mask=tp.masks.causal()). Pairs are the kept ones, N (N + 1) / 2."""
+    wid = 6
+    mask = "causal"
 
     def __init__(self, dev):
         super().__init__(dev)
@@ -367,7 +518,10 @@ class CausalAttention(Attention):
 
 class Svgd(Workload):
     """Workload 5: SVGD direction fp64, x [131072,8], score = -x, rbf gamma 0.1, one fused sweep."""
+    wid = 5
     dtype = "f64"
+    steps = 3
+    cpu_rows = 512
 
     def __init__(self, dev):
         from lazy_score_matrix_gb300 import ops, synth
@@ -387,7 +541,6 @@ class Svgd(Workload):
         D = self.D
         # one sweep with V = [score | x | 1]: distance 2D+2, -gamma scale 1, accumulate 2(2D+1)
         self.flops_per_pair = {"fwd_sweep_svgd": (2 * D + 3 + 2 * (2 * D + 1), "alu")}
-        self.step_flops_per_pair = 2 * D + 3 + 2 * (2 * D + 1)
 
     def step(self):
         return self.ops.svgd_direction(self.x, self.sc, self.gamma)
@@ -397,6 +550,17 @@ class Svgd(Workload):
         self.s_d.copy_(self.s_h, non_blocking=True)
         phi = self.ops.svgd_direction(self.x_d, self.s_d, self.gamma)
         self.phi_h.copy_(phi, non_blocking=True)
+
+    @staticmethod
+    def oracle_sample(rows):
+        from lazy_score_matrix_gb300 import synth
+        from oracle import oracle
+        w = synth.workload(5)
+        r = _sample_rows(w["x"].shape[0], rows, 55)
+        t0 = time.perf_counter()
+        oracle.svgd_direction(w["x"][r], w["score"], w["gamma"], y=w["x"])
+        return (time.perf_counter() - t0, len(r) * w["x"].shape[0], oracle.get_threads(),
+                f"oracle SVGD direction of {len(r)} seeded sampled particles against all 131072")
 
 
 WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd, 6: CausalAttention}
@@ -457,40 +621,30 @@ def capture_step(wl):
         return None
 
 
-def gpu_arm(args, rank, world):
+def bench_workload(wl, steps, warmup, flush, world, dev):
+    """Graph-replayed timed steps (value), a second eager pass with per-launch events (kernel durations
+    and the roofline), and the end-to-end pass through the public API with host buffers."""
     from lazy_score_matrix_gb300 import _lib
-
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    wl = WORKLOADS[args.workload](dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > 129 MB L2
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         wl.step()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dev.index)
-    if rank == 0:
-        clocks.start()
-        time.sleep(0.3)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # The timed steps: replays of the step captured in a CUDA graph, nothing recorded between its launches.
     graph = capture_step(wl)
-    clocks.t0 = time.time()
-    ms = time_steps(graph.replay if graph is not None else wl.step, args.steps, flush)
-    clocks.t1 = time.time()
-    torch.cuda.synchronize()
-    # Kernel durations for the roofline: the same steps again, eagerly, with CUDA events around every
-    # launch on its stream (events between launches would add gaps to the timed steps above).
-    _lib.launch_count(reset=True)
-    timer = KernelTimer(capacity=64 * args.steps + 64)
-    with timer:
-        time_steps(wl.step, args.steps, flush)
-    launches = _lib.launch_count()
+    ms = time_steps(graph.replay if graph is not None else wl.step, steps, flush)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ms = max_over_ranks(ms, world, dev)
+    # kernel durations: the same steps again, eagerly, with CUDA events around every launch on its stream
+    # (events between launches would add gaps to the timed steps above)
+    _lib.launch_count(reset=True)
+    timer = KernelTimer(capacity=64 * steps + 64)
+    with timer:
+        time_steps(wl.step, steps, flush)
+    launches = _lib.launch_count()
+    torch.cuda.synchronize()
     # end to end: host buffers, copies inside the timed region
     for _ in range(2):
         wl.e2e_step()
@@ -498,64 +652,114 @@ def gpu_arm(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         wl.e2e_step()
         torch.cuda.current_stream().synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
-    clocks.stop()
-    if rank != 0:
-        return None
-    pk = peaks()
-    ms_step = ms / args.steps
-    value = whole_job_gpairs(world, wl.pairs, args.steps, ms / 1e3)
     ksum = timer.summary()
-    dom = max(ksum.items(), key=lambda kv: kv[1]["total_ms"])
-    dname, dstat = dom
+    dname, dstat = max(ksum.items(), key=lambda kv: kv[1]["total_ms"])
     credit = wl.flops_per_pair.get(dname)
     roof = None
     if credit is not None:
-        fpp, bound = credit
-        ach = fpp * wl.pairs / (dstat["avg_ms"] / 1e3) / 1e12
-        if bound == "tensor-f16":
-            peak = pk["f16_tflops"]
-            src = f"fp16 tensor (kind::f16 operands): measured bf16 {pk['f16_tflops']:.0f} TFLOP/s, same rate, of measured"
-        elif bound == "tensor-tf32":
-            peak = pk["tf32_tflops"]
-            src = (f"tf32 tensor: measured bf16 {pk['f16_tflops']:.0f} TFLOP/s x 1.1/2.25 "
-                   f"(nominal tf32/bf16), of measured")
-        else:
-            peak = pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]
-            src = (f"FP32 pipe: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x {pk['sm_max_mhz']:.0f} MHz "
-                   f"(derived from unit counts and the measured max clock)")
-        roof = {"kernel": dname, "bound": "tensor" if bound.startswith("tensor") else bound,
-                "operands": bound[len("tensor-"):] if bound.startswith("tensor") else "fp32",
-                "achieved": round(ach, 3), "peak": round(peak, 2),
-                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic_for(dname, wl.name),
-                "peak_source": src, "flop_per_pair": fpp}
-    step_tflops = wl.step_flops_per_pair * wl.pairs / (ms_step / 1e3) / 1e12
-    line = {
-        "metric": METRIC, "value": round(value, 4), "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the workload)",
-        "config": {"workload": wl.name, "N": wl.N, "M": getattr(wl, "M", wl.N), "D": wl.D, "pairs_per_step": wl.pairs,
-                   "l2": "flushed before every timed step (256 MB write, untimed)",
-                   "launch": ("step captured once in a CUDA graph, replayed per timed step" if graph is not None
-                              else "eager"),
-                   "kernel_times": "CUDA events around every launch, in a second pass of the same steps",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "impl": "libtp",
+        roof = roofline_for(dname, credit[0], credit[1], wl.pairs, dstat["avg_ms"], wl.dtype, wl.name)
+    total = sum(x["total_ms"] for x in ksum.values())
+    return {
+        "workload": wl.name, "value": round(whole_job_gpairs(world, wl.pairs, steps, ms / 1e3), 4), "unit": "Gpairs/s",
+        "ms_per_step": round(ms / steps, 5), "steps": steps, "warmup": warmup, "dtype": wl.dtype,
+        "config": wl.config(),
+        "launch": "step captured once in a CUDA graph, replayed per timed step" if graph is not None else "eager",
         "roofline": roof,
-        "step_roofline": {"achieved_tflops": round(step_tflops, 3), "flop_per_pair": wl.step_flops_per_pair,
-                          "frac_fp32_pipe" if wl.dtype == "f32" else "frac_fp64_pipe":
-                              round(step_tflops / (pk["fp32_tflops"] if wl.dtype == "f32" else pk["fp64_tflops"]), 4)},
         "kernels": {k: {"launches": v["launches"], "avg_us": round(v["avg_ms"] * 1e3, 2),
-                        "share": round(v["total_ms"] / sum(x["total_ms"] for x in ksum.values()), 4)}
+                        "share": round(v["total_ms"] / total, 4),
+                        **({"roofline_frac": roofline_for(k, *wl.flops_per_pair[k], wl.pairs, v["avg_ms"], wl.dtype,
+                                                          wl.name)["frac"]}
+                           if k in wl.flops_per_pair else {})}
                     for k, v in sorted(ksum.items(), key=lambda kv: -kv[1]["total_ms"])},
         "gpu_launches": launches,
-        "e2e": {"value": round(whole_job_gpairs(world, wl.pairs, args.steps, e2e_s), 4), "unit": "Gpairs/s",
+        "e2e": {"value": round(whole_job_gpairs(world, wl.pairs, steps, e2e_s), 4), "unit": "Gpairs/s",
                 "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h},
-        "clocks": clocks.result(),
+        "_graph": graph,
     }
+
+
+def clock_pass(wl, graph, dev, seconds=1.2):
+    """Replays the step for at least `seconds` with nvidia-smi sampling the clocks every 50 ms: the clock
+    record under load, and the throughput of that pass (L2 not flushed between replays)."""
+    fn = graph.replay if graph is not None else wl.step
+    fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    fn()
+    b.record()
+    torch.cuda.synchronize()
+    per = max(a.elapsed_time(b), 1e-3)
+    n = max(int(seconds * 1e3 / per) + 1, 10)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.4)
+    clocks.t0 = time.time()
+    a.record()
+    for _ in range(n):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    clocks.t1 = time.time()
+    time.sleep(0.1)
+    clocks.stop()
+    ms = a.elapsed_time(b)
+    res = clocks.result()
+    res.update({"pass_s": round(ms / 1e3, 3), "pass_steps": n,
+                "pass_value": round(wl.pairs * n / (ms / 1e3) / 1e9, 3),
+                "how": "nvidia-smi every 50 ms during a >= 1 s pass of graph replays of the step"})
+    return res
+
+
+def gpu_arm(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > 129 MB L2
+    order = [args.workload] + [w for w in args.workloads if w != args.workload]
+    results, top, top_wl = {}, None, None
+    for wid in order:
+        wl = WORKLOADS[wid](dev)
+        steps = args.steps if wid == args.workload else min(args.steps, wl.steps)
+        r = bench_workload(wl, steps, args.warmup, flush, world, dev)
+        graph = r.pop("_graph")
+        if wid == args.workload:
+            top, top_wl = r, wl
+            r["clocks"] = clock_pass(wl, graph, dev) if rank == 0 else None
+        if rank == 0 and not args.no_cpu_baseline and wid in args.workloads:
+            r["cpu_baseline"] = cpu_baseline(wl)
+        results[str(wid)] = r
+        del graph, wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    pk = peaks()
+    line = {
+        "metric": METRIC, "value": top["value"], "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": top["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": top["dtype"], "data": "synthetic (seeded, shapes of the workload)",
+        "config": dict(top["config"], l2="flushed before every timed step (256 MB write, untimed)",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "impl": "libtp",
+        "timing": {"launch": top["launch"],
+                   "kernel_times": "CUDA events around every launch on its stream, in a second pass of the steps"},
+        "roofline": top["roofline"],
+        "kernels": top["kernels"],
+        "gpu_launches": top["gpu_launches"],
+        "e2e": top["e2e"],
+        "clocks": top["clocks"],
+        "peaks": {k: pk[k] for k in ("sms", "sm_max_mhz", "fp32_tflops", "fp32_derived_tflops", "fp64_tflops",
+                                     "ex2_tops", "f16_tflops", "tf32_tflops", "hbm_gbs", "source")},
+        "workloads": {k: v for k, v in results.items() if int(k) in args.workloads},
+    }
+    if "cpu_baseline" in top:
+        line["cpu_baseline"] = top["cpu_baseline"]
     return line
 
 
@@ -573,19 +777,22 @@ def traffic_for(kernel, workload):
     return None
 
 
-# The sources the tensor-core kernels (the only ones with traffic entries) are compiled from: their
-# translation units and every header those include.
-TC_SOURCES = ("tp_args.h", "tp_device.cuh", "tp_launch.h", "tp_tc.cuh", "tp_tc_attn.cu", "tp_tc_host.h",
-              "tp_tc_lse.cu", "tp_tc_topk.cu")
+# Traffic entries are keyed to a hash of every source the kernels are compiled from: all of csrc/ and the
+# public header.
+CSRC = os.path.join(ROOT, "lazy_score_matrix_gb300", "csrc")
+HEADER = os.path.join(ROOT, "include", "tp.h")
+
+
+def kernel_sources():
+    return sorted([os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))] + [HEADER])
 
 
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "lazy_score_matrix_gb300", "csrc")
-    for f in TC_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    for path in kernel_sources():
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode() + fh.read())
     return h.hexdigest()[:12]
 
 
@@ -596,7 +803,7 @@ def source_hash():
 
 def oracle_infonce(rows: int, threads: int = 0):
     """Oracle forward + backward of the InfoNCE workload on its first `rows` rows against all columns.
-    Returns (seconds, pairs, threads used)."""
+    Returns (seconds, pairs, threads used, description)."""
     from lazy_score_matrix_gb300 import synth
     from oracle import oracle
     w = synth.workload(2)
@@ -610,37 +817,46 @@ def oracle_infonce(rows: int, threads: int = 0):
     lse = oracle.logsumexp(pb, exclude_self=True)
     oracle.logsumexp_backward(pb, lse, np.full(rows, -1.0 / N), exclude_self=True)
     dt = time.perf_counter() - t0
-    return dt, rows * N, used
+    return dt, rows * N, used, f"oracle fwd + bwd of rows 0..{rows - 1} of z against all {N} columns"
 
 
-def cpu_baseline(sample_rows=8192):
-    dt, pairs, used = oracle_infonce(sample_rows)
+def cpu_baseline(wl):
+    """The oracle as it stands, on all host cores, on a bounded sample of the workload (a few seconds)."""
+    from oracle import oracle
+    oracle.set_threads(0)
+    wl.oracle_sample(max(1, wl.cpu_rows // 8))  # warm-up (page-in, thread start)
+    dt, pairs, used, what = wl.oracle_sample(wl.cpu_rows)
     return {"value": round(pairs / dt / 1e9, 6), "unit": "Gpairs/s", "cores": used, "kind": "oracle",
-            "sample": f"oracle fwd+bwd on all {pairs} pairs of the 8192x8192 InfoNCE workload "
-                      f"({sample_rows} rows), {dt:.1f} s"}
+            "sample": f"{what}: {pairs} pairs in {dt:.2f} s"}
 
 
 def reference_arm(args, rank, world):
-    if rank != 0:
+    """The oracle timed as the reference implementation: each step a bounded row sample of the top-level
+    workload (InfoNCE: 2048 of the 8192 rows against all columns, forward + backward)."""
+    if rank != 0 or args.workload != 2:
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the oracle on the "
+                              "InfoNCE workload (--workload 2) only"}), flush=True)
         return None
-    rows = 2048 if args.workload == 2 else 0
-    times = []
+    rows = 2048
     for _ in range(args.warmup):
         oracle_infonce(256)
-    used = 0
+    times, used, pairs = [], 0, 0
     for _ in range(args.steps):
-        dt, pairs, used = oracle_infonce(rows)
+        dt, pairs, used, _ = oracle_infonce(rows)
         times.append(dt)
     tot = sum(times)
     value = pairs * args.steps / tot / 1e9
+    cfg = {"workload": "infonce_logsumexp_f32_z8192x64_fwd+bwd", "N": 8192, "M": 8192, "D": 64,
+           "pairs_per_step": 8192 * 8192, "l2": "flushed before every timed step (256 MB write, untimed)",
+           "parallelism": "replicas" if world > 1 else "single GPU"}
     return {"metric": METRIC, "value": round(value, 6), "unit": "Gpairs/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": "infonce_logsumexp_f32_z8192x64_fwd+bwd", "N": 8192, "M": 8192, "D": 64,
-                       "sample_rows_per_step": rows},
-            "impl": "reference",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shapes of the workload)",
+            "config": cfg, "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": "Gpairs/s", "cores": used, "kind": "oracle",
-                             "sample": f"{rows} of 8192 rows against all 8192 columns per step"},
+                             "sample": f"rows 0..{rows - 1} of the 8192 against all 8192 columns per step "
+                                       f"(forward + backward); value = sampled pairs / time"},
             "e2e": {"value": round(value, 6), "unit": "Gpairs/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -648,13 +864,16 @@ def reference_arm(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="libtp", choices=["libtp", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--workloads", default="1,2,3,4,5,6",
+                    help="workloads of the line's 'workloads' object (comma-separated; empty for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.workloads = [int(w) for w in args.workloads.split(",") if w.strip()]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
@@ -666,8 +885,6 @@ def main():
         torch.distributed.init_process_group("nccl")
     line = gpu_arm(args, rank, world)
     if line is not None:
-        if not args.no_cpu_baseline and args.workload == 2:
-            line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtp.so")
+# calibration library of the benchmark (measured fp32 / fp64 FMA and exp2 rates), not part of libtp
+PEAKS_SRC = os.path.join(PKG, "peaks", "tp_peaks.cu")
+PEAKS_LIB = os.path.join(PKG, "libtp_peaks.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -67,6 +70,14 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False, e
         for obj, out in errors:
             sys.stderr.write(f"--- {os.path.basename(obj)} ---\n{out[-4000:]}\n")
         raise RuntimeError(f"libtp build failed in {len(errors)} translation unit(s)")
+    if force or not os.path.exists(PEAKS_LIB) or os.path.getmtime(PEAKS_LIB) < os.path.getmtime(PEAKS_SRC):
+        tmp = PEAKS_LIB + f".tmp{os.getpid()}"
+        r = subprocess.run([nvcc(), *ARCH, "-O3", "-Xcompiler", "-fPIC", "-shared", "-o", tmp, PEAKS_SRC],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("libtp_peaks build failed")
+        os.replace(tmp, PEAKS_LIB)
     objs = [os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
     if todo or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"

@@ -1,6 +1,6 @@
-"""The DRAM-traffic figures bench.py reports are keyed to a hash of the sources the tensor-core kernels
-are compiled from (CPU only): that set must be the whole include closure of their translation units, so
-that a change to any file those kernels are built from voids the recorded figures."""
+"""The DRAM-traffic figures bench.py reports are keyed to a hash of the sources the kernels are compiled
+from (CPU only): that set must hold the whole include closure of every kernel translation unit, so that a
+change to any file a kernel is built from voids the recorded figures."""
 import os
 import re
 
@@ -9,16 +9,18 @@ import bench
 CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "lazy_score_matrix_gb300", "csrc")
 
 
-def test_traffic_hash_covers_every_source_of_the_tensor_core_kernels():
-    units = [f for f in os.listdir(CSRC) if f.startswith("tp_tc") and f.endswith(".cu")]
+def test_traffic_hash_covers_every_source_of_the_kernels():
+    inc = os.path.join(os.path.dirname(CSRC), os.pardir, "include")
+    units = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu")]
     seen, todo = set(), list(units)
     while todo:
-        f = todo.pop()
+        f = os.path.realpath(todo.pop())
         if f in seen:
             continue
         seen.add(f)
-        todo += re.findall(r'#include "([^"]+)"', open(os.path.join(CSRC, f)).read())
-    assert sorted(seen) == sorted(bench.TC_SOURCES)
+        for name in re.findall(r'#include "([^"]+)"', open(f).read()):
+            todo.append(os.path.join(CSRC, name) if os.path.exists(os.path.join(CSRC, name)) else os.path.join(inc, name))
+    assert seen <= {os.path.realpath(p) for p in bench.kernel_sources()}
 
 
 def test_bench_reports_only_traffic_taken_on_the_current_sources():
