@@ -14,7 +14,7 @@ Map and Stein Variational Gradient Descent sections), with seeded synthetic inpu
   6  workload 4 under the causal mask (kept pairs N (N + 1) / 2)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libtp|reference] [--workload 2]
-                    [--workloads 1,2,3,4,5,6] [--no-cpu-baseline]
+                    [--workloads 1,2,3,4,5,6] [--no-cpu-baseline] [--small] [--no-clock-pass] [--no-peaks]
 
 The top-level JSON line is workload --workload (default 2, timed for exactly K steps); the line's
 "workloads" object holds every workload of --workloads, each with its own step count, roofline, e2e and
@@ -262,10 +262,11 @@ class InfoNCE(Workload):
     wid = 2
     cpu_rows = 1024
 
-    def __init__(self, dev, N=8192, D=64):
+    def __init__(self, dev, over=None):
         from lazy_score_matrix_gb300 import ops, synth
         self.ops = ops
-        w = synth.workload(2, N=N, D=D)
+        w = synth.workload(2, **(over or {}))
+        N, D = w["z"].shape
         self.N, self.D = N, D
         self.pairs = N * N
         self.name = f"infonce_logsumexp_f32_z{N}x{D}_fwd+bwd"
@@ -317,15 +318,15 @@ class RbfMatmul(Workload):
     wid = 1
     cpu_rows = 1024
 
-    def __init__(self, dev):
+    def __init__(self, dev, over=None):
         from lazy_score_matrix_gb300 import ops, synth
         self.ops = ops
-        w = synth.workload(1)
+        w = synth.workload(1, **(over or {}))
         self.N, self.D = w["X"].shape
         self.M = w["Y"].shape[0]
         self.C = w["V"].shape[1]
         self.pairs = self.N * self.M
-        self.name = "rbf_kernel_matmul_f32_X1024x3_Y1024x3_V1024x4_fwd+bwd"
+        self.name = (f"rbf_kernel_matmul_f32_X{self.N}x{self.D}_Y{self.M}x{self.D}_V{self.M}x{self.C}_fwd+bwd")
         self.score = ops.Score("rbf", gamma=w["gamma"])
         self.X, self.Y, self.V, self.G = (w[k].to(dev) for k in ("X", "Y", "V", "grad_out"))
         self.host = {k: w[k].pin_memory() for k in ("X", "Y", "V", "grad_out")}
@@ -378,15 +379,15 @@ class Knn(Workload):
     steps = 10
     cpu_rows = 64
 
-    def __init__(self, dev):
+    def __init__(self, dev, over=None):
         from lazy_score_matrix_gb300 import ops, synth
         self.ops = ops
-        w = synth.workload(3)
+        w = synth.workload(3, **(over or {}))
         self.N, self.D = w["X"].shape
         self.M = w["R"].shape[0]
         self.k = w["k"]
         self.pairs = self.N * self.M
-        self.name = "knn_topk16_f32_X65536x16_R1048576x16_fwd"
+        self.name = f"knn_topk{self.k}_f32_X{self.N}x{self.D}_R{self.M}x{self.D}_fwd"
         self.score = ops.Score("sqeuclidean")
         self.X, self.R = w["X"].to(dev), w["R"].to(dev)
         self.X_h, self.R_h = w["X"].pin_memory(), w["R"].pin_memory()
@@ -428,15 +429,15 @@ class Attention(Workload):
     cpu_rows = 256
     mask = "all"
 
-    def __init__(self, dev):
+    def __init__(self, dev, over=None):
         from lazy_score_matrix_gb300 import ops, synth
         self.ops = ops
-        w = synth.workload(4)
+        w = synth.workload(4, **(over or {}))
         self.N, self.D = w["Q"].shape
         self.M = w["K"].shape[0]
         self.C = w["V"].shape[1]
         self.pairs = self.N * self.M
-        self.name = "attention_softmax_matmul_f32_QKV16384x64_fwd+bwd"
+        self.name = f"attention_softmax_matmul_f32_QKV{self.N}x{self.D}_fwd+bwd"
         self.score = ops.Score("linear", scale=w["scale"])
         self.Q, self.K, self.V, self.G = (w[k].to(dev) for k in ("Q", "K", "V", "grad_out"))
         self.host = {k: w[k].pin_memory() for k in ("Q", "K", "V", "grad_out")}
@@ -509,9 +510,9 @@ class CausalAttention(Attention):
     wid = 6
     mask = "causal"
 
-    def __init__(self, dev):
-        super().__init__(dev)
-        self.name = "causal_attention_softmax_matmul_f32_QKV16384x64_fwd+bwd"
+    def __init__(self, dev, over=None):
+        super().__init__(dev, over)
+        self.name = f"causal_attention_softmax_matmul_f32_QKV{self.N}x{self.D}_fwd+bwd"
         self.score = self.ops.Score("linear", scale=self.score.scale, pair_mask="causal")
         self.pairs = self.N * (self.N + 1) // 2
 
@@ -523,15 +524,15 @@ class Svgd(Workload):
     steps = 3
     cpu_rows = 512
 
-    def __init__(self, dev):
+    def __init__(self, dev, over=None):
         from lazy_score_matrix_gb300 import ops, synth
         self.ops = ops
-        w = synth.workload(5)
+        w = synth.workload(5, **(over or {}))
         self.N, self.D = w["x"].shape
         self.M = self.N
         self.gamma = w["gamma"]
         self.pairs = self.N * self.N
-        self.name = "svgd_direction_f64_x131072x8_fwd"
+        self.name = f"svgd_direction_f64_x{self.N}x{self.D}_fwd"
         self.x, self.sc = w["x"].to(dev), w["score"].to(dev)
         self.x_h, self.s_h = w["x"].pin_memory(), w["score"].pin_memory()
         self.x_d, self.s_d = torch.empty_like(self.x), torch.empty_like(self.sc)
@@ -539,7 +540,8 @@ class Svgd(Workload):
         self.h2d = 2 * self.N * self.D * 8
         self.d2h = self.N * self.D * 8
         D = self.D
-        # one sweep with V = [score | x | 1]: distance 2D+2, -gamma scale 1, accumulate 2(2D+1)
+        # credited: the per-pair cost of one sweep with V = [score | x | 1] (distance 2D+2, -gamma scale 1,
+        # accumulate 2(2D+1)); the kernel accumulates [score - 2 gamma x | 1] instead (2(D+1)), one fp64 exp
         self.flops_per_pair = {"fwd_sweep_svgd": (2 * D + 3 + 2 * (2 * D + 1), "alu")}
 
     def step(self):
@@ -564,6 +566,10 @@ class Svgd(Workload):
 
 
 WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd, 6: CausalAttention}
+# --small: the same kernels on reduced sizes, for profiler captures (a few hundred MB and launches of
+# milliseconds at most); never the benchmark's numbers
+SMALL = {1: {}, 2: {}, 3: dict(N=8192, M=131072), 4: dict(N=4096, M=4096), 5: dict(N=16384, M=16384),
+         6: dict(N=4096, M=4096)}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -719,18 +725,18 @@ def clock_pass(wl, graph, dev, seconds=1.2):
 def gpu_arm(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    peaks(dev)
+    peaks(None if args.no_peaks else dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 256 MB > 129 MB L2
     order = [args.workload] + [w for w in args.workloads if w != args.workload]
     results, top, top_wl = {}, None, None
     for wid in order:
-        wl = WORKLOADS[wid](dev)
+        wl = WORKLOADS[wid](dev, SMALL[wid] if args.small else None)
         steps = args.steps if wid == args.workload else min(args.steps, wl.steps)
         r = bench_workload(wl, steps, args.warmup, flush, world, dev)
         graph = r.pop("_graph")
         if wid == args.workload:
             top, top_wl = r, wl
-            r["clocks"] = clock_pass(wl, graph, dev) if rank == 0 else None
+            r["clocks"] = clock_pass(wl, graph, dev) if rank == 0 and not args.no_clock_pass else None
         if rank == 0 and not args.no_cpu_baseline and wid in args.workloads:
             r["cpu_baseline"] = cpu_baseline(wl)
         results[str(wid)] = r
@@ -871,6 +877,9 @@ def main():
     ap.add_argument("--workloads", default="1,2,3,4,5,6",
                     help="workloads of the line's 'workloads' object (comma-separated; empty for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true", help="reduced sizes of the same kernels (profiler captures)")
+    ap.add_argument("--no-clock-pass", action="store_true", help="skip the >= 1 s clock-sampling pass")
+    ap.add_argument("--no-peaks", action="store_true", help="skip the ALU peak measurement (derived peaks)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     args.workloads = [int(w) for w in args.workloads.split(",") if w.strip()]

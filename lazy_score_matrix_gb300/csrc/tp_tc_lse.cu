@@ -1429,6 +1429,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     const LseBwdTcPlan pl = lse_bwd_tc_plan(a.nP);
     int* err = device_error_word();
     if (!err) return -3;
+    const bool glob = a.metric == kLinear && !a.apply_exp;
     char* ws = static_cast<char*>(a.ws);
     __half2* zh = reinterpret_cast<__half2*>(ws + pl.off_zh);
     __half2* zl = reinterpret_cast<__half2*>(ws + pl.off_zl);
@@ -1444,7 +1445,6 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     // linear score without exp: one power of two for z and one for kappa, fixed for the whole sweep (a
     // reduction finds max|z| and max|g|), and the two-group kernel lse_bwd_lin_tc; otherwise per-row powers
     // of two and lse_bwd_sym_tc with its per-tile row-maximum exchange
-    const bool glob = a.metric == kLinear && !a.apply_exp;
     if (glob) {
         cudaMemsetAsync(gm, 0, 2 * sizeof(int), s);
         {
