@@ -66,6 +66,7 @@ SIGNATURES = {
     "tp_timer_read": ([_I64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)], _INT),
     "tp_device_status": ([_INT], _INT),
     "tp_selftest_bounded_wait": ([_I64, _P], _INT),
+    "tp_selftest_exp64": ([_P, _P, _I64, _P], _INT),
 }
 
 LAUNCH_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_char_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p)

@@ -354,8 +354,7 @@ int fwd_width(int mode, int D, int C) {
         case kMatmul: return C;
         case kSoftmax: return 2 + C;
         case kLse: return 2;
-        case kDisp: return D + 1;
-        default: return 2 * D + 1;
+        default: return D + 1;  // kDisp, kSvgd: D sums and the row mass
     }
 }
 

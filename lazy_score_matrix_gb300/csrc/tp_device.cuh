@@ -37,7 +37,7 @@ struct Vec16<double> {
 
 // exp in the working precision. fp32: the hardware base-2 exponential on a pre-scaled argument;
 // every fp32 kernel keeps log-sum-exp state in base 2 (kLogB = log2 e) and converts at the end.
-// fp64: the CUDA math library's exp (no fp64 special-function unit).
+// fp64: exp_table below (no fp64 special-function unit).
 template <class T>
 struct ExpTraits;
 template <>
@@ -61,13 +61,60 @@ struct ExpTraits<float> {
         return fmaf(m, kLn2Hi, fmaf(m, kLn2Lo, logf(L)));
     }
 };
+// 2^(j/64), j = 0..63, each correctly rounded to fp64 (computed in 60-digit decimal arithmetic; a CPU test
+// recomputes every entry).
+static __device__ const double kExp2Tab64[64] = {
+    0x1.0000000000000p+0, 0x1.02c9a3e778061p+0, 0x1.059b0d3158574p+0, 0x1.0874518759bc8p+0,
+    0x1.0b5586cf9890fp+0, 0x1.0e3ec32d3d1a2p+0, 0x1.11301d0125b51p+0, 0x1.1429aaea92de0p+0,
+    0x1.172b83c7d517bp+0, 0x1.1a35beb6fcb75p+0, 0x1.1d4873168b9aap+0, 0x1.2063b88628cd6p+0,
+    0x1.2387a6e756238p+0, 0x1.26b4565e27cddp+0, 0x1.29e9df51fdee1p+0, 0x1.2d285a6e4030bp+0,
+    0x1.306fe0a31b715p+0, 0x1.33c08b26416ffp+0, 0x1.371a7373aa9cbp+0, 0x1.3a7db34e59ff7p+0,
+    0x1.3dea64c123422p+0, 0x1.4160a21f72e2ap+0, 0x1.44e086061892dp+0, 0x1.486a2b5c13cd0p+0,
+    0x1.4bfdad5362a27p+0, 0x1.4f9b2769d2ca7p+0, 0x1.5342b569d4f82p+0, 0x1.56f4736b527dap+0,
+    0x1.5ab07dd485429p+0, 0x1.5e76f15ad2148p+0, 0x1.6247eb03a5585p+0, 0x1.6623882552225p+0,
+    0x1.6a09e667f3bcdp+0, 0x1.6dfb23c651a2fp+0, 0x1.71f75e8ec5f74p+0, 0x1.75feb564267c9p+0,
+    0x1.7a11473eb0187p+0, 0x1.7e2f336cf4e62p+0, 0x1.82589994cce13p+0, 0x1.868d99b4492edp+0,
+    0x1.8ace5422aa0dbp+0, 0x1.8f1ae99157736p+0, 0x1.93737b0cdc5e5p+0, 0x1.97d829fde4e50p+0,
+    0x1.9c49182a3f090p+0, 0x1.a0c667b5de565p+0, 0x1.a5503b23e255dp+0, 0x1.a9e6b5579fdbfp+0,
+    0x1.ae89f995ad3adp+0, 0x1.b33a2b84f15fbp+0, 0x1.b7f76f2fb5e47p+0, 0x1.bcc1e904bc1d2p+0,
+    0x1.c199bdd85529cp+0, 0x1.c67f12e57d14bp+0, 0x1.cb720dcef9069p+0, 0x1.d072d4a07897cp+0,
+    0x1.d5818dcfba487p+0, 0x1.da9e603db3285p+0, 0x1.dfc97337b9b5fp+0, 0x1.e502ee78b3ff6p+0,
+    0x1.ea4afa2a490dap+0, 0x1.efa1bee615a27p+0, 0x1.f50765b6e4540p+0, 0x1.fa7c1819e90d8p+0,
+};
+
+// fp64 exp by the table-driven method of P. T. P. Tang ("Table-driven implementation of the exponential
+// function in IEEE floating-point arithmetic", ACM Trans. Math. Softw. 15(2), 1989): with N the integer
+// nearest x 64/ln2, x = N ln2/64 + r, |r| <= ln2/128, and exp(x) = 2^(N >> 6) 2^((N & 63)/64) e^r.
+// 2^(j/64) comes from the table above, e^r - 1 from its degree-5 Taylor polynomial (the first omitted
+// term r^6/720 is below 4e-17 relative for |r| <= ln2/128), and r from a two-part ln2/64 whose leading
+// part has 36 significant bits, so N L1 is exact for every N that occurs. About ten fp64 operations
+// (a general library exp takes about twice as many, on a pipe the fp64 sweeps saturate). Arguments
+// below -707 give 0 (exp(-707) ~ 1e-307: a term that small changes no fp64 sum of larger ones); above
+// 709.78, +inf; NaN is not handled (non-finite inputs are unsupported).
+__device__ __forceinline__ double exp_table(double x) {
+    constexpr double kInvL = 0x1.71547652b82fep+6;                            // 64 / ln 2
+    constexpr double kL1 = 0x1.62e42fefa0000p-7, kL2 = 0x1.cf79abc9e3b3ap-46;  // ln2/64 = L1 + L2
+    constexpr double kShift = 0x1.8p52;  // adding 1.5 2^52 rounds to an integer kept in the low word
+    const double xc = fmin(fmax(x, -707.0), 709.78);
+    const double s = fma(xc, kInvL, kShift);
+    const int N = __double2loint(s);
+    const double Nd = s - kShift;
+    const double r = fma(-Nd, kL2, fma(-Nd, kL1, xc));
+    const double q = fma(r, fma(r, fma(r, 1.0 / 120.0, 1.0 / 24.0), 1.0 / 6.0), 0.5);
+    const double t = __ldg(kExp2Tab64 + (N & 63));
+    const double y = fma(t, fma(r * r, q, r), t);  // 2^(j/64) e^r, in [0.99, 1.99]
+    // times 2^(N >> 6), N >> 6 in [-1020, 1023]: added to the exponent field (the result stays normal)
+    const double res = __hiloint2double(__double2hiint(y) + (int)((unsigned)(N >> 6) << 20), __double2loint(y));
+    return x < -707.0 ? 0.0 : (x > 709.78 ? __longlong_as_double(0x7ff0000000000000ULL) : res);
+}
+
 template <>
 struct ExpTraits<double> {
     static constexpr double kLogB = 1.0;
     static constexpr double kLnB = 1.0;
-    __device__ __forceinline__ static double bexp(double x) { return ::exp(x); }
+    __device__ __forceinline__ static double bexp(double x) { return exp_table(x); }
     __device__ __forceinline__ static double blog(double x) { return ::log(x); }
-    __device__ __forceinline__ static double exp(double x) { return ::exp(x); }
+    __device__ __forceinline__ static double exp(double x) { return exp_table(x); }
     __device__ __forceinline__ static double lse(double m, double L) { return m + ::log(L); }
 };
 

@@ -95,7 +95,7 @@ template <class T, int DP, int CP, int MODE, bool AFFINE>
 struct FwdSmem {
     static constexpr bool HAS_V = MODE == kMatmul || MODE == kSoftmax || MODE == kSvgd;
     static constexpr int VW = MODE == kSvgd ? DP : CP;
-    static constexpr int NRUN = (MODE == kMatmul || MODE == kSoftmax) ? CP : (MODE == kDisp ? DP : (MODE == kSvgd ? 2 * DP : 0));
+    static constexpr int NRUN = (MODE == kMatmul || MODE == kSoftmax) ? CP : (MODE == kDisp || MODE == kSvgd ? DP : 0);
     static constexpr size_t bytes = al16<T>(kTile * DP) + (HAS_V ? al16<T>(kTile * VW) : 0) + al16<T>(kTile) +
                                     (AFFINE ? 2 * al16<T>(kTile) : 0) + al16<T>((size_t)NRUN * kThreads);
 };
@@ -130,7 +130,7 @@ struct SmemCursor {
 
 template <int MODE>
 __host__ __device__ inline int fwd_state_width(int D, int C) {
-    return MODE == kMatmul ? C : MODE == kSoftmax ? 2 + C : MODE == kLse ? 2 : MODE == kDisp ? D + 1 : 2 * D + 1;
+    return MODE == kMatmul ? C : MODE == kSoftmax ? 2 + C : MODE == kLse ? 2 : D + 1;  // kDisp, kSvgd: D sums + mass
 }
 
 template <class T, int DP, int CP, int MODE, bool AFFINE>
@@ -140,7 +140,6 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
     constexpr bool HAS_V = SM::HAS_V;
     constexpr int VW = SM::VW;
     constexpr int NACC = (MODE == kMatmul || MODE == kSoftmax) ? CP : (MODE == kLse ? 1 : DP);
-    constexpr int NACC2 = MODE == kSvgd ? DP : 1;
     constexpr bool VEC_RUN = SM::NRUN > 0;
 
     extern __shared__ __align__(16) unsigned char tp_smem[];
@@ -151,7 +150,6 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
     T* sw = AFFINE ? cur.take<T>(kTile) : nullptr;
     T* sb = AFFINE ? cur.take<T>(kTile) : nullptr;
     RunningVec<T, NACC> run1{cur.take<T>((size_t)SM::NRUN * kThreads)};
-    RunningVec<T, NACC2> run2{run1.base + (size_t)NACC * kThreads};
 
     const T* __restrict__ P = static_cast<const T*>(a.P);
     const T* __restrict__ Q = static_cast<const T*>(a.Q);
@@ -174,14 +172,10 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
 
     // tile accumulators (registers); running accumulators (shared memory / scalars)
     T acc[NACC];
-    T acc2[NACC2];
 #pragma unroll
     for (int c = 0; c < NACC; ++c) acc[c] = T(0);
-#pragma unroll
-    for (int c = 0; c < NACC2; ++c) acc2[c] = T(0);
     if constexpr (VEC_RUN) {
         run1.init();
-        if constexpr (MODE == kSvgd) run2.init();
     }
     T m = ninf<T>();
     Running<T> l, mass;
@@ -204,6 +198,10 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
             __syncthreads();
             if (a.metric != kLinear) {
                 stage_norms<T, DP>(sn, sq, cnt);
+                if constexpr (MODE == kSvgd) {  // the staged values become w_j = score_j - 2 gamma x_j
+                    const T g2 = T(2 * a.gamma);
+                    for (int e = threadIdx.x; e < cnt * DP; e += kThreads) sv[e] = fma(-g2, sq[e], sv[e]);
+                }
                 __syncthreads();
             }
             const T m0 = m;  // the running state is relative to the max at the start of the tile
@@ -237,9 +235,8 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                 } else if constexpr (MODE == kDisp) {
                     axpy_smem<T, DP>(acc, S, q);
                     mass.tile += S;
-                } else {  // kSvgd: S is the bare rbf kernel value k_ij
+                } else {  // kSvgd: S is the bare rbf kernel value k_ij; the staged row is w_j = score_j - 2 gamma x_j
                     axpy_smem<T, DP>(acc, S, sv + jj * DP);
-                    axpy_smem<T, DP>(acc2, S, q);
                     mass.tile += S;
                 }
             }
@@ -251,7 +248,6 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
                 if constexpr (MODE == kSoftmax) run1.flush(acc, r);
             } else {
                 if constexpr (VEC_RUN) run1.flush(acc);
-                if constexpr (MODE == kSvgd) run2.flush(acc2);
                 mass.flush();
             }
         }
@@ -286,11 +282,8 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
         } else {
 #pragma unroll
             for (int d = 0; d < DP; ++d)
-                if (d < a.D) {
-                    o[(int64_t)d * a.nP] = run1.get(d);
-                    o[(int64_t)(a.D + d) * a.nP] = run2.get(d);
-                }
-            o[(int64_t)(2 * a.D) * a.nP] = MASS;
+                if (d < a.D) o[(int64_t)d * a.nP] = run1.get(d);
+            o[(int64_t)a.D * a.nP] = MASS;
         }
         return;
     }
@@ -313,10 +306,11 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
         for (int d = 0; d < DP; ++d)
             if (d < a.D) out[pi * a.D + d] = run1.get(d) - MASS * p[d];
     } else {
+        // phi_i = (sum_j k_ij (score_j - 2 gamma x_j) + 2 gamma x_i sum_j k_ij) / n
         const T g2 = T(2 * a.gamma), inv_n = T(a.inv_n);
 #pragma unroll
         for (int d = 0; d < DP; ++d)
-            if (d < a.D) out[pi * a.D + d] = (run1.get(d) - g2 * (run2.get(d) - MASS * p[d])) * inv_n;
+            if (d < a.D) out[pi * a.D + d] = fma(g2 * MASS, p[d], run1.get(d)) * inv_n;
     }
 }
 
@@ -362,17 +356,13 @@ __global__ void __launch_bounds__(kThreads) fwd_merge(const SweepArgs a) {
     } else {
         const T* P = static_cast<const T*>(a.P);
         T mass = T(0);
-        const int mi = MODE == kDisp ? a.D : 2 * a.D;
-        for (int sp = 0; sp < a.splits; ++sp) mass += ws[sp * sstride + (int64_t)mi * a.nP + pi];
+        for (int sp = 0; sp < a.splits; ++sp) mass += ws[sp * sstride + (int64_t)a.D * a.nP + pi];
         for (int d = 0; d < a.D; ++d) {
-            T s1 = T(0), s2 = T(0);
-            for (int sp = 0; sp < a.splits; ++sp) {
-                s1 += ws[sp * sstride + (int64_t)d * a.nP + pi];
-                if (MODE == kSvgd) s2 += ws[sp * sstride + (int64_t)(a.D + d) * a.nP + pi];
-            }
+            T s1 = T(0);
+            for (int sp = 0; sp < a.splits; ++sp) s1 += ws[sp * sstride + (int64_t)d * a.nP + pi];
             const T pd = P[pi * a.D + d];
             if (MODE == kDisp) out[pi * a.D + d] = s1 - mass * pd;
-            else out[pi * a.D + d] = (s1 - T(2 * a.gamma) * (s2 - mass * pd)) * T(a.inv_n);
+            else out[pi * a.D + d] = fma(T(2 * a.gamma) * mass, pd, s1) * T(a.inv_n);
         }
     }
 }

@@ -17,6 +17,7 @@
 #include <string>
 
 #include "tp.h"
+#include "tp_device.cuh"
 #include "tp_launch.h"
 #include "tp_tc.cuh"
 
@@ -53,6 +54,12 @@ __global__ void bounded_wait_selftest(int* err, unsigned long long limit_ns) {
     }
     __syncwarp();
     if (threadIdx.x == 0) tc::mbar_wait(&bar, 0, err, tc::kSelfTestCode, limit_ns);
+}
+
+// y = the fp64 exp the kernels use (exp_table), element by element.
+__global__ void exp64_selftest(const double* __restrict__ x, double* __restrict__ y, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = ExpTraits<double>::exp(x[i]);
 }
 
 }  // namespace
@@ -124,6 +131,20 @@ TP_API tp_status tp_selftest_bounded_wait(int64_t limit_ns, void* stream) {
     {
         tp::HookScope h("bounded_wait_selftest", s);
         tp::bounded_wait_selftest<<<1, 32, 0, s>>>(w, (unsigned long long)limit_ns);
+    }
+    return tp::launched(1);
+}
+
+TP_API tp_status tp_selftest_exp64(const double* x, double* y, int64_t n, void* stream) {
+    if (n < 0 || (n > 0 && (!x || !y))) {
+        tp::set_last_error("tp_selftest_exp64: x and y must be device arrays of n >= 0 doubles");
+        return TP_ERR_INVALID_ARG;
+    }
+    if (n == 0) return TP_OK;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        tp::HookScope h("exp64_selftest", s);
+        tp::exp64_selftest<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, y, n);
     }
     return tp::launched(1);
 }

@@ -33,7 +33,7 @@ def score(metric=1, **kw):
 
 def test_exports_every_header_symbol(lib):
     declared = _lib.header_symbols()
-    assert len(declared) == 22, declared
+    assert len(declared) == 23, declared
     out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     missing = [s for s in declared if s not in exported]
@@ -242,3 +242,32 @@ def test_noalloc_rejects_problems_beyond_its_fixed_array(lib):
     for D, dt in ((32, _lib.TP_F32), (64, _lib.TP_F64), (3, _lib.TP_F64)):
         for N in (1000, 65536, 10 ** 6):
             assert ws(lib, "pairwise_logsumexp", pairs(N, 10 ** 6, D, dtype=dt)) <= 2 << 20
+
+
+def test_exp64_table_is_correctly_rounded():
+    """The 64-entry table 2^(j/64) of the fp64 exp (csrc/tp_device.cuh), recomputed here in 60-digit
+    decimal arithmetic (ln 2 from its series, exp from its series) and rounded to the nearest double."""
+    import os
+    import re
+    from decimal import Decimal, getcontext
+    getcontext().prec = 60
+    src = open(os.path.join(os.path.dirname(_lib.PKG), "lazy_score_matrix_gb300", "csrc", "tp_device.cuh")).read()
+    body = src[src.index("kExp2Tab64[64] = {"):]
+    body = body[body.index("{") + 1:body.index("};")]
+    tab = [float.fromhex(v) for v in re.findall(r"0x[0-9a-f.]+p[+-]\d+", body)]
+    assert len(tab) == 64
+    ln2 = sum(Decimal(1) / (k * Decimal(2) ** k) for k in range(1, 400))
+
+    def dexp(x):
+        s, t = Decimal(1), Decimal(1)
+        for k in range(1, 120):
+            t = t * x / k
+            s += t
+        return s
+
+    for j, v in enumerate(tab):
+        exact = dexp(ln2 * j / 64)
+        assert v == float(exact), j
+        # correctly rounded: no double is closer
+        import math
+        assert abs(Decimal(v) - exact) <= Decimal(math.ulp(v)) / 2, j
