@@ -45,7 +45,12 @@ struct TopkTcShape {
     static constexpr int kCols = kKBN / kParts;
     static constexpr int kThreads = 32 * (2 + kSel);
     static constexpr size_t kKeyBuf = (size_t)kSel * 32 * 32 * 4;  // per selection warp: 32 columns x 32 lanes
-    static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + 256 + 1024;
+    // thresholds shared by the column parts of a row ([part][row], each tagged with its unit), where there
+    // is room (the four-part layout); the two-part layout (D > 32) fills shared memory without them
+    static constexpr bool kShare = kParts == 4;
+    static constexpr size_t kThrBuf = kShare ? (size_t)kParts * kKBM * 8 : 0;
+    static constexpr size_t kSmem =
+        (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + kThrBuf + 256 + 1024;
     static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
@@ -60,8 +65,25 @@ struct TopkTcParams {
     const float* yn;   // padded to CT * 128 entries
     float* pv;         // [U][kKLists][K][128] keys (parts beyond `parts` unused)
     int* pi;           // same layout, column indices
+    const int* lo_any; // nonzero when some point has a nonzero tf32 low part (written by the split pre-pass)
     int* err;
 };
+
+// The smaller of three floats (one instruction on this architecture).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// The smallest of 32 values.
+__device__ __forceinline__ float min32(const float (&v)[32]) {
+    float m[11];
+#pragma unroll
+    for (int g = 0; g < 10; ++g) m[g] = fmin3(v[3 * g], v[3 * g + 1], v[3 * g + 2]);
+    m[10] = fminf(v[30], v[31]);
+    const float a = fmin3(m[0], m[1], m[2]), b = fmin3(m[3], m[4], m[5]), c = fmin3(m[6], m[7], m[8]);
+    return fmin3(fmin3(a, b, c), m[9], m[10]);
+}
 
 // Work units are (row block, chunk of column tiles), numbered u = rb * H + chunk and dealt round-robin:
 // CTA c takes u = c, c + G, c + 2G, ... At any moment the CTAs work on one "wave" of G consecutive
@@ -115,7 +137,8 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     unsigned char* sB = sm + SH::kPair;
     float* sYn = reinterpret_cast<float*>(sB + (size_t)SH::kPair * SH::kStages);  // [stage][128]
     float* sKeys = sYn + SH::kStages * kKBN;                                         // [warp][32 u][32 lanes]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sKeys + SH::kKeyBuf / 4);
+    uint64_t* sThr = reinterpret_cast<uint64_t*>(sKeys + SH::kKeyBuf / 4);         // [kParts][128]
+    uint64_t* bars = sThr + SH::kThrBuf / 8;
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
     uint64_t* b_full = bars + 2;               // [kStages]
@@ -139,6 +162,9 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
             mbar_init(acc_empty + b, 32 * SH::kSel);
         }
         mbar_fence_init();
+    }
+    if constexpr (SH::kShare) {  // no shared threshold yet: tag 0 (units are counted from 1), value +inf
+        for (int e = threadIdx.x; e < SH::kParts * kKBM; e += blockDim.x) sThr[e] = 0x7f800000ull;
     }
     if (warp == 1) tmem_alloc(tslot, 256);
     fence_before_sync();
@@ -179,6 +205,9 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     } else if (warp == 1) {
         if (lane == 0) {  // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_tf32(kKBM, kKBN);
+            // every low part zero (points exact in tf32, integers for instance): the two products with a low
+            // part add exact zeros, so only Xh Yh is issued (the same result, a third of the MMAs)
+            const int prod0 = *reinterpret_cast<const volatile int*>(p.lo_any) ? 0 : 2;
             constexpr int KS = DP / 8;
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
@@ -202,8 +231,8 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 const uint32_t ao[3] = {0u, (uint32_t)SH::kOperand, 0u};  // Xh Yl, Xl Yh, then Xh Yh
                 const uint32_t bo[3] = {(uint32_t)SH::kOperand, 0u, 0u};
                 uint32_t acc = 0;
-#pragma unroll
-                for (int prod = 0; prod < 3; ++prod) {
+#pragma unroll 1
+                for (int prod = prod0; prod < 3; ++prod) {
 #pragma unroll
                     for (int ks = 0; ks < KS; ++ks) {
                         const uint32_t koff = (uint32_t)((ks >> 2) * kChunk + (ks & 3) * 32);
@@ -222,10 +251,17 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
         const int lr = q * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * SH::kCols);
         const float sgn = p.largest ? -1.f : 1.f;
+        // sqeuclidean, k smallest, no exp, positive scale: a key is scale * max(d, 0) with d the unclamped
+        // distance, nondecreasing in d, so the chunk's smallest key is that of its smallest d, found with one
+        // FFMA and a third of a min per element; the keys themselves are formed only when that one could
+        // enter the list (the same operations, so the selection is unchanged)
+        const bool fast = METRIC == kSqeuclidean && !EXP && !p.largest && p.scale > 0.f;
         float kv[K];
         int ki[K];
         float xn = 0.f;
         bool ok = true;
+        uint32_t units = 0;  // units begun by this CTA: the tag of this unit's shared thresholds
+        volatile uint64_t* thr_row = sThr + lr;
         auto reset = [&]() {
 #pragma unroll
             for (int t = 0; t < K; ++t) {
@@ -249,34 +285,69 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 reset();
                 const int64_t row = (int64_t)rb * kKBM + lr;
                 xn = (METRIC != kLinear && row < p.N) ? p.xn[row] : 0.f;
+                ++units;
                 fresh = false;
             }
             const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
             ok = mbar_wait(acc_full + b, rr & 1, p.err, 86);
             if (!ok) break;
             fence_after_sync();
+            // The smallest k-th key over this row's column parts in this unit: each part's list holds k keys
+            // at or below its k-th, so a key above that minimum can never be among the row's final k (keys
+            // equal to it still go to the part's own strict test, which keeps the exact tie order). Each
+            // entry carries the unit it was written in (one 64-bit store); entries of another unit (other
+            // rows: a part may enter a unit before the others leave the previous one) are ignored, and older
+            // entries of this unit are larger, hence safe.
+            float shared = pinf<float>();
+            if constexpr (SH::kShare) {
+#pragma unroll
+                for (int pp = 0; pp < SH::kParts; ++pp) {
+                    const uint64_t e = thr_row[pp * kKBM];
+                    if ((uint32_t)(e >> 32) == units) shared = fminf(shared, __uint_as_float((uint32_t)e));
+                }
+            }
             const int j0 = ct * kKBN + half * SH::kCols;
             const int lim = (int)(p.M - j0 < SH::kCols ? p.M - j0 : SH::kCols);  // valid columns of this part
             const float* yn = sYn + s * kKBN + half * SH::kCols;
             float* wkeys = sKeys + (warp - 2) * 32 * 32;
+            bool inserted = false;
 #pragma unroll 1
             for (int c = 0; c < SH::kCols / 32; ++c) {
                 float v[32];
                 tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
-                // keys, and the columns that beat this row's current k-th key (the threshold only falls,
-                // so every column the insertion would take is in the mask)
+                // the columns whose key beats both this row's own k-th key and the parts' shared bound (the
+                // thresholds only fall, so every column the insertion would take is in the mask)
                 const float thr = kv[K - 1];
                 uint32_t cand = 0;
+                if (fast) {
 #pragma unroll
-                for (int u4 = 0; u4 < 8; ++u4) {
-                    const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
-                    const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
+                        v[u4 * 4 + 0] = fmaf(-2.f, v[u4 * 4 + 0], xn + y4.x);  // unclamped distances
+                        v[u4 * 4 + 1] = fmaf(-2.f, v[u4 * 4 + 1], xn + y4.y);
+                        v[u4 * 4 + 2] = fmaf(-2.f, v[u4 * 4 + 2], xn + y4.z);
+                        v[u4 * 4 + 3] = fmaf(-2.f, v[u4 * 4 + 3], xn + y4.w);
+                    }
+                    const float kmin = p.scale * fmaxf(min32(v), 0.f);
+                    if (!__any_sync(0xffffffffu, kmin < thr && kmin <= shared)) continue;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int u = u4 * 4 + w;
-                        const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yv[w], p.scale, p.neg_gamma_log2);
+                    for (int u = 0; u < 32; ++u) {
+                        const float key = p.scale * fmaxf(v[u], 0.f);
                         v[u] = key;
-                        cand |= (c * 32 + u < lim && key < thr) ? (1u << u) : 0u;
+                        cand |= (c * 32 + u < lim && key < thr && key <= shared) ? (1u << u) : 0u;
+                    }
+                } else {
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
+                        const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int u = u4 * 4 + w;
+                            const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yv[w], p.scale, p.neg_gamma_log2);
+                            v[u] = key;
+                            cand |= (c * 32 + u < lim && key < thr && key <= shared) ? (1u << u) : 0u;
+                        }
                     }
                 }
                 // rare once the lists are full: stage the keys and insert the candidates in column order
@@ -284,6 +355,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
 #pragma unroll
                     for (int u = 0; u < 32; ++u) wkeys[u * 32 + lane] = v[u];
                     __syncwarp();
+                    inserted |= cand != 0u;
                     while (cand) {
                         const int u = __ffs(cand) - 1;
                         cand &= cand - 1u;
@@ -291,6 +363,9 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                     }
                     __syncwarp();
                 }
+            }
+            if constexpr (SH::kShare) {
+                if (inserted) thr_row[half * kKBM] = ((uint64_t)units << 32) | __float_as_uint(kv[K - 1]);
             }
             fence_before_sync();
             mbar_arrive(acc_empty + b);
@@ -340,27 +415,31 @@ __global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_
 // hi/lo split of a [n, D] fp32 array into [n, DP] (zero padded), row squared norms, and (for the
 // streamed set) norms padded with zeros to `npad` rows.
 __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int DP, float* __restrict__ hi,
-                             float* __restrict__ lo, float* __restrict__ norm, int64_t npad) {
-    const int64_t r = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;
+                             float* __restrict__ lo, float* __restrict__ norm, int64_t npad, int* __restrict__ lo_any) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;  // one warp per row
     if (r >= npad) return;
     float s = 0.f;
+    bool nz = false;
     for (int f = threadIdx.x; f < DP; f += 32) {
         const float e = (r < n && f < D) ? x[r * D + f] : 0.f;
         const float h = tf32_hi(e);
         if (r < n) {
+            const float l = tf32_lo(e, h);
             hi[r * DP + f] = h;
-            lo[r * DP + f] = tf32_lo(e, h);
+            lo[r * DP + f] = l;
+            nz |= l != 0.f;
         }
         s = fmaf(e, e, s);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (threadIdx.x == 0) norm[r] = s;
+    if (__any_sync(0xffffffffu, nz) && threadIdx.x == 0) atomicOr(lo_any, 1);
 }
 
 struct TopkTcPlan {
     int CT, G, DP, KB, H, U, chunk;
-    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, bytes;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, off_flag, bytes;
 };
 
 inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
@@ -391,6 +470,7 @@ inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     const size_t lists = (size_t)pl.U * kKLists * pl.KB * kKBM;
     pl.off_pv = o; o += al256(lists * 4);
     pl.off_pi = o; o += al256(lists * 4);
+    pl.off_flag = o; o += 256;
     pl.bytes = o;
     return pl;
 }
@@ -419,10 +499,12 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
         !make_map_2d(&myh, yh, pl.DP, a.nQ, 128) || !make_map_2d(&myl, yl, pl.DP, a.nQ, 128))
         return -1;
     int n = 0;
+    int* lo_any = reinterpret_cast<int*>(ws + pl.off_flag);
+    cudaMemsetAsync(lo_any, 0, sizeof(int), s);
     {
         HookScope h("tc_split_pad", s);
         tc_split_pad<<<(unsigned)((a.nP + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.P), a.nP, a.D,
-                                                                        pl.DP, xh, xl, xn, a.nP);
+                                                                        pl.DP, xh, xl, xn, a.nP, lo_any);
         ++n;
     }
     {
@@ -430,7 +512,7 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
         HookScope h("tc_split_pad", s);
         const int64_t npad = (int64_t)pl.CT * kKBN;
         tc_split_pad<<<(unsigned)((npad + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.Q), a.nQ, a.D,
-                                                                        pl.DP, yh, yl, yn, npad);
+                                                                        pl.DP, yh, yl, yn, npad, lo_any);
         ++n;
     }
     TopkTcParams p;
@@ -452,6 +534,7 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     p.yn = yn;
     p.pv = reinterpret_cast<float*>(ws + pl.off_pv);
     p.pi = reinterpret_cast<int*>(ws + pl.off_pi);
+    p.lo_any = lo_any;
     p.err = err;
     auto go = [&](auto kernel, size_t smem) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
