@@ -104,8 +104,29 @@ def peaks(dev=None):
 
 
 def roofline_for(kernel, fpp, bound, pairs, avg_ms, dtype, workload):
-    """The roofline object of one kernel: algorithmic flop per pair x pairs per launch / launch time."""
+    """The roofline object of one kernel: algorithmic flop per pair x pairs per launch / launch time.
+    A kernel whose time goes to instruction issue rather than to one pipe ("issue-tf32": the k-NN
+    top-k, whose selection runs on the ALUs behind a tf32 contraction) is held against the issue rate
+    instead: warp instructions per launch, counted by ncu on the current sources, over the launch time,
+    against one warp instruction per clock in each of the SM's four schedulers. Without a count taken
+    on the current sources it falls back to its algorithmic tf32 credit."""
     pk = peaks()
+    if bound.startswith("issue-"):
+        inst = issue_for(kernel, workload)
+        tensor = roofline_for(kernel, fpp, "tensor-" + bound[len("issue-"):], pairs, avg_ms, dtype, workload)
+        if inst is None:
+            tensor["issue"] = None
+            return tensor
+        ach = inst / (avg_ms / 1e3) / 1e9
+        peak = pk["sms"] * 4 * pk["sm_max_mhz"] * 1e6 / 1e9
+        return {"kernel": kernel, "bound": "alu", "operands": "warp instructions, every pipe",
+                "achieved": round(ach, 2), "peak": round(peak, 2), "unit": "Ginst/s", "frac": round(ach / peak, 4),
+                "traffic": traffic_for(kernel, workload),
+                "peak_source": (f"issue: {pk['sms']} SMs x 4 schedulers x 1 warp instruction per clock x "
+                                f"{pk['sm_max_mhz']:.0f} MHz, derived"),
+                "inst_per_launch": inst, "inst_per_pair": round(inst * 32 / pairs, 3),
+                "pairs_per_launch": pairs, "avg_launch_us": round(avg_ms * 1e3, 2),
+                "tensor_credit": {k: tensor[k] for k in ("achieved", "peak", "unit", "frac", "flop_per_pair")}}
     ach = fpp * pairs / (avg_ms / 1e3) / 1e12
     if bound == "tensor-f16":
         peak = pk["f16_tflops"]
@@ -398,7 +419,8 @@ class Knn(Workload):
         self.d2h = self.N * self.k * 12
         # the SIMT sweep runs the distance on the FP32 pipe; the tensor-core kernel runs the contraction
         # on tcgen05 (tf32) and the selection on the ALUs: it is credited with the same algorithmic flop
-        self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu"), "topk_tc": (2 * self.D + 2, "tensor-tf32")}
+        # (and held against the issue rate, where its selection's instructions are counted)
+        self.flops_per_pair = {"topk_sweep": (2 * self.D + 2, "alu"), "topk_tc": (2 * self.D + 2, "issue-tf32")}
 
     def step(self):
         return self.ops.pairwise_topk(self.X, self.R, self.score, self.k, False)
@@ -567,8 +589,10 @@ class Svgd(Workload):
 
 WORKLOADS = {1: RbfMatmul, 2: InfoNCE, 3: Knn, 4: Attention, 5: Svgd, 6: CausalAttention}
 # --small: the same kernels on reduced sizes, for profiler captures (a few hundred MB and launches of
-# milliseconds at most); never the benchmark's numbers
-SMALL = {1: {}, 2: {}, 3: dict(N=8192, M=131072), 4: dict(N=4096, M=4096), 5: dict(N=16384, M=16384),
+# tens of milliseconds at most); never the benchmark's numbers. The k-NN case keeps the whole reference
+# set and the length of a work unit (two column chunks of 524288 columns per row block), so its
+# selection sees lists that fill and tighten as on the full workload, with 19/32 of the rows.
+SMALL = {1: {}, 2: {}, 3: dict(N=38912, M=1048576), 4: dict(N=4096, M=4096), 5: dict(N=16384, M=16384),
          6: dict(N=4096, M=4096)}
 
 
@@ -767,6 +791,20 @@ def gpu_arm(args, rank, world):
     if "cpu_baseline" in top:
         line["cpu_baseline"] = top["cpu_baseline"]
     return line
+
+
+def issue_for(kernel, workload):
+    """Warp instructions per launch of `kernel` on `workload` (ncu smsp__inst_executed.sum) from the
+    committed summary (lines `kernel workload count src=<hash>`), if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", "issue.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash()
+    for l in open(path):
+        parts = l.split()
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[3] == f"src={cur}":
+            return float(parts[2])
+    return None
 
 
 def traffic_for(kernel, workload):

@@ -60,7 +60,9 @@ tp_status fail(tp_status s, const std::string& msg) {
     return s;
 }
 
-constexpr int64_t kTargetCtas = 152 * 4;  // 152 SMs on GB300, ~4 resident 128-thread CTAs each
+// Split heuristic of the streamed sweeps (part of the workspace size, so from the shapes only, never the
+// device): enough CTAs for a GB300's 152 SMs at ~4 resident 128-thread CTAs each.
+constexpr int64_t kTargetCtas = 152 * 4;
 constexpr int kMaxSplits = 64;
 constexpr size_t kAlign = 256;
 

@@ -708,7 +708,7 @@ static int run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scal
     p.C = C;
     p.sc = sc;
     p.T = T;
-    p.G = (int)(T < kGrid ? T : kGrid);
+    p.G = capped_grid((int)(T < kGrid ? T : kGrid));
     p.scale = scale;
     p.rstat = rstat;
     p.cstat = cstat;

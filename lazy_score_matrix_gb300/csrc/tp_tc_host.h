@@ -80,5 +80,19 @@ void launch_sched_prefix(const Sched& sc, int64_t* pfx, cudaStream_t s);
 
 inline size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
+// Persistent grids: at most one CTA per SM of the current device (looked up once per device). Workspaces are
+// sized for the GB300's 152 (shapes only); a device with fewer SMs runs that many CTAs over the same work.
+inline int capped_grid(int g) {
+    static int sms[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return g;
+    if (!sms[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return g;
+        sms[dev] = v;
+    }
+    return g < sms[dev] ? g : sms[dev];
+}
+
 }  // namespace tc
 }  // namespace tp

@@ -1327,7 +1327,7 @@ static LseBwdTcPlan lse_bwd_tc_plan(int64_t N) {
     pl.CT = (int)((N + kBNb - 1) / kBNb);
     pl.Npad = (int64_t)pl.CT * kBNb;
     pl.T = RB * pl.CT;
-    pl.G = (int)(pl.T < kGrid ? pl.T : kGrid);
+    pl.G = capped_grid((int)(pl.T < kGrid ? pl.T : kGrid));  // at most one CTA per SM of this device
     const int64_t per = (pl.T + pl.G - 1) / pl.G;
     pl.smax = (int)((per + pl.CT - 1) / pl.CT + 1);
     size_t o = 0;
@@ -1388,7 +1388,7 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
         ++n;
     }
     const int64_t T = sched_total(sc);
-    const int G = (int)(T < kGrid ? T : kGrid);
+    const int G = capped_grid((int)(T < kGrid ? T : kGrid));
     LseTcParams p;
     p.N = a.nP;
     p.M = a.nQ;
@@ -1450,7 +1450,8 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
         {
             HookScope h("lse_bwd_reduce", s);
             const int64_t blocks = (a.nP + 7) / 8;  // one block per SM at most: few atomics on the two slots
-            lse_bwd_reduce<<<(unsigned)(blocks < kGrid ? blocks : kGrid), 256, 0, s>>>(
+            const int rg = capped_grid(kGrid);
+            lse_bwd_reduce<<<(unsigned)(blocks < rg ? blocks : rg), 256, 0, s>>>(
                 static_cast<const float*>(a.P), static_cast<const float*>(a.glse), a.nP, gm);
             ++n;
         }

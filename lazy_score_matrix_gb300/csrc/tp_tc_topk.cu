@@ -5,7 +5,9 @@
 // The contraction X R^T runs on tcgen05.mma kind::tf32 with the hi/lo split of both operands (three
 // products); points whose coordinates are exact in tf32 (integers up to 2^11, for instance) have lo = 0,
 // so their dot products, norms and distances are exact and the selection is bit-identical to an exact
-// evaluation. The 128 x 128 score tile lands in TMEM; the selection warps (sixteen for D <= 32, four
+// evaluation. For the distance metrics, where two spare feature columns exist (D <= DP - 2), the norms
+// ride in the contraction: rows [x, |x|^2, 1] against columns [-2y, 1, |y|^2] give the unclamped squared
+// distance |x|^2 + |y|^2 - 2 x.y straight out of the accumulator, with no per-element norm loads. The 128 x 128 score tile lands in TMEM; the selection warps (sixteen for D <= 32, four
 // per TMEM lane quarter owning 32 of the tile's columns each; eight for D <= 64, two per quarter
 // owning 64 columns) turn each dot product into the score and keep a sorted
 // (value, index) list per row in registers, inserting only on a strict improvement, so equal values
@@ -60,6 +62,7 @@ struct TopkTcParams {
     int H, U, chunk;   // column chunks per row block, units (row block, chunk), column tiles per chunk
     int parts;         // selection parts (sorted lists) per row and unit
     int metric, apply_exp, largest;
+    int fold;          // the accumulator holds |x|^2 + |y|^2 - 2 x.y (norms folded into the operands)
     float scale, neg_gamma_log2;
     const float* xn;
     const float* yn;   // padded to CT * 128 entries
@@ -112,13 +115,22 @@ struct UnitCursor {
     }
 };
 
+// The smallest float above x (x itself for +inf and NaN): key <= x exactly when key < next_up(x).
+__device__ __forceinline__ float next_up(float x) {
+    if (!(x < pinf<float>())) return x;
+    if (x == 0.f) return __uint_as_float(1u);
+    const uint32_t u = __float_as_uint(x);
+    return __uint_as_float(x > 0.f ? u + 1u : u - 1u);
+}
+
+// The score of one accumulator value: a dot product, or with folded norms the unclamped squared distance.
 template <int METRIC, bool EXP>
-__device__ __forceinline__ float topk_score(float dot, float xn, float yn, float scale, float ngl2) {
+__device__ __forceinline__ float topk_score(float acc, bool fold, float xn, float yn, float scale, float ngl2) {
     float base;
     if (METRIC == kLinear) {
-        base = dot;
+        base = acc;
     } else {
-        const float d2 = fmaxf(fmaf(-2.f, dot, xn + yn), 0.f);
+        const float d2 = fmaxf(fold ? acc : fmaf(-2.f, acc, xn + yn), 0.f);
         base = METRIC == kRbf ? ExpTraits<float>::bexp(ngl2 * d2) : d2;
     }
     const float t = scale * base;
@@ -174,6 +186,9 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
 
     if (warp == 0) {
         if (lane == 0) {  // ---------------- TMA producer
+            // with every low part zero the MMAs read only the high parts: the low tiles are not loaded
+            const bool lo = *reinterpret_cast<const volatile int*>(p.lo_any) != 0;
+            const uint32_t bytes = lo ? SH::kPair : SH::kOperand;
             int rb_cur = -1, a_uses = 0;
             bool ok = true;
             int64_t i = 0;
@@ -182,10 +197,10 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 if (rb != rb_cur) {
                     if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 81);
                     if (!ok) break;
-                    mbar_expect_tx(a_full, SH::kPair);
+                    mbar_expect_tx(a_full, bytes);
                     for (int c = 0; c < SH::kChunks; ++c) {
                         tma_load_2d(sA + c * kChunk, &mXh, c * 32, rb * kKBM, a_full);
-                        tma_load_2d(sA + SH::kOperand + c * kChunk, &mXl, c * 32, rb * kKBM, a_full);
+                        if (lo) tma_load_2d(sA + SH::kOperand + c * kChunk, &mXl, c * 32, rb * kKBM, a_full);
                     }
                     ++a_uses;
                     rb_cur = rb;
@@ -194,10 +209,10 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 82);
                 if (!ok) break;
                 unsigned char* dst = sB + (size_t)s * SH::kPair;
-                mbar_expect_tx(b_full + s, SH::kPair + kKBN * 4);
+                mbar_expect_tx(b_full + s, bytes + kKBN * 4);
                 for (int c = 0; c < SH::kChunks; ++c) {
                     tma_load_2d(dst + c * kChunk, &mYh, c * 32, ct * kKBN, b_full + s);
-                    tma_load_2d(dst + SH::kOperand + c * kChunk, &mYl, c * 32, ct * kKBN, b_full + s);
+                    if (lo) tma_load_2d(dst + SH::kOperand + c * kChunk, &mYl, c * 32, ct * kKBN, b_full + s);
                 }
                 bulk_load(sYn + s * kKBN, p.yn + (size_t)ct * kKBN, kKBN * 4, b_full + s);
             }
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
             if (fresh) {
                 reset();
                 const int64_t row = (int64_t)rb * kKBM + lr;
-                xn = (METRIC != kLinear && row < p.N) ? p.xn[row] : 0.f;
+                xn = (METRIC != kLinear && !p.fold && row < p.N) ? p.xn[row] : 0.f;
                 ++units;
                 fresh = false;
             }
@@ -316,25 +331,31 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 float v[32];
                 tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
                 // the columns whose key beats both this row's own k-th key and the parts' shared bound (the
-                // thresholds only fall, so every column the insertion would take is in the mask)
+                // thresholds only fall, so every column the insertion would take is in the mask): key < thr and
+                // key <= shared, one comparison against the smaller of thr and the float above shared
                 const float thr = kv[K - 1];
+                const float bnd = fminf(thr, next_up(shared));
+                const int left = lim - c * 32;  // valid columns of these 32
+                const uint32_t valid = left >= 32 ? 0xffffffffu : (left > 0 ? (1u << left) - 1u : 0u);
                 uint32_t cand = 0;
                 if (fast) {
+                    if (!p.fold) {
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
-                        v[u4 * 4 + 0] = fmaf(-2.f, v[u4 * 4 + 0], xn + y4.x);  // unclamped distances
-                        v[u4 * 4 + 1] = fmaf(-2.f, v[u4 * 4 + 1], xn + y4.y);
-                        v[u4 * 4 + 2] = fmaf(-2.f, v[u4 * 4 + 2], xn + y4.z);
-                        v[u4 * 4 + 3] = fmaf(-2.f, v[u4 * 4 + 3], xn + y4.w);
+                        for (int u4 = 0; u4 < 8; ++u4) {
+                            const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
+                            v[u4 * 4 + 0] = fmaf(-2.f, v[u4 * 4 + 0], xn + y4.x);  // unclamped distances
+                            v[u4 * 4 + 1] = fmaf(-2.f, v[u4 * 4 + 1], xn + y4.y);
+                            v[u4 * 4 + 2] = fmaf(-2.f, v[u4 * 4 + 2], xn + y4.z);
+                            v[u4 * 4 + 3] = fmaf(-2.f, v[u4 * 4 + 3], xn + y4.w);
+                        }
                     }
                     const float kmin = p.scale * fmaxf(min32(v), 0.f);
-                    if (!__any_sync(0xffffffffu, kmin < thr && kmin <= shared)) continue;
+                    if (!__any_sync(0xffffffffu, kmin < bnd)) continue;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const float key = p.scale * fmaxf(v[u], 0.f);
                         v[u] = key;
-                        cand |= (c * 32 + u < lim && key < thr && key <= shared) ? (1u << u) : 0u;
+                        cand |= key < bnd ? (1u << u) : 0u;
                     }
                 } else {
 #pragma unroll
@@ -344,12 +365,14 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             const int u = u4 * 4 + w;
-                            const float key = sgn * topk_score<METRIC, EXP>(v[u], xn, yv[w], p.scale, p.neg_gamma_log2);
+                            const float key =
+                                sgn * topk_score<METRIC, EXP>(v[u], p.fold != 0, xn, yv[w], p.scale, p.neg_gamma_log2);
                             v[u] = key;
-                            cand |= (c * 32 + u < lim && key < thr && key <= shared) ? (1u << u) : 0u;
+                            cand |= key < bnd ? (1u << u) : 0u;
                         }
                     }
                 }
+                cand &= valid;
                 // rare once the lists are full: stage the keys and insert the candidates in column order
                 if (__any_sync(0xffffffffu, cand != 0u)) {
 #pragma unroll
@@ -413,18 +436,23 @@ __global__ void topk_tc_merge(TopkTcParams p, float* __restrict__ values, int64_
 }
 
 // hi/lo split of a [n, D] fp32 array into [n, DP] (zero padded), row squared norms, and (for the
-// streamed set) norms padded with zeros to `npad` rows.
+// streamed set) norms padded with zeros to `npad` rows. With the norms folded into the contraction
+// (aug = 1: the rows, aug = 2: the columns) the two last feature columns carry them: a row becomes
+// [x, 0.., |x|^2, 1], a column [-2y, 0.., 1, |y|^2] (both parts split like every other element).
 __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int DP, float* __restrict__ hi,
-                             float* __restrict__ lo, float* __restrict__ norm, int64_t npad, int* __restrict__ lo_any) {
+                             float* __restrict__ lo, float* __restrict__ norm, int64_t npad, int* __restrict__ lo_any,
+                             int aug) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;  // one warp per row
     if (r >= npad) return;
+    const float mul = aug == 2 ? -2.f : 1.f;
+    const int last = aug ? DP - 2 : DP;  // feature columns written in the loop
     float s = 0.f;
     bool nz = false;
     for (int f = threadIdx.x; f < DP; f += 32) {
         const float e = (r < n && f < D) ? x[r * D + f] : 0.f;
-        const float h = tf32_hi(e);
-        if (r < n) {
-            const float l = tf32_lo(e, h);
+        if (r < n && f < last) {
+            const float h = tf32_hi(mul * e);
+            const float l = tf32_lo(mul * e, h);
             hi[r * DP + f] = h;
             lo[r * DP + f] = l;
             nz |= l != 0.f;
@@ -434,17 +462,28 @@ __global__ void tc_split_pad(const float* __restrict__ x, int64_t n, int D, int 
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (threadIdx.x == 0) norm[r] = s;
+    if (aug && r < n && threadIdx.x < 2) {
+        // column DP - 2 + t: the norm on one side, 1 on the other
+        const float e = (threadIdx.x == 0) == (aug == 1) ? s : 1.f;
+        const float h = tf32_hi(e);
+        const float l = tf32_lo(e, h);
+        hi[r * DP + DP - 2 + threadIdx.x] = h;
+        lo[r * DP + DP - 2 + threadIdx.x] = l;
+        nz |= l != 0.f;
+    }
     if (__any_sync(0xffffffffu, nz) && threadIdx.x == 0) atomicOr(lo_any, 1);
 }
 
 struct TopkTcPlan {
     int CT, G, DP, KB, H, U, chunk;
+    bool foldable;  // two spare feature columns: the distance metrics fold the norms into the contraction
     size_t off_xh, off_xl, off_yh, off_yl, off_xn, off_yn, off_pv, off_pi, off_flag, bytes;
 };
 
 inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     TopkTcPlan pl;
     pl.DP = D <= 32 ? 32 : 64;
+    pl.foldable = D + 2 <= pl.DP;
     pl.KB = topk_bucket(k);
     const int64_t RB = (N + kKBM - 1) / kKBM;
     pl.CT = (int)((M + kKBN - 1) / kKBN);
@@ -458,7 +497,7 @@ inline TopkTcPlan topk_tc_plan(int64_t N, int64_t M, int D, int k, bool same) {
     size_t o = 0;
     pl.off_xh = o; o += al256((size_t)N * pl.DP * 4);
     pl.off_xl = o; o += al256((size_t)N * pl.DP * 4);
-    if (same) {
+    if (same && !pl.foldable) {  // with folded norms the two sides differ even for the same points
         pl.off_yh = pl.off_xh;
         pl.off_yl = pl.off_xl;
     } else {
@@ -501,10 +540,11 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     int n = 0;
     int* lo_any = reinterpret_cast<int*>(ws + pl.off_flag);
     cudaMemsetAsync(lo_any, 0, sizeof(int), s);
+    const bool fold = pl.foldable && a.metric != kLinear;
     {
         HookScope h("tc_split_pad", s);
         tc_split_pad<<<(unsigned)((a.nP + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.P), a.nP, a.D,
-                                                                        pl.DP, xh, xl, xn, a.nP, lo_any);
+                                                                        pl.DP, xh, xl, xn, a.nP, lo_any, fold ? 1 : 0);
         ++n;
     }
     {
@@ -512,14 +552,14 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
         HookScope h("tc_split_pad", s);
         const int64_t npad = (int64_t)pl.CT * kKBN;
         tc_split_pad<<<(unsigned)((npad + 7) / 8), dim3(32, 8), 0, s>>>(static_cast<const float*>(a.Q), a.nQ, a.D,
-                                                                        pl.DP, yh, yl, yn, npad, lo_any);
+                                                                        pl.DP, yh, yl, yn, npad, lo_any, fold ? 2 : 0);
         ++n;
     }
     TopkTcParams p;
     p.N = a.nP;
     p.M = a.nQ;
     p.CT = pl.CT;
-    p.G = pl.G;
+    p.G = capped_grid(pl.G);  // units are dealt round-robin: any grid size covers them
     p.H = pl.H;
     p.U = pl.U;
     p.chunk = pl.chunk;
@@ -528,6 +568,7 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     p.metric = a.metric;
     p.apply_exp = a.apply_exp;
     p.largest = a.largest;
+    p.fold = fold ? 1 : 0;
     p.scale = (float)a.scale;
     p.neg_gamma_log2 = (float)(-a.gamma * 1.4426950408889634);
     p.xn = xn;
@@ -539,7 +580,7 @@ int launch_topk_tc(const SweepArgs& a, void* values, int64_t* indices, bool same
     auto go = [&](auto kernel, size_t smem) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         HookScope h("topk_tc", s);
-        kernel<<<pl.G, 32 * (2 + sel_warps(pl.DP, pl.KB)), smem, s>>>(mxh, mxl, myh, myl, p);
+        kernel<<<p.G, 32 * (2 + sel_warps(pl.DP, pl.KB)), smem, s>>>(mxh, mxl, myh, myl, p);
     };
     auto with_metric = [&](auto dp, auto kk) {
         constexpr int DP = decltype(dp)::value, KB = decltype(kk)::value;

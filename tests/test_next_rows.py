@@ -1,5 +1,10 @@
 """GPU parity of the column-direction reductions, boolean row/column masks, MMD statistics and the
-Sinkhorn divergence (compositions of the fused consumers) against the oracle and dense fp64 torch."""
+Sinkhorn divergence (compositions of the fused consumers) against the oracle. A reduction over dim -2 of
+S(X, Y) is the oracle's row reduction of the transposed problem S(Y, X) (every metric here is symmetric
+in its two points). A boolean keep mask is the oracle's same-group pair mask with kept rows and columns
+in group 0 and dropped ones in groups of their own, so the pair is removed from the consumer: the
+library's lowering (a -inf bias for log-sum-exp, softmax and top-k, a zero weight for sums) is checked
+against removal, not against itself. The MMD gradient alone is held against dense fp64 autograd."""
 import numpy as np
 import pytest
 import torch
@@ -20,62 +25,63 @@ def _pts(seed, n, d, dtype=torch.float32, integers=False):
     return torch.randn(n, d, generator=g, dtype=dtype)
 
 
-def _dense(X, Y, metric, gamma=1.0):
-    X, Y = X.double(), Y.double()
-    d2 = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
-    return {"sqeuclidean": d2, "linear": X @ Y.T, "rbf": torch.exp(-gamma * d2)}[metric]
-
-
 @pytest.mark.parametrize("N,M", [(300, 700), (129, 33)])
-def test_chamfer_min_both_directions_exact(N, M):
+def test_chamfer_min_both_directions_exact(oracle, N, M):
     X, Y = _pts(1, N, 16, integers=True), _pts(2, M, 16, integers=True)
     D = tp.lazy(X.to(DEV), Y.to(DEV), "sqeuclidean")
     v2, i2 = D.min(-2)
     rv, ri = OL.column_min(X.numpy(), Y.numpy())
     assert np.array_equal(v2.cpu().double().numpy(), rv) and np.array_equal(i2.cpu().numpy(), ri)
     v1, i1 = D.min(-1)
-    dv, di = _dense(X, Y, "sqeuclidean").min(1)
-    assert torch.equal(v1.cpu().double(), dv) and torch.equal(i1.cpu(), di)
+    ov, oi = oracle.topk(oracle.Problem(X, Y, metric="sqeuclidean"), 1)
+    assert np.array_equal(v1.cpu().double().numpy(), ov[:, 0]) and np.array_equal(i1.cpu().numpy(), oi[:, 0])
 
 
-def test_topk_over_columns_matches_stable_sort():
+def test_topk_over_columns_matches_oracle(oracle):
     X, Y = _pts(3, 90, 8, integers=True), _pts(4, 200, 8, integers=True)
     v, i = tp.lazy(X.to(DEV), Y.to(DEV), "sqeuclidean").topk(5, dim=-2, largest=False)
-    D = _dense(X, Y, "sqeuclidean")
-    sv, si = torch.sort(D, dim=0, stable=True)
-    assert torch.equal(v.cpu().double(), sv[:5]) and torch.equal(i.cpu(), si[:5])
+    ov, oi = oracle.topk(oracle.Problem(Y, X, metric="sqeuclidean"), 5)  # the transposed problem, rows = y
+    assert np.array_equal(v.cpu().double().numpy(), ov.T) and np.array_equal(i.cpu().numpy(), oi.T)
 
 
 @pytest.mark.parametrize("dtype,tol", [(torch.float32, TOL_F32_FWD), (torch.float64, TOL_F64)])
-def test_logsumexp_sum_mean_over_columns(dtype, tol):
+def test_logsumexp_sum_mean_over_columns(oracle, dtype, tol):
     X, Y = _pts(5, 150, 6, dtype), _pts(6, 260, 6, dtype)
     L = tp.lazy(X.to(DEV), Y.to(DEV), "rbf", gamma=0.4) * 2.0
-    S = 2.0 * _dense(X, Y, "rbf", 0.4)
-    assert_close(L.logsumexp(dim=-2), torch.logsumexp(S, 0), tol, "lse dim -2")
-    assert_close(L.sum(-2), S.sum(0), tol, "sum dim -2")
-    assert_close(L.mean(-1), S.mean(1), tol, "mean dim -1")
-    assert_close(L.mean(-2), S.mean(0), tol, "mean dim -2")
+    rows = oracle.Problem(X, Y, metric="rbf", gamma=0.4, scale=2.0)
+    cols = oracle.Problem(Y, X, metric="rbf", gamma=0.4, scale=2.0)
+    assert_close(L.logsumexp(dim=-2), oracle.logsumexp(cols), tol, "lse dim -2")
+    assert_close(L.sum(-2), oracle.matmul(cols, np.ones((260, 1)))[:, 0], tol, "sum dim -2")
+    assert_close(L.mean(-1), oracle.matmul(rows, np.ones((260, 1)))[:, 0] / 260, tol, "mean dim -1")
+    assert_close(L.mean(-2), oracle.matmul(cols, np.ones((150, 1)))[:, 0] / 150, tol, "mean dim -2")
 
 
-def test_column_mask_on_every_row_consumer():
+def _keep_groups(keep):
+    """Group ids under which the oracle's same-group mask keeps exactly the pairs of kept points."""
+    return np.where(np.asarray(keep), 0, -1).astype(np.int32)
+
+
+def test_column_mask_on_every_row_consumer(oracle):
     X, Y, V = _pts(7, 120, 5), _pts(8, 300, 5), _pts(9, 300, 4)
     keep = torch.rand(300, generator=torch.Generator().manual_seed(10)) > 0.3
     L = tp.lazy(X.to(DEV), Y.to(DEV), "linear") * 0.5
     Lm = L.mask_columns(keep.to(DEV))
-    S = 0.5 * _dense(X, Y, "linear")
-    Sm = S.masked_fill(~keep[None, :], float("-inf"))
-    assert_close(Lm.logsumexp(-1), torch.logsumexp(Sm, 1), TOL_F32_FWD, "masked lse")
-    assert_close(Lm.softmax_matmul(V.to(DEV)), torch.softmax(Sm, 1) @ V.double(), TOL_F32_FWD, "masked softmax")
-    assert_close(Lm.matmul(V.to(DEV)), (S * keep[None, :]) @ V.double(), TOL_F32_FWD, "masked K@V")
-    assert_close(Lm.mean(-1), (S * keep[None, :]).sum(1) / keep.sum(), TOL_F32_FWD, "masked mean")
+    pm = oracle.Problem(X, Y, metric="linear", scale=0.5, pair_mask="same_group",
+                        row_group=np.zeros(120, np.int32), col_group=_keep_groups(keep))
+    assert_close(Lm.logsumexp(-1), oracle.logsumexp(pm), TOL_F32_FWD, "masked lse")
+    assert_close(Lm.softmax_matmul(V.to(DEV)), oracle.softmax_matmul(pm, V)[0], TOL_F32_FWD, "masked softmax")
+    assert_close(Lm.matmul(V.to(DEV)), oracle.matmul(pm, V), TOL_F32_FWD, "masked K@V")
+    assert_close(Lm.mean(-1), oracle.matmul(pm, np.ones((300, 1)))[:, 0] / int(keep.sum()), TOL_F32_FWD,
+                 "masked mean")
     v, i = Lm.topk(3, largest=True)
-    sv, si = torch.sort(Sm, dim=1, descending=True, stable=True)
-    assert_close(v, sv[:, :3], TOL_F32_FWD, "masked topk values")
+    ov, oi = oracle.topk(pm, 3, largest=True)
+    assert_close(v, ov, TOL_F32_FWD, "masked topk values")
     assert bool(keep[i.cpu()].all())
-    # a row mask affects the reductions over columns
+    # a row mask affects the reductions over columns: the transposed problem with the mask on its columns
     rkeep = torch.rand(120, generator=torch.Generator().manual_seed(11)) > 0.5
-    Sr = S.masked_fill(~rkeep[:, None], float("-inf"))
-    assert_close(L.mask_rows(rkeep.to(DEV)).logsumexp(dim=-2), torch.logsumexp(Sr, 0), TOL_F32_FWD, "row-masked lse")
+    pr = oracle.Problem(Y, X, metric="linear", scale=0.5, pair_mask="same_group",
+                        row_group=np.zeros(300, np.int32), col_group=_keep_groups(rkeep))
+    assert_close(L.mask_rows(rkeep.to(DEV)).logsumexp(dim=-2), oracle.logsumexp(pr), TOL_F32_FWD, "row-masked lse")
 
 
 def test_column_mask_gradient_is_zero_on_masked_columns():
@@ -142,11 +148,11 @@ def test_sinkhorn_gradient_is_the_plan():
     assert_close(X.grad, torch.from_numpy(ref), 1e-8, "sinkhorn grad")
 
 
-def test_minus_inf_column_bias_over_leading_columns():
+def test_minus_inf_column_bias_over_leading_columns(oracle):
     # a run of -inf scores at the start of a row's stream adds nothing (it once produced NaN)
     X, Y = _pts(40, 70, 5), _pts(41, 130, 5)
     b = torch.zeros(130)
     b[:45] = float("-inf")
     got = tp.lazy(X.to(DEV), Y.to(DEV), "linear").add_columns(b.to(DEV)).logsumexp(-1)
-    want = torch.logsumexp(_dense(X, Y, "linear") + b.double()[None, :], 1)
+    want = oracle.logsumexp(oracle.Problem(X, Y, metric="linear", col_bias=b))
     assert_close(got, want, TOL_F32_FWD, "lse with -inf column bias")

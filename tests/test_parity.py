@@ -214,6 +214,36 @@ def test_topk_integer_exact(oracle, NMD, k, largest, metric, dt):
     np.testing.assert_array_equal(v.cpu().double().numpy(), ov)
 
 
+@pytest.mark.parametrize("metric", ["sqeuclidean", "rbf", "linear"])
+@pytest.mark.parametrize("D", [2, 30, 31, 32, 33, 62, 63, 64])
+def test_topk_tc_feature_widths_exact(oracle, D, metric):
+    """The tensor-core top-k at every feature-width boundary: the distance metrics fold the norms into
+    the contraction where two spare feature columns exist (D <= 30, and 33 <= D <= 62) and add them per
+    element otherwise. Integer points: the distances are exact, so the selection (indices, and for the
+    distances the values) equals the oracle's; rbf values are fp32 exps of exact distances."""
+    X = int_points(60 + D, (300, D), -4, 4)
+    Y = int_points(61 + D, (1100, D), -4, 4)
+    v, i = ops.pairwise_topk(X.to(DEV), Y.to(DEV), Score(metric, gamma=0.02), 16, metric == "linear")
+    ov, oi = oracle.topk(oracle.Problem(X, Y, metric=metric, gamma=0.02), 16, metric == "linear")
+    np.testing.assert_array_equal(i.cpu().numpy(), oi)
+    if metric == "rbf":
+        assert_close(v, ov, TOL_F32_FWD, "rbf topk values")
+    else:
+        np.testing.assert_array_equal(v.cpu().double().numpy(), ov)
+
+
+@pytest.mark.parametrize("D", [16, 32, 48])
+def test_topk_tc_same_points_exact(oracle, D):
+    """X and Y the same tensor (self k-NN, every row's own point at distance 0 comes first among its
+    ties): with folded norms the two operand sides differ, so they are split separately."""
+    X = int_points(70 + D, (700, D), -3, 3).to(DEV)
+    v, i = ops.pairwise_topk(X, X, Score("sqeuclidean"), 8, False)
+    Xc = X.cpu()
+    ov, oi = oracle.topk(oracle.Problem(Xc, Xc, metric="sqeuclidean"), 8, False)
+    np.testing.assert_array_equal(i.cpu().numpy(), oi)
+    np.testing.assert_array_equal(v.cpu().double().numpy(), ov)
+
+
 @pytest.mark.parametrize("affine", [False, True])
 @pytest.mark.parametrize("metric", ["sqeuclidean", "linear", "rbf"])
 def test_topk_float(oracle, metric, affine):
