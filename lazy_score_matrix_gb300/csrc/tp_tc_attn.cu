@@ -182,6 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t n = t_end - t_begin;
 
     if (threadIdx.x == 0) {
+        prefetch_map(&mA1h);
+        prefetch_map(&mA1l);
+        prefetch_map(&mA2h);
+        prefetch_map(&mA2l);
+        prefetch_map(&mB1h);
+        prefetch_map(&mB1l);
+        prefetch_map(&mB2h);
+        prefetch_map(&mB2l);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int s = 0; s < kStages; ++s) {

@@ -180,6 +180,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
 
     if (threadIdx.x == 0) {
+        prefetch_map(&mXh);
+        prefetch_map(&mXl);
+        prefetch_map(&mYh);
+        prefetch_map(&mYl);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int s = 0; s < kStagesF; ++s) {
@@ -540,6 +544,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t n = t_end - t_begin;
 
     if (threadIdx.x == 0) {
+        prefetch_map(&mAh);
+        prefetch_map(&mAl);
+        prefetch_map(&mBh);
+        prefetch_map(&mBl);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int s = 0; s < kStagesS; ++s) {
@@ -893,6 +901,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t n = t_end - t_begin;
 
     if (threadIdx.x == 0) {
+        prefetch_map(&mAh);
+        prefetch_map(&mAl);
+        prefetch_map(&mBh);
+        prefetch_map(&mBl);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int s = 0; s < kStagesS; ++s) {

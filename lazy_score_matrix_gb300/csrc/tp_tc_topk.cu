@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        prefetch_map(&mXh);
+        prefetch_map(&mXl);
+        prefetch_map(&mYh);
+        prefetch_map(&mYl);
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int s = 0; s < SH::kStages; ++s) {
