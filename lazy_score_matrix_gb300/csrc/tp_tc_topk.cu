@@ -7,10 +7,11 @@
 // so their dot products, norms and distances are exact and the selection is bit-identical to an exact
 // evaluation. For the distance metrics, where two spare feature columns exist (D <= DP - 2), the norms
 // ride in the contraction: rows [x, |x|^2, 1] against columns [-2y, 1, |y|^2] give the unclamped squared
-// distance |x|^2 + |y|^2 - 2 x.y straight out of the accumulator, with no per-element norm loads. The 128 x 128 score tile lands in TMEM; the selection warps (sixteen for D <= 32, four
-// per TMEM lane quarter owning 32 of the tile's columns each; eight for D <= 64, two per quarter
-// owning 64 columns) turn each dot product into the score and keep a sorted
-// (value, index) list per row in registers, inserting only on a strict improvement, so equal values
+// distance |x|^2 + |y|^2 - 2 x.y straight out of the accumulator, with no per-element norm loads. The
+// 128 x 128 score tile lands in TMEM; eight selection warps, two per TMEM lane quarter, each take 64 of
+// its columns into registers (which frees the accumulator for the next tile), turn each value into the
+// score and keep a sorted (value, index) list per row in registers, inserting only on a strict
+// improvement, so equal values
 // keep ascending index order. The lists of the column parts and of every unit (column chunk) of a row
 // block are merged lexicographically on (value, index) by a second kernel: the result is unique.
 //
@@ -32,9 +33,10 @@ constexpr int kKBM = 128, kKBN = 128;
 constexpr int kKLists = 4;   // sorted lists per row and unit in the partials (the most selection parts)
 constexpr int kKGrid = 152;
 
-// selection warps: 16 (four per TMEM lane quarter, 32 columns each) where shared memory and registers
-// allow it (D <= 32, k <= 16), else 8 (two per quarter, 64 columns each)
-__host__ __device__ constexpr int sel_warps(int DP, int K) { return DP == 32 && K <= 16 ? 16 : 8; }
+// selection warps: eight, two per TMEM lane quarter, each owning 64 of a tile's 128 columns. (Sixteen
+// warps of 32 columns, four per quarter, measured 21% slower on the k-NN workload: 18 warps leave a thread
+// 96 registers and the lists spilled; 10 warps leave 128.)
+__host__ __device__ constexpr int sel_warps(int DP, int K) { return 8; }
 
 template <int DP, int SEL>
 struct TopkTcShape {
@@ -47,12 +49,8 @@ struct TopkTcShape {
     static constexpr int kCols = kKBN / kParts;
     static constexpr int kThreads = 32 * (2 + kSel);
     static constexpr size_t kKeyBuf = (size_t)kSel * 32 * 32 * 4;  // per selection warp: 32 columns x 32 lanes
-    // thresholds shared by the column parts of a row ([part][row], each tagged with its unit), where there
-    // is room (the four-part layout); the two-part layout (D > 32) fills shared memory without them
-    static constexpr bool kShare = kParts == 4;
-    static constexpr size_t kThrBuf = kShare ? (size_t)kParts * kKBM * 8 : 0;
-    static constexpr size_t kSmem =
-        (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + kThrBuf + 256 + 1024;
+    static constexpr size_t kSmem = (size_t)kPair * (1 + kStages) + (size_t)kStages * kKBN * 4 + kKeyBuf + 256 + 1024;
+    static_assert(kCols == 64, "two 32-column blocks per selection warp");
     static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 };
 
@@ -115,14 +113,6 @@ struct UnitCursor {
     }
 };
 
-// The smallest float above x (x itself for +inf and NaN): key <= x exactly when key < next_up(x).
-__device__ __forceinline__ float next_up(float x) {
-    if (!(x < pinf<float>())) return x;
-    if (x == 0.f) return __uint_as_float(1u);
-    const uint32_t u = __float_as_uint(x);
-    return __uint_as_float(x > 0.f ? u + 1u : u - 1u);
-}
-
 // The score of one accumulator value: a dot product, or with folded norms the unclamped squared distance.
 template <int METRIC, bool EXP>
 __device__ __forceinline__ float topk_score(float acc, bool fold, float xn, float yn, float scale, float ngl2) {
@@ -149,8 +139,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     unsigned char* sB = sm + SH::kPair;
     float* sYn = reinterpret_cast<float*>(sB + (size_t)SH::kPair * SH::kStages);  // [stage][128]
     float* sKeys = sYn + SH::kStages * kKBN;                                         // [warp][32 u][32 lanes]
-    uint64_t* sThr = reinterpret_cast<uint64_t*>(sKeys + SH::kKeyBuf / 4);         // [kParts][128]
-    uint64_t* bars = sThr + SH::kThrBuf / 8;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKeys + SH::kKeyBuf / 4);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
     uint64_t* b_full = bars + 2;               // [kStages]
@@ -170,17 +159,15 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
         mbar_init(a_empty, 1);
         for (int s = 0; s < SH::kStages; ++s) {
             mbar_init(b_full + s, 1);
-            // freed by the MMA (operands consumed) and by the 256 selection threads (norms consumed)
-            mbar_init(b_empty + s, 1 + 32 * SH::kSel);
+            // freed by the MMA (operands consumed) and, where the selection reads the stage's column norms
+            // (norms not folded into the contraction), by the selection warps, one arrival each
+            mbar_init(b_empty + s, p.fold ? 1 : 1 + SH::kSel);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, 32 * SH::kSel);
+            mbar_init(acc_empty + b, SH::kSel);
         }
         mbar_fence_init();
-    }
-    if constexpr (SH::kShare) {  // no shared threshold yet: tag 0 (units are counted from 1), value +inf
-        for (int e = threadIdx.x; e < SH::kParts * kKBM; e += blockDim.x) sThr[e] = 0x7f800000ull;
     }
     if (warp == 1) tmem_alloc(tslot, 256);
     fence_before_sync();
@@ -213,12 +200,12 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 82);
                 if (!ok) break;
                 unsigned char* dst = sB + (size_t)s * SH::kPair;
-                mbar_expect_tx(b_full + s, bytes + kKBN * 4);
+                mbar_expect_tx(b_full + s, bytes + (p.fold ? 0 : kKBN * 4));
                 for (int c = 0; c < SH::kChunks; ++c) {
                     tma_load_2d(dst + c * kChunk, &mYh, c * 32, ct * kKBN, b_full + s);
                     if (lo) tma_load_2d(dst + SH::kOperand + c * kChunk, &mYl, c * 32, ct * kKBN, b_full + s);
                 }
-                bulk_load(sYn + s * kKBN, p.yn + (size_t)ct * kKBN, kKBN * 4, b_full + s);
+                if (!p.fold) bulk_load(sYn + s * kKBN, p.yn + (size_t)ct * kKBN, kKBN * 4, b_full + s);
             }
         }
     } else if (warp == 1) {
@@ -279,8 +266,6 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
         int ki[K];
         float xn = 0.f;
         bool ok = true;
-        uint32_t units = 0;  // units begun by this CTA: the tag of this unit's shared thresholds
-        volatile uint64_t* thr_row = sThr + lr;
         auto reset = [&]() {
 #pragma unroll
             for (int t = 0; t < K; ++t) {
@@ -304,41 +289,30 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 reset();
                 const int64_t row = (int64_t)rb * kKBM + lr;
                 xn = (METRIC != kLinear && !p.fold && row < p.N) ? p.xn[row] : 0.f;
-                ++units;
                 fresh = false;
             }
             const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
-            ok = mbar_wait(acc_full + b, rr & 1, p.err, 86);
+            ok = mbar_wait_warp(acc_full + b, rr & 1, p.err, 86);
             if (!ok) break;
             fence_after_sync();
-            // The smallest k-th key over this row's column parts in this unit: each part's list holds k keys
-            // at or below its k-th, so a key above that minimum can never be among the row's final k (keys
-            // equal to it still go to the part's own strict test, which keeps the exact tie order). Each
-            // entry carries the unit it was written in (one 64-bit store); entries of another unit (other
-            // rows: a part may enter a unit before the others leave the previous one) are ignored, and older
-            // entries of this unit are larger, hence safe.
-            float shared = pinf<float>();
-            if constexpr (SH::kShare) {
-#pragma unroll
-                for (int pp = 0; pp < SH::kParts; ++pp) {
-                    const uint64_t e = thr_row[pp * kKBM];
-                    if ((uint32_t)(e >> 32) == units) shared = fminf(shared, __uint_as_float((uint32_t)e));
-                }
-            }
+            // both 32-column blocks of this part into registers, then the accumulator goes back to the MMA
+            float v[32], vn[32];
+            tmem_ld32x2(lane_base + (uint32_t)(b * kKBN), lane_base + (uint32_t)(b * kKBN + 32), v, vn);
+            fence_before_sync();
+            mbar_arrive_warp(acc_empty + b);
             const int j0 = ct * kKBN + half * SH::kCols;
             const int lim = (int)(p.M - j0 < SH::kCols ? p.M - j0 : SH::kCols);  // valid columns of this part
             const float* yn = sYn + s * kKBN + half * SH::kCols;
             float* wkeys = sKeys + (warp - 2) * 32 * 32;
-            bool inserted = false;
 #pragma unroll 1
             for (int c = 0; c < SH::kCols / 32; ++c) {
-                float v[32];
-                tmem_ld32(lane_base + (uint32_t)(b * kKBN + c * 32), v);
-                // the columns whose key beats both this row's own k-th key and the parts' shared bound (the
-                // thresholds only fall, so every column the insertion would take is in the mask): key < thr and
-                // key <= shared, one comparison against the smaller of thr and the float above shared
+                if (c == 1) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) v[u] = vn[u];
+                }
+                // the columns whose key beats this row's k-th key (the threshold only falls, so every column
+                // the insertion would take is in the mask)
                 const float thr = kv[K - 1];
-                const float bnd = fminf(thr, next_up(shared));
                 const int left = lim - c * 32;  // valid columns of these 32
                 const uint32_t valid = left >= 32 ? 0xffffffffu : (left > 0 ? (1u << left) - 1u : 0u);
                 uint32_t cand = 0;
@@ -354,17 +328,19 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                         }
                     }
                     const float kmin = p.scale * fmaxf(min32(v), 0.f);
-                    if (!__any_sync(0xffffffffu, kmin < bnd)) continue;
+                    if (!__any_sync(0xffffffffu, kmin < thr)) continue;
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const float key = p.scale * fmaxf(v[u], 0.f);
                         v[u] = key;
-                        cand |= key < bnd ? (1u << u) : 0u;
+                        cand |= key < thr ? (1u << u) : 0u;
                     }
                 } else {
 #pragma unroll
                     for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 y4 = reinterpret_cast<const float4*>(yn + c * 32)[u4];
+                        // with folded norms the stage holds no norms (and may already hold a later tile)
+                        const float4 y4 = p.fold ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                 : reinterpret_cast<const float4*>(yn + c * 32)[u4];
                         const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
@@ -372,7 +348,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                             const float key =
                                 sgn * topk_score<METRIC, EXP>(v[u], p.fold != 0, xn, yv[w], p.scale, p.neg_gamma_log2);
                             v[u] = key;
-                            cand |= key < bnd ? (1u << u) : 0u;
+                            cand |= key < thr ? (1u << u) : 0u;
                         }
                     }
                 }
@@ -382,7 +358,6 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
 #pragma unroll
                     for (int u = 0; u < 32; ++u) wkeys[u * 32 + lane] = v[u];
                     __syncwarp();
-                    inserted |= cand != 0u;
                     while (cand) {
                         const int u = __ffs(cand) - 1;
                         cand &= cand - 1u;
@@ -391,12 +366,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                     __syncwarp();
                 }
             }
-            if constexpr (SH::kShare) {
-                if (inserted) thr_row[half * kKBM] = ((uint64_t)units << 32) | __float_as_uint(kv[K - 1]);
-            }
-            fence_before_sync();
-            mbar_arrive(acc_empty + b);
-            mbar_arrive(b_empty + s);
+            if (!p.fold) mbar_arrive_warp(b_empty + s);
             const int u_done = cur.u;
             if (cur.next(p)) {  // the unit is complete: its lists are final
                 flush(u_done);
