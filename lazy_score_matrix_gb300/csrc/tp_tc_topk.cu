@@ -32,6 +32,7 @@ namespace tc {
 constexpr int kKBM = 128, kKBN = 128;
 constexpr int kKLists = 4;   // sorted lists per row and unit in the partials (the most selection parts)
 constexpr int kKGrid = 152;
+constexpr int kAcc = 4;      // accumulators of 128 TMEM columns: the MMA may run three tiles ahead
 
 // selection warps: eight, two per TMEM lane quarter, each owning 64 of a tile's 128 columns. (Sixteen
 // warps of 32 columns, four per quarter, measured 21% slower on the k-NN workload: 18 warps leave a thread
@@ -144,9 +145,9 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     uint64_t* a_empty = bars + 1;
     uint64_t* b_full = bars + 2;               // [kStages]
     uint64_t* b_empty = bars + 2 + SH::kStages;
-    uint64_t* acc_full = bars + 2 + 2 * SH::kStages;   // [2]
-    uint64_t* acc_empty = acc_full + 2;                // [2]
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* acc_full = bars + 2 + 2 * SH::kStages;   // [kAcc]
+    uint64_t* acc_empty = acc_full + kAcc;             // [kAcc]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + kAcc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -163,13 +164,13 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
             // (norms not folded into the contraction), by the selection warps, one arrival each
             mbar_init(b_empty + s, p.fold ? 1 : 1 + SH::kSel);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAcc; ++b) {
             mbar_init(acc_full + b, 1);
             mbar_init(acc_empty + b, SH::kSel);
         }
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, 256);
+    if (warp == 1) tmem_alloc(tslot, 128 * kAcc);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                     ++a_uses;
                     rb_cur = rb;
                 }
-                const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages), b = (int)(i & 1), rr = (int)(i >> 1);
+                const int s = (int)(i % SH::kStages), r = (int)(i / SH::kStages), b = (int)(i % kAcc), rr = (int)(i / kAcc);
                 ok = mbar_wait(b_full + s, r & 1, p.err, 84);
                 if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 85);
                 if (!ok) break;
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
                 xn = (METRIC != kLinear && !p.fold && row < p.N) ? p.xn[row] : 0.f;
                 fresh = false;
             }
-            const int b = (int)(i & 1), rr = (int)(i >> 1), s = (int)(i % SH::kStages);
+            const int b = (int)(i % kAcc), rr = (int)(i / kAcc), s = (int)(i % SH::kStages);
             ok = mbar_wait_warp(acc_full + b, rr & 1, p.err, 86);
             if (!ok) break;
             fence_after_sync();
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
 
     fence_before_sync();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 128 * kAcc);
 }
 
 // Per row: the lists of every (unit, part) of its row block, merged on (key, index).
