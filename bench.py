@@ -46,7 +46,7 @@ FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
 FALLBACK_SMS = 152       # GB300, used only when no device can be queried
 
 # ------------------------------------------------------------------------------------------------
-# peaks: the driver's measured copy / bf16 GEMM figures, the device's SM count, and our own measured
+# peaks: the measured copy / bf16 GEMM figures of MEASURED_PEAKS.json, the device's SM count, and our own measured
 # fp32 / fp64 FMA and exp2 rates (libtp_peaks)
 # ------------------------------------------------------------------------------------------------
 

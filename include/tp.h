@@ -36,7 +36,7 @@
  *       TP_ERR_INVALID_ARG  NULL required pointer, size out of range, bad metric/dtype/k, exclude_self
  *                           with N != M, output aliasing an input or another output (except the
  *                           documented dX/dY alias), misaligned pointer, workspace too small.
- *       TP_ERR_UNSUPPORTED  a valid request this build has no kernel for.
+ *       TP_ERR_UNSUPPORTED  a valid request the library has no kernel for.
  *       TP_ERR_CUDA         a CUDA launch error (the runtime's error text is in tp_last_error()), or a
  *                           fault injected before launch (TP_FAULT_INJECT, see tp_device_status).
  *     Device-side conditions are not known when a call returns: the warps of the tensor-core kernels

@@ -588,7 +588,7 @@ const char* tp_status_string(tp_status s) {
     switch (s) {
         case TP_OK: return "TP_OK";
         case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG: invalid argument";
-        case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: not supported by this build";
+        case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: not supported by the library";
         case TP_ERR_CUDA: return "TP_ERR_CUDA: CUDA error";
         case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE: workspace error";
         case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT: device wait timed out";
@@ -812,7 +812,7 @@ tp_status tp_pairwise_topk(const tp_pairs* pr, const tp_score* sc, int k, int la
     TP_CHECK(check_pairs(pr));
     TP_CHECK(check_score(sc, pr));
     if (k < 1 || k > pr->M || k > 128) return fail(TP_ERR_INVALID_ARG, "k must be in [1, min(M, 128)]");
-    if (k > kTopkMax) return fail(TP_ERR_UNSUPPORTED, "k above 32 is not compiled in this build");
+    if (k > kTopkMax) return fail(TP_ERR_UNSUPPORTED, "k above 32 is not compiled into the library");
     const size_t es = esize(pr->dtype);
     TP_CHECK(check_ptr(values, "values", es));
     TP_CHECK(check_ptr(indices, "indices", 8));
