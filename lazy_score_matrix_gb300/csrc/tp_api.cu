@@ -736,10 +736,9 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
     a.ws = ws;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (attn_tc_eligible(pr, sc, C, {V, out, lse})) {
-        // the row log-sum-exp first, then P V with P = exp(S - lse): no running rescale of the output
+        // one sweep with an online softmax writes out and lse
         const bool same = same_points(pr);
-        const int n1 = launch_lse_tc(a, lse, same, st);
-        if (n1 < 0) return tc_launched(n1);
+        const int n1 = 0;
         AttnTcArgs t{};
         t.Q = static_cast<const float*>(pr->X);
         t.K = static_cast<const float*>(pr->Y);
@@ -747,7 +746,7 @@ tp_status tp_pairwise_softmax_matmul(const tp_pairs* pr, const tp_score* sc, con
         t.N = pr->N;
         t.M = pr->M;
         t.scale = sc->scale;
-        t.lse = static_cast<const float*>(lse);
+        t.lse_out = static_cast<float*>(lse);
         t.out = static_cast<float*>(out);
         t.pm = (int)sc->pair_mask;
         t.band = pair_band(sc, pr);

@@ -51,9 +51,10 @@ struct AttnTcArgs {
     const float *Q, *K, *V;
     int64_t N, M;
     double scale;
-    const float* lse;
+    const float* lse;        // backward: the forward's row log-sum-exp [N]
     const float *O, *dO;     // backward: the forward output and its upstream gradient [N, 64]
     float* out;              // forward output [N, 64]
+    float* lse_out;          // forward output: the row log-sum-exp [N]
     float *dQ, *dK, *dV;     // backward outputs (null: not wanted)
     int accumulate_dK;       // add dK into its buffer (dQ and dK of the same points summed in one buffer)
     int pm;                  // pair mask: 0 none, 1 causal (j <= i), 2 band (|i - j| <= band)

@@ -9,9 +9,11 @@
 // per-row power of two gives within a row, and the unscale factors of S and dP become constants. A dot
 // product is (xh.yh + (xh.yl + xl.yh)) 2^-(e_x + e_y), with hi*hi in TMEM columns of its own.
 //
-// Forward: the row log-sum-exp first (lse_fwd_tc), then one sweep that forms P_ij = exp(S_ij - lse_i)
-// tile by tile and accumulates P V on the tensor core. With lse known, the output needs no running
-// rescale. Backward, with dO = d loss / d out, delta_i = dO_i . out_i, dP_ij = dO_i . V_j and
+// Forward: one sweep with an online softmax. The four warps that share a row agree on its running
+// maximum m (base 2) through shared memory each tile and raise it only when a tile's maximum exceeds it by
+// more than 2^8 (otherwise the stale m stands), so that kappa = 2^(s2 - m + 6) <= 2^14 stays in fp16's
+// range; the row's output and sum are rescaled by 2^(m_old - m_new) on the rare raise. The log-sum-exp
+// comes out of the same sweep. Backward, with dO = d loss / d out, delta_i = dO_i . out_i, dP_ij = dO_i . V_j and
 // dS_ij = P_ij (dP_ij - delta_i):
 //   row sweep     dQ_i = scale sum_j dS_ij K_j
 //   column sweep  dK_j = scale sum_i dS_ij Q_i,   dV_j = sum_i P_ij dO_i
@@ -52,7 +54,10 @@ constexpr int kParts = kEpi / 4;              // warps per lane quarter, each ow
 constexpr int kCols = kBN / kParts;           // 16: one K step of the output MMA
 constexpr int kThreads = 32 * (2 + kEpi);
 constexpr int kGrid = 152;                    // persistent CTAs: one per GB300 SM
-constexpr size_t kSmem = (size_t)kABytes + (size_t)kStage * kStages + (size_t)kStages * kBN * 16 + 512 + 1024;
+constexpr size_t kXm = 2 * 4 * kBM * 4;       // forward: the four parts' tile maxima per row, two tile parities
+constexpr size_t kSmem = (size_t)kABytes + (size_t)kStage * kStages + (size_t)kStages * kBN * 16 + kXm + 512 + 1024;
+constexpr float kKapShift = 6.f;              // forward kappa = 2^(s2 - m + 6): at most 2^14 with the lazy maximum
+constexpr float kLazy = 8.f;                  // the running maximum is raised when a tile's exceeds it by more
 static_assert(kSmem <= 232448, "dynamic shared memory per CTA");
 static_assert(kCols == 16, "one output K step per epilogue warp");
 constexpr float kL2E = 1.4426950408889634f;
@@ -76,6 +81,8 @@ struct Shape {
     static constexpr int kBuf = kDP ? 1 : 2;                        // S (+ dP) buffers
     static constexpr bool kColStats = MODE == kColSweep;            // the stage carries per-column stats
     static constexpr int kF = 64 * kOuts;                           // features of one partial row
+    // rows of one partial: the features, and for the forward the row maximum and the four parts' sums
+    static constexpr int kPartRows = MODE == kFwd ? kF + 1 + kParts : kF;
     // One output: kappa_hi [B_hi | B_lo] (N 128, hi*hi and hi*lo in 128 accumulator columns) and
     // kappa_lo B_hi (N 64) into the hi*lo half. Two outputs (column sweep): TMEM holds one 64-column
     // accumulator each, fed by three N 64 MMAs.
@@ -108,6 +115,7 @@ struct Params {
     float* out0;           // [R][64] (null: not wanted)
     float* out1;
     int acc0;              // add output 0 into out0 instead of writing it
+    float* lse;            // forward: the row log-sum-exp [R]
     int* err;
 };
 
@@ -130,12 +138,39 @@ __device__ __noinline__ void merge_row(const Params& p, int rb, int lr, int fg) 
     float acc[FG];
 #pragma unroll
     for (int f = 0; f < FG; ++f) acc[f] = 0.f;
+    float4* d4 = reinterpret_cast<float4*>(dst + row * 64 + (fb & 63));
+    if constexpr (MODE == kFwd) {
+        // each CTA's part in its own frame: maximum m_c, sum l_c (four parts), output sums; in CTA order
+        float M = ninf<float>();
+        for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, __ldcg(p.part + ((size_t)(v + c) * SH::kPartRows + SH::kF) * kBM + lr));
+        float L = 0.f;
+        if (M != ninf<float>()) {
+            for (int c = c_lo; c <= c_hi; ++c) {
+                const float* o = p.part + (size_t)(v + c) * SH::kPartRows * kBM + lr;
+                const float mc = __ldcg(o + (size_t)SH::kF * kBM);
+                if (mc == ninf<float>()) continue;
+                const float w = ExpTraits<float>::bexp(mc - M);
+                float lc = 0.f;
+#pragma unroll
+                for (int h = 0; h < kParts; ++h) lc += __ldcg(o + (size_t)(SH::kF + 1 + h) * kBM);
+                L = fmaf(w, lc, L);
+#pragma unroll
+                for (int f = 0; f < FG; ++f) acc[f] = fmaf(w, __ldcg(o + (size_t)(fb + f) * kBM), acc[f]);
+            }
+        }
+        const float invL = L > 0.f ? 1.f / L : 0.f;  // a row with every pair masked returns 0
+#pragma unroll
+        for (int f4 = 0; f4 < FG / 4; ++f4)
+            d4[f4] = make_float4(acc[4 * f4] * invL, acc[4 * f4 + 1] * invL, acc[4 * f4 + 2] * invL, acc[4 * f4 + 3] * invL);
+        // kappa carries 2^(6 - m): sum_j 2^(s2_j) = L 2^(M - 6)
+        if (fg == 0 && p.lse) p.lse[row] = L > 0.f ? ExpTraits<float>::lse(M - kKapShift, L) : ninf<float>();
+        return;
+    }
     for (int c = c_lo; c <= c_hi; ++c) {
-        const float* o = p.part + (size_t)(v + c) * SH::kF * kBM + lr;
+        const float* o = p.part + (size_t)(v + c) * SH::kPartRows * kBM + lr;
 #pragma unroll
         for (int f = 0; f < FG; ++f) acc[f] += __ldcg(o + (size_t)(fb + f) * kBM);
     }
-    float4* d4 = reinterpret_cast<float4*>(dst + row * 64 + (fb & 63));
     const bool add = p.acc0 && fb < 64;
 #pragma unroll
     for (int f4 = 0; f4 < FG / 4; ++f4) {
@@ -163,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sA = sm;
     unsigned char* sB = sm + kABytes;
     float4* sStat = reinterpret_cast<float4*>(sB + (size_t)kStage * kStages);   // [stage][64]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sStat + kStages * kBN);
+    float* xm = reinterpret_cast<float*>(sStat + kStages * kBN);                // forward: [2][4 parts][128 rows]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xm + kXm / 4);
     uint64_t* a_full = bars + 0;
     uint64_t* a_empty = bars + 1;
     uint64_t* bs_full = bars + 2;              // [kStages]
@@ -174,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* o_full = w_full + 1;             // the output MMAs of a tile finished
     uint64_t* fl_bar = o_full + 1;             // the epilogue wrote its partials of a row block
     uint64_t* dec_bar = fl_bar + 1;            // the CTA knows whether it merges that row block
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(dec_bar + 1);
+    uint64_t* x_bar = dec_bar + 1;             // forward: [4 quarters][2 parities] the quarter's tile maxima are in xm
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(x_bar + 8);
     volatile int* sflag = reinterpret_cast<volatile int*>(tslot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(o_full, 1);
         mbar_init(fl_bar, 32 * kEpi);
         mbar_init(dec_bar, 1);
+        for (int x = 0; x < 8; ++x) mbar_init(x_bar + x, kParts);  // one arrival per warp of the quarter
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tslot, 512);
@@ -346,6 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
         }
+        // forward: the row's running maximum (base 2; the four parts of a row agree on it), the frames (maxima)
+        // of the accumulator and of the pending tile's output, and this part's share of the row sum
+        float fm = ninf<float>(), fm_acc = ninf<float>(), fm_pend = ninf<float>(), fl = 0.f;
         bool ok = true;
         // tile j's output MMAs have finished (its kappa is no longer read)
         auto wait_out = [&](int64_t j) -> bool {
@@ -358,7 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
                 const uint32_t a = tmem + SH::acc(o) + lane_off + (uint32_t)(part * kCols);
-                if (SH::kWide) {
+                if (MODE == kFwd) {
+                    // the accumulator into the current frame fm, the pending block from its own frame
+                    const float fa = fm_acc == fm ? 1.f : ExpTraits<float>::bexp(fm_acc - fm);
+                    const float fo = fm_pend == fm ? inv[o] : (fm_pend == ninf<float>() ? 0.f : inv[o] * ExpTraits<float>::bexp(fm_pend - fm));
+                    float v[kCols], w[kCols];
+                    tmem_ld16x2(a, a + 64, v, w);  // hi*hi, hi*lo + lo*hi
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u) acc[o][u] = fmaf(v[u] + w[u], fo, acc[o][u] * fa);
+                    fm_acc = fm;
+                } else if (SH::kWide) {
                     float v[kCols], w[kCols];
                     tmem_ld16x2(a, a + 64, v, w);  // hi*hi, hi*lo + lo*hi
 #pragma unroll
@@ -377,11 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the CTAs whose tile ranges meet it to count itself in) merges it into the outputs.
         auto write_partial = [&]() {
             const int64_t v = sched_pos(p.sc, rb_cur);
-            float* o = p.part + (size_t)(v + blockIdx.x) * SH::kF * kBM;
+            float* o = p.part + (size_t)(v + blockIdx.x) * SH::kPartRows * kBM;
 #pragma unroll
             for (int oo = 0; oo < NO; ++oo)
 #pragma unroll
                 for (int f = 0; f < kCols; ++f) o[(size_t)(oo * 64 + part * kCols + f) * kBM + lr] = acc[oo][f];
+            if (MODE == kFwd) {
+                if (part == 0) o[(size_t)SH::kF * kBM + lr] = fm;  // the accumulators are in frame fm
+                o[(size_t)(SH::kF + 1 + part) * kBM + lr] = fl;
+            }
             __threadfence();
             mbar_arrive(fl_bar);
             if (etid == 0) {
@@ -415,10 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int o = 0; o < NO; ++o)
 #pragma unroll
                     for (int f = 0; f < kCols; ++f) acc[o][f] = 0.f;
+                fm = fm_acc = fm_pend = ninf<float>();
+                fl = 0.f;
                 // row stats, padded to whole row blocks: queries (14 - lse_i log2 e, delta_i, E_i - lse_i log2 e,
                 // 2^-E_i), keys (2^(E_j - 14), 2^-E_j, 0, 0)
                 rst = p.rstat[(int64_t)rb * kBM + lr];
-                if (MODE == kFwd) inv[0] = pow2i(-14) * pow2i(-eV);
+                if (MODE == kFwd) inv[0] = pow2i(-eV);  // kappa's 2^(6 - m) cancels against the row sum's
                 if (MODE == kRowSweep) inv[0] = rst.w * pow2i(-eK) * p.scale;
                 if (MODE == kColSweep) {
                     inv[0] = rst.y * pow2i(-eQ) * p.scale;
@@ -434,13 +490,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t reg = tmem + lane_off + (uint32_t)(b * SH::kRegion + part * kCols);
             float k0[kCols], k1[kCols];
             if (MODE == kFwd) {
-                // O: kappa = P 2^14 = 2^(s2 + 14 - lse2)
+                // O: kappa = 2^(s2 - m + 6) in the row's running frame m
                 float v[kCols], w[kCols];
                 tmem_ld16x2(reg, reg + 64, v, w);  // S: hi*hi, hi*lo + lo*hi
                 fence_before_sync();
                 mbar_arrive(s_free + b);
+                // kept columns of this slice (past the streamed set's end or outside a pair mask: -inf)
+                const int64_t base = (int64_t)ct * kBN + part * kCols, me = (int64_t)rb * kBM + lr;
+                int64_t lo = 0, hi = p.C - base;
+                if (p.sc.pm == kPairsCausal) {
+                    hi = min(hi, me - base + 1);
+                } else if (p.sc.pm == kPairsBand) {
+                    lo = me - p.sc.band - base;
+                    hi = min(hi, me + p.sc.band - base + 1);
+                }
+                float s2[kCols], lm = ninf<float>();
 #pragma unroll
-                for (int u = 0; u < kCols; ++u) k0[u] = ExpTraits<float>::bexp(fmaf(v[u] + w[u], cS, rst.x));
+                for (int u = 0; u < kCols; ++u) {
+                    s2[u] = (u >= lo && u < hi) ? (v[u] + w[u]) * cS : ninf<float>();
+                    lm = fmaxf(lm, s2[u]);
+                }
+                // the tile maximum of the row over its four parts, through shared memory (one arrival per warp)
+                const int xp = (int)(i & 1);
+                xm[(xp * 4 + part) * kBM + lr] = lm;
+                mbar_arrive_warp(x_bar + q * 2 + xp);
+                ok = mbar_wait_warp(x_bar + q * 2 + xp, (uint32_t)((i >> 1) & 1), p.err, 54);
+                if (!ok) break;
+                const float* xr = xm + xp * 4 * kBM + lr;
+                const float tmax = fmaxf(fmaxf(xr[0], xr[kBM]), fmaxf(xr[2 * kBM], xr[3 * kBM]));
+                if (tmax > fm + kLazy) {  // also the first tile with a kept pair (fm = -inf)
+                    if (fm != ninf<float>()) fl *= ExpTraits<float>::bexp(fm - tmax);
+                    fm = tmax;
+                }
+                const float sh = kKapShift - fm;
+#pragma unroll
+                for (int u = 0; u < kCols; ++u) {
+                    k0[u] = fm == ninf<float>() ? 0.f : ExpTraits<float>::bexp(s2[u] + sh);
+                    fl += k0[u];
+                }
             } else {
                 // P (with the row's or the column's power of two) from S, then dP
                 float pr[kCols];
@@ -518,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_before_sync();
             mbar_arrive(w_full);
             pending = i;
+            fm_pend = fm;
         }
         if (ok && pending >= 0) {
             ok = wait_out(pending);
@@ -641,7 +729,7 @@ __global__ void __launch_bounds__(256) attn_split(const float* __restrict__ A, c
     }
     if (lane != 0) return;
     if (QUERY) {
-        const float l2 = lse[r] * kL2E;
+        const float l2 = lse ? lse[r] * kL2E : 0.f;  // the forward computes lse itself
         if (bounds) {
             const int E = f16_row_exponent(fmaf(sqrtf(ss), __int_as_float(__ldg(gm + gVn)), fabsf(d)));
             stat[r] = make_float4(14.f - l2, d, (float)E - l2, pow2i(-E));
@@ -683,7 +771,7 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
     pl.off_vl = o; o += al256(kb);
     pl.off_kst = o; o += al256((size_t)pl.Mpad * 16);
     // partial slots position + CTA: at most RB + G (consecutive CTA ranges never go back a position)
-    size_t part = (size_t)(RBq + kGrid) * 64 * kBM * 4;
+    size_t part = (size_t)(RBq + kGrid) * Shape<kFwd>::kPartRows * kBM * 4;
     if (backward) {
         const size_t pc = (size_t)(RBk + kGrid) * 128 * kBM * 4;
         part = part > pc ? part : pc;
@@ -703,7 +791,8 @@ static Plan plan_of(int64_t N, int64_t M, bool backward) {
 template <int MODE>
 static int run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scale, const float4* rstat,
                      const float4* cstat, const int* gmax, float* part, int* cnt, float* out0, float* out1, int acc0,
-                     int pm, int64_t band, int64_t* pfx, int* err, const char* name, cudaStream_t s) {
+                     int pm, int64_t band, int64_t* pfx, int* err, const char* name, cudaStream_t s,
+                     float* lse = nullptr) {
     const Sched sc = make_sched(pm, MODE == kColSweep ? 1 : 0, band, R, C, kBM, kBN, pm ? pfx : nullptr);
     int n = 0;
     if (pm) {
@@ -726,6 +815,7 @@ static int run_sweep(const CUtensorMap (&m)[8], int64_t R, int64_t C, float scal
     p.out0 = out0;
     p.out1 = out1;
     p.acc0 = acc0;
+    p.lse = lse;
     p.err = err;
     cudaFuncSetAttribute(attn_tc<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     HookScope h(name, s);
@@ -746,6 +836,7 @@ size_t attn_tc_workspace(int64_t N, int64_t M, bool backward) { return tc::attn:
 // Forward: a.lse holds the row log-sum-exp (already computed on the stream); writes a.out. Returns the
 // number of kernels launched, or -1 if a tensor map could not be encoded.
 int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
+    // one sweep writes out and lse
     using namespace tc;
     using namespace tc::attn;
     const Plan pl = plan_of(a.N, a.M, false);
@@ -780,8 +871,8 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     }
     {
         HookScope h("attn_split", s);
-        attn_split<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, nullptr, nullptr, a.lse, a.N, pl.Npad, gm, gQ, -1,
-                                                                0, qh, ql, nullptr, nullptr, qst, cntq, pl.Npad / kBM);
+        attn_split<true><<<(unsigned)(pl.Npad / 8), 256, 0, s>>>(a.Q, nullptr, nullptr, nullptr, a.N, pl.Npad, gm, gQ,
+                                                                -1, 0, qh, ql, nullptr, nullptr, qst, cntq, pl.Npad / kBM);
     }
     {
         HookScope h("attn_split", s);
@@ -790,7 +881,7 @@ int launch_attn_fwd_tc(const AttnTcArgs& a, cudaStream_t s) {
     }
     return 4 + run_sweep<kFwd>(m, a.N, a.M, (float)a.scale, qst, kst, gm, reinterpret_cast<float*>(ws + pl.off_part),
                                cntq, a.out, nullptr, 0, a.pm, a.band, reinterpret_cast<int64_t*>(ws + pl.off_pfxq),
-                               err, "attn_fwd_tc", s);
+                               err, "attn_fwd_tc", s, a.lse_out);
 }
 
 // Backward: dQ (row sweep) and dK, dV (column sweep); null outputs are not written (a sweep none of whose

@@ -83,7 +83,8 @@ def test_attention_tc_runs_on_the_tensor_cores():
     def fwd():
         holder["o"], holder["l"] = ops.pairwise_softmax_matmul(Q, K, V, sc)
 
-    assert {"lse_fwd_tc", "attn_fwd_tc"} <= _tc_kernels(fwd)
+    names = _tc_kernels(fwd)
+    assert "attn_fwd_tc" in names and "lse_fwd_tc" not in names, names  # one sweep gives out and lse
     names = _tc_kernels(lambda: ops.pairwise_softmax_matmul_backward(Q, K, V, sc, holder["o"], holder["l"], G))
     assert {"attn_bwd_row_tc", "attn_bwd_col_tc"} <= names
 
