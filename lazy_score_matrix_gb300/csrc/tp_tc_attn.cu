@@ -396,6 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // add this part of the finished output blocks into the row accumulators
         auto add_out = [&]() {
+            if constexpr (NO == 2 && !SH::kWide) {
+                // both outputs' blocks with one wait
+                float v0[kCols], v1[kCols];
+                tmem_ld16x2(tmem + SH::acc(0) + lane_off + (uint32_t)(part * kCols),
+                            tmem + SH::acc(1) + lane_off + (uint32_t)(part * kCols), v0, v1);
+#pragma unroll
+                for (int u = 0; u < kCols; ++u) {
+                    acc[0][u] = fmaf(v0[u], inv[0], acc[0][u]);
+                    acc[1][u] = fmaf(v1[u], inv[1], acc[1][u]);
+                }
+                return;
+            }
 #pragma unroll
             for (int o = 0; o < NO; ++o) {
                 const uint32_t a = tmem + SH::acc(o) + lane_off + (uint32_t)(part * kCols);
