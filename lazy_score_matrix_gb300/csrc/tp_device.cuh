@@ -22,6 +22,14 @@ namespace tp {
 
 enum Metric : int { kSqeuclidean = 0, kLinear = 1, kRbf = 2 };
 
+// Programmatic dependent launch (kernels started with launch_pdl, tp_launch.h): such a kernel may begin
+// while the kernel before it on the stream is still running. griddep_wait returns once that grid has
+// completed and its memory operations are visible, so nothing before it may read or write global memory;
+// griddep_launch lets the next such kernel on the stream begin its prologue. In a kernel launched without
+// the attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <class T>
 struct Vec16;
 template <>

@@ -135,6 +135,7 @@ __host__ __device__ inline int fwd_state_width(int D, int C) {
 
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     using E = ExpTraits<T>;
     using SM = FwdSmem<T, DP, CP, MODE, AFFINE>;
     constexpr bool HAS_V = SM::HAS_V;
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kThreads) fwd_sweep(const SweepArgs a) {
 // Combine the per-split partial states of a forward sweep, splits in ascending order.
 template <class T, int MODE>
 __global__ void __launch_bounds__(kThreads) fwd_merge(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     using E = ExpTraits<T>;
     const int64_t pi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if (pi >= a.nP) return;
@@ -375,6 +377,7 @@ constexpr int kNoIndex = 0x7fffffff;
 
 template <class T, int DP, int K, bool AFFINE>
 __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     using E = ExpTraits<T>;
     __shared__ __align__(16) T sq[kTile * DP];
     __shared__ T sn[kTile];
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kThreads) topk_sweep(const SweepArgs a) {
 
 template <class T, int K>
 __global__ void __launch_bounds__(kThreads) topk_merge(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     const int64_t pi = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if (pi >= a.nP) return;
     const T* wv = static_cast<const T*>(a.ws);
@@ -520,6 +524,7 @@ __host__ __device__ inline int bwd_state_width(int D, int C) {
 
 template <class T, int DP, int CP, int MODE, int SIDE, bool DO_G, bool DO_V>
 __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     using E = ExpTraits<T>;
     constexpr bool VALS = MODE == kBMatmul || MODE == kBSoftmax;
     // own value vector: row sweep dO_i (CP; DP for disp); column sweep V_j (CP) when DO_G
@@ -764,6 +769,7 @@ __global__ void __launch_bounds__(kThreads) bwd_sweep(const SweepArgs a) {
 // feature-0 thread of a point also writes its bias and weight gradients.
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 __global__ void __launch_bounds__(kThreads) bwd_merge(const SweepArgs a) {
+    griddep_wait();  // launched with launch_pdl: nothing before this touches global memory
     const int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int F = DO_G && DO_V ? (a.D > a.C ? a.D : a.C) : (DO_G ? a.D : a.C);
     if (e >= (int64_t)F * a.nP) return;
@@ -978,35 +984,35 @@ void launch_fwd(const SweepArgs& a, cudaStream_t s) {
     constexpr size_t smem = FwdSmem<T, DP, CP, MODE, AFFINE>::bytes;
     allow_smem(fwd_sweep<T, DP, CP, MODE, AFFINE>, smem);
     HookScope h(kFwdNames[MODE], s);
-    fwd_sweep<T, DP, CP, MODE, AFFINE><<<sweep_grid(a), kThreads, smem, s>>>(a);
+    launch_pdl(fwd_sweep<T, DP, CP, MODE, AFFINE>, sweep_grid(a), dim3(kThreads), smem, s, a);
 }
 template <class T, int MODE>
 void launch_fwd_merge(const SweepArgs& a, cudaStream_t s) {
     HookScope h(kFwdMergeNames[MODE], s);
-    fwd_merge<T, MODE><<<row_grid(a.nP), kThreads, 0, s>>>(a);
+    launch_pdl(fwd_merge<T, MODE>, row_grid(a.nP), dim3(kThreads), 0, s, a);
 }
 template <class T, int DP, int K, bool AFFINE>
 void launch_topk(const SweepArgs& a, cudaStream_t s) {
     HookScope h("topk_sweep", s);
-    topk_sweep<T, DP, K, AFFINE><<<sweep_grid(a), kThreads, 0, s>>>(a);
+    launch_pdl(topk_sweep<T, DP, K, AFFINE>, sweep_grid(a), dim3(kThreads), 0, s, a);
 }
 template <class T, int K>
 void launch_topk_merge(const SweepArgs& a, cudaStream_t s) {
     HookScope h("topk_merge", s);
-    topk_merge<T, K><<<row_grid(a.nP), kThreads, 0, s>>>(a);
+    launch_pdl(topk_merge<T, K>, row_grid(a.nP), dim3(kThreads), 0, s, a);
 }
 template <class T, int DP, int CP, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd(const SweepArgs& a, cudaStream_t s) {
     constexpr size_t smem = BwdSmem<T, DP, CP, MODE, SIDE, DO_G, DO_V>::bytes;
     allow_smem(bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V>, smem);
     HookScope h(kBwdNames[MODE][SIDE][DO_G ? 0 : 1], s);
-    bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V><<<sweep_grid(a), kThreads, smem, s>>>(a);
+    launch_pdl(bwd_sweep<T, DP, CP, MODE, SIDE, DO_G, DO_V>, sweep_grid(a), dim3(kThreads), smem, s, a);
 }
 template <class T, int MODE, int SIDE, bool DO_G, bool DO_V>
 void launch_bwd_merge(const SweepArgs& a, cudaStream_t s) {
     const int F = DO_G && DO_V ? (a.D > a.C ? a.D : a.C) : (DO_G ? a.D : a.C);
     HookScope h(kBwdMergeNames[MODE][SIDE], s);
-    bwd_merge<T, MODE, SIDE, DO_G, DO_V><<<row_grid((int64_t)F * a.nP), kThreads, 0, s>>>(a);
+    launch_pdl(bwd_merge<T, MODE, SIDE, DO_G, DO_V>, row_grid((int64_t)F * a.nP), dim3(kThreads), 0, s, a);
 }
 // rows: P = X, Q = Y; cols: P = Y, Q = X (parameters swapped). count/start/cursor/bucket come from
 // the workspace; count must be zero on entry.

@@ -18,6 +18,24 @@ struct HookScope {
     ~HookScope() { launch_hook(name, 1, s); }
 };
 
+// Launch with programmatic stream serialization: the kernel may start before the previous kernel on the
+// stream has finished (its prologue overlaps that kernel's tail) and calls griddep_wait (tp_device.cuh) before
+// it touches global memory. A launch error is left for cudaGetLastError, like a <<<>>> launch's.
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <class T, int DP, int CP, int MODE, bool AFFINE>
 void launch_fwd(const SweepArgs& a, cudaStream_t s);
 template <class T, int MODE>

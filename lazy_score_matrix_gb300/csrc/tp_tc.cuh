@@ -9,15 +9,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "tp_device.cuh"
+
 namespace tp {
 namespace tc {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait on an mbarrier gives up after 2 s
 // Site codes recorded by a wait that gives up: 1 the self-test (tp_status.cu), 11-18 lse_fwd_tc, 21-34
-// lse_bwd_sym_tc, 41-53 the attention sweeps, 61-71 lse_bwd_lin_tc, 81-86 topk_tc.
+// lse_bwd_sym_tc, 41-54 the attention sweeps, 61-71 lse_bwd_lin_tc, 81-86 topk_tc.
 constexpr int kSelfTestCode = 1;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// The kernel's dynamic shared memory from its first 1024-byte boundary (the repeat of the 128-byte swizzle),
+// taken as an offset into the array: pointers derived from it stay shared-memory pointers to the compiler,
+// so their loads and stores are shared-memory instructions (a round trip through an integer address would
+// make them generic ones, which wait on the long scoreboard).
+__device__ __forceinline__ unsigned char* smem_base1024(unsigned char* raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

@@ -7,6 +7,8 @@
 
 #include <mutex>
 
+#include "tp_launch.h"
+
 namespace tp {
 
 // The library's device error word on the current device (tp_status.cu), written by a bounded wait that

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(256) tc_split16(const float* __restrict__ x, i
                                                   __half2* __restrict__ hi, __half2* __restrict__ lo,
                                                   float* __restrict__ inv_scale, float* __restrict__ norm,
                                                   int* __restrict__ cnt, int64_t ncnt) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (cnt && lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(256) tc_split16(const float* __restrict__ x, i
 void launch_split16(const float* x, int64_t rows, int64_t rows_pad, void* hi, void* lo, float* inv_scale, float* norm,
                     int* cnt, int64_t ncnt, cudaStream_t s) {
     HookScope h("tc_split16", s);
-    tc_split16<<<(unsigned)((rows_pad + 7) / 8), 256, 0, s>>>(x, rows, rows_pad, static_cast<__half2*>(hi),
-                                                             static_cast<__half2*>(lo), inv_scale, norm, cnt, ncnt);
+    launch_pdl(tc_split16, dim3((unsigned)((rows_pad + 7) / 8)), dim3(256), 0, s, x, rows, rows_pad,
+               static_cast<__half2*>(hi), static_cast<__half2*>(lo), inv_scale, norm, cnt, ncnt);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     lse_fwd_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
                const __grid_constant__ CUtensorMap mYh, const __grid_constant__ CUtensorMap mYl, const LseTcParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sm = smem_base1024(smem_raw);
     unsigned char* sA = sm;               // [hi 128 rows | lo 128 rows]
     unsigned char* sB = sm + kPairF;      // stage s at sB + s * kPairF: [hi 128 points | lo 128 points]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)kPairF * (1 + kStagesF));
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
+    griddep_wait();
+    griddep_launch();
 
     if (warp == 0) {
         if (lane == 0) {  // ---------------- TMA producer
@@ -519,6 +523,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const LseBwdTcParams p) {
     constexpr float kL2E = 1.4426950408889634f;
     extern __shared__ unsigned char smem_raw[];
+    // aligned through an integer address (generic loads): derived from the array itself, this kernel's
+    // register allocation spills 150-200 bytes
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                        // row block: [hi 128 rows | lo 128 rows]
     unsigned char* sB = sm + kPairF;                               // stage s: [hi 64 points | lo 64 points]
@@ -570,6 +576,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
+    griddep_wait();
+    griddep_launch();
     const uint32_t tDZ = tmem + kDZCol;
 
     if (warp == 0) {
@@ -878,6 +886,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    const LseBwdTcParams p) {
     constexpr float kL2E = 1.4426950408889634f;
     extern __shared__ unsigned char smem_raw[];
+    // aligned through an integer address (generic loads): derived from the array itself, this kernel
+    // measured 2% slower
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* sA = sm;                                        // row block: [hi 128 rows | lo 128 rows]
     unsigned char* sB = sm + kPairF;                               // stage s: [hi 64 points | lo 64 points]
@@ -926,6 +936,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tslot;
+    griddep_wait();
+    griddep_launch();
     // group g: S buffer at column 128 g (hi*hi 0..63, hi*lo + lo*hi 64..127), dZ at 256 + 128 g
     auto tS = [&](int g) { return tmem + (uint32_t)(128 * g); };
     auto tD = [&](int g) { return tmem + (uint32_t)(256 + 128 * g); };
@@ -1169,6 +1181,8 @@ __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ 
                                                       __half2* __restrict__ hi, __half2* __restrict__ lo,
                                                       float* __restrict__ zn, float4* __restrict__ stat,
                                                       int* __restrict__ cnt, int64_t ncnt) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
@@ -1201,6 +1215,8 @@ __global__ void __launch_bounds__(256) lse_bwd_prep16(const float* __restrict__ 
 // non-negative) for the sweep's two powers of two. One warp per row, grid-stride; one atomic per block.
 __global__ void __launch_bounds__(256) lse_bwd_reduce(const float* __restrict__ z, const float* __restrict__ g,
                                                       int64_t N, int* __restrict__ gm) {
+    griddep_wait();
+    griddep_launch();
     __shared__ float red[2][8];
     const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float mz = 0.f, mg = 0.f;
@@ -1243,6 +1259,8 @@ __global__ void __launch_bounds__(256) lse_bwd_prep_lin(const float* __restrict_
                                                         int64_t Npad, const int* __restrict__ gm,
                                                         __half2* __restrict__ hi, __half2* __restrict__ lo,
                                                         float4* __restrict__ stat, int* __restrict__ cnt, int64_t ncnt) {
+    griddep_wait();
+    griddep_launch();
     const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (lane == 0 && r < ncnt) cnt[r] = 0;  // the main kernel's per-row-block arrival counters
@@ -1265,6 +1283,8 @@ __global__ void __launch_bounds__(256) lse_bwd_prep_lin(const float* __restrict_
 // pfx[v] = tiles of the positions before v of a masked schedule, pfx[RB] = all of them: one block, each
 // thread sums a run of consecutive positions, then an inclusive scan over the threads.
 __global__ void __launch_bounds__(1024) sched_prefix(const Sched sc, int64_t* __restrict__ pfx) {
+    griddep_wait();
+    griddep_launch();
     __shared__ int64_t run[1024];
     const int t = threadIdx.x;
     const int64_t per = (sc.RB + 1023) / 1024;
@@ -1289,7 +1309,7 @@ __global__ void __launch_bounds__(1024) sched_prefix(const Sched sc, int64_t* __
 
 void launch_sched_prefix(const Sched& sc, int64_t* pfx, cudaStream_t s) {
     HookScope h("sched_prefix", s);
-    sched_prefix<<<1, 1024, 0, s>>>(sc, pfx);
+    launch_pdl(sched_prefix, dim3(1), dim3(1024), 0, s, sc, pfx);
 }
 
 struct LseTcPlan {
@@ -1381,14 +1401,14 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     const int64_t xrows = same ? (pl.Xpad > pl.Ypad ? pl.Xpad : pl.Ypad) : pl.Xpad;
     {
         HookScope h("tc_split16", s);
-        tc_split16<<<(unsigned)((xrows + 7) / 8), 256, 0, s>>>(static_cast<const float*>(a.P), a.nP, xrows, xh, xl, xs,
-                                                              xn, cnt, pl.Xpad / kBM);
+        launch_pdl(tc_split16, dim3((unsigned)((xrows + 7) / 8)), dim3(256), 0, s, static_cast<const float*>(a.P), a.nP,
+                   xrows, xh, xl, xs, xn, cnt, (int64_t)(pl.Xpad / kBM));
         ++n;
     }
     if (!same) {
         HookScope h("tc_split16", s);
-        tc_split16<<<(unsigned)((pl.Ypad + 7) / 8), 256, 0, s>>>(static_cast<const float*>(a.Q), a.nQ, pl.Ypad, yh, yl,
-                                                                ys, yn, nullptr, 0);
+        launch_pdl(tc_split16, dim3((unsigned)((pl.Ypad + 7) / 8)), dim3(256), 0, s, static_cast<const float*>(a.Q),
+                   a.nQ, pl.Ypad, yh, yl, ys, yn, (int*)nullptr, (int64_t)0);
         ++n;
     }
     // causal or band only (callers route same-group masks to the streamed sweeps): the row blocks stream
@@ -1424,7 +1444,7 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemF);
         HookScope h("lse_fwd_tc", s);
-        kernel<<<G, kTcThreads, kSmemF, s>>>(mxh, mxl, myh, myl, p);
+        launch_pdl(kernel, dim3(G), dim3(kTcThreads), kSmemF, s, mxh, mxl, myh, myl, p);
     };
     const bool ex = a.apply_exp != 0;
     if (a.metric == kLinear) ex ? go(lse_fwd_tc<kLinear, true>) : go(lse_fwd_tc<kLinear, false>);
@@ -1463,20 +1483,20 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
             HookScope h("lse_bwd_reduce", s);
             const int64_t blocks = (a.nP + 7) / 8;  // one block per SM at most: few atomics on the two slots
             const int rg = capped_grid(kGrid);
-            lse_bwd_reduce<<<(unsigned)(blocks < rg ? blocks : rg), 256, 0, s>>>(
-                static_cast<const float*>(a.P), static_cast<const float*>(a.glse), a.nP, gm);
+            launch_pdl(lse_bwd_reduce, dim3((unsigned)(blocks < rg ? blocks : rg)), dim3(256), 0, s,
+                       static_cast<const float*>(a.P), static_cast<const float*>(a.glse), a.nP, gm);
             ++n;
         }
         HookScope h("lse_bwd_prep_lin", s);
-        lse_bwd_prep_lin<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
-            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
-            (float)a.scale, a.nP, pl.Npad, gm, zh, zl, stat, cnt, (a.nP + kBM - 1) / kBM);
+        launch_pdl(lse_bwd_prep_lin, dim3((unsigned)((pl.Npad + 7) / 8)), dim3(256), 0, s,
+                   static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
+                   (float)a.scale, a.nP, pl.Npad, (const int*)gm, zh, zl, stat, cnt, (int64_t)((a.nP + kBM - 1) / kBM));
         ++n;
     } else {
         HookScope h("lse_bwd_prep16", s);
-        lse_bwd_prep16<<<(unsigned)((pl.Npad + 7) / 8), 256, 0, s>>>(
-            static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
-            (float)a.scale, a.nP, pl.Npad, zh, zl, zn, stat, cnt, (a.nP + kBM - 1) / kBM);
+        launch_pdl(lse_bwd_prep16, dim3((unsigned)((pl.Npad + 7) / 8)), dim3(256), 0, s,
+                   static_cast<const float*>(a.P), static_cast<const float*>(a.lse), static_cast<const float*>(a.glse),
+                   (float)a.scale, a.nP, pl.Npad, zh, zl, zn, stat, cnt, (int64_t)((a.nP + kBM - 1) / kBM));
         ++n;
     }
     LseBwdTcParams p;
@@ -1503,7 +1523,7 @@ int launch_lse_bwd_sym_tc(const SweepArgs& a, cudaStream_t s) {
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemB);
         HookScope h(glob ? "lse_bwd_lin_tc" : "lse_bwd_sym_tc", s);
-        kernel<<<pl.G, kTcThreads, kSmemB, s>>>(mah, mal, mbh, mbl, p);
+        launch_pdl(kernel, dim3(pl.G), dim3(kTcThreads), kSmemB, s, mah, mal, mbh, mbl, p);
     };
     const bool ex = a.apply_exp != 0;
     if (glob) go(lse_bwd_lin_tc);

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(TopkTcShape<DP, sel_warps(DP, K)>::kThreads, 1
     using SH = TopkTcShape<DP, sel_warps(DP, K)>;
     constexpr int kChunk = 128 * 128;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* sm = smem_base1024(smem_raw);
     unsigned char* sA = sm;
     unsigned char* sB = sm + SH::kPair;
     float* sYn = reinterpret_cast<float*>(sB + (size_t)SH::kPair * SH::kStages);  // [stage][128]
