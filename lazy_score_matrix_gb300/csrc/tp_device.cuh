@@ -103,7 +103,9 @@ __device__ __forceinline__ double exp_table(double x) {
     constexpr double kInvL = 0x1.71547652b82fep+6;                            // 64 / ln 2
     constexpr double kL1 = 0x1.62e42fefa0000p-7, kL2 = 0x1.cf79abc9e3b3ap-46;  // ln2/64 = L1 + L2
     constexpr double kShift = 0x1.8p52;  // adding 1.5 2^52 rounds to an integer kept in the low word
-    const double xc = fmin(fmax(x, -707.0), 709.78);
+    // one compare per bound, shared by the clamp and the result (fmin/fmax would compare again)
+    const bool under = x < -707.0, over = x > 709.78;
+    const double xc = under ? -707.0 : (over ? 709.78 : x);
     const double s = fma(xc, kInvL, kShift);
     const int N = __double2loint(s);
     const double Nd = s - kShift;
@@ -113,7 +115,7 @@ __device__ __forceinline__ double exp_table(double x) {
     const double y = fma(t, fma(r * r, q, r), t);  // 2^(j/64) e^r, in [0.99, 1.99]
     // times 2^(N >> 6), N >> 6 in [-1020, 1023]: added to the exponent field (the result stays normal)
     const double res = __hiloint2double(__double2hiint(y) + (int)((unsigned)(N >> 6) << 20), __double2loint(y));
-    return x < -707.0 ? 0.0 : (x > 709.78 ? __longlong_as_double(0x7ff0000000000000ULL) : res);
+    return under ? 0.0 : (over ? __longlong_as_double(0x7ff0000000000000ULL) : res);
 }
 
 template <>
@@ -307,9 +309,11 @@ __device__ __forceinline__ T pair_base(int metric, const T (&p)[DP], const T* __
     if (metric == kLinear) return dot_regs_smem<T, DP>(p, q);
     T d2;
     if constexpr (sizeof(T) == 4) d2 = dist2_regs_smem<T, DP>(p, q);
-    else d2 = fmax(fma(T(-2), dot_regs_smem<T, DP>(p, q), pn + qn), T(0));
+    else d2 = fma(T(-2), dot_regs_smem<T, DP>(p, q), pn + qn);  // the norm expansion may round below 0
+    // rbf needs no clamp (a d2 a rounding below 0 gives exp 1 + O(eps)); in fp64 the compare it saves
+    // runs on the FP64 pipe that bounds the sweep
     if (metric == kRbf) return ExpTraits<T>::exp(neg_gamma * d2);
-    return d2;
+    return sizeof(T) == 4 ? d2 : fmax(d2, T(0));
 }
 
 // Insert (key, idx) into the sorted list when it beats the last entry. Entries of equal key keep
