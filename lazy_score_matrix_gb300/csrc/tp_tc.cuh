@@ -16,7 +16,7 @@ namespace tc {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // a wait on an mbarrier gives up after 2 s
 // Site codes recorded by a wait that gives up: 1 the self-test (tp_status.cu), 11-18 lse_fwd_tc, 21-34
-// lse_bwd_sym_tc, 41-54 the attention sweeps, 61-71 lse_bwd_lin_tc, 81-86 topk_tc.
+// lse_bwd_sym_tc, 41-54 the attention sweeps, 61-71 lse_bwd_lin_tc, 81-86 topk_tc, 91-96 lse_fwd_sym_tc.
 constexpr int kSelfTestCode = 1;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }

@@ -128,6 +128,12 @@ struct LseTcParams {
     int* cnt;              // [RB] CTAs done with each row block (zeroed by the split pre-pass)
     float* lse;            // [N] output
     int* err;
+    // after lse_fwd_sym_tc (null otherwise): sym[0] == 0 means that sweep covered the rows and this kernel
+    // only merges its partials (prow, pcol; Gs its CTAs) before anything else; 1 means it sweeps as usual
+    const int* sym;
+    const float* prow;
+    const float* pcol;
+    int Gs;
 };
 
 // lse of row `row` of row block rb from the partials of every CTA that saw it, in CTA order (one
@@ -158,10 +164,59 @@ __device__ __noinline__ float lse_merge_row(const LseTcParams& p, int rb, int lr
     return l > 0.f ? ExpTraits<float>::lse(m, l) : ninf<float>();
 }
 
+// First tile of row block I in the triangle numbering (row-block major, J from I to RB - 1).
+__host__ __device__ inline int64_t sym_start(int64_t I, int64_t RB) { return I * RB - I * (I - 1) / 2; }
+
+// lse of rows from the triangle sweep's partials (lse_fwd_tc in merge mode): eight threads per row, each
+// adding every eighth term (the row partials of the CTAs that swept the row's block, in CTA order, then the
+// column partials of the tiles (I, R), I < R, in order of I), the eight sums combined in a fixed tree.
+__device__ __noinline__ void sym_merge(const LseTcParams& p) {
+    const int RB = (int)((p.N + kBM - 1) / kBM);
+    const int64_t T = (int64_t)RB * (RB + 1) / 2;
+    const float M = __int_as_float(__ldcg(p.sym + 1));
+    const int64_t wpb = blockDim.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t base = ((int64_t)blockIdx.x * wpb + (threadIdx.x >> 5)) * 4; base < p.N;
+         base += (int64_t)gridDim.x * wpb * 4) {  // warp-uniform: four rows per warp, eight lanes per row
+        const int64_t row = base + (lane >> 3);
+        const int k = (int)(lane & 7);
+        float l = 0.f;
+        if (row < p.N) {
+            const int R = (int)(row / kBM), lr = (int)(row % kBM);
+            const int64_t t0 = sym_start(R, RB);
+            const int c_lo = cta_of_tile(T, p.Gs, t0), c_hi = cta_of_tile(T, p.Gs, t0 + (RB - R) - 1);
+            const int nrow = c_hi - c_lo + 1, nterm = nrow + R;
+            for (int m0 = k; m0 < nterm; m0 += 32) {  // four independent loads in flight, added in order
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int m = m0 + 8 * u;
+                    const float* src = m < nrow ? p.prow + ((size_t)(R + c_lo + m) * kBM + lr) * 4
+                                                : p.pcol + ((size_t)(sym_start(m - nrow, RB) + R - (m - nrow)) * kBM + lr) * 4;
+                    v[u] = m < nterm ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) l += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+            }
+        }
+        l += __shfl_down_sync(0xffffffffu, l, 1, 8);
+        l += __shfl_down_sync(0xffffffffu, l, 2, 8);
+        l += __shfl_down_sync(0xffffffffu, l, 4, 8);
+        if (k == 0 && row < p.N) p.lse[row] = l > 0.f ? ExpTraits<float>::lse(M, l) : ninf<float>();
+    }
+}
+
 template <int METRIC, bool EXP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     lse_fwd_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
                const __grid_constant__ CUtensorMap mYh, const __grid_constant__ CUtensorMap mYl, const LseTcParams p) {
+    if (p.sym) {  // after the triangle sweep: merge its partials, unless it fell back
+        griddep_wait();
+        if (__ldcg(p.sym) == 0) {
+            griddep_launch();
+            sym_merge(p);
+            return;
+        }
+    }
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_base1024(smem_raw);
     unsigned char* sA = sm;               // [hi 128 rows | lo 128 rows]
@@ -410,6 +465,276 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 32; ++u) s4[u & 3] += ExpTraits<float>::bexp(v[u] - m);
                 l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            }
+        }
+        if (ok && rb_cur >= 0) flush();
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Forward over the upper triangle, for X = Y with a linear score without exp and no pair mask (the
+// InfoNCE row). The score matrix is symmetric, so each tile (I, J), J >= I, of 128 x 128 is evaluated
+// once for the rows of both blocks. The terms are taken against one fixed offset, e_ij = 2^(s2_ij - M)
+// with M = |scale| log2(e) max|x|^2 >= every s2 (Cauchy-Schwarz), which makes them symmetric as well:
+// a tile's row sums belong to the rows of I and its column sums to the rows of J. When 2 M <= 120 every
+// term is a normal fp32 number, so nothing underflows and no running maximum is needed; otherwise the
+// kernel sets the fallback flag and returns, and lse_fwd_tc runs the full sweep with running maxima.
+// A diagonal tile (J = I) covers both orders of its pairs and counts for its rows only. Each CTA walks a
+// contiguous range of the triangle's tiles numbered row-block major; it writes one row partial per row
+// block of its range and one column partial per off-diagonal tile, and lse_fwd_tc (merge mode) adds
+// them in a fixed order.
+// ------------------------------------------------------------------------------------------------
+constexpr float kSymSpan = 120.f;  // 2 M: the widest range of exponents the terms may span
+constexpr int kSymCap = 96;        // row blocks: the column partials grow with their square
+constexpr int kTrW = 36;           // the epilogue warps' transpose buffers: 32 rows x 32 columns, padded
+constexpr int kStY = 3;            // column stages (the transposes take the fourth's room)
+constexpr size_t kSmemS = (size_t)kPairF * (1 + kStY) + 256 + 1024 + (size_t)kEpi * 32 * kTrW * 4;
+static_assert(kSmemS <= 232448, "dynamic shared memory per CTA");
+
+struct LseSymParams {
+    int64_t N;
+    int RB;       // row blocks of 128
+    int64_t T;    // tiles of the triangle: RB (RB + 1) / 2
+    int G;        // CTAs
+    int exclude_self;
+    float scale;
+    const float* xs;    // 2^-e of each point (padded to whole row blocks, zeros past N)
+    const float* xn;    // |x_i|^2 (zeros past N)
+    float* prow;        // [RB + G][128][4 column parts]: row sums, slot row block + CTA
+    float* pcol;        // [T][128][4 row quarters]: column sums of each off-diagonal tile
+    int* sym;           // [2]: 1 if the sweep fell back (lse_fwd_tc sweeps), 0 if done; M as float bits
+    int* err;
+};
+
+// (row block, column block) of consecutive tiles of the triangle.
+struct SymCursor {
+    int I, J, RB;
+    __device__ __forceinline__ SymCursor(int64_t t, int RB_) : I(0), J(0), RB(RB_) {
+        while (I + 1 < RB && sym_start(I + 1, RB) <= t) ++I;
+        J = I + (int)(t - sym_start(I, RB));
+    }
+    __device__ __forceinline__ void next() {
+        if (++J == RB) {
+            ++I;
+            J = I;
+        }
+    }
+};
+
+// M (base 2) from the largest |x|^2, the same value in every CTA and in the merge.
+__device__ float sym_offset(const float* __restrict__ xn, int64_t N, float scale, float* red) {
+    float w[16];  // sixteen independent loads in flight per thread (the array sits in L2)
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = 0.f;
+    for (int64_t r0 = threadIdx.x; r0 < N; r0 += 16 * (int64_t)blockDim.x) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int64_t r = r0 + (int64_t)k * blockDim.x;
+            if (r < N) w[k] = fmaxf(w[k], __ldg(xn + r));
+        }
+    }
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v = fmaxf(v, w[k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    __syncthreads();
+    return fabsf(scale) * 1.4426950408889634f * m;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    lse_fwd_sym_tc(const __grid_constant__ CUtensorMap mXh, const __grid_constant__ CUtensorMap mXl,
+                   const LseSymParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_base1024(smem_raw);
+    unsigned char* sA = sm;                     // [hi 128 rows | lo 128 rows]
+    unsigned char* sB = sm + kPairF;            // stage s at sB + s * kPairF: [hi 128 points | lo 128 points]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)kPairF * (1 + kStY));
+    uint64_t* a_full = bars + 0;
+    uint64_t* a_empty = bars + 1;
+    uint64_t* b_full = bars + 2;                 // [kStY]
+    uint64_t* b_empty = b_full + kStY;           // [kStY]
+    uint64_t* acc_full = b_empty + kStY;         // [2]
+    uint64_t* acc_empty = acc_full + 2;          // [2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    float* red = reinterpret_cast<float*>(tslot + 2);                 // [18] block maxima (barrier area: 176 B)
+    float* trb = reinterpret_cast<float*>(sm + (size_t)kPairF * (1 + kStY) + 256);  // [kEpi][32][kTrW]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t_begin = range_start(p.T, p.G, blockIdx.x), t_end = range_start(p.T, p.G, blockIdx.x + 1);
+
+    if (threadIdx.x == 0) {
+        prefetch_map(&mXh);
+        prefetch_map(&mXl);
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int s = 0; s < kStY; ++s) {
+            mbar_init(b_full + s, 1);
+            mbar_init(b_empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, kEpi);  // one arrival per epilogue warp
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, 512);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tslot;
+    griddep_wait();
+    griddep_launch();
+    const float M = sym_offset(p.xn, p.N, p.scale, red);
+    const bool bounded = 2.f * M <= kSymSpan;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        p.sym[0] = bounded ? 0 : 1;
+        p.sym[1] = __float_as_int(M);
+    }
+
+    if (!bounded) {
+        // the full sweep runs instead
+    } else if (warp == 0) {
+        if (lane == 0) {  // ---------------- TMA producer: row block I and column block J of each tile
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            SymCursor cur(t_begin, p.RB);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+                const int64_t i = t - t_begin;
+                if (cur.I != rb_cur) {
+                    if (a_uses > 0) ok = mbar_wait(a_empty, (a_uses - 1) & 1, p.err, 91);
+                    if (!ok) break;
+                    mbar_expect_tx(a_full, kPairF);
+                    tma_load_2d(sA, &mXh, 0, cur.I * kBM, a_full);
+                    tma_load_2d(sA + kHalfTile, &mXl, 0, cur.I * kBM, a_full);
+                    ++a_uses;
+                    rb_cur = cur.I;
+                }
+                const int s = (int)(i % kStY), r = (int)(i / kStY);
+                if (r >= 1) ok = mbar_wait(b_empty + s, (r - 1) & 1, p.err, 92);
+                if (!ok) break;
+                unsigned char* dst = sB + (size_t)s * kPairF;
+                mbar_expect_tx(b_full + s, kPairF);
+                tma_load_2d(dst, &mXh, 0, cur.J * kBN, b_full + s);
+                tma_load_2d(dst + kHalfTile, &mXl, 0, cur.J * kBN, b_full + s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---------------- MMA issuer (as lse_fwd_tc)
+            constexpr uint32_t id256 = idesc_f16(kBM, 2 * kBN, false);
+            constexpr uint32_t id128 = idesc_f16(kBM, kBN, false);
+            int rb_cur = -1, a_uses = 0;
+            bool ok = true;
+            SymCursor cur(t_begin, p.RB);
+            for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+                const int64_t i = t - t_begin;
+                if (cur.I != rb_cur) {
+                    if (a_uses > 0) mma_commit(a_empty);
+                    ok = mbar_wait(a_full, a_uses & 1, p.err, 93);
+                    if (!ok) break;
+                    ++a_uses;
+                    rb_cur = cur.I;
+                }
+                const int s = (int)(i % kStY), r = (int)(i / kStY), b = (int)(i & 1), rr = (int)(i >> 1);
+                ok = mbar_wait(b_full + s, r & 1, p.err, 94);
+                if (ok && rr >= 1) ok = mbar_wait(acc_empty + b, (rr - 1) & 1, p.err, 95);
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(b * 256);
+                const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB + (size_t)s * kPairF);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t ko = (uint32_t)(ks * 32);
+                    mma_f16(d, desc_sw128(a0 + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), id256, ks > 0 ? 1u : 0u);
+                    mma_f16(d + 128, desc_sw128(a0 + kHalfTile + ko, 16, 1024), desc_sw128(b0 + ko, 16, 1024), id128,
+                            1u);
+                }
+                mma_commit(b_empty + s);
+                mma_commit(acc_full + b);
+            }
+        }
+    } else {  // ---------------- epilogue: one row per thread, 32 of the tile's columns per warp
+        constexpr float kL2E = 1.4426950408889634f;
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int sub = (warp - 2) >> 2;        // columns [32 sub, 32 sub + 32) of each tile
+        const int lr = q * 32 + lane;           // row within the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(sub * 32);
+        float* tr = trb + (size_t)(warp - 2) * 32 * kTrW;
+        int rb_cur = -1;
+        float rs = 0.f, c1r = 0.f;
+        bool ok = true;
+        auto flush = [&]() {
+            p.prow[((size_t)(rb_cur + blockIdx.x) * kBM + lr) * 4 + sub] = rs;
+        };
+        SymCursor cur(t_begin, p.RB);
+        for (int64_t t = t_begin; t < t_end && ok; ++t, cur.next()) {
+            const int64_t i = t - t_begin;
+            const int I = cur.I, J = cur.J;
+            const int64_t row = (int64_t)I * kBM + lr;
+            if (I != rb_cur) {
+                if (rb_cur >= 0) flush();
+                rs = 0.f;
+                rb_cur = I;
+                c1r = p.scale * kL2E * __ldg(p.xs + row);  // 0 for padding rows
+            }
+            const int b = (int)(i & 1), rr = (int)(i >> 1);
+            ok = mbar_wait_warp(acc_full + b, rr & 1, p.err, 96);
+            if (!ok) break;
+            fence_after_sync();
+            float e[32];  // hi*hi + (hi*lo + lo*hi), then the terms
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                float t0[16], t1[16];
+                tmem_ld16x2(lane_base + (uint32_t)(b * 256 + hlf * 16), lane_base + (uint32_t)(b * 256 + 128 + hlf * 16),
+                            t0, t1);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) e[hlf * 16 + u] = t0[u] + t1[u];
+            }
+            fence_before_sync();
+            mbar_arrive_warp(acc_empty + b);  // the values are in registers: the MMA may reuse the buffer
+            const int64_t j0 = (int64_t)J * kBN + sub * 32;
+            const float4* ys4 = reinterpret_cast<const float4*>(p.xs + j0);  // padded: 32 readable entries
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4) {
+                const float4 c4 = __ldg(ys4 + u4);
+                e[u4 * 4 + 0] = ExpTraits<float>::bexp(fmaf(e[u4 * 4 + 0] * c4.x, c1r, -M));
+                e[u4 * 4 + 1] = ExpTraits<float>::bexp(fmaf(e[u4 * 4 + 1] * c4.y, c1r, -M));
+                e[u4 * 4 + 2] = ExpTraits<float>::bexp(fmaf(e[u4 * 4 + 2] * c4.z, c1r, -M));
+                e[u4 * 4 + 3] = ExpTraits<float>::bexp(fmaf(e[u4 * 4 + 3] * c4.w, c1r, -M));
+            }
+            // columns past N, and the pair (i, i) when it is excluded, add nothing (rows past N occur in the
+            // last diagonal tile only, whose row sums are not merged)
+            const bool diag = I == J;
+            const int64_t lim = p.N - j0, self = (diag && p.exclude_self) ? row - j0 : -1;
+            if (__any_sync(0xffffffffu, lim < 32 || (self >= 0 && self < 32))) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) e[u] = (u >= lim || u == self) ? 0.f : e[u];
+            }
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 32; ++u) s4[u & 3] += e[u];
+            rs += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            if (!diag) {
+                // column sums over the warp's 32 rows through shared memory (row stride 36 floats: the
+                // 16-byte stores of eight lanes and the column reads of 32 lanes hit distinct banks)
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4*>(tr + lane * kTrW + 4 * k) =
+                        make_float4(e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
+                __syncwarp();
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int r = 0; r < 32; ++r) c4[r & 3] += tr[r * kTrW + lane];
+                p.pcol[((size_t)t * kBM + sub * 32 + lane) * 4 + q] = (c4[0] + c4[1]) + (c4[2] + c4[3]);
             }
         }
         if (ok && rb_cur >= 0) flush();
@@ -1315,7 +1640,8 @@ void launch_sched_prefix(const Sched& sc, int64_t* pfx, cudaStream_t s) {
 struct LseTcPlan {
     int64_t Xpad, Ypad;
     int CT;
-    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_cnt, off_pfx, bytes;
+    size_t off_xh, off_xl, off_yh, off_yl, off_xs, off_ys, off_xn, off_yn, off_part, off_cnt, off_pfx, off_prow,
+        off_pcol, off_sym, bytes;
 };
 
 static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
@@ -1343,6 +1669,11 @@ static LseTcPlan lse_tc_plan(int64_t N, int64_t M, bool same) {
     pl.off_part = o; o += al256((size_t)(RB + kGrid) * 4 * 2 * kBM * 4);  // slot rb + CTA
     pl.off_cnt = o; o += al256((size_t)RB * 4);
     pl.off_pfx = o; o += al256((size_t)(RB + 1) * 8);
+    // the symmetric sweep (lse_fwd_sym_tc) when the points are shared and its column partials stay small
+    const bool symw = same && RB <= kSymCap;
+    pl.off_prow = o; o += symw ? al256((size_t)(RB + kGrid) * kBM * 4 * 4) : 0;
+    pl.off_pcol = o; o += symw ? al256((size_t)(RB * (RB + 1) / 2) * kBM * 4 * 4) : 0;
+    pl.off_sym = o; o += symw ? 256 : 0;
     pl.bytes = o;
     return pl;
 }
@@ -1419,6 +1750,29 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
         launch_sched_prefix(sc, pfx, s);
         ++n;
     }
+    // X = Y, linear score without exp, no mask, a triangle small enough: the symmetric sweep first; it
+    // falls back (flag) to the full sweep below when the scores span too wide a range
+    const int RB = (int)(pl.Xpad / kBM);
+    const bool sym = same && a.metric == kLinear && !a.apply_exp && !a.pm && RB <= kSymCap;
+    LseSymParams q;
+    if (sym) {
+        q.N = a.nP;
+        q.RB = RB;
+        q.T = (int64_t)RB * (RB + 1) / 2;
+        q.G = capped_grid((int)(q.T < kGrid ? q.T : kGrid));
+        q.exclude_self = a.exclude_self;
+        q.scale = (float)a.scale;
+        q.xs = xs;
+        q.xn = xn;
+        q.prow = reinterpret_cast<float*>(ws + pl.off_prow);
+        q.pcol = reinterpret_cast<float*>(ws + pl.off_pcol);
+        q.sym = reinterpret_cast<int*>(ws + pl.off_sym);
+        q.err = err;
+        cudaFuncSetAttribute(lse_fwd_sym_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemS);
+        HookScope h("lse_fwd_sym_tc", s);
+        launch_pdl(lse_fwd_sym_tc, dim3(q.G), dim3(kTcThreads), kSmemS, s, mxh, mxl, q);
+        ++n;
+    }
     const int64_t T = sched_total(sc);
     const int G = capped_grid((int)(T < kGrid ? T : kGrid));
     LseTcParams p;
@@ -1441,6 +1795,10 @@ int launch_lse_tc(const SweepArgs& a, void* lse, bool same, cudaStream_t s) {
     p.cnt = cnt;
     p.lse = static_cast<float*>(lse);
     p.err = err;
+    p.sym = sym ? q.sym : nullptr;
+    p.prow = sym ? q.prow : nullptr;
+    p.pcol = sym ? q.pcol : nullptr;
+    p.Gs = sym ? q.G : 0;
     auto go = [&](auto kernel) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemF);
         HookScope h("lse_fwd_tc", s);

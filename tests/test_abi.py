@@ -81,8 +81,11 @@ def test_workspace_sizes_from_shapes(lib):
     assert ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 32, _lib.TP_F64)) >= 2 * a32 - 512
     # fp32, D = 64: room for the tensor-core path's fp16 hi/lo split (256 bytes per distinct point)
     assert a >= 2 * 8192 * 256
+    # Y = X: one split, plus the triangle sweep's column partials (2 KB per tile of the upper triangle of
+    # 64 x 64 tiles of 128 points)
     same = ws(lib, "pairwise_logsumexp", pairs(8192, 8192, 64, X=FAKE, Y=FAKE))
-    assert 8192 * 256 <= same < a
+    tri = 64 * 65 // 2 * 128 * 4 * 4
+    assert 8192 * 256 + tri <= same and same - tri < a
 
 
 def call_matmul(lib, p, s, V=FAKE + 0x200000, C=4, out=FAKE + 0x300000, w=None, n=0):

@@ -69,3 +69,25 @@ def test_infonce_mixed_magnitudes(oracle, N, spread):
     assert_close(holder["lse"], ol, achievable(p_lse.detach(), ol, TOL_F32_FWD, slack=TC_SLACK), f"lse {spread}")
     assert_close(holder["g"]["dX"], want, achievable(pl.grads(p_lse, gl)["dX"], want, TOL_F32_GRAD, slack=TC_SLACK),
                  f"z.grad {spread}")
+
+
+@pytest.mark.parametrize("scale", [1 / 0.07, 60.0])
+@pytest.mark.parametrize("N", [129, 1000, 4097])
+@pytest.mark.parametrize("excl", [True, False])
+def test_infonce_forward_triangle_and_fallback(oracle, N, scale, excl):
+    """X = Y, linear score without exp: the forward sweeps the upper triangle of tiles against one fixed
+    offset M = |scale| log2(e) max|z|^2 when 2 M <= 120 (scale 1/0.07 on unit rows: M = 20.6), and falls
+    back to the full sweep with running maxima otherwise (scale 60: M = 86.6). Both are held to the fp32
+    forward tolerance against the oracle, on row counts with a ragged last block."""
+    g0 = torch.Generator().manual_seed(900 + N)
+    z = torch.nn.functional.normalize(torch.randn(N, 64, generator=g0), dim=1)
+    zd = z.to(DEV)
+    sc = Score("linear", scale=scale)
+    holder = {}
+    names = _kernels(lambda: holder.setdefault("lse", ops.pairwise_logsumexp(zd, zd, sc, excl)))
+    assert {"lse_fwd_sym_tc", "lse_fwd_tc"} <= names, names
+    pb = oracle.Problem(z, z, metric="linear", scale=scale)
+    want = oracle.logsumexp(pb, excl)
+    plain = Plain(z, z, metric="linear", scale=scale, same=True).logsumexp(excl)
+    assert_close(holder["lse"], want, achievable(plain.detach(), want, TOL_F32_FWD, slack=TC_SLACK),
+                 f"lse N={N} scale={scale} exclude_self={excl}")
