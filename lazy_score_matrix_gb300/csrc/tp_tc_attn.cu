@@ -1,7 +1,7 @@
 // Pairwise attention out = softmax(scale Q K^T) V and its replay backward on the Blackwell tensor
 // cores (fp32 data, D = C = 64, linear score without exp or row/column parameters): torchpairwise
 // guide "Using Torchpairwise in Models", Task Map (attention: softmax_matmul(V) on lazy(Q, K, "linear")
-// times a scale), and the introduction ("First derivatives replay the tiles").
+// times a scale), and the introduction (first derivatives by re-evaluating the tiles).
 //
 // Operands. Each of Q, K, V and dO is multiplied by one power of two of its own (its largest |element|
 // brought into [2^14, 2^15)) and split into hi = fp16(x 2^e) and lo = fp16(x 2^e - hi), both rounded to
