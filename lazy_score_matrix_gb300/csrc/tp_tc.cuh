@@ -316,6 +316,25 @@ __host__ __device__ inline int rb_of_tile(int64_t t, int CT) {
     return t < (1ll << 32) ? (int)((uint32_t)t / (uint32_t)CT) : (int)(t / CT);
 }
 
+// The upper triangle of a symmetric sweep (the log-sum-exp forward for X = Y): tiles (I, J), J >= I, of
+// RB row blocks, numbered row-block major. First tile of row block I:
+__host__ __device__ inline int64_t sym_start(int64_t I, int64_t RB) { return I * RB - I * (I - 1) / 2; }
+
+// (row block, column block) of consecutive tiles of the triangle.
+struct SymCursor {
+    int I, J, RB;
+    __host__ __device__ SymCursor(int64_t t, int RB_) : I(0), J(0), RB(RB_) {
+        while (I + 1 < RB && sym_start(I + 1, RB) <= t) ++I;
+        J = I + (int)(t - sym_start(I, RB));
+    }
+    __host__ __device__ void next() {
+        if (++J == RB) {
+            ++I;
+            J = I;
+        }
+    }
+};
+
 // Pack two floats into fp16x2 (a in the low half), rounded to nearest.
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);

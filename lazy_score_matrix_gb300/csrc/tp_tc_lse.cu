@@ -164,9 +164,6 @@ __device__ __noinline__ float lse_merge_row(const LseTcParams& p, int rb, int lr
     return l > 0.f ? ExpTraits<float>::lse(m, l) : ninf<float>();
 }
 
-// First tile of row block I in the triangle numbering (row-block major, J from I to RB - 1).
-__host__ __device__ inline int64_t sym_start(int64_t I, int64_t RB) { return I * RB - I * (I - 1) / 2; }
-
 // lse of rows from the triangle sweep's partials (lse_fwd_tc in merge mode): eight threads per row, each
 // adding every eighth term (the row partials of the CTAs that swept the row's block, in CTA order, then the
 // column partials of the tiles (I, R), I < R, in order of I), the eight sums combined in a fixed tree.
@@ -508,21 +505,6 @@ struct LseSymParams {
     float* pcol;        // [T][128][4 row quarters]: column sums of each off-diagonal tile
     int* sym;           // [2]: 1 if the sweep fell back (lse_fwd_tc sweeps), 0 if done; M as float bits
     int* err;
-};
-
-// (row block, column block) of consecutive tiles of the triangle.
-struct SymCursor {
-    int I, J, RB;
-    __device__ __forceinline__ SymCursor(int64_t t, int RB_) : I(0), J(0), RB(RB_) {
-        while (I + 1 < RB && sym_start(I + 1, RB) <= t) ++I;
-        J = I + (int)(t - sym_start(I, RB));
-    }
-    __device__ __forceinline__ void next() {
-        if (++J == RB) {
-            ++I;
-            J = I;
-        }
-    }
 };
 
 // M (base 2) from the largest |x|^2, the same value in every CTA and in the merge.

@@ -5,7 +5,8 @@
 // RB + G; the CTAs a merge reads are exactly those whose ranges met the row block. The device-side table
 // lookups (tile_start, pos_of_tile, SchedCursor) are restated here over a host prefix table; the interval
 // of each row block (live_tiles), the order, the tile count (sched_total) and the CTA ranges
-// (range_start, cta_of_tile) are the header's own.
+// (range_start, cta_of_tile) are the header's own, as are the triangle's numbering and cursor (sym_start,
+// SymCursor).
 #include <cstdio>
 #include <cstdlib>
 #include <set>
@@ -90,6 +91,43 @@ static void run(int pm, int col, long long band, long long R, long long C, int B
     }
 }
 
+// The triangle of the X = Y log-sum-exp forward: every tile (I, J >= I) visited once by the CTA ranges in
+// order (SymCursor); the row partial slots (I + CTA) distinct and below RB + G; the CTAs the merge reads for
+// row block R (cta_of_tile of R's first and last tile) exactly those that swept R's row tiles; every
+// off-diagonal tile (I, R) at sym_start(I) + R - I.
+static void run_tri(long long N, int grid) {
+    const int RB = (int)((N + 127) / 128);
+    const long long T = (long long)RB * (RB + 1) / 2;
+    const int G = (int)(T < grid ? T : grid);
+    std::set<std::pair<int, int>> seen;
+    std::set<long long> slots;
+    std::vector<std::set<int>> rows(RB);
+    std::vector<std::vector<long long>> cols(RB);
+    for (int c = 0; c < G; ++c) {
+        const long long tb = range_start(T, G, c), te = range_start(T, G, c + 1);
+        CHECK(te > tb, "empty triangle range of CTA %d\n", c);
+        SymCursor cur(tb, RB);
+        for (long long t = tb; t < te; ++t, cur.next()) {
+            CHECK(cur.I >= 0 && cur.I <= cur.J && cur.J < RB && sym_start(cur.I, RB) + cur.J - cur.I == t,
+                  "triangle tile %lld at (%d, %d)\n", t, cur.I, cur.J);
+            CHECK(seen.insert({cur.I, cur.J}).second, "triangle tile (%d, %d) twice\n", cur.I, cur.J);
+            rows[cur.I].insert(c);
+            if (cur.J != cur.I) cols[cur.J].push_back(t);
+        }
+    }
+    CHECK((long long)seen.size() == T, "%zu triangle tiles of %lld\n", seen.size(), T);
+    for (int R = 0; R < RB; ++R) {
+        for (int c : rows[R]) CHECK(slots.insert(R + c).second && R + c < RB + G, "triangle slot %d\n", R + c);
+        const long long t0 = sym_start(R, RB);
+        const int lo = cta_of_tile(T, G, t0), hi = cta_of_tile(T, G, t0 + (RB - R) - 1);
+        CHECK((int)rows[R].size() == hi - lo + 1 && *rows[R].begin() == lo && *rows[R].rbegin() == hi,
+              "triangle merge CTAs of row block %d\n", R);
+        CHECK((int)cols[R].size() == R, "row block %d has %zu column tiles\n", R, cols[R].size());
+        for (int I = 0; I < R && I < (int)cols[R].size(); ++I)
+            CHECK(cols[R][I] == sym_start(I, RB) + R - I, "column tile (%d, %d)\n", I, R);
+    }
+}
+
 int main() {
     const long long sizes[] = {1, 5, 64, 127, 128, 129, 300, 517, 1000, 2049};
     const long long bands[] = {0, 1, 17, 63, 64, 200, 5000};
@@ -104,6 +142,12 @@ int main() {
                         for (long long b : bands) run(kPairsBand, col, b, R, C, 128, BN, grid);
                         cases += 9;
                     }
-    std::printf("%d schedules, %d failures\n", cases, fails);
+    int tri = 0;
+    for (int grid : {1, 3, 7, 152})
+        for (long long N = 1; N <= 96 * 128; N += (N < 1100 ? 37 : 1021)) {
+            run_tri(N, grid);
+            ++tri;
+        }
+    std::printf("%d schedules, %d triangles, %d failures\n", cases, tri, fails);
     return fails ? 1 : 0;
 }
