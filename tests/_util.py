@@ -19,11 +19,6 @@ def to_np(t):
 
 # Floor of the relative error, as a fraction of the tensor's largest magnitude.
 FLOOR = 1e-3
-# The stress matrix (random biases, weights and exp on top of every metric) builds outputs that
-# cancel far below their terms (weighted averages of many random-sign rows, exp of exp); there plain
-# fp32 arithmetic on the exact inputs, with pairwise sums, already misses the 1e-3 floor by up to 3x,
-# so those cases are measured with a 1e-2 floor.
-STRESS_FLOOR = 1e-2
 
 
 def rel_err(got, want, floor_frac=FLOOR, abs_floor=0.0):
