@@ -91,3 +91,21 @@ def test_infonce_forward_triangle_and_fallback(oracle, N, scale, excl):
     plain = Plain(z, z, metric="linear", scale=scale, same=True).logsumexp(excl)
     assert_close(holder["lse"], want, achievable(plain.detach(), want, TOL_F32_FWD, slack=TC_SLACK),
                  f"lse N={N} scale={scale} exclude_self={excl}")
+
+
+@pytest.mark.parametrize("N", [12288, 12289])
+def test_infonce_forward_triangle_cap(oracle, N):
+    """The triangle forward runs up to 96 row blocks (N = 12288) and the full sweep beyond (N = 12289),
+    where the triangle's column partials would outgrow their cap; both against the oracle, unit rows,
+    scale 1/0.07, exclude_self."""
+    g0 = torch.Generator().manual_seed(1200 + N)
+    z = torch.nn.functional.normalize(torch.randn(N, 64, generator=g0), dim=1)
+    zd = z.to(DEV)
+    sc = Score("linear", scale=1 / 0.07)
+    holder = {}
+    names = _kernels(lambda: holder.setdefault("lse", ops.pairwise_logsumexp(zd, zd, sc, True)))
+    assert ("lse_fwd_sym_tc" in names) == (N <= 96 * 128), names
+    want = oracle.logsumexp(oracle.Problem(z, z, metric="linear", scale=1 / 0.07), True)
+    plain = Plain(z, z, metric="linear", scale=1 / 0.07, same=True).logsumexp(True)
+    assert_close(holder["lse"], want, achievable(plain.detach(), want, TOL_F32_FWD, slack=TC_SLACK),
+                 f"lse N={N}")
